@@ -1,0 +1,69 @@
+/*
+ * Oracle for the MegaMoE expert path: a plain, slow CPU restatement used only
+ * as test infrastructure (tests, the smoke check and the CPU baseline timing).
+ * It shares no code with the CUDA library.
+ */
+#ifndef MEGAMOE_ORACLE_H
+#define MEGAMOE_ORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+  int T;          /* tokens                                  */
+  int H;          /* hidden size (K of L1, N of L2)          */
+  int I;          /* intermediate size (N of L1 is 2I)       */
+  int E;          /* routed experts                          */
+  int k;          /* routed slots per token                  */
+  int S;          /* shared experts (0 or more), weight 1    */
+  float clamp;    /* SwiGLU clamp c (<= 0: off)              */
+  int weight_in_combine; /* diagnosis only: apply top-k weight in the combine instead of L1 */
+} orc_dims;
+
+/* Format decoders / encoders (OCP Microscaling v1.0, OCP FP8, bfloat16). */
+float orc_e4m3_to_float(uint8_t b);
+float orc_e2m1_to_float(uint8_t nibble);
+float orc_ue8m0_to_float(uint8_t b);
+uint8_t orc_float_to_e4m3(float v);      /* nearest even, saturating to +-448 */
+uint16_t orc_float_to_bf16(float v);     /* nearest even */
+float orc_bf16_to_float(uint16_t h);
+uint8_t orc_requant_code(float amax);    /* UE8M0 code for the L2-activation scale */
+
+void orc_decode_e4m3(const uint8_t* in, float* out, long n);
+void orc_decode_e2m1(const uint8_t* in, float* out, long n);
+void orc_decode_ue8m0(const uint8_t* in, float* out, long n);
+void orc_encode_e4m3(const float* in, uint8_t* out, long n);
+void orc_encode_bf16(const float* in, uint16_t* out, long n);
+void orc_requant_codes(const float* amax, uint8_t* out, long n);
+
+/* Routing: counting sort of the T*(k+S) slots by expert, stable in slot order.
+ * counts[E+S], offsets[E+S+1], perm[T*(k+S)] (pool row -> slot), pos[T*(k+S)]
+ * (slot -> pool row or -1). Returns the number of out-of-range expert ids
+ * (treated as disabled slots). */
+int orc_route(int T, int k, int S, int E, const int32_t* topk_idx,
+              int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* pos);
+
+/* Whole path. Optional intermediates (pool order, NULL to skip):
+ *   acc1 [R][2I] float   L1 accumulators (gate | up)
+ *   q    [R][I]  uint8   E4M3 L2 activations;  qsf [R][I/32] UE8M0 codes
+ *   z    [R][H]  uint16  BF16 L2 outputs per slot row
+ * with R = T*(k+S). Rows beyond the valid count are left untouched.
+ * Returns the out-of-range count from orc_route, or a negative error. */
+int orc_forward(const orc_dims* d, const uint8_t* x, const uint8_t* x_sf, const int32_t* topk_idx,
+                const float* topk_w, const uint8_t* w1, const uint8_t* w1_sf, const uint8_t* w2,
+                const uint8_t* w2_sf, uint16_t* out, float* acc1, uint8_t* q, uint8_t* qsf, uint16_t* z,
+                int nthreads);
+
+/* L2 alone from given E4M3 activations (used to pin the L2 contraction):
+ * acc2[r][h] = sum_i deq(q[r][i]) * deq(W2[e_r][h][i]), float, ascending i. */
+void orc_l2_rows(int R, int H, int I, const int32_t* expert_of_row, const uint8_t* q, const uint8_t* qsf,
+                 const uint8_t* w2, const uint8_t* w2_sf, float* acc2);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,254 @@
+"""Seeded synthetic workloads for the MoE expert path.
+
+The five workloads mirror the model shapes the MegaMoE pages benchmark
+(DeepSeek-style hidden 7168 x intermediate 2048, 256 routed experts, top-8)
+plus a tiny case and a mid-size case with the SwiGLU clamp enabled:
+
+  tiny     T=32    H=512  I=256  E=8   k=2          (seed 0)
+  decode   T=8     H=7168 I=2048 E=256 k=8          (seed 1)
+  mid      T=1024  H=4096 I=1536 E=128 k=8 clamp 7  (seed 2)
+  skewed   T=4096  H=7168 I=2048 E=256 k=8 + 1 shared expert, Zipf(1.2) routing (seed 3)
+  prefill  T=16384 H=7168 I=2048 E=256 k=8          (seed 4)
+
+Value recipe (identical bytes from the host and the device builds):
+  x   : bf16(N(0,1)) quantised to FP8 E4M3 with one UE8M0 scale per 32 along H
+  W1  : [E+S, 2I, H] (gate rows [0,I), up rows [I,2I)), N(0, 1/H) -> E2M1 + UE8M0 per 32 along H
+  W2  : [E+S, H, I], N(0, 1/I) -> E2M1 + UE8M0 per 32 along I
+  topk: uniform without replacement (or Zipf for "skewed"), weights = softmax of N(0,1) logits
+
+This module holds no step of the expert computation; it only produces inputs.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_HOST_SO = os.path.join(_HERE, "libsynth.so")
+_DEV_SO = os.path.join(_HERE, "libsynth_cuda.so")
+
+TAG_W1 = 2
+TAG_W2 = 3
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    H: int
+    I: int
+    E: int
+    k: int
+    S: int = 0
+    clamp: float = 0.0
+    zipf: float = 0.0
+    seed: int = 0
+
+    @property
+    def Ep(self) -> int:
+        """Experts including the shared ones (stacked after the routed experts)."""
+        return self.E + self.S
+
+    @property
+    def Kp(self) -> int:
+        """Slots per token: k routed + S shared."""
+        return self.k + self.S
+
+    @property
+    def rows(self) -> int:
+        """Routed + shared rows when every slot is valid."""
+        return self.T * self.Kp
+
+    @property
+    def std1(self) -> float:
+        return float(np.float32(1.0 / math.sqrt(self.H)))
+
+    @property
+    def std2(self) -> float:
+        return float(np.float32(1.0 / math.sqrt(self.I)))
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+    def flops(self, n_rows: int | None = None) -> float:
+        """Algorithmic FLOPs: 2*H*2I (L1) + 2*I*H (L2) per routed or shared row."""
+        n = self.rows if n_rows is None else n_rows
+        return 6.0 * self.H * self.I * n
+
+    def expert_bytes(self) -> float:
+        """Weight bytes one expert streams: W1 + W2 codes (1/2 B) and scales (1/32 B)."""
+        return 3.0 * self.H * self.I * (0.5 + 1.0 / 32.0)
+
+
+CONFIGS = {
+    "tiny": Workload("tiny", T=32, H=512, I=256, E=8, k=2, seed=0),
+    "decode": Workload("decode", T=8, H=7168, I=2048, E=256, k=8, seed=1),
+    "mid": Workload("mid", T=1024, H=4096, I=1536, E=128, k=8, clamp=7.0, seed=2),
+    "skewed": Workload("skewed", T=4096, H=7168, I=2048, E=256, k=8, S=1, zipf=1.2, seed=3),
+    "prefill": Workload("prefill", T=16384, H=7168, I=2048, E=256, k=8, seed=4),
+}
+
+
+# ----------------------------------------------------------------------------- build / load
+def build(cuda: bool = True, verbose: bool = False) -> None:
+    """Compile the host generator (gcc) and, if asked, the device generator (nvcc, sm_103a)."""
+    src = os.path.join(_HERE, "synth.c")
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+           "-o", _HOST_SO, src, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=not verbose)
+    if cuda:
+        cu = os.path.join(_HERE, "synth_cuda.cu")
+        nvcc = os.environ.get("NVCC", "nvcc")
+        cmd = [nvcc, "-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-fmad=false",
+               "-Xcompiler", "-fPIC", "-shared", "-o", _DEV_SO, cu]
+        subprocess.run(cmd, check=True, capture_output=not verbose)
+
+
+_host = None
+_dev = None
+
+
+def _lib_host():
+    global _host
+    if _host is None:
+        if not os.path.exists(_HOST_SO):
+            build(cuda=False)
+        lib = ctypes.CDLL(_HOST_SO)
+        u64, i32, f32, p = ctypes.c_uint64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+        lib.syn_gen_x.argtypes = [u64, i32, i32, i32, p, p]
+        lib.syn_gen_x.restype = None
+        lib.syn_gen_w.argtypes = [u64, i32, i32, i32, i32, i32, f32, p, p, i32]
+        lib.syn_gen_w.restype = None
+        lib.syn_gen_routing.argtypes = [u64, i32, i32, i32, ctypes.c_double, p, p]
+        lib.syn_gen_routing.restype = i32
+        lib.syn_u64_at.argtypes = [u64, u64]
+        lib.syn_u64_at.restype = u64
+        lib.syn_key.argtypes = [u64, u64]
+        lib.syn_key.restype = u64
+        lib.syn_normal_at.argtypes = [u64, u64]
+        lib.syn_normal_at.restype = f32
+        _host = lib
+    return _host
+
+
+def _lib_dev():
+    global _dev
+    if _dev is None:
+        if not os.path.exists(_DEV_SO):
+            build(cuda=True)
+        lib = ctypes.CDLL(_DEV_SO)
+        u64, i32, f32, p = ctypes.c_uint64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+        lib.syn_dev_gen_x.argtypes = [u64, i32, i32, p, p, p]
+        lib.syn_dev_gen_x.restype = i32
+        lib.syn_dev_gen_w.argtypes = [u64, i32, i32, i32, i32, i32, f32, p, p, p]
+        lib.syn_dev_gen_w.restype = i32
+        _dev = lib
+    return _dev
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _nthreads() -> int:
+    return max(1, min(64, os.cpu_count() or 1))
+
+
+# ----------------------------------------------------------------------------- host generation
+def routing(w: Workload, T: int | None = None):
+    """(topk_idx int32 [T,k], topk_w float32 [T,k]) for the workload's routing recipe."""
+    T = w.T if T is None else T
+    idx = np.zeros((T, w.k), np.int32)
+    wt = np.zeros((T, w.k), np.float32)
+    rc = _lib_host().syn_gen_routing(w.seed, T, w.E, w.k, float(w.zipf), _ptr(idx), _ptr(wt))
+    if rc != 0:
+        raise ValueError(f"routing generator failed ({rc})")
+    return idx, wt
+
+
+def x_host(w: Workload, t0: int = 0, t1: int | None = None):
+    """Activation rows [t0, t1): (x_fp8 uint8 [n,H], x_sf uint8 [n,H/32])."""
+    t1 = w.T if t1 is None else t1
+    n = max(0, t1 - t0)
+    x = np.zeros((n, w.H), np.uint8)
+    sf = np.zeros((n, w.H // 32), np.uint8)
+    if n:
+        _lib_host().syn_gen_x(w.seed, w.H, t0, t1, _ptr(x), _ptr(sf))
+    return x, sf
+
+
+def weight_shape(w: Workload, which: int):
+    """(rows per expert, K) of W1 (which=TAG_W1) or W2 (which=TAG_W2)."""
+    return (2 * w.I, w.H) if which == TAG_W1 else (w.H, w.I)
+
+
+def w_host(w: Workload, which: int, e0: int = 0, e1: int | None = None, nthreads: int | None = None):
+    """Weights of experts [e0, e1): (codes uint8 [n,rows,K/2], scales uint8 [n,rows,K/32])."""
+    e1 = w.Ep if e1 is None else e1
+    rows, K = weight_shape(w, which)
+    n = max(0, e1 - e0)
+    codes = np.zeros((n, rows, K // 2), np.uint8)
+    sf = np.zeros((n, rows, K // 32), np.uint8)
+    std = w.std1 if which == TAG_W1 else w.std2
+    if n:
+        _lib_host().syn_gen_w(w.seed, which, rows, K, e0, e1, std, _ptr(codes), _ptr(sf),
+                              nthreads or _nthreads())
+    return codes, sf
+
+
+def host_inputs(w: Workload):
+    """Every input of the workload generated on the host (small workloads only)."""
+    idx, wt = routing(w)
+    x, xsf = x_host(w)
+    w1, w1sf = w_host(w, TAG_W1)
+    w2, w2sf = w_host(w, TAG_W2)
+    return dict(topk_idx=idx, topk_w=wt, x=x, x_sf=xsf, w1=w1, w1_sf=w1sf, w2=w2, w2_sf=w2sf)
+
+
+# ----------------------------------------------------------------------------- device generation
+def x_device(w: Workload, x, x_sf, stream=None):
+    """Fill torch CUDA uint8 tensors x [T,H] and x_sf [T,H/32] on the device."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = _lib_dev().syn_dev_gen_x(w.seed, x.shape[0], w.H, x.data_ptr(), x_sf.data_ptr(), s.cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"device x generator failed ({rc})")
+
+
+def w_device(w: Workload, which: int, codes, sf, e0: int = 0, e1: int | None = None, stream=None):
+    """Fill torch CUDA uint8 tensors with the weights of experts [e0, e1)."""
+    import torch
+    e1 = w.Ep if e1 is None else e1
+    rows, K = weight_shape(w, which)
+    std = w.std1 if which == TAG_W1 else w.std2
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = _lib_dev().syn_dev_gen_w(w.seed, which, rows, K, e0, e1, std, codes.data_ptr(), sf.data_ptr(),
+                                  s.cuda_stream)
+    if rc != 0:
+        raise RuntimeError(f"device weight generator failed ({rc})")
+
+
+def device_inputs(w: Workload, device="cuda"):
+    """Every input of the workload resident in device memory (weights generated in HBM)."""
+    import torch
+    idx, wt = routing(w)
+    out = dict(topk_idx=torch.from_numpy(idx).to(device), topk_w=torch.from_numpy(wt).to(device))
+    x = torch.empty((w.T, w.H), dtype=torch.uint8, device=device)
+    xsf = torch.empty((w.T, w.H // 32), dtype=torch.uint8, device=device)
+    if w.T:
+        x_device(w, x, xsf)
+    out.update(x=x, x_sf=xsf)
+    for which, name in ((TAG_W1, "w1"), (TAG_W2, "w2")):
+        rows, K = weight_shape(w, which)
+        c = torch.empty((w.Ep, rows, K // 2), dtype=torch.uint8, device=device)
+        s = torch.empty((w.Ep, rows, K // 32), dtype=torch.uint8, device=device)
+        w_device(w, which, c, s)
+        out[name] = c
+        out[name + "_sf"] = s
+    return out
