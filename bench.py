@@ -1,0 +1,360 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 MoE expert path (route -> L1 -> SwiGLU/requant -> L2 -> combine).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|tiny|mid|skewed|prefill]
+                    [--impl ours|reference]
+
+Prints one JSON line. A step is one mm_run over the workload's batch with all
+inputs resident in HBM (weights generated in device memory); L2 is flushed
+between steps (a 256 MB write, outside the timed events). `value` is tokens per
+second over all ranks. `e2e` repeats the measurement through the public Python
+API with the step's activations and routing copied from pinned host memory and
+the output copied back inside the timed region. `--impl reference` times the CPU
+oracle on the host cores on a bounded sample of the same workload.
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+(tokens are independent; there is no data-path collective); a barrier and a
+max-reduction of the elapsed time are the only cross-rank operations.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and TFLOP/s on 1 GB300; % of HBM or FP8xFP4 tensor roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+KERNEL_NAMES = ["route", "gather", "l1_gemm", "l2_gemm", "combine"]
+
+# DRAM bytes (read + write) per launch of the dominant kernel from one ncu
+# capture, keyed by workload, valid only while mm_gemm.cu hashes to `src`.
+NCU_TRAFFIC = {}
+
+
+def gemm_source_hash() -> str:
+    with open(os.path.join(ROOT, "moe_expert_layer_scan_gb300", "csrc", "mm_gemm.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def algorithmic(w, counts):
+    """Algorithmic work of one step from the routing counts (per-expert rows)."""
+    counts = np.asarray(counts)
+    R = int(counts.sum())
+    touched = int((counts > 0).sum())
+    sf = 1.0 / 32.0
+    w1 = touched * 2 * w.I * w.H * (0.5 + sf)
+    w2 = touched * w.H * w.I * (0.5 + sf)
+    l1_act = R * w.H * (1 + sf) + R * w.I * (1 + sf)          # pool rows in, FP8 L2 operand out
+    l2_act = R * w.I * (1 + sf) + R * w.H * 2                  # FP8 L2 operand in, BF16 slot rows out
+    return dict(rows=R, touched=touched, flops=6.0 * w.H * w.I * R, l1_flops=4.0 * w.H * w.I * R,
+                l2_flops=2.0 * w.H * w.I * R, l1_bytes=w1 + l1_act, l2_bytes=w2 + l2_act,
+                weight_bytes=w1 + w2)
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample(w, n_tokens):
+    """Inputs of a bounded sample (the first n_tokens tokens) for the oracle:
+    the sub-problem over only the experts those tokens touch."""
+    tokens = list(range(min(n_tokens, w.T)))
+    idx, wt = workloads.routing(w)
+    xs = [workloads.x_host(w, t, t + 1) for t in tokens]
+    routed = sorted({int(e) for e in idx[tokens].ravel()})
+    remap = {e: i for i, e in enumerate(routed)}
+    sub_idx = np.vectorize(remap.get)(idx[tokens]).astype(np.int32)
+    experts = routed + list(range(w.E, w.E + w.S))
+    parts1 = [workloads.w_host(w, workloads.TAG_W1, e, e + 1) for e in experts]
+    parts2 = [workloads.w_host(w, workloads.TAG_W2, e, e + 1) for e in experts]
+    cat = lambda ps, i: np.ascontiguousarray(np.concatenate([p[i] for p in ps]))
+    dims = dict(T=len(tokens), H=w.H, I=w.I, E=len(routed), k=w.k, S=w.S, clamp=w.clamp)
+    args = (np.concatenate([a for a, _ in xs]), np.concatenate([b for _, b in xs]), sub_idx,
+            np.ascontiguousarray(wt[tokens]), cat(parts1, 0), cat(parts1, 1), cat(parts2, 0), cat(parts2, 1))
+    return dims, args, len(tokens), len(experts)
+
+
+def time_oracle(w, n_tokens, reps=1):
+    import oracle
+    o = oracle.get()
+    dims, args, nt, ne = oracle_sample(w, n_tokens)
+    cores = os.cpu_count() or 1
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        o.forward(dims, *args, nthreads=cores)
+        times.append(time.perf_counter() - t0)
+    return times, nt, ne, cores
+
+
+def sample_tokens_for(w):
+    """Tokens per oracle step: about 10-30 s of CPU work on a 16-core host for one sample."""
+    per_token = 6.0 * w.H * w.I * w.Kp
+    return int(max(1, min(w.T, round(2.0e10 / per_token))))
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = workloads.CONFIGS[args.workload]
+    n_tok = max(1, min(w.T, sample_tokens_for(w) // 4))  # one step: a quarter of the CPU-baseline sample
+    times, nt, ne, cores = time_oracle(w, n_tok, reps=args.warmup + args.steps)
+    timed = times[args.warmup:]
+    step_s = sum(timed) / len(timed)
+    value = nt / step_s
+    sample = f"first {nt} of {w.T} tokens of the {w.name} workload ({nt * w.Kp} slot rows, {ne} experts), per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8xfp4 (fp32 accumulate)", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "topk": w.k, "shared": w.S,
+            "swiglu_clamp": w.clamp, "routing": f"zipf({w.zipf})" if w.zipf else "uniform", "seed": w.seed,
+            "l2": "flushed between steps (256 MB write outside the timed events)"}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, world, rank, local):
+    import torch
+    import moe_expert_layer_scan_gb300 as mm
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = workloads.CONFIGS[args.workload]
+    d = workloads.device_inputs(w)
+    moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
+    moe.workspace(w.T)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ins = (d["x"], d["x_sf"], d["topk_idx"], d["topk_w"], d["w1"], d["w1_sf"], d["w2"], d["w2_sf"])
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        moe.run(*ins, out=out)
+    torch.cuda.synchronize()
+    if moe.status() != 0:
+        raise RuntimeError(f"device status {moe.status()} after warm-up")
+    counts = torch.empty(w.Ep, dtype=torch.int32)
+    v = moe.views(w.T)
+    counts.copy_(moe.ws[v.counts - moe.ws.data_ptr():v.counts - moe.ws.data_ptr() + 4 * w.Ep].view(torch.int32).cpu())
+    alg = algorithmic(w, counts.numpy())
+
+    # ---- device-resident timing
+    mm.mm_profile_enable(moe.h, True)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    per_kernel = []
+    clocks = Clocks(torch.cuda.current_device()) if rank == 0 else None
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    for i in range(args.steps):
+        flush.zero_()
+        e0[i].record()
+        moe.run(*ins, out=out)
+        e1[i].record()
+        per_kernel.append(mm.mm_profile_last(moe.h))
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    if dist:
+        dist.barrier()
+    mm.mm_profile_enable(moe.h, False)
+    step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
+    total_ms = sum(step_ms)
+    if moe.status() != 0:
+        raise RuntimeError(f"device status {moe.status()} after the timed steps")
+
+    # ---- end-to-end through the public API with host buffers
+    pin = lambda t: t.cpu().pin_memory()
+    hx, hxs, hidx, hw = pin(d["x"]), pin(d["x_sf"]), pin(d["topk_idx"]), pin(d["topk_w"])
+    hout = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+    dx, dxs, didx, dw = (torch.empty_like(d[k]) for k in ("x", "x_sf", "topk_idx", "topk_w"))
+    h2d = sum(t.numel() * t.element_size() for t in (hx, hxs, hidx, hw))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dxs.copy_(hxs, non_blocking=True)
+        didx.copy_(hidx, non_blocking=True)
+        dw.copy_(hw, non_blocking=True)
+        moe.run(dx, dxs, didx, dw, d["w1"], d["w1_sf"], d["w2"], d["w2_sf"], out=out)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    f0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    f1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        f0[i].record()
+        e2e_step()
+        f1[i].record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(f0, f1))
+    assert torch.equal(hout, out.cpu()), "end-to-end output differs from the device output"
+
+    if dist:
+        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return
+
+    ms = total_ms / args.steps
+    tokens = w.T * world
+    value = tokens / (ms / 1e3)
+    kern = {n: statistics.mean(p[i] for p in per_kernel) for i, n in enumerate(KERNEL_NAMES)
+            if all(len(p) > i for p in per_kernel)}
+    peaks, peak_src = load_peaks()
+    # the dominant kernel is the L1 grouped GEMM (W1 is two thirds of the weights and of the FLOPs)
+    l1_ms = kern.get("l1_gemm")
+    hbm = float(peaks["hbm_gbs"])
+    fp8_peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
+    balance = fp8_peak * 1e12 / (hbm * 1e9)
+    intensity = alg["l1_flops"] / alg["l1_bytes"]
+    if intensity < balance:
+        achieved = alg["l1_bytes"] / (l1_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"}
+    else:
+        achieved = alg["l1_flops"] / (l1_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak,
+                "peak_source": f"{peak_src} bf16_tflops (burst) x {FP8_OVER_BF16} nominal FP8/BF16 ratio"}
+    tr = NCU_TRAFFIC.get(w.name)
+    roof["traffic"] = tr["bytes"] if tr and tr.get("src") == gemm_source_hash() else None
+    roof["kernel"] = "gemm_kernel<L1> (mm_gemm.cu)"
+    roof["algorithmic_bytes_per_launch"] = alg["l1_bytes"]
+    roof["algorithmic_flops_per_launch"] = alg["l1_flops"]
+    roof["kernel_ms"] = l1_ms
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp8xfp4 (fp32 accumulate)", "data": "synthetic",
+            "config": dict(workload_config(w), parallelism=f"{world} independent replicas" if world > 1 else "1 GPU"),
+            "tflops": alg["flops"] * world / (ms / 1e3) / 1e12,
+            "hbm_gbs_whole_step": (alg["l1_bytes"] + alg["l2_bytes"]) / (ms / 1e3) / 1e9,
+            "kernels_ms": kern, "rows": alg["rows"], "experts_touched": alg["touched"],
+            "roofline": roof,
+            "e2e": {"value": tokens / (e2e_ms / args.steps / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+            "gpu_launches": moe.launches(w.T) * args.steps,
+            "clocks": clk}
+    if world == 1 and not args.no_cpu_baseline:
+        n_tok = sample_tokens_for(w)
+        times, nt, ne, cores = time_oracle(w, n_tok, reps=1)
+        line["cpu_baseline"] = {"value": nt / times[0], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"first {nt} of {w.T} tokens ({nt * w.Kp} slot rows, {ne} experts), "
+                                          f"{times[0]:.1f} s wall"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode", choices=list(workloads.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,166 @@
+/*
+ * megamoe.h — C ABI of the GB300 (sm_103a) MegaMoE expert path.
+ *
+ * One call computes, for T tokens on one GPU, the expert part of a
+ * Mixture-of-Experts layer as the DeepGEMM MegaMoE pages describe it
+ * ("MegaMoE on SM100/SM90 research report", sec. 4.1 "pr-304: SM100 Fused
+ * MegaMoE", Linear1 / Linear2 phases and the combine; "MEGAMOE_SM90_DESIGN",
+ * sec. 9 dispatch, 10 L1 epilogue, 11 L2 epilogue + combine):
+ *
+ *   route    per-expert counts, prefix offsets and an expert-sorted permutation
+ *            of the T*(k+S) slots (stable in slot order)
+ *   L1       acc1[r, n] = sum_k x[t_r, k] * W1[e_r, n, k],  n in [0, 2I)
+ *   SwiGLU   y = silu(clamp(gate)) * clamp(up) * w_r       (gate = acc1[:, :I], up = acc1[:, I:])
+ *   requant  per row and 32 columns of y: UE8M0 scale = smallest power of two
+ *            >= amax/448, E4M3 = round_nearest_even(y / scale)
+ *   L2       z[r, h] = bf16( sum_i q[r, i] * W2[e_r, h, i] )
+ *   combine  out[t, h] = bf16( sum over the token's valid slots j, ascending, of z[row(t, j), h] )
+ *
+ * Activations are FP8 E4M3 with one UE8M0 scale per 32 along K; expert
+ * weights are MXFP4: E2M1 codes packed two per byte (even K index in the low
+ * nibble) with one UE8M0 scale per 32 along K. Accumulation is FP32.
+ * Shared experts (num_shared = S) are stacked after the E routed experts in
+ * W1/W2 (indices E..E+S-1) and applied to every token with weight 1.
+ *
+ * Threading: a handle may be used from one host thread at a time. All device
+ * work is enqueued on the caller's stream; no call synchronises the device
+ * except mm_get_status (which synchronises the given stream).
+ */
+#ifndef MEGAMOE_H
+#define MEGAMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MM_API __attribute__((visibility("default")))
+#else
+#define MM_API
+#endif
+
+/* Same type as cudaStream_t / CUstream (NULL = the legacy default stream). */
+struct CUstream_st;
+typedef struct CUstream_st* mm_stream_t;
+
+typedef struct mm_handle* mm_handle_t;
+
+typedef enum {
+  MM_OK = 0,
+  MM_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad option value      */
+  MM_ERR_UNSUPPORTED = 2,        /* shape outside the supported set (see mm_create)    */
+  MM_ERR_WORKSPACE_TOO_SMALL = 3,/* ws_bytes < mm_workspace_bytes(T)                   */
+  MM_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed                  */
+  MM_ERR_DEVICE_TIMEOUT = 5,     /* (device status) a bounded device wait expired      */
+  MM_ERR_BAD_ROUTING = 6,        /* (device status) a topk_idx entry was out of range  */
+  MM_ERR_ALIGNMENT = 7           /* a pointer violates the alignment stated below      */
+} mm_status_t;
+
+/* Device status bits written into the workspace by the kernels and returned
+ * by mm_get_status (0 = no error). */
+#define MM_DEV_BAD_ROUTING 0x1u   /* an out-of-range expert id was skipped (slot disabled) */
+#define MM_DEV_TIMEOUT 0x2u       /* a pipeline wait exceeded its time limit; outputs invalid */
+
+/* Human-readable name of a status code (static string). */
+MM_API const char* mm_status_string(mm_status_t s);
+
+/* Creates a handle for one layer shape (the pages' get_block_m_for_mega_moe /
+ * fp8_fp4_mega_moe setup; "MegaMoE research report" sec. 6, I1).
+ *   E           routed experts, 1 <= E and E + S <= 1024
+ *   H           hidden size; multiple of 128, 128 <= H <= 16384
+ *   I           intermediate size; multiple of 128, 128 <= I <= 16384
+ *   topk        routed slots per token, 1 <= topk <= 16
+ *   num_shared  shared experts S, 0 <= S <= 4, topk + S <= 16
+ * The handle owns only host memory. Returns MM_ERR_UNSUPPORTED for shapes
+ * outside these limits and MM_ERR_CUDA if the device is not sm_103 (GB300). */
+MM_API mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_shared);
+
+/* SwiGLU options (the SM90 design's activation_clamp / fast_math arguments,
+ * "MEGAMOE_SM90_DESIGN" sec. 10.1): swiglu_clamp > 0 clamps gate and up to
+ * [-c, c] before the SiLU, <= 0 disables the clamp; fast_math != 0 uses the
+ * fast approximate exponential (__expf) in the SiLU. Defaults: no clamp, accurate exp. */
+MM_API mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_math);
+
+/* Bytes of device workspace mm_run needs for T tokens (T >= 0). The
+ * workspace holds the routing tables, the gathered FP8 L1 operand, the FP8 L2
+ * operand, the BF16 per-slot L2 output and a status word. */
+MM_API mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes);
+
+/* Runs the path for T tokens, asynchronously on `stream`.
+ *   x_fp8    device, [T][H] E4M3                                  (16-byte aligned)
+ *   x_sf     device, [T][H/32] UE8M0                               (4-byte aligned)
+ *   topk_idx device, [T][topk] int32, each in [0, E) or -1 (slot disabled);
+ *            other values disable the slot and set MM_DEV_BAD_ROUTING
+ *   topk_w   device, [T][topk] float32 (need not sum to 1)
+ *   w1       device, [E+S][2I][H/2] E2M1 packed; rows [0,I) gate, [I,2I) up   (32-byte aligned)
+ *   w1_sf    device, [E+S][2I][H/32] UE8M0                                     (4-byte aligned)
+ *   w2       device, [E+S][H][I/2] E2M1 packed                                  (32-byte aligned)
+ *   w2_sf    device, [E+S][H][I/32] UE8M0                                      (4-byte aligned)
+ *   out_bf16 device, [T][H] bfloat16, fully overwritten               (16-byte aligned)
+ *   ws       device workspace of ws_bytes >= mm_workspace_bytes(T) (256-byte aligned),
+ *            fully re-initialised by every call, so it can be reused; two calls that
+ *            share a workspace must be ordered on the device (same stream).
+ * All buffers are owned by the caller and must stay valid until the work on
+ * `stream` completes. T == 0 is valid: only the status word is reset.
+ * Returns synchronous argument errors only; device-side errors are read with
+ * mm_get_status. */
+MM_API mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, const int32_t* topk_idx,
+                   const float* topk_w, const void* w1, const void* w1_sf, const void* w2, const void* w2_sf,
+                   void* out_bf16, void* ws, size_t ws_bytes, mm_stream_t stream);
+
+/* Synchronises `stream` and returns in *device_status the MM_DEV_* bits the
+ * last mm_run on this workspace recorded (0 = none). */
+MM_API mm_status_t mm_get_status(mm_handle_t h, const void* ws, mm_stream_t stream, uint32_t* device_status);
+
+/* Number of kernel launches one mm_run for T tokens enqueues. */
+MM_API mm_status_t mm_launches_per_run(mm_handle_t h, int T, int* launches);
+
+/* Debug/test views into a workspace after mm_run for T tokens (device
+ * pointers; contents valid once the stream has reached them):
+ *   counts [E+S] int32, offsets [E+S+1] int32, perm [T(k+S)] int32 (pool row -> slot
+ *   t*(k+S)+j), pos [T(k+S)] int32 (slot -> pool row or -1), row_w [T(k+S)] float,
+ *   pool_x [rows][H] u8, pool_sf [rows][H/32] u8, l2a [rows][I] u8 (E4M3),
+ *   l2a_sf [rows][I/32] u8 (UE8M0), z [rows][H] bf16, status (uint32). Rows are in
+ *   pool order (expert-sorted); only the first offsets[E+S] rows are defined. */
+typedef struct {
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* pos;
+  float* row_w;
+  uint8_t* pool_x;
+  uint8_t* pool_sf;
+  uint8_t* l2a;
+  uint8_t* l2a_sf;
+  uint16_t* z;
+  uint32_t* status;
+  int rows_capacity;
+} mm_debug_views_t;
+
+MM_API mm_status_t mm_debug_views(mm_handle_t h, void* ws, int T, mm_debug_views_t* views);
+
+/* Test hook for the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier nothing ever arrives on, gives up after timeout_ns nanoseconds,
+ * sets MM_DEV_TIMEOUT in the workspace status word and returns. The GPU stays
+ * usable. ws must hold at least 256 bytes. */
+MM_API mm_status_t mm_debug_timeout_probe(void* ws, uint64_t timeout_ns, mm_stream_t stream);
+
+/* Per-launch timing for measurement: with profiling on, mm_run records a CUDA
+ * event on its stream before each launch and after the last one. mm_profile_last
+ * waits for the last recorded event and writes up to n durations in
+ * milliseconds (route, gather, L1 GEMM, L2 GEMM, combine) into ms, returning the
+ * count in *written. Events are created on the handle's device and freed by
+ * mm_destroy or mm_profile_enable(h, 0). */
+MM_API mm_status_t mm_profile_enable(mm_handle_t h, int on);
+MM_API mm_status_t mm_profile_last(mm_handle_t h, float* ms, int n, int* written);
+
+/* Destroys a handle (NULL is ignored). */
+MM_API void mm_destroy(mm_handle_t h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MEGAMOE_H */

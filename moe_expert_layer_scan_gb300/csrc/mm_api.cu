@@ -1,0 +1,320 @@
+// Host side of the C ABI declared in include/megamoe.h: argument checks,
+// workspace carving, TMA tensor-map encoding and the five launches of one
+// forward (route -> gather -> L1 GEMM -> L2 GEMM -> combine).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "mm_internal.h"
+
+using namespace mm;
+
+struct mm_handle {
+  int E, H, I, k, S;
+  float clamp;
+  int fast_math;
+  int device;
+  int num_sms;
+  unsigned long long timeout_ns;
+  // cached weight tensor maps (keyed by base pointer)
+  const void* w1_key;
+  const void* w2_key;
+  CUtensorMap tm_w1;
+  CUtensorMap tm_w2;
+  // optional per-launch events (route, gather, L1, L2, combine, end)
+  bool profile;
+  int n_recorded;
+  cudaEvent_t ev[6];
+};
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2D map over a row-major [rows][k_elems] tensor, box = 128 elements of K x box_rows rows, 128-byte swizzle.
+bool encode_2d(CUtensorMap* m, const void* base, bool fp4, uint64_t k_elems, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {k_elems, rows};
+  cuuint64_t strides[1] = {fp4 ? k_elems / 2 : k_elems};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int variant_for(int T) { return T <= kSmallMaxTokens ? 0 : 1; }
+
+}  // namespace
+
+extern "C" {
+
+const char* mm_status_string(mm_status_t s) {
+  switch (s) {
+    case MM_OK: return "ok";
+    case MM_ERR_INVALID_ARG: return "invalid argument";
+    case MM_ERR_UNSUPPORTED: return "unsupported shape";
+    case MM_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MM_ERR_CUDA: return "CUDA error";
+    case MM_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case MM_ERR_BAD_ROUTING: return "top-k index out of range";
+    case MM_ERR_ALIGNMENT: return "pointer misaligned";
+  }
+  return "unknown status";
+}
+
+mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_shared) {
+  if (!out) return MM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (E < 1 || topk < 1 || num_shared < 0) return MM_ERR_INVALID_ARG;
+  if (E + num_shared > kMaxExperts || topk + num_shared > kMaxSlots || num_shared > 4) return MM_ERR_UNSUPPORTED;
+  if (H < 128 || I < 128 || H % 128 || I % 128 || H > 16384 || I > 16384) return MM_ERR_UNSUPPORTED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MM_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MM_ERR_CUDA;
+  if (major != 10 || minor != 3) return MM_ERR_CUDA;  // built for sm_103a only
+  if (!encode_fn()) return MM_ERR_CUDA;
+  if (mm_gemm_prepare() != 0) return MM_ERR_CUDA;
+  mm_handle* h = new (std::nothrow) mm_handle();
+  if (!h) return MM_ERR_INVALID_ARG;
+  h->E = E; h->H = H; h->I = I; h->k = topk; h->S = num_shared;
+  h->clamp = 0.0f; h->fast_math = 0; h->device = dev; h->num_sms = sms;
+  h->timeout_ns = 4000000000ull;
+  if (const char* t = getenv("MM_DEVICE_TIMEOUT_MS")) {
+    long ms = atol(t);
+    if (ms > 0) h->timeout_ns = (unsigned long long)ms * 1000000ull;
+  }
+  h->w1_key = h->w2_key = nullptr;
+  h->profile = false;
+  h->n_recorded = 0;
+  *out = h;
+  return MM_OK;
+}
+
+mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_math) {
+  if (!h || swiglu_clamp != swiglu_clamp) return MM_ERR_INVALID_ARG;
+  h->clamp = swiglu_clamp > 0.0f ? swiglu_clamp : 0.0f;
+  h->fast_math = fast_math ? 1 : 0;
+  return MM_OK;
+}
+
+mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes) {
+  if (!h || !bytes || T < 0) return MM_ERR_INVALID_ARG;
+  *bytes = make_layout(h->E, h->S, h->H, h->I, h->k, T).total;
+  return MM_OK;
+}
+
+mm_status_t mm_launches_per_run(mm_handle_t h, int T, int* launches) {
+  if (!h || !launches || T < 0) return MM_ERR_INVALID_ARG;
+  *launches = T == 0 ? 1 : 5;
+  return MM_OK;
+}
+
+mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, const int32_t* topk_idx,
+                   const float* topk_w, const void* w1, const void* w1_sf, const void* w2, const void* w2_sf,
+                   void* out_bf16, void* ws, size_t ws_bytes, mm_stream_t stream) {
+  if (!h || T < 0 || !ws) return MM_ERR_INVALID_ARG;
+  const Layout L = make_layout(h->E, h->S, h->H, h->I, h->k, T);
+  if (ws_bytes < L.total) return MM_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned(ws, 256)) return MM_ERR_ALIGNMENT;
+  if (T > 0) {
+    if (!x_fp8 || !x_sf || !topk_idx || !topk_w || !w1 || !w1_sf || !w2 || !w2_sf || !out_bf16)
+      return MM_ERR_INVALID_ARG;
+    if (!aligned(x_fp8, 16) || !aligned(x_sf, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+        !aligned(w1, 32) || !aligned(w2, 32) || !aligned(w1_sf, 4) || !aligned(w2_sf, 4) || !aligned(out_bf16, 16))
+      return MM_ERR_ALIGNMENT;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return MM_ERR_CUDA;
+
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const int Ep = h->E + h->S, Kp = h->k + h->S;
+  const int variant = variant_for(T);
+  const int bn1 = variant == 0 ? kBnSmall : kBnL1Large;
+  const int bn2 = variant == 0 ? kBnSmall : kBnL2Large;
+
+  RouteArgs ra;
+  ra.topk_idx = topk_idx;
+  ra.topk_w = topk_w;
+  ra.counts = reinterpret_cast<int32_t*>(base + L.counts);
+  ra.offsets = reinterpret_cast<int32_t*>(base + L.offsets);
+  ra.tiles_l1 = reinterpret_cast<int32_t*>(base + L.tiles_l1);
+  ra.tiles_l2 = reinterpret_cast<int32_t*>(base + L.tiles_l2);
+  ra.perm = reinterpret_cast<int32_t*>(base + L.perm);
+  ra.pos = reinterpret_cast<int32_t*>(base + L.pos);
+  ra.row_w = reinterpret_cast<float*>(base + L.row_w);
+  ra.status = reinterpret_cast<uint32_t*>(base + L.status);
+  ra.T = T; ra.E = h->E; ra.k = h->k; ra.S = h->S;
+  ra.bn_l1 = bn1; ra.bn_l2 = bn2;
+  ra.fb_l1 = h->I / 128; ra.fb_l2 = h->H / 128;
+  int ev_i = 0;
+  auto mark = [&]() {
+    if (h->profile && ev_i < 6) cudaEventRecord(h->ev[ev_i++], (cudaStream_t)stream);
+  };
+  h->n_recorded = 0;
+  mark();
+  if (mm_launch_route(&ra, stream) != 0) return MM_ERR_CUDA;
+  if (T == 0) {
+    mark();
+    h->n_recorded = ev_i;
+    return MM_OK;
+  }
+
+  GatherArgs ga;
+  ga.x = static_cast<const uint8_t*>(x_fp8);
+  ga.x_sf = static_cast<const uint8_t*>(x_sf);
+  ga.perm = ra.perm;
+  ga.offsets = ra.offsets;
+  ga.pool_x = base + L.pool_x;
+  ga.pool_sf = base + L.pool_sf;
+  ga.H = h->H; ga.Kp = Kp; ga.Ep = Ep;
+  mark();
+  if (mm_launch_gather(&ga, T * Kp, stream) != 0) return MM_ERR_CUDA;
+
+  // Tensor maps: weights are cached per base pointer, activations live in the workspace.
+  if (h->w1_key != w1) {
+    if (!encode_2d(&h->tm_w1, w1, true, (uint64_t)h->H, (uint64_t)Ep * 2 * h->I, 128)) return MM_ERR_CUDA;
+    h->w1_key = w1;
+  }
+  if (h->w2_key != w2) {
+    if (!encode_2d(&h->tm_w2, w2, true, (uint64_t)h->I, (uint64_t)Ep * h->H, 128)) return MM_ERR_CUDA;
+    h->w2_key = w2;
+  }
+  CUtensorMap tm_x, tm_q;
+  if (!encode_2d(&tm_x, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, (uint32_t)bn1)) return MM_ERR_CUDA;
+  if (!encode_2d(&tm_q, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)bn2)) return MM_ERR_CUDA;
+
+  GemmArgs g1;
+  memset(&g1, 0, sizeof(g1));
+  g1.w_sf = static_cast<const uint8_t*>(w1_sf);
+  g1.act_sf = base + L.pool_sf;
+  g1.offsets = ra.offsets;
+  g1.tile_start = ra.tiles_l1;
+  g1.row_w = ra.row_w;
+  g1.out_q = base + L.l2a;
+  g1.out_sf = base + L.l2a_sf;
+  g1.status = ra.status;
+  g1.Ep = Ep; g1.K = h->H; g1.rows_w = 2 * h->I; g1.I = h->I; g1.H = h->H;
+  g1.clamp = h->clamp; g1.fast_math = h->fast_math; g1.timeout_ns = h->timeout_ns;
+  mark();
+  if (mm_launch_gemm(1, variant, &h->tm_w1, &tm_x, &g1, h->num_sms, stream) != 0) return MM_ERR_CUDA;
+
+  GemmArgs g2 = g1;
+  g2.w_sf = static_cast<const uint8_t*>(w2_sf);
+  g2.act_sf = base + L.l2a_sf;
+  g2.tile_start = ra.tiles_l2;
+  g2.row_w = nullptr;
+  g2.out_q = nullptr;
+  g2.out_sf = nullptr;
+  g2.out_z = reinterpret_cast<uint16_t*>(base + L.z);
+  g2.K = h->I; g2.rows_w = h->H;
+  mark();
+  if (mm_launch_gemm(0, variant, &h->tm_w2, &tm_q, &g2, h->num_sms, stream) != 0) return MM_ERR_CUDA;
+
+  CombineArgs ca;
+  ca.z = g2.out_z;
+  ca.pos = ra.pos;
+  ca.out = static_cast<uint16_t*>(out_bf16);
+  ca.T = T; ca.H = h->H; ca.Kp = Kp;
+  mark();
+  if (mm_launch_combine(&ca, stream) != 0) return MM_ERR_CUDA;
+  mark();
+  h->n_recorded = ev_i;
+  return MM_OK;
+}
+
+mm_status_t mm_profile_enable(mm_handle_t h, int on) {
+  if (!h) return MM_ERR_INVALID_ARG;
+  if (on && !h->profile) {
+    for (int i = 0; i < 6; ++i)
+      if (cudaEventCreate(&h->ev[i]) != cudaSuccess) return MM_ERR_CUDA;
+    h->profile = true;
+  } else if (!on && h->profile) {
+    for (int i = 0; i < 6; ++i) cudaEventDestroy(h->ev[i]);
+    h->profile = false;
+  }
+  h->n_recorded = 0;
+  return MM_OK;
+}
+
+mm_status_t mm_profile_last(mm_handle_t h, float* ms, int n, int* written) {
+  if (!h || !written || (n > 0 && !ms)) return MM_ERR_INVALID_ARG;
+  *written = 0;
+  if (!h->profile || h->n_recorded < 2) return MM_OK;
+  if (cudaEventSynchronize(h->ev[h->n_recorded - 1]) != cudaSuccess) return MM_ERR_CUDA;
+  int k = 0;
+  for (int i = 0; i + 1 < h->n_recorded && k < n; ++i, ++k)
+    if (cudaEventElapsedTime(&ms[k], h->ev[i], h->ev[i + 1]) != cudaSuccess) return MM_ERR_CUDA;
+  *written = k;
+  return MM_OK;
+}
+
+mm_status_t mm_get_status(mm_handle_t h, const void* ws, mm_stream_t stream, uint32_t* device_status) {
+  if (!h || !ws || !device_status) return MM_ERR_INVALID_ARG;
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+    return MM_ERR_CUDA;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MM_ERR_CUDA;
+  *device_status = v;
+  return MM_OK;
+}
+
+mm_status_t mm_debug_views(mm_handle_t h, void* ws, int T, mm_debug_views_t* v) {
+  if (!h || !ws || !v || T < 0) return MM_ERR_INVALID_ARG;
+  const Layout L = make_layout(h->E, h->S, h->H, h->I, h->k, T);
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  v->counts = reinterpret_cast<int32_t*>(b + L.counts);
+  v->offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+  v->perm = reinterpret_cast<int32_t*>(b + L.perm);
+  v->pos = reinterpret_cast<int32_t*>(b + L.pos);
+  v->row_w = reinterpret_cast<float*>(b + L.row_w);
+  v->pool_x = b + L.pool_x;
+  v->pool_sf = b + L.pool_sf;
+  v->l2a = b + L.l2a;
+  v->l2a_sf = b + L.l2a_sf;
+  v->z = reinterpret_cast<uint16_t*>(b + L.z);
+  v->status = reinterpret_cast<uint32_t*>(b + L.status);
+  v->rows_capacity = L.rows_cap;
+  return MM_OK;
+}
+
+mm_status_t mm_debug_timeout_probe(void* ws, uint64_t timeout_ns, mm_stream_t stream) {
+  if (!ws || timeout_ns == 0 || timeout_ns > 10000000000ull) return MM_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(ws, 0, 4, (cudaStream_t)stream) != cudaSuccess) return MM_ERR_CUDA;
+  if (mm_launch_timeout_probe(static_cast<uint32_t*>(ws), timeout_ns, stream) != 0) return MM_ERR_CUDA;
+  return MM_OK;
+}
+
+void mm_destroy(mm_handle_t h) {
+  if (!h) return;
+  if (h->profile)
+    for (int i = 0; i < 6; ++i) cudaEventDestroy(h->ev[i]);
+  delete h;
+}
+
+}  // extern "C"

@@ -1,0 +1,253 @@
+// Router, row gather, combine and the bounded-wait probe.
+//
+// Router: the pages' dispatch bookkeeping ("MegaMoE research report" sec. 4.1,
+// WG0: expert counts, source metadata; "MEGAMOE_SM90_DESIGN" sec. 9.2 pool
+// fill) on one GPU. Slots s = t*(k+S)+j are counted per expert, the counts
+// prefix-summed into pool offsets, and every slot placed at
+// offsets[e] + (number of earlier slots of the same expert) — a stable
+// counting sort, so the result is unique and bit-reproducible.
+// Combine: "MEGAMOE_SM90_DESIGN" sec. 11.2 — per token, the BF16 rows of its
+// active slots are summed in FP32 in slot order and cast to BF16.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "mm_internal.h"
+#include "mm_ptx.cuh"
+
+namespace mm {
+
+__device__ __forceinline__ int slot_expert(const RouteArgs& a, long s, bool* bad) {
+  const int Kp = a.k + a.S;
+  const long t = s / Kp;
+  const int j = (int)(s - t * Kp);
+  if (j >= a.k) return a.E + (j - a.k);
+  const int e = a.topk_idx[t * a.k + j];
+  if (e == -1) return -1;
+  if (e < 0 || e >= a.E) {
+    *bad = true;
+    return -1;
+  }
+  return e;
+}
+
+// Exclusive prefix sum over blockDim.x (= 1024) threads; returns the
+// exclusive value of this thread and writes the total to *total.
+__device__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = scratch[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    scratch[32 + lane] = wi - w;  // exclusive warp prefix
+    if (lane == 31) scratch[64] = wi;
+  }
+  __syncthreads();
+  const int excl = incl - v + scratch[32 + warp];
+  *total = scratch[64];
+  __syncthreads();
+  return excl;
+}
+
+// One CTA of 1024 threads (32 warps). Warp w owns a contiguous chunk of slots;
+// hist[w][e] first holds its per-expert counts, then its write cursors.
+__global__ void __launch_bounds__(1024, 1) route_kernel(RouteArgs a) {
+  extern __shared__ int sh[];
+  const int Ep = a.E + a.S, Kp = a.k + a.S;
+  const long R = (long)a.T * Kp;
+  int* hist = sh;                 // [32][Ep]
+  int* scratch = sh + 32 * Ep;    // [72]
+  __shared__ int bad_any;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) bad_any = 0;
+  for (int i = tid; i < 32 * Ep; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+
+  const long chunk = (R + 31) / 32;
+  const long s0 = warp * chunk, s1 = (s0 + chunk < R) ? s0 + chunk : R;
+  bool bad = false;
+  for (long s = s0 + lane; s < s1; s += 32) {
+    int e = slot_expert(a, s, &bad);
+    if (e >= 0) atomicAdd(&hist[warp * Ep + e], 1);
+  }
+  if (bad) bad_any = 1;
+  __syncthreads();
+
+  // per-expert totals -> counts and offsets; per-warp write cursors
+  int tot = 0;
+  if (tid < Ep)
+    for (int w = 0; w < 32; ++w) tot += hist[w * Ep + tid];
+  int total_rows;
+  const int excl = block_exclusive_scan(tid < Ep ? tot : 0, scratch, &total_rows);
+  if (tid < Ep) {
+    a.counts[tid] = tot;
+    a.offsets[tid] = excl;
+    int run = excl;
+    for (int w = 0; w < 32; ++w) {
+      int c = hist[w * Ep + tid];
+      hist[w * Ep + tid] = run;
+      run += c;
+    }
+  }
+  if (tid == 0) a.offsets[Ep] = total_rows;
+
+  // tile tables: (ceil(count / BN) token tiles) x (weight row blocks) per expert
+  int t1 = 0, t2 = 0;
+  if (tid < Ep) {
+    t1 = (tot + a.bn_l1 - 1) / a.bn_l1 * a.fb_l1;
+    t2 = (tot + a.bn_l2 - 1) / a.bn_l2 * a.fb_l2;
+  }
+  int n1, n2;
+  const int e1 = block_exclusive_scan(t1, scratch, &n1);
+  const int e2 = block_exclusive_scan(t2, scratch, &n2);
+  if (tid < Ep) {
+    a.tiles_l1[tid] = e1;
+    a.tiles_l2[tid] = e2;
+  }
+  if (tid == 0) {
+    a.tiles_l1[Ep] = n1;
+    a.tiles_l2[Ep] = n2;
+  }
+  __syncthreads();
+
+  // stable scatter: each warp walks its chunk 32 slots at a time, in order
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (long base = s0; base < s1; base += 32) {
+    const long s = base + lane;
+    const bool in = s < s1;
+    bool dummy = false;
+    const int e = in ? slot_expert(a, s, &dummy) : -2;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    if (e >= 0) {
+      const int p = hist[warp * Ep + e] + rank;
+      a.perm[p] = (int32_t)s;
+      a.pos[s] = p;
+      const long t = s / Kp;
+      const int j = (int)(s - t * Kp);
+      a.row_w[p] = (j < a.k) ? a.topk_w[t * a.k + j] : 1.0f;
+    } else if (in) {
+      a.pos[s] = -1;
+    }
+    __syncwarp();
+    if (e >= 0 && rank == 0) hist[warp * Ep + e] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  if (tid == 0) *a.status = bad_any ? MM_DEV_BAD_ROUTING : 0u;
+}
+
+// One warp per pool row: copies the token's FP8 row and its scale row into
+// expert-sorted pool order (the local form of the pages' L1 pool fill).
+__global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
+  const int n = a.offsets[a.Ep];
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int vec = a.H / 16, sfw = a.H / 128;
+  for (int r = gw; r < n; r += nw) {
+    const long t = a.perm[r] / a.Kp;
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + t * a.H);
+    uint4* dst = reinterpret_cast<uint4*>(a.pool_x + (size_t)r * a.H);
+    for (int i = lane; i < vec; i += 32) dst[i] = __ldg(src + i);
+    const uint32_t* ss = reinterpret_cast<const uint32_t*>(a.x_sf + t * (a.H / 32));
+    uint32_t* ds = reinterpret_cast<uint32_t*>(a.pool_sf + (size_t)r * (a.H / 32));
+    for (int i = lane; i < sfw; i += 32) ds[i] = __ldg(ss + i);
+  }
+}
+
+// One CTA per token (grid-stride); each thread owns 8 consecutive columns at a time.
+__global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
+  __shared__ int rows[kMaxSlots];
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+    __syncthreads();
+    if (threadIdx.x < a.Kp) rows[threadIdx.x] = a.pos[(long)t * a.Kp + threadIdx.x];
+    __syncthreads();
+    for (int h = threadIdx.x * 8; h < a.H; h += blockDim.x * 8) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+      for (int j = 0; j < a.Kp; ++j) {
+        const int r = rows[j];
+        if (r < 0) continue;
+        const uint4 v = *reinterpret_cast<const uint4*>(a.z + (size_t)r * a.H + h);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] += __uint_as_float(w[i] << 16);
+          acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i]));
+        const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i + 1]));
+        o[i] = lo | (hi << 16);
+      }
+      *reinterpret_cast<uint4*>(a.out + (size_t)t * a.H + h) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// Waits on an mbarrier nobody arrives on, with the same bounded wait the GEMM
+// pipeline uses, and records the expiry in the status word.
+__global__ void timeout_probe_kernel(uint32_t* status, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status, timeout_ns);
+  __syncthreads();
+}
+
+}  // namespace mm
+
+extern "C" int mm_launch_route(const mm::RouteArgs* a, void* stream) {
+  const int Ep = a->E + a->S;
+  const size_t smem = sizeof(int) * (32 * (size_t)Ep + 72);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(mm::route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(sizeof(int) * (32 * mm::kMaxExperts + 72)));
+    if (e != cudaSuccess) return (int)e;
+    attr_set = true;
+  }
+  mm::route_kernel<<<1, 1024, smem, (cudaStream_t)stream>>>(*a);
+  return (int)cudaGetLastError();
+}
+
+extern "C" int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream) {
+  if (rows_upper_bound <= 0) return 0;
+  int blocks = (rows_upper_bound + 7) / 8;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  mm::gather_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(*a);
+  return (int)cudaGetLastError();
+}
+
+extern "C" int mm_launch_combine(const mm::CombineArgs* a, void* stream) {
+  if (a->T <= 0) return 0;
+  int blocks = a->T < 152 * 8 ? a->T : 152 * 8;
+  mm::combine_kernel<<<blocks, 128, 0, (cudaStream_t)stream>>>(*a);
+  return (int)cudaGetLastError();
+}
+
+extern "C" int mm_launch_timeout_probe(uint32_t* status, unsigned long long timeout_ns, void* stream) {
+  mm::timeout_probe_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(status, timeout_ns);
+  return (int)cudaGetLastError();
+}

@@ -1,0 +1,350 @@
+// Persistent grouped GEMM over experts for the two linears of the MegaMoE
+// expert path, on 5th-generation tensor cores (tcgen05, kind::mxf8f6f4 with
+// UE8M0 block scales, FP32 accumulators in TMEM).
+//
+//   L1 ("MegaMoE research report" sec. 4.1, Linear1 phase):
+//     acc[n, r] = sum_k W1[e, n, k] * x[r, k] for the gate rows n and the
+//     matching up rows I + n of one 128-row block, then the fused epilogue
+//     y = silu(clamp(gate)) * clamp(up) * w_r, per (row, 32 columns) amax ->
+//     UE8M0 scale (smallest power of two >= amax/448) -> E4M3
+//     ("MEGAMOE_SM90_DESIGN" sec. 10.1, steps 2-5; UE8M0 per the SM100 kernel).
+//   L2 (Linear2 phase; sec. 11.1): acc[h, r] = sum_i W2[e, h, i] * q[r, i],
+//     written as BF16 into the per-slot row r.
+//
+// Orientation: the weights are the MMA's M=128 operand (E2M1, read by TMA as
+// 16 x 4-bit groups padded to 16 bytes in SMEM) and the expert's token rows are
+// the N operand (E4M3), N = the tile's rows rounded up to 16. One CTA per SM
+// walks a flat list of (expert, weight block, token tile) tiles.
+//
+// Warp roles (256 threads): warp 0 = TMA + scale-factor producer, warp 1 = MMA
+// issuer (one thread), warp 2 = TMEM allocator, warps 4-7 = epilogue (warp w
+// reads TMEM lanes 32*(w%4) .. +31, i.e. 32 consecutive weight rows).
+// Pipelines: STAGES shared-memory stages (full/empty mbarriers) and two TMEM
+// accumulator buffers (tmem_full/tmem_empty) so the epilogue of one tile
+// overlaps the main loop of the next. Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "mm_internal.h"
+#include "mm_ptx.cuh"
+
+namespace mm {
+
+template <bool kL1, int BN, int STAGES>
+struct GemmCfg {
+  static constexpr int BM = 128;                         // weight rows per MMA
+  static constexpr int BK = 128;                         // K per stage
+  static constexpr int NA = kL1 ? 2 : 1;                 // weight tiles per stage (gate, up)
+  static constexpr int A_BYTES = BM * BK;                // 16 KB in SMEM (4-bit codes padded to bytes)
+  static constexpr int A_TX = BM * BK;                   // bytes the TMA writes to SMEM per weight tile
+  static constexpr int B_BYTES = BN * BK;
+  static constexpr int SFB_ROWS = BN <= 128 ? 128 : 256;
+  static constexpr int SF_STAGE_BYTES = NA * 512 + SFB_ROWS * 4;
+  static constexpr int A_OFF = 0;
+  static constexpr int B_OFF = A_OFF + STAGES * NA * A_BYTES;
+  static constexpr int SF_OFF = B_OFF + STAGES * B_BYTES;
+  static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+  // TMEM columns: two accumulator buffers, then two scale-factor slots
+  static constexpr int ACC_COLS = NA * BN;
+  static constexpr int SF_SLOT_COLS = 16;
+  static constexpr int SF_BASE = 2 * ACC_COLS;
+  static constexpr int TMEM_USED = SF_BASE + 2 * SF_SLOT_COLS;
+  static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
+                                   : TMEM_USED <= 256 ? 256 : 512;
+  static_assert(TMEM_USED <= 512, "TMEM budget");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(B_BYTES % 1024 == 0, "B tiles must keep 1024-byte alignment");
+};
+
+struct Tile {
+  int e, fb, row0, nrows;
+};
+
+__device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a, int bn) {
+  int lo = 0, hi = a.Ep - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (a.tile_start[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  Tile t;
+  t.e = lo;
+  const int local = tile - a.tile_start[lo];
+  const int cnt = a.offsets[lo + 1] - a.offsets[lo];
+  const int ntt = (cnt + bn - 1) / bn;
+  t.fb = local / ntt;
+  const int tt = local - t.fb * ntt;
+  t.row0 = a.offsets[lo] + tt * bn;
+  t.nrows = min(bn, cnt - tt * bn);
+  return t;
+}
+
+// UE8M0 code of the smallest power of two >= amax / 448 (IEEE quotient),
+// 127 for amax == 0, clamped to [1, 254].
+__device__ __forceinline__ uint32_t requant_code(float amax) {
+  if (!(amax > 0.0f)) return 127u;
+  const uint32_t b = __float_as_uint(__fdiv_rn(amax, 448.0f));
+  const int e = (int)(b >> 23);
+  int code = (e == 0) ? 1 : (((b & 0x7FFFFFu) == 0u) ? e : e + 1);
+  code = code < 1 ? 1 : (code > 254 ? 254 : code);
+  return (uint32_t)code;
+}
+
+// 2^(127 - code) exactly (a normal or subnormal float for code in [1, 254]).
+__device__ __forceinline__ float inv_scale(uint32_t code) {
+  const int n = 127 - (int)code;
+  return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(1u << (n + 149));
+}
+
+template <bool kL1, int BN, int STAGES>
+__global__ void __launch_bounds__(256, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_act,
+                const GemmArgs a) {
+  using C = GemmCfg<kL1, BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1 + 32);  // producer expect_tx arrival + 32 cp.async arrivals
+      mbar_init(&empty[s], 1);      // tcgen05.commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);   // tcgen05.commit after the last K step
+      mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_act);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int num_tiles = a.tile_start[a.Ep];
+  const int kblocks = a.K / C::BK;
+  const int sf_ld = a.K / 32;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      const Tile t = decode_tile(tile, a, BN);
+      const int wrow = t.e * a.rows_w + t.fb * C::BM;
+      for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        const int s = (int)(it % STAGES);
+        const uint32_t ph = (it / STAGES) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status, a.timeout_ns)) { ok = false; break; }
+        uint8_t* sA = smem + C::A_OFF + s * C::NA * C::A_BYTES;
+        uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
+        uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], C::NA * C::A_TX + C::B_BYTES);
+          tma_load_2d(sA, &tm_w, &full[s], kb * C::BK, wrow);
+          if (kL1) tma_load_2d(sA + C::A_BYTES, &tm_w, &full[s], kb * C::BK, wrow + a.I);
+          tma_load_2d(sB, &tm_act, &full[s], kb * C::BK, t.row0);
+        }
+        // Scale factors of this K step (4 UE8M0 bytes per row) go straight into
+        // the layout tcgen05.cp.32x128b.warpx4 reads: 16 bytes per lane l holding
+        // rows l, l+32, l+64, l+96 of each 128-row group.
+#pragma unroll
+        for (int op = 0; op < C::NA; ++op) {
+          const uint8_t* src = a.w_sf + (size_t)(wrow + op * a.I) * sf_ld + kb * 4;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            cp_async_4(sF + op * 512 + lane * 16 + i * 4, src + (size_t)(32 * i + lane) * sf_ld);
+        }
+#pragma unroll
+        for (int g = 0; g < C::SFB_ROWS / 128; ++g) {
+          const uint8_t* src = a.act_sf + (size_t)(t.row0 + 128 * g) * sf_ld + kb * 4;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            cp_async_4(sF + C::NA * 512 + g * 512 + lane * 16 + i * 4, src + (size_t)(32 * i + lane) * sf_ld);
+        }
+        cp_async_arrive_noinc(&full[s]);
+      }
+    }
+    if (!ok) {
+      // Let the copies already issued land before the CTA can exit.
+      const uint32_t issued = it;
+      for (uint32_t j = (issued > (uint32_t)STAGES ? issued - STAGES : 0u); j < issued; ++j) {
+        int dummy = 0;
+        mbar_wait(&full[j % STAGES], (j / STAGES) & 1u, reinterpret_cast<volatile int*>(&dummy), a.status,
+                  a.timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, tcount = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tcount) {
+        const Tile t = decode_tile(tile, a, BN);
+        const int buf = (int)(tcount & 1u);
+        const uint32_t bph = (tcount >> 1) & 1u;
+        if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, a.status, a.timeout_ns)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem + (uint32_t)(buf * C::ACC_COLS);
+        const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = (int)(it % STAGES);
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&full[s], ph, abort_flag, a.status, a.timeout_ns)) { ok = false; break; }
+          tc_fence_after();
+          fence_proxy_async_smem();  // scale factors were written by cp.async (generic proxy)
+          const uint8_t* sA = smem + C::A_OFF + s * C::NA * C::A_BYTES;
+          const uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
+          const uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
+          const uint32_t sf_col = tmem + (uint32_t)(C::SF_BASE + (int)(it & 1u) * C::SF_SLOT_COLS);
+          const uint32_t sfb_col = sf_col + 4u * C::NA;
+#pragma unroll
+          for (int op = 0; op < C::NA; ++op) tc_cp_32x128b_warpx4(sf_col + 4u * op, sdesc_sf_32x16(smem_u32(sF + op * 512)));
+#pragma unroll
+          for (int g = 0; g < C::SFB_ROWS / 128; ++g)
+            tc_cp_32x128b_warpx4(sfb_col + 4u * g, sdesc_sf_32x16(smem_u32(sF + C::NA * 512 + g * 512)));
+          const uint64_t da0 = sdesc_kmajor_sw128(smem_u32(sA));
+          const uint64_t da1 = sdesc_kmajor_sw128(smem_u32(sA + C::A_BYTES));
+          const uint64_t db = sdesc_kmajor_sw128(smem_u32(sB));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t id = idesc_mxf8f6f4(5u, 0u, n_mma, (uint32_t)k);
+            const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+            // +32 bytes of K per step inside the 128-byte swizzle atom (2 in 16-byte units)
+            tc_mma_mxf8f6f4(d0, da0 + 2u * k, db + 2u * k, id, sf_col, sfb_col, acc);
+            if (kL1) tc_mma_mxf8f6f4(d0 + BN, da1 + 2u * k, db + 2u * k, id, sf_col + 4u, sfb_col, acc);
+          }
+          tc_commit(&empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(&tfull[buf]);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;
+    uint32_t tcount = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
+      const Tile t = decode_tile(tile, a, BN);
+      const int buf = (int)(tcount & 1u);
+      const uint32_t bph = (tcount >> 1) & 1u;
+      if (!mbar_wait(&tfull[buf], bph, abort_flag, a.status, a.timeout_ns)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::ACC_COLS);
+      const int feat = t.fb * C::BM + 32 * q + lane;  // L1: intermediate column; L2: hidden column
+      for (int c0 = 0; c0 < t.nrows; c0 += 16) {
+        uint32_t g[16];
+        tmem_ld_x16(tbase + (uint32_t)c0, g);
+        if constexpr (kL1) {
+          uint32_t u[16];
+          tmem_ld_x16(tbase + (uint32_t)(BN + c0), u);
+          tmem_ld_wait();
+          const int wc = c0 + (lane & 15);
+          const float wl = wc < t.nrows ? a.row_w[t.row0 + wc] : 0.0f;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, wl, j);
+            float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
+            if (a.clamp > 0.0f) {
+              gv = fminf(fmaxf(gv, -a.clamp), a.clamp);
+              uv = fminf(fmaxf(uv, -a.clamp), a.clamp);
+            }
+            const float ex = a.fast_math ? __expf(-gv) : expf(-gv);
+            const float silu = __fdiv_rn(gv, __fadd_rn(1.0f, ex));
+            const float y = __fmul_rn(__fmul_rn(silu, uv), wj);
+            float am = fabsf(y);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+            const uint32_t code = requant_code(am);
+            const uint8_t qb = (uint8_t)__nv_cvt_float_to_fp8(__fmul_rn(y, inv_scale(code)), __NV_SATFINITE, __NV_E4M3);
+            const int col = c0 + j;
+            if (col < t.nrows) {
+              a.out_q[(size_t)(t.row0 + col) * a.I + feat] = qb;
+              if (lane == 0) a.out_sf[(size_t)(t.row0 + col) * (a.I / 32) + t.fb * 4 + q] = (uint8_t)code;
+            }
+          }
+        } else {
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col < t.nrows)
+              a.out_z[(size_t)(t.row0 + col) * a.H + feat] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(g[j])));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <bool kL1, int BN, int STAGES>
+static int set_smem_attr() {
+  using C = GemmCfg<kL1, BN, STAGES>;
+  return (int)cudaFuncSetAttribute(gemm_kernel<kL1, BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   C::SMEM_BYTES);
+}
+
+template <bool kL1, int BN, int STAGES>
+static int launch(const void* tw, const void* ta, const GemmArgs* a, int num_ctas, cudaStream_t st) {
+  using C = GemmCfg<kL1, BN, STAGES>;
+  gemm_kernel<kL1, BN, STAGES><<<num_ctas, 256, C::SMEM_BYTES, st>>>(*static_cast<const CUtensorMap*>(tw),
+                                                                      *static_cast<const CUtensorMap*>(ta), *a);
+  return (int)cudaGetLastError();
+}
+
+// Pipeline depths: as many stages as the 227 KB of shared memory allows.
+constexpr int kStagesL1Small = 6, kStagesL2Small = 8, kStagesL1Large = 4, kStagesL2Large = 4;
+
+}  // namespace mm
+
+extern "C" int mm_gemm_prepare(void) {
+  using namespace mm;
+  int e = 0;
+  if ((e = set_smem_attr<true, kBnSmall, kStagesL1Small>())) return e;
+  if ((e = set_smem_attr<false, kBnSmall, kStagesL2Small>())) return e;
+  if ((e = set_smem_attr<true, kBnL1Large, kStagesL1Large>())) return e;
+  if ((e = set_smem_attr<false, kBnL2Large, kStagesL2Large>())) return e;
+  return 0;
+}
+
+extern "C" int mm_launch_gemm(int l1, int variant, const void* tmap_w, const void* tmap_act, const mm::GemmArgs* a,
+                              int num_ctas, void* stream) {
+  using namespace mm;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (l1) {
+    return variant == 0 ? launch<true, kBnSmall, kStagesL1Small>(tmap_w, tmap_act, a, num_ctas, st)
+                        : launch<true, kBnL1Large, kStagesL1Large>(tmap_w, tmap_act, a, num_ctas, st);
+  }
+  return variant == 0 ? launch<false, kBnSmall, kStagesL2Small>(tmap_w, tmap_act, a, num_ctas, st)
+                      : launch<false, kBnL2Large, kStagesL2Large>(tmap_w, tmap_act, a, num_ctas, st);
+}

@@ -1,0 +1,119 @@
+// Internal host/device definitions shared by the MegaMoE CUDA translation units:
+// workspace layout, kernel argument blocks and tile-shape constants.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/megamoe.h"
+
+namespace mm {
+
+constexpr int kMaxExperts = 1024;  // E + S
+constexpr int kMaxSlots = 16;      // topk + S
+constexpr int kRowMargin = 256;    // pool rows beyond the last valid row that tiles may touch
+
+// Token-tile widths (the MMA N dimension) and pipeline depths of the two GEMM
+// variants. "small" serves decode-like calls (few rows per expert), "large"
+// everything else; the N of each tile is the expert's remaining rows rounded up
+// to 16, so ragged tails never pay for a full tile.
+constexpr int kBnSmall = 16;
+constexpr int kBnL1Large = 112;
+constexpr int kBnL2Large = 224;
+constexpr int kSmallMaxTokens = 16;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Byte offsets of every workspace region for one (shape, T).
+struct Layout {
+  size_t status, counts, offsets, tiles_l1, tiles_l2, perm, pos, row_w;
+  size_t pool_x, pool_sf, l2a, l2a_sf, z, total;
+  int rows_cap;
+};
+
+inline Layout make_layout(int E, int S, int H, int I, int k, int T) {
+  Layout L{};
+  const int Ep = E + S, Kp = k + S;
+  const size_t R = (size_t)T * Kp;
+  L.rows_cap = (int)R + kRowMargin;
+  size_t o = 0;
+  auto take = [&](size_t bytes, size_t align) { o = align_up(o, align); size_t at = o; o += bytes; return at; };
+  L.status = take(256, 256);
+  L.counts = take(sizeof(int32_t) * Ep, 256);
+  L.offsets = take(sizeof(int32_t) * (Ep + 1), 256);
+  L.tiles_l1 = take(sizeof(int32_t) * (Ep + 1), 256);
+  L.tiles_l2 = take(sizeof(int32_t) * (Ep + 1), 256);
+  L.perm = take(sizeof(int32_t) * (R + 1), 256);
+  L.pos = take(sizeof(int32_t) * (R + 1), 256);
+  L.row_w = take(sizeof(float) * (R + 1), 256);
+  L.pool_x = take((size_t)L.rows_cap * H, 1024);
+  L.pool_sf = take((size_t)L.rows_cap * (H / 32), 1024);
+  L.l2a = take((size_t)L.rows_cap * I, 1024);
+  L.l2a_sf = take((size_t)L.rows_cap * (I / 32), 1024);
+  L.z = take((size_t)L.rows_cap * H * 2, 1024);
+  L.total = align_up(o, 1024);
+  return L;
+}
+
+struct RouteArgs {
+  const int32_t* topk_idx;
+  const float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* tiles_l1;
+  int32_t* tiles_l2;
+  int32_t* perm;
+  int32_t* pos;
+  float* row_w;
+  uint32_t* status;
+  int T, E, k, S;
+  int bn_l1, bn_l2;  // token-tile widths of the two GEMMs
+  int fb_l1, fb_l2;  // 128-row weight blocks per expert: I/128 and H/128
+};
+
+struct GatherArgs {
+  const uint8_t* x;
+  const uint8_t* x_sf;
+  const int32_t* perm;
+  const int32_t* offsets;
+  uint8_t* pool_x;
+  uint8_t* pool_sf;
+  int H, Kp, Ep;
+};
+
+struct GemmArgs {
+  const uint8_t* w_sf;        // [Ep * rows_w][K/32] UE8M0
+  const uint8_t* act_sf;      // [rows_cap][K/32]     UE8M0
+  const int32_t* offsets;     // [Ep + 1]
+  const int32_t* tile_start;  // [Ep + 1]
+  const float* row_w;         // L1: top-k weight per pool row
+  uint8_t* out_q;             // L1: [rows_cap][I] E4M3
+  uint8_t* out_sf;            // L1: [rows_cap][I/32] UE8M0
+  uint16_t* out_z;            // L2: [rows_cap][H] BF16
+  uint32_t* status;
+  int Ep, K, rows_w, I, H;
+  float clamp;
+  int fast_math;
+  unsigned long long timeout_ns;
+};
+
+struct CombineArgs {
+  const uint16_t* z;
+  const int32_t* pos;
+  uint16_t* out;
+  int T, H, Kp;
+};
+
+}  // namespace mm
+
+// Kernel launchers (one translation unit each); return cudaError_t as int.
+extern "C" {
+int mm_launch_route(const mm::RouteArgs* a, void* stream);
+int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream);
+int mm_launch_combine(const mm::CombineArgs* a, void* stream);
+// variant: 0 = small tiles, 1 = large tiles. tmaps: two 128-byte CUtensorMap blobs (weights, activations).
+int mm_launch_gemm(int l1, int variant, const void* tmap_w, const void* tmap_act, const mm::GemmArgs* a,
+                   int num_ctas, void* stream);
+int mm_gemm_prepare(void);  // sets the dynamic shared-memory limits once
+int mm_launch_timeout_probe(uint32_t* status, unsigned long long timeout_ns, void* stream);
+}

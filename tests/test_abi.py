@@ -1,0 +1,61 @@
+"""The C-ABI library builds, loads and exports every symbol include/megamoe.h
+declares; host-side argument checks work without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import moe_expert_layer_scan_gb300 as mm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    hdr = open(os.path.join(ROOT, "include", "megamoe.h")).read()
+    return sorted(set(re.findall(r"MM_API\s+[\w\s\*]+?\b(mm_\w+)\s*\(", hdr)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mm.build()
+    return mm.lib()
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for need in ("mm_create", "mm_set_options", "mm_workspace_bytes", "mm_run", "mm_get_status", "mm_destroy"):
+        assert need in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_binding_mirrors_the_c_names():
+    for name in declared_symbols():
+        assert hasattr(mm, name), f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    assert mm.mm_status_string(0) == "ok"
+    assert mm.mm_status_string(3) == "workspace too small"
+
+
+def test_create_rejects_bad_shapes_before_touching_the_device(lib):
+    h = ctypes.c_void_p()
+    assert lib.mm_create(None, 8, 512, 256, 2, 0) == 1                          # null out-pointer
+    assert lib.mm_create(ctypes.byref(h), 0, 512, 256, 2, 0) == 1               # no experts
+    assert lib.mm_create(ctypes.byref(h), 8, 500, 256, 2, 0) == 2               # H not a multiple of 128
+    assert lib.mm_create(ctypes.byref(h), 8, 512, 200, 2, 0) == 2               # I not a multiple of 128
+    assert lib.mm_create(ctypes.byref(h), 1020, 512, 256, 2, 5) == 2            # E + S > 1024
+    assert lib.mm_create(ctypes.byref(h), 8, 512, 256, 16, 1) == 2              # topk + S > 16
+
+
+def test_null_handle_calls_are_rejected(lib):
+    n = ctypes.c_size_t()
+    assert lib.mm_workspace_bytes(None, 4, ctypes.byref(n)) == 1
+    assert lib.mm_set_options(None, 1.0, 0) == 1
+    assert lib.mm_run(None, 1, *([None] * 10), 0, None) == 1
+    lib.mm_destroy(None)

@@ -1,0 +1,123 @@
+"""Edge cases of the CUDA path: empty and single-token calls, disabled and
+out-of-range slots, duplicate experts, hot experts spanning many token tiles,
+workspace reuse, determinism, fast-math SiLU and the bounded-wait status."""
+import numpy as np
+import pytest
+
+import gpu_util as G
+import workloads
+from workloads import Workload
+
+pytestmark = pytest.mark.gpu
+
+
+def dims(w):
+    return dict(T=w.T, H=w.H, I=w.I, E=w.E, k=w.k, S=w.S, clamp=w.clamp)
+
+
+def bits(t):
+    import torch
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def ref_out(orc, w, h):
+    return orc.forward(dims(w), h["x"], h["x_sf"], h["topk_idx"], h["topk_w"], h["w1"], h["w1_sf"], h["w2"],
+                       h["w2_sf"])
+
+
+def test_zero_tokens():
+    import torch
+    w = Workload("t0", T=0, H=256, I=128, E=4, k=2, seed=201)
+    run = G.GpuRun(w)
+    out = run.run()
+    assert out.shape == (0, 256)
+    assert run.status() == 0
+    assert run.moe.launches(0) == 1
+
+
+@pytest.mark.parametrize("T", [1, 17])
+def test_single_and_boundary_token_counts(orc, T):
+    w = Workload(f"t{T}", T=T, H=512, I=256, E=8, k=2, S=1, seed=202)
+    h = workloads.host_inputs(w)
+    run = G.GpuRun(w, inputs=h)
+    G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
+
+
+def test_disabled_and_out_of_range_slots(orc):
+    w = Workload("bad", T=20, H=256, I=128, E=6, k=3, S=1, seed=203)
+    h = workloads.host_inputs(w)
+    idx = h["topk_idx"].copy()
+    idx[0, :] = -1            # token 0: only the shared expert
+    idx[3, 1] = 6             # out of range
+    idx[5, 0] = -9            # out of range
+    h["topk_idx"] = idx
+    ref = ref_out(orc, w, h)
+    assert ref["bad"] == 2
+    run = G.GpuRun(w, inputs=h)
+    out = bits(run.run())
+    assert run.status() & 0x1
+    G.assert_out_close(out, ref["out"])
+
+
+def test_all_slots_disabled_gives_zero():
+    w = Workload("none", T=5, H=256, I=128, E=3, k=2, seed=204)
+    h = workloads.host_inputs(w)
+    h["topk_idx"] = np.full_like(h["topk_idx"], -1)
+    run = G.GpuRun(w, inputs=h)
+    out = bits(run.run())
+    assert (out == 0).all() and run.status() == 0
+
+
+def test_duplicate_experts_small_variant(orc):
+    """T <= 16 with every slot on one expert: 64 rows over 16-wide token tiles."""
+    w = Workload("dup", T=16, H=512, I=256, E=4, k=4, seed=205)
+    h = workloads.host_inputs(w)
+    h["topk_idx"] = np.full_like(h["topk_idx"], 2)
+    run = G.GpuRun(w, inputs=h)
+    G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
+
+
+def test_hot_expert_many_tiles(orc):
+    """One expert receives every token: several full token tiles plus a ragged tail."""
+    w = Workload("hot", T=300, H=256, I=256, E=4, k=1, seed=206)
+    h = workloads.host_inputs(w)
+    h["topk_idx"] = np.zeros_like(h["topk_idx"])
+    run = G.GpuRun(w, inputs=h)
+    G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
+
+
+def test_workspace_reuse_and_determinism():
+    w = Workload("reuse", T=40, H=512, I=256, E=6, k=2, S=1, seed=207)
+    a = workloads.host_inputs(w)
+    b = workloads.host_inputs(w.replace(seed=208))
+    run = G.GpuRun(w, inputs=a)
+    first = bits(run.run())
+    import torch
+    bd = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in b.items()}
+    other = bits(run.run(**bd))
+    again = bits(run.run())
+    assert np.array_equal(first, again)          # no pollution from the previous call, deterministic
+    fresh = G.GpuRun(w, inputs=b)
+    assert np.array_equal(other, bits(fresh.run()))
+
+
+def test_fast_math_silu(orc):
+    w = Workload("fast", T=24, H=512, I=256, E=4, k=2, seed=209)
+    h = workloads.host_inputs(w)
+    run = G.GpuRun(w, inputs=h, fast_math=True)
+    G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
+
+
+def test_bounded_wait_reports_timeout_and_gpu_stays_usable(orc):
+    import torch
+    import moe_expert_layer_scan_gb300 as mm
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    mm.mm_debug_timeout_probe(ws.data_ptr(), 5_000_000, s)   # 5 ms
+    torch.cuda.synchronize()
+    status = int(ws[:4].view(torch.int32).item())
+    assert status & 0x2
+    w = Workload("after", T=8, H=256, I=128, E=4, k=2, seed=210)
+    h = workloads.host_inputs(w)
+    run = G.GpuRun(w, inputs=h)
+    G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])

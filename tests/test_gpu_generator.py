@@ -1,0 +1,31 @@
+"""The device build of the input generator writes the same bytes as the host
+build, so oracle inputs (host) and CUDA-path inputs (HBM) are identical."""
+import numpy as np
+import pytest
+
+import workloads
+from workloads import CONFIGS
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", list(CONFIGS))
+def test_device_generator_matches_host(name):
+    import torch
+    w = CONFIGS[name]
+    x = torch.empty((w.T, w.H), dtype=torch.uint8, device="cuda")
+    xs = torch.empty((w.T, w.H // 32), dtype=torch.uint8, device="cuda")
+    workloads.x_device(w, x, xs)
+    rows = sorted({0, w.T // 2, w.T - 1})
+    for t in rows:
+        hx, hs = workloads.x_host(w, t, t + 1)
+        assert np.array_equal(x[t:t + 1].cpu().numpy(), hx) and np.array_equal(xs[t:t + 1].cpu().numpy(), hs)
+    for which in (workloads.TAG_W1, workloads.TAG_W2):
+        rows_w, K = workloads.weight_shape(w, which)
+        for e in sorted({0, w.Ep - 1}):
+            c = torch.empty((1, rows_w, K // 2), dtype=torch.uint8, device="cuda")
+            s = torch.empty((1, rows_w, K // 32), dtype=torch.uint8, device="cuda")
+            workloads.w_device(w, which, c, s, e, e + 1)
+            hc, hs = workloads.w_host(w, which, e, e + 1)
+            assert np.array_equal(c.cpu().numpy(), hc), f"W{which - 1} expert {e} codes differ"
+            assert np.array_equal(s.cpu().numpy(), hs), f"W{which - 1} expert {e} scales differ"
