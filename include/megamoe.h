@@ -63,6 +63,10 @@ typedef enum {
  * by mm_get_status (0 = no error). */
 #define MM_DEV_BAD_ROUTING 0x1u   /* an out-of-range expert id was skipped (slot disabled) */
 #define MM_DEV_TIMEOUT 0x2u       /* a pipeline wait exceeded its time limit; outputs invalid */
+/* With MM_DEV_TIMEOUT, bits 8..23 name the wait that expired (diagnostic):
+ * bit 8 + s for the L1 GEMM and 16 + s for the L2 GEMM, s = 0 stage free,
+ * 1 accumulator free, 2 stage loaded, 3 accumulator ready, 4 copy drain;
+ * bit 15 for mm_debug_timeout_probe. */
 
 /* Human-readable name of a status code (static string). */
 MM_API const char* mm_status_string(mm_status_t s);

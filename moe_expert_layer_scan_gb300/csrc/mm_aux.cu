@@ -212,7 +212,7 @@ __global__ void timeout_probe_kernel(uint32_t* status, unsigned long long timeou
     fence_mbar_init();
   }
   __syncthreads();
-  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status, timeout_ns);
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status, timeout_ns, 7);
   __syncthreads();
 }
 

@@ -38,7 +38,7 @@ struct GemmCfg {
   static constexpr int BK = 128;                         // K per stage
   static constexpr int NA = kL1 ? 2 : 1;                 // weight tiles per stage (gate, up)
   static constexpr int A_BYTES = BM * BK;                // 16 KB in SMEM (4-bit codes padded to bytes)
-  static constexpr int A_TX = BM * BK;                   // bytes the TMA writes to SMEM per weight tile
+  static constexpr int A_TX = BM * BK / 2;               // transaction bytes of one weight box (packed 4-bit size)
   static constexpr int B_BYTES = BN * BK;
   static constexpr int SFB_ROWS = BN <= 128 ? 128 : 256;
   static constexpr int SF_STAGE_BYTES = NA * 512 + SFB_ROWS * 4;
@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int num_tiles = a.tile_start[a.Ep];
+  // wait sites reported in the status word on expiry (L2 kernel: +8)
+  const uint32_t site0 = kL1 ? 0u : 8u;
   const int kblocks = a.K / C::BK;
   const int sf_ld = a.K / 32;
 
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
         const int s = (int)(it % STAGES);
         const uint32_t ph = (it / STAGES) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status, a.timeout_ns)) { ok = false; break; }
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status, a.timeout_ns, site0 + 0)) { ok = false; break; }
         uint8_t* sA = smem + C::A_OFF + s * C::NA * C::A_BYTES;
         uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
         uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(256, 1)
       for (uint32_t j = (issued > (uint32_t)STAGES ? issued - STAGES : 0u); j < issued; ++j) {
         int dummy = 0;
         mbar_wait(&full[j % STAGES], (j / STAGES) & 1u, reinterpret_cast<volatile int*>(&dummy), a.status,
-                  a.timeout_ns);
+                  a.timeout_ns, site0 + 4);
       }
     }
   } else if (warp == 1) {
@@ -201,14 +203,14 @@ __global__ void __launch_bounds__(256, 1)
         const Tile t = decode_tile(tile, a, BN);
         const int buf = (int)(tcount & 1u);
         const uint32_t bph = (tcount >> 1) & 1u;
-        if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, a.status, a.timeout_ns)) break;
+        if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, a.status, a.timeout_ns, site0 + 1)) break;
         tc_fence_after();
         const uint32_t d0 = tmem + (uint32_t)(buf * C::ACC_COLS);
         const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&full[s], ph, abort_flag, a.status, a.timeout_ns)) { ok = false; break; }
+          if (!mbar_wait(&full[s], ph, abort_flag, a.status, a.timeout_ns, site0 + 2)) { ok = false; break; }
           tc_fence_after();
           fence_proxy_async_smem();  // scale factors were written by cp.async (generic proxy)
           const uint8_t* sA = smem + C::A_OFF + s * C::NA * C::A_BYTES;
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(256, 1)
       const Tile t = decode_tile(tile, a, BN);
       const int buf = (int)(tcount & 1u);
       const uint32_t bph = (tcount >> 1) & 1u;
-      if (!mbar_wait(&tfull[buf], bph, abort_flag, a.status, a.timeout_ns)) break;
+      if (!mbar_wait(&tfull[buf], bph, abort_flag, a.status, a.timeout_ns, site0 + 3)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::ACC_COLS);
       const int feat = t.fb * C::BM + 32 * q + lane;  // L1: intermediate column; L2: hidden column
