@@ -161,6 +161,33 @@ MM_API mm_status_t mm_debug_timeout_probe(void* ws, uint64_t timeout_ns, mm_stre
 MM_API mm_status_t mm_profile_enable(mm_handle_t h, int on);
 MM_API mm_status_t mm_profile_last(mm_handle_t h, float* ms, int n, int* written);
 
+/* Allocation-free variant of mm_run (the pages have no counterpart; this is a
+ * convenience of this library). Some callers cannot allocate device memory
+ * where they run the layer: plugin hosts that own every device allocation and
+ * forbid allocating inside their execute callback, and latency-critical loops
+ * that avoid cudaMalloc/cudaFree because those calls can synchronise the
+ * device. mm_run_noalloc computes exactly what mm_run computes, with the
+ * workspace taken from a fixed 32 MiB array of device memory inside this
+ * library instead of a caller buffer; every GPU that loads the library holds
+ * that array until the process exits. The caller still passes the inputs and
+ * the output, with the layouts and alignments of mm_run.
+ *   - Calls whose workspace (mm_workspace_bytes(h, T)) exceeds 32 MiB are
+ *     rejected with MM_ERR_WORKSPACE_TOO_SMALL before anything is enqueued
+ *     (up to T = 143 tokens at H = 7168, I = 2048, E = 256, top-8).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture on the device.
+ *   - Nothing is allocated or freed: no cudaMalloc, cudaFree or allocating
+ *     library routine is called.
+ *   - All calls in the process share the one array, which keeps the last
+ *     call's contents. Nothing in it has to start at zero (every call rewrites
+ *     the routing tables and the status word before use), but calls that
+ *     overlap on the GPU (different streams, or different handles without
+ *     ordering between them) race on it and give undefined results. */
+MM_API mm_status_t mm_run_noalloc(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, const int32_t* topk_idx,
+                                  const float* topk_w, const void* w1, const void* w1_sf, const void* w2,
+                                  const void* w2_sf, void* out_bf16, mm_stream_t stream);
+
 /* Destroys a handle (NULL is ignored). */
 MM_API void mm_destroy(mm_handle_t h);
 

@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3:
                 4: "MM_ERR_CUDA", 5: "MM_ERR_DEVICE_TIMEOUT", 6: "MM_ERR_BAD_ROUTING", 7: "MM_ERR_ALIGNMENT"}
 EXPORTS = ["mm_status_string", "mm_create", "mm_set_options", "mm_workspace_bytes", "mm_run", "mm_get_status",
            "mm_launches_per_run", "mm_debug_views", "mm_debug_timeout_probe", "mm_profile_enable", "mm_profile_last",
-           "mm_destroy"]
+           "mm_run_noalloc", "mm_destroy"]
 
 
 class MMError(RuntimeError):
@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
         L.mm_debug_timeout_probe.argtypes = [p, ctypes.c_uint64, p]
         L.mm_profile_enable.argtypes = [p, i32]
         L.mm_profile_last.argtypes = [p, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(ctypes.c_int)]
+        L.mm_run_noalloc.argtypes = [p, i32] + [p] * 9 + [p]
         L.mm_destroy.argtypes = [p]
         L.mm_destroy.restype = None
         for n in EXPORTS:
@@ -103,6 +104,13 @@ def mm_run(h: int, T: int, x_fp8: int, x_sf: int, topk_idx: int, topk_w: int, w1
            w2_sf: int, out_bf16: int, ws: int, ws_bytes: int, stream: int) -> int:
     """Raw call with device pointers; returns the status code (not raised)."""
     return lib().mm_run(h, T, x_fp8, x_sf, topk_idx, topk_w, w1, w1_sf, w2, w2_sf, out_bf16, ws, ws_bytes, stream)
+
+
+def mm_run_noalloc(h: int, T: int, x_fp8: int, x_sf: int, topk_idx: int, topk_w: int, w1: int, w1_sf: int, w2: int,
+                   w2_sf: int, out_bf16: int, stream: int) -> int:
+    """Raw call of the allocation-free variant (scratch inside the library);
+    returns the status code (not raised)."""
+    return lib().mm_run_noalloc(h, T, x_fp8, x_sf, topk_idx, topk_w, w1, w1_sf, w2, w2_sf, out_bf16, stream)
 
 
 def mm_get_status(h: int, ws: int, stream: int) -> int:

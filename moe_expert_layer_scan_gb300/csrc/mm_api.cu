@@ -6,6 +6,7 @@
 
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "mm_internal.h"
@@ -308,6 +309,42 @@ mm_status_t mm_debug_timeout_probe(void* ws, uint64_t timeout_ns, mm_stream_t st
   if (cudaMemsetAsync(ws, 0, 4, (cudaStream_t)stream) != cudaSuccess) return MM_ERR_CUDA;
   if (mm_launch_timeout_probe(static_cast<uint32_t*>(ws), timeout_ns, stream) != 0) return MM_ERR_CUDA;
   return MM_OK;
+}
+
+}  // extern "C"
+
+// Scratch for mm_run_noalloc: fixed-size device memory owned by this library
+// (callers of that entry point cannot allocate). Host code must not use the
+// symbol as an address; the device address is looked up once per device.
+namespace {
+constexpr size_t kStaticWorkspaceBytes = size_t(32) << 20;
+constexpr int kMaxDevices = 64;
+static __device__ __align__(256) uint8_t mm_static_ws[kStaticWorkspaceBytes];
+void* g_static_ws[kMaxDevices];
+std::mutex g_static_ws_mu;
+}  // namespace
+
+extern "C" {
+
+mm_status_t mm_run_noalloc(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, const int32_t* topk_idx,
+                           const float* topk_w, const void* w1, const void* w1_sf, const void* w2, const void* w2_sf,
+                           void* out_bf16, mm_stream_t stream) {
+  if (!h || T < 0) return MM_ERR_INVALID_ARG;
+  if (make_layout(h->E, h->S, h->H, h->I, h->k, T).total > kStaticWorkspaceBytes) return MM_ERR_WORKSPACE_TOO_SMALL;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device || dev < 0 || dev >= kMaxDevices) return MM_ERR_CUDA;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_ws_mu);
+    if (!g_static_ws[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, mm_static_ws) != cudaSuccess || !p) return MM_ERR_CUDA;
+      g_static_ws[dev] = p;
+    }
+    ws = g_static_ws[dev];
+  }
+  return mm_run(h, T, x_fp8, x_sf, topk_idx, topk_w, w1, w1_sf, w2, w2_sf, out_bf16, ws, kStaticWorkspaceBytes,
+                stream);
 }
 
 void mm_destroy(mm_handle_t h) {
