@@ -249,6 +249,20 @@ def run_ours(args, world, rank, local):
         raise RuntimeError(f"device status {moe.status()} after the timed steps")
 
     # ---- end-to-end through the public API with host buffers
+    e2e_ms, h2d, d2h = None, 0, 0
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = measure_e2e(args, w, d, moe, out, flush, dist)
+    if dist:
+        t = torch.tensor([total_ms, e2e_ms or 0.0], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), (float(t[1]) if e2e_ms is not None else None)
+    if rank != 0:
+        return
+    report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk)
+
+
+def measure_e2e(args, w, d, moe, out, flush, dist):
+    import torch
     pin = lambda t: t.cpu().pin_memory()
     hx, hxs, hidx, hw = pin(d["x"]), pin(d["x_sf"]), pin(d["topk_idx"]), pin(d["topk_w"])
     hout = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
@@ -282,14 +296,10 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     e2e_ms = sum(a.elapsed_time(b) for a, b in zip(f0, f1))
     assert torch.equal(hout, out.cpu()), "end-to-end output differs from the device output"
+    return e2e_ms, h2d, d2h
 
-    if dist:
-        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
-    if rank != 0:
-        return
 
+def report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk):
     ms = total_ms / args.steps
     tokens = w.T * world
     value = tokens / (ms / 1e3)
@@ -326,8 +336,9 @@ def run_ours(args, world, rank, local):
             "hbm_gbs_whole_step": (alg["l1_bytes"] + alg["l2_bytes"]) / (ms / 1e3) / 1e9,
             "kernels_ms": kern, "rows": alg["rows"], "experts_touched": alg["touched"],
             "roofline": roof,
-            "e2e": {"value": tokens / (e2e_ms / args.steps / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
+            "e2e": None if e2e_ms is None else
+            {"value": tokens / (e2e_ms / args.steps / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps},
             "gpu_launches": moe.launches(w.T) * args.steps,
             "clocks": clk}
     if world == 1 and not args.no_cpu_baseline:
@@ -347,9 +358,19 @@ def main():
     ap.add_argument("--workload", default="decode", choices=list(workloads.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (smaller cases for profiler captures; not a bench line)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override T (smaller cases for profiler captures; not a bench line)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
     world, rank, local = dist_setup()
+    w = workloads.CONFIGS[args.workload]
+    if args.experts or args.tokens:
+        w = w.replace(E=args.experts or w.E, T=args.tokens or w.T, name=w.name + "-capture")
+        workloads.CONFIGS[w.name] = w
+        args.workload = w.name
     if args.impl == "reference":
         run_reference(args, world, rank)
     else:

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -20,6 +21,7 @@ struct mm_handle {
   int device;
   int num_sms;
   unsigned long long timeout_ns;
+  int prefetch[2][2];  // [variant][l1 ? 0 : 1]: weight K steps pulled into L2 ahead of the loads
   // cached weight tensor maps (keyed by base pointer)
   const void* w1_key;
   const void* w2_key;
@@ -109,6 +111,15 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
   if (const char* t = getenv("MM_DEVICE_TIMEOUT_MS")) {
     long ms = atol(t);
     if (ms > 0) h->timeout_ns = (unsigned long long)ms * 1000000ull;
+  }
+  // small tiles stream weights (decode): keep ~256 KB per SM in flight;
+  // large tiles reuse weights across token tiles: a few microseconds ahead
+  h->prefetch[0][0] = 16; h->prefetch[0][1] = 32;
+  h->prefetch[1][0] = 8;  h->prefetch[1][1] = 12;
+  if (const char* p = getenv("MM_PREFETCH_STAGES")) {  // "small_l1,small_l2,large_l1,large_l2"
+    int v[4];
+    if (sscanf(p, "%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3]) == 4)
+      for (int i = 0; i < 4; ++i) h->prefetch[i / 2][i % 2] = v[i] < 0 ? 0 : (v[i] > 256 ? 256 : v[i]);
   }
   h->w1_key = h->w2_key = nullptr;
   h->profile = false;
@@ -222,6 +233,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g1.status = ra.status;
   g1.Ep = Ep; g1.K = h->H; g1.rows_w = 2 * h->I; g1.I = h->I; g1.H = h->H;
   g1.clamp = h->clamp; g1.fast_math = h->fast_math; g1.timeout_ns = h->timeout_ns;
+  g1.prefetch_stages = h->prefetch[variant][0];
   mark();
   if (mm_launch_gemm(1, variant, &h->tm_w1, &tm_x, &g1, h->num_sms, stream) != 0) return MM_ERR_CUDA;
 
@@ -234,6 +246,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g2.out_sf = nullptr;
   g2.out_z = reinterpret_cast<uint16_t*>(base + L.z);
   g2.K = h->I; g2.rows_w = h->H;
+  g2.prefetch_stages = h->prefetch[variant][1];
   mark();
   if (mm_launch_gemm(0, variant, &h->tm_w2, &tm_q, &g2, h->num_sms, stream) != 0) return MM_ERR_CUDA;
 

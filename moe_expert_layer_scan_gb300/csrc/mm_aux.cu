@@ -167,37 +167,43 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
   }
 }
 
-// One CTA per token (grid-stride); each thread owns 8 consecutive columns at a time.
+// Each thread owns one 16-byte column chunk (8 BF16 values) of one token: it
+// issues the loads of all the token's slot rows first, then sums them in FP32
+// in slot order and stores the BF16 result.
 __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
-  __shared__ int rows[kMaxSlots];
-  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
-    __syncthreads();
-    if (threadIdx.x < a.Kp) rows[threadIdx.x] = a.pos[(long)t * a.Kp + threadIdx.x];
-    __syncthreads();
-    for (int h = threadIdx.x * 8; h < a.H; h += blockDim.x * 8) {
-      float acc[8];
+  const int chunks = a.H / 8;
+  const long total = (long)a.T * chunks;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
+    const long t = i / chunks;
+    const int c = (int)(i - t * chunks);
+    uint4 v[kMaxSlots];
+    int r[kMaxSlots];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-      for (int j = 0; j < a.Kp; ++j) {
-        const int r = rows[j];
-        if (r < 0) continue;
-        const uint4 v = *reinterpret_cast<const uint4*>(a.z + (size_t)r * a.H + h);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[2 * i] += __uint_as_float(w[i] << 16);
-          acc[2 * i + 1] += __uint_as_float(w[i] & 0xFFFF0000u);
-        }
-      }
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i]));
-        const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * i + 1]));
-        o[i] = lo | (hi << 16);
-      }
-      *reinterpret_cast<uint4*>(a.out + (size_t)t * a.H + h) = make_uint4(o[0], o[1], o[2], o[3]);
+    for (int j = 0; j < kMaxSlots; ++j) {
+      r[j] = j < a.Kp ? __ldg(a.pos + t * a.Kp + j) : -1;
+      v[j] = r[j] >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.z + (size_t)r[j] * a.H) + c) : make_uint4(0, 0, 0, 0);
     }
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxSlots; ++j) {
+      if (r[j] < 0) continue;
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[2 * e] += __uint_as_float(w[e] << 16);
+        acc[2 * e + 1] += __uint_as_float(w[e] & 0xFFFF0000u);
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * e]));
+      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * e + 1]));
+      o[e] = lo | (hi << 16);
+    }
+    reinterpret_cast<uint4*>(a.out + (size_t)t * a.H)[c] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -242,8 +248,10 @@ extern "C" int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, v
 
 extern "C" int mm_launch_combine(const mm::CombineArgs* a, void* stream) {
   if (a->T <= 0) return 0;
-  int blocks = a->T < 152 * 8 ? a->T : 152 * 8;
-  mm::combine_kernel<<<blocks, 128, 0, (cudaStream_t)stream>>>(*a);
+  const long threads = (long)a->T * (a->H / 8);
+  long blocks = (threads + 127) / 128;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  mm::combine_kernel<<<(int)blocks, 128, 0, (cudaStream_t)stream>>>(*a);
   return (int)cudaGetLastError();
 }
 

@@ -147,6 +147,43 @@ __global__ void __launch_bounds__(256, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // A prefetch cursor runs prefetch_stages K steps ahead of the loads and
+    // pulls the weight boxes into L2 (and, when it enters a tile, the lines
+    // holding that tile's weight scale rows), so the TMA loads that fill the
+    // shared-memory ring find their data in L2: the DRAM requests in flight
+    // are no longer limited by the ring's size.
+    int pf_tile = blockIdx.x, pf_kb = 0, pf_wrow = 0;
+    if (pf_tile < num_tiles) {
+      const Tile p = decode_tile(pf_tile, a, BN);
+      pf_wrow = p.e * a.rows_w + p.fb * C::BM;
+    }
+    auto prefetch_next = [&]() {
+      if (pf_tile >= num_tiles) return;
+      if (pf_kb == 0) {
+#pragma unroll
+        for (int op = 0; op < C::NA; ++op)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint8_t* row = a.w_sf + (size_t)(pf_wrow + op * a.I + 32 * i + lane) * sf_ld;
+            for (int off = 0; off < sf_ld; off += 128) prefetch_l2(row + off);
+            prefetch_l2(row + sf_ld - 1);
+          }
+      }
+      if (lane == 0) {
+        tma_prefetch_l2_2d(&tm_w, pf_kb * C::BK, pf_wrow);
+        if (kL1) tma_prefetch_l2_2d(&tm_w, pf_kb * C::BK, pf_wrow + a.I);
+      }
+      if (++pf_kb == kblocks) {
+        pf_kb = 0;
+        pf_tile += gridDim.x;
+        if (pf_tile < num_tiles) {
+          const Tile p = decode_tile(pf_tile, a, BN);
+          pf_wrow = p.e * a.rows_w + p.fb * C::BM;
+        }
+      }
+    };
+    for (int i = 0; i < a.prefetch_stages; ++i) prefetch_next();
+
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
@@ -165,6 +202,7 @@ __global__ void __launch_bounds__(256, 1)
           if (kL1) tma_load_2d(sA + C::A_BYTES, &tm_w, &full[s], kb * C::BK, wrow + a.I);
           tma_load_2d(sB, &tm_act, &full[s], kb * C::BK, t.row0);
         }
+        prefetch_next();
         // Scale factors of this K step (4 UE8M0 bytes per row) go straight into
         // the layout tcgen05.cp.32x128b.warpx4 reads: 16 bytes per lane l holding
         // rows l, l+32, l+64, l+96 of each 128-row group.

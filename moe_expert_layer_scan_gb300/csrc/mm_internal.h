@@ -94,6 +94,7 @@ struct GemmArgs {
   int Ep, K, rows_w, I, H;
   float clamp;
   int fast_math;
+  int prefetch_stages;  // weight boxes pulled into L2 this many K steps ahead of the loads
   unsigned long long timeout_ns;
 };
 
