@@ -65,7 +65,8 @@ typedef enum {
 #define MM_DEV_TIMEOUT 0x2u       /* a pipeline wait exceeded its time limit; outputs invalid */
 /* With MM_DEV_TIMEOUT, bits 8..23 name the wait that expired (diagnostic):
  * bit 8 + s for the L1 GEMM and 16 + s for the L2 GEMM, s = 0 stage free,
- * 1 accumulator free, 2 stage loaded, 3 accumulator ready, 4 copy drain;
+ * 1 accumulator free, 2 stage loaded, 3 accumulator ready, 4 copy drain,
+ * 5 stage free (scale-factor writer);
  * bit 15 for mm_debug_timeout_probe. */
 
 /* Human-readable name of a status code (static string). */

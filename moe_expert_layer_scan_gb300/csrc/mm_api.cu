@@ -112,10 +112,10 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
     long ms = atol(t);
     if (ms > 0) h->timeout_ns = (unsigned long long)ms * 1000000ull;
   }
-  // small tiles stream weights (decode): keep ~256 KB per SM in flight;
-  // large tiles reuse weights across token tiles: a few microseconds ahead
-  h->prefetch[0][0] = 16; h->prefetch[0][1] = 32;
-  h->prefetch[1][0] = 8;  h->prefetch[1][1] = 12;
+  // off by default: on GB300 the L2 prefetch cursor measured slower for both
+  // the decode and the prefill workloads (kept as a tuning knob)
+  h->prefetch[0][0] = 0; h->prefetch[0][1] = 0;
+  h->prefetch[1][0] = 0; h->prefetch[1][1] = 0;
   if (const char* p = getenv("MM_PREFETCH_STAGES")) {  // "small_l1,small_l2,large_l1,large_l2"
     int v[4];
     if (sscanf(p, "%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3]) == 4)
@@ -234,6 +234,8 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g1.Ep = Ep; g1.K = h->H; g1.rows_w = 2 * h->I; g1.I = h->I; g1.H = h->H;
   g1.clamp = h->clamp; g1.fast_math = h->fast_math; g1.timeout_ns = h->timeout_ns;
   g1.prefetch_stages = h->prefetch[variant][0];
+  g1.w_sf_vec = aligned(w1_sf, 16) && (h->H / 32) % 16 == 0;
+  g1.act_sf_vec = (h->H / 32) % 16 == 0;
   mark();
   if (mm_launch_gemm(1, variant, &h->tm_w1, &tm_x, &g1, h->num_sms, stream) != 0) return MM_ERR_CUDA;
 
@@ -247,6 +249,8 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g2.out_z = reinterpret_cast<uint16_t*>(base + L.z);
   g2.K = h->I; g2.rows_w = h->H;
   g2.prefetch_stages = h->prefetch[variant][1];
+  g2.w_sf_vec = aligned(w2_sf, 16) && (h->I / 32) % 16 == 0;
+  g2.act_sf_vec = (h->I / 32) % 16 == 0;
   mark();
   if (mm_launch_gemm(0, variant, &h->tm_w2, &tm_q, &g2, h->num_sms, stream) != 0) return MM_ERR_CUDA;
 

@@ -16,8 +16,9 @@
 // the N operand (E4M3), N = the tile's rows rounded up to 16. One CTA per SM
 // walks a flat list of (expert, weight block, token tile) tiles.
 //
-// Warp roles (256 threads): warp 0 = TMA + scale-factor producer, warp 1 = MMA
-// issuer (one thread), warp 2 = TMEM allocator, warps 4-7 = epilogue (warp w
+// Warp roles (256 threads): warp 0 = TMA producer, warp 1 = MMA issuer (one
+// thread), warp 2 = TMEM allocator, warp 3 = scale-factor producer, warps 4-7 =
+// epilogue (warp w
 // reads TMEM lanes 32*(w%4) .. +31, i.e. 32 consecutive weight rows).
 // Pipelines: STAGES shared-memory stages (full/empty mbarriers) and two TMEM
 // accumulator buffers (tmem_full/tmem_empty) so the epilogue of one tile
@@ -83,6 +84,26 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a, int bn)
   return t;
 }
 
+// Four K steps of one row's UE8M0 scales (16 bytes); `avail` steps exist.
+__device__ __forceinline__ uint4 load_sf4(const uint8_t* p, bool vec16, int avail) {
+  if (vec16) return __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t* q = reinterpret_cast<const uint32_t*>(p);
+  uint4 r = make_uint4(__ldg(q), 0u, 0u, 0u);
+  if (avail > 1) r.y = __ldg(q + 1);
+  if (avail > 2) r.z = __ldg(q + 2);
+  if (avail > 3) r.w = __ldg(q + 3);
+  return r;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int c) {
+  return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ void st_shared_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
 // UE8M0 code of the smallest power of two >= amax / 448 (IEEE quotient),
 // 127 for amax == 0, clamped to [1, 254].
 __device__ __forceinline__ uint32_t requant_code(float amax) {
@@ -117,7 +138,7 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1 + 32);  // producer expect_tx arrival + 32 cp.async arrivals
+      mbar_init(&full[s], 1 + 32);  // TMA expect_tx arrival + one arrival per scale-factor lane
       mbar_init(&empty[s], 1);      // tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -203,33 +224,65 @@ __global__ void __launch_bounds__(256, 1)
           tma_load_2d(sB, &tm_act, &full[s], kb * C::BK, t.row0);
         }
         prefetch_next();
-        // Scale factors of this K step (4 UE8M0 bytes per row) go straight into
-        // the layout tcgen05.cp.32x128b.warpx4 reads: 16 bytes per lane l holding
-        // rows l, l+32, l+64, l+96 of each 128-row group.
-#pragma unroll
-        for (int op = 0; op < C::NA; ++op) {
-          const uint8_t* src = a.w_sf + (size_t)(wrow + op * a.I) * sf_ld + kb * 4;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            cp_async_4(sF + op * 512 + lane * 16 + i * 4, src + (size_t)(32 * i + lane) * sf_ld);
-        }
-#pragma unroll
-        for (int g = 0; g < C::SFB_ROWS / 128; ++g) {
-          const uint8_t* src = a.act_sf + (size_t)(t.row0 + 128 * g) * sf_ld + kb * 4;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            cp_async_4(sF + C::NA * 512 + g * 512 + lane * 16 + i * 4, src + (size_t)(32 * i + lane) * sf_ld);
-        }
-        cp_async_arrive_noinc(&full[s]);
       }
     }
     if (!ok) {
-      // Let the copies already issued land before the CTA can exit.
+      // Let the copies already issued land before the CTA can exit (the
+      // stage's barrier may never complete if another role gave up, so the
+      // limit here is short).
       const uint32_t issued = it;
       for (uint32_t j = (issued > (uint32_t)STAGES ? issued - STAGES : 0u); j < issued; ++j) {
         int dummy = 0;
         mbar_wait(&full[j % STAGES], (j / STAGES) & 1u, reinterpret_cast<volatile int*>(&dummy), a.status,
-                  a.timeout_ns, site0 + 4);
+                  a.timeout_ns < 10000000ull ? a.timeout_ns : 10000000ull, site0 + 4);
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ scale-factor producer
+    // Loads each row's UE8M0 bytes for four K steps at once (one 16-byte
+    // request per row per four steps) and, per K step, writes the layout
+    // tcgen05.cp.32x128b.warpx4 reads: 16 bytes per lane l holding the step's
+    // four scale bytes of rows l, l+32, l+64, l+96 of each 128-row group.
+    constexpr int NB = C::SFB_ROWS / 32;  // 32-row blocks of the token operand
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      const Tile t = decode_tile(tile, a, BN);
+      const int wrow = t.e * a.rows_w + t.fb * C::BM;
+      const int nb = (t.nrows + 31) / 32;
+      for (int g = 0; g < kblocks && ok; g += 4) {
+        const int avail = kblocks - g;
+        const bool wvec = a.w_sf_vec && avail >= 4, bvec = a.act_sf_vec && avail >= 4;
+        uint4 wa[C::NA][4];
+        uint4 wb[NB];
+#pragma unroll
+        for (int op = 0; op < C::NA; ++op)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            wa[op][i] = load_sf4(a.w_sf + (size_t)(wrow + op * a.I + 32 * i + lane) * sf_ld + 4 * g, wvec, avail);
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+          wb[j] = j < nb ? load_sf4(a.act_sf + (size_t)(t.row0 + 32 * j + lane) * sf_ld + 4 * g, bvec, avail)
+                         : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (c >= avail) break;
+          const int s = (int)(it % STAGES);
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status, a.timeout_ns, site0 + 5)) { ok = false; break; }
+          uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
+#pragma unroll
+          for (int op = 0; op < C::NA; ++op)
+            st_shared_v4(sF + op * 512 + lane * 16, word(wa[op][0], c), word(wa[op][1], c), word(wa[op][2], c),
+                         word(wa[op][3], c));
+#pragma unroll
+          for (int q = 0; q < NB / 4; ++q)
+            st_shared_v4(sF + C::NA * 512 + q * 512 + lane * 16, word(wb[4 * q], c), word(wb[4 * q + 1], c),
+                         word(wb[4 * q + 2], c), word(wb[4 * q + 3], c));
+          fence_proxy_async_smem();  // generic-proxy writes, read next by tcgen05.cp
+          mbar_arrive(&full[s]);
+          ++it;
+        }
       }
     }
   } else if (warp == 1) {
@@ -250,7 +303,6 @@ __global__ void __launch_bounds__(256, 1)
           const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait(&full[s], ph, abort_flag, a.status, a.timeout_ns, site0 + 2)) { ok = false; break; }
           tc_fence_after();
-          fence_proxy_async_smem();  // scale factors were written by cp.async (generic proxy)
           const uint8_t* sA = smem + C::A_OFF + s * C::NA * C::A_BYTES;
           const uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
           const uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;

@@ -95,6 +95,7 @@ struct GemmArgs {
   float clamp;
   int fast_math;
   int prefetch_stages;  // weight boxes pulled into L2 this many K steps ahead of the loads
+  int w_sf_vec, act_sf_vec;  // scale rows allow 16-byte loads (16-byte aligned base and row stride)
   unsigned long long timeout_ns;
 };
 
