@@ -17,8 +17,8 @@
 // walks a flat list of (expert, weight block, token tile) tiles.
 //
 // Warp roles (256 threads): warp 0 = TMA producer, warp 1 = MMA issuer (one
-// thread), warp 2 = TMEM allocator, warp 3 = scale-factor producer, warps 4-7 =
-// epilogue (warp w
+// thread; L1: gate tile), warp 2 = TMEM allocator (L1: also the up tile's MMA
+// issuer), warp 3 = scale-factor producer, warps 4-7 = epilogue (warp w
 // reads TMEM lanes 32*(w%4) .. +31, i.e. 32 consecutive weight rows).
 // Pipelines: STAGES shared-memory stages (full/empty mbarriers) and two TMEM
 // accumulator buffers (tmem_full/tmem_empty) so the epilogue of one tile
@@ -38,6 +38,7 @@ struct GemmCfg {
   static constexpr int BM = 128;                         // weight rows per MMA
   static constexpr int BK = 128;                         // K per stage
   static constexpr int NA = kL1 ? 2 : 1;                 // weight tiles per stage (gate, up)
+  static constexpr int NI = NA;                          // MMA-issuing threads, one per weight tile
   static constexpr int A_BYTES = BM * BK;                // 16 KB in SMEM (4-bit codes padded to bytes)
   static constexpr int A_TX = BM * BK / 2;               // transaction bytes of one weight box (packed 4-bit size)
   static constexpr int B_BYTES = BN * BK;
@@ -48,11 +49,13 @@ struct GemmCfg {
   static constexpr int SF_OFF = B_OFF + STAGES * B_BYTES;
   static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE_BYTES;
   static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
-  // TMEM columns: two accumulator buffers, then two scale-factor slots
+  // TMEM columns: two accumulator buffers, then two scale-factor slots per
+  // issuing thread (weight scales: 4 columns, token scales: 4 or 8 columns;
+  // every scale-factor address stays a multiple of 4 columns)
   static constexpr int ACC_COLS = NA * BN;
-  static constexpr int SF_SLOT_COLS = 16;
+  static constexpr int SF_ISSUER_COLS = 4 + SFB_ROWS / 32;
   static constexpr int SF_BASE = 2 * ACC_COLS;
-  static constexpr int TMEM_USED = SF_BASE + 2 * SF_SLOT_COLS;
+  static constexpr int TMEM_USED = SF_BASE + 2 * NI * SF_ISSUER_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
   static_assert(TMEM_USED <= 512, "TMEM budget");
@@ -139,10 +142,10 @@ __global__ void __launch_bounds__(256, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1 + 32);  // TMA expect_tx arrival + one arrival per scale-factor lane
-      mbar_init(&empty[s], 1);      // tcgen05.commit
+      mbar_init(&empty[s], C::NI);  // one tcgen05.commit per issuing thread
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&tfull[b], 1);   // tcgen05.commit after the last K step
+      mbar_init(&tfull[b], C::NI);  // tcgen05.commit after the last K step, per issuing thread
       mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
     }
     *abort_flag = 0;
@@ -285,9 +288,13 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || (kL1 && warp == 2)) {
+    // ------------------------------------------------------------ MMA issuers
+    // One thread per weight tile (L1: warp 1 gate, warp 2 up; L2: warp 1): the
+    // tcgen05 instruction stream of a K step is split between them. Each
+    // copies its own scale factors to TMEM and commits its own work.
     if (lane == 0) {
+      const int u = warp - 1;
       uint32_t it = 0, tcount = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tcount) {
@@ -296,33 +303,29 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t bph = (tcount >> 1) & 1u;
         if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, a.status, a.timeout_ns, site0 + 1)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem + (uint32_t)(buf * C::ACC_COLS);
+        const uint32_t d = tmem + (uint32_t)(buf * C::ACC_COLS + u * BN);
         const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait(&full[s], ph, abort_flag, a.status, a.timeout_ns, site0 + 2)) { ok = false; break; }
           tc_fence_after();
-          const uint8_t* sA = smem + C::A_OFF + s * C::NA * C::A_BYTES;
+          const uint8_t* sA = smem + C::A_OFF + (s * C::NA + u) * C::A_BYTES;
           const uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
           const uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
-          const uint32_t sf_col = tmem + (uint32_t)(C::SF_BASE + (int)(it & 1u) * C::SF_SLOT_COLS);
-          const uint32_t sfb_col = sf_col + 4u * C::NA;
-#pragma unroll
-          for (int op = 0; op < C::NA; ++op) tc_cp_32x128b_warpx4(sf_col + 4u * op, sdesc_sf_32x16(smem_u32(sF + op * 512)));
+          const uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + ((int)(it & 1u) * C::NI + u) * C::SF_ISSUER_COLS);
+          const uint32_t sfb = sfa + 4u;
+          tc_cp_32x128b_warpx4(sfa, sdesc_sf_32x16(smem_u32(sF + u * 512)));
 #pragma unroll
           for (int g = 0; g < C::SFB_ROWS / 128; ++g)
-            tc_cp_32x128b_warpx4(sfb_col + 4u * g, sdesc_sf_32x16(smem_u32(sF + C::NA * 512 + g * 512)));
-          const uint64_t da0 = sdesc_kmajor_sw128(smem_u32(sA));
-          const uint64_t da1 = sdesc_kmajor_sw128(smem_u32(sA + C::A_BYTES));
+            tc_cp_32x128b_warpx4(sfb + 4u * g, sdesc_sf_32x16(smem_u32(sF + C::NA * 512 + g * 512)));
+          const uint64_t da = sdesc_kmajor_sw128(smem_u32(sA));
           const uint64_t db = sdesc_kmajor_sw128(smem_u32(sB));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint32_t id = idesc_mxf8f6f4(5u, 0u, n_mma, (uint32_t)k);
-            const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
             // +32 bytes of K per step inside the 128-byte swizzle atom (2 in 16-byte units)
-            tc_mma_mxf8f6f4(d0, da0 + 2u * k, db + 2u * k, id, sf_col, sfb_col, acc);
-            if (kL1) tc_mma_mxf8f6f4(d0 + BN, da1 + 2u * k, db + 2u * k, id, sf_col + 4u, sfb_col, acc);
+            tc_mma_mxf8f6f4(d, da + 2u * k, db + 2u * k, id, sfa, sfb, (kb > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(&empty[s]);
         }
@@ -414,8 +417,9 @@ static int launch(const void* tw, const void* ta, const GemmArgs* a, int num_cta
   return (int)cudaGetLastError();
 }
 
-// Pipeline depths: as many stages as the 227 KB of shared memory allows.
-constexpr int kStagesL1Small = 6, kStagesL2Small = 8, kStagesL1Large = 4, kStagesL2Large = 4;
+// Pipeline depths: as many stages as the 227 KB of shared memory allows (small L1:
+// five, measured as fast as six).
+constexpr int kStagesL1Small = 5, kStagesL2Small = 8, kStagesL1Large = 4, kStagesL2Large = 4;
 
 }  // namespace mm
 
