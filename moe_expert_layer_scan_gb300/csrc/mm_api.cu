@@ -21,7 +21,6 @@ struct mm_handle {
   int device;
   int num_sms;
   unsigned long long timeout_ns;
-  int prefetch[2][2];  // [variant][l1 ? 0 : 1]: weight K steps pulled into L2 ahead of the loads
   // cached weight tensor maps (keyed by base pointer)
   const void* w1_key;
   const void* w2_key;
@@ -112,15 +111,6 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
     long ms = atol(t);
     if (ms > 0) h->timeout_ns = (unsigned long long)ms * 1000000ull;
   }
-  // off by default: on GB300 the L2 prefetch cursor measured slower for both
-  // the decode and the prefill workloads (kept as a tuning knob)
-  h->prefetch[0][0] = 0; h->prefetch[0][1] = 0;
-  h->prefetch[1][0] = 0; h->prefetch[1][1] = 0;
-  if (const char* p = getenv("MM_PREFETCH_STAGES")) {  // "small_l1,small_l2,large_l1,large_l2"
-    int v[4];
-    if (sscanf(p, "%d,%d,%d,%d", &v[0], &v[1], &v[2], &v[3]) == 4)
-      for (int i = 0; i < 4; ++i) h->prefetch[i / 2][i % 2] = v[i] < 0 ? 0 : (v[i] > 256 ? 256 : v[i]);
-  }
   h->w1_key = h->w2_key = nullptr;
   h->profile = false;
   h->n_recorded = 0;
@@ -167,8 +157,8 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   uint8_t* base = static_cast<uint8_t*>(ws);
   const int Ep = h->E + h->S, Kp = h->k + h->S;
   const int variant = variant_for(T);
-  const int bn1 = variant == 0 ? kBnSmall : kBnL1Large;
-  const int bn2 = variant == 0 ? kBnSmall : kBnL2Large;
+  const int bn1 = variant == 0 ? kBnSmall : kBnLarge;
+  const int bn2 = bn1;
 
   RouteArgs ra;
   ra.topk_idx = topk_idx;
@@ -183,7 +173,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ra.status = reinterpret_cast<uint32_t*>(base + L.status);
   ra.T = T; ra.E = h->E; ra.k = h->k; ra.S = h->S;
   ra.bn_l1 = bn1; ra.bn_l2 = bn2;
-  ra.fb_l1 = h->I / 128; ra.fb_l2 = h->H / 128;
+  ra.fb_l1 = h->I / 128; ra.fb_l2 = (h->H + 255) / 256;
   int ev_i = 0;
   auto mark = [&]() {
     if (h->profile && ev_i < 6) cudaEventRecord(h->ev[ev_i++], (cudaStream_t)stream);
@@ -233,7 +223,6 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g1.status = ra.status;
   g1.Ep = Ep; g1.K = h->H; g1.rows_w = 2 * h->I; g1.I = h->I; g1.H = h->H;
   g1.clamp = h->clamp; g1.fast_math = h->fast_math; g1.timeout_ns = h->timeout_ns;
-  g1.prefetch_stages = h->prefetch[variant][0];
   g1.w_sf_vec = aligned(w1_sf, 16) && (h->H / 32) % 16 == 0;
   g1.act_sf_vec = (h->H / 32) % 16 == 0;
   mark();
@@ -248,7 +237,6 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g2.out_sf = nullptr;
   g2.out_z = reinterpret_cast<uint16_t*>(base + L.z);
   g2.K = h->I; g2.rows_w = h->H;
-  g2.prefetch_stages = h->prefetch[variant][1];
   g2.w_sf_vec = aligned(w2_sf, 16) && (h->I / 32) % 16 == 0;
   g2.act_sf_vec = (h->I / 32) % 16 == 0;
   mark();

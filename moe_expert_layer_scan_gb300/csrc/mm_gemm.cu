@@ -8,8 +8,9 @@
 //     y = silu(clamp(gate)) * clamp(up) * w_r, per (row, 32 columns) amax ->
 //     UE8M0 scale (smallest power of two >= amax/448) -> E4M3
 //     ("MEGAMOE_SM90_DESIGN" sec. 10.1, steps 2-5; UE8M0 per the SM100 kernel).
-//   L2 (Linear2 phase; sec. 11.1): acc[h, r] = sum_i W2[e, h, i] * q[r, i],
-//     written as BF16 into the per-slot row r.
+//   L2 (Linear2 phase; sec. 11.1): acc[h, r] = sum_i W2[e, h, i] * q[r, i]
+//     for two consecutive 128-row blocks of W2, written as BF16 into the
+//     per-slot row r.
 //
 // Orientation: the weights are the MMA's M=128 operand (E2M1, read by TMA as
 // 16 x 4-bit groups padded to 16 bytes in SMEM) and the expert's token rows are
@@ -37,7 +38,10 @@ template <bool kL1, int BN, int STAGES>
 struct GemmCfg {
   static constexpr int BM = 128;                         // weight rows per MMA
   static constexpr int BK = 128;                         // K per stage
-  static constexpr int NA = kL1 ? 2 : 1;                 // weight tiles per stage (gate, up)
+  // Two 128-row weight tiles per stage: L1 the gate rows and the matching up
+  // rows; L2 two consecutive 128-row blocks of W2 (the second may be absent
+  // when H / 128 is odd).
+  static constexpr int NA = 2;
   static constexpr int NI = NA;                          // MMA-issuing threads, one per weight tile
   static constexpr int A_BYTES = BM * BK;                // 16 KB in SMEM (4-bit codes padded to bytes)
   static constexpr int A_TX = BM * BK / 2;               // transaction bytes of one weight box (packed 4-bit size)
@@ -85,6 +89,21 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a, int bn)
   t.row0 = a.offsets[lo] + tt * bn;
   t.nrows = min(bn, cnt - tt * bn);
   return t;
+}
+
+// First weight row of a tile's first 128-row block, the offset of its second
+// block, and whether the second block exists.
+template <bool kL1>
+__device__ __forceinline__ int tile_wrow(const Tile& t, const GemmArgs& a) {
+  return t.e * a.rows_w + t.fb * (kL1 ? 128 : 256);
+}
+template <bool kL1>
+__device__ __forceinline__ int second_off(const GemmArgs& a) {
+  return kL1 ? a.I : 128;
+}
+template <bool kL1>
+__device__ __forceinline__ bool has_second(const Tile& t, const GemmArgs& a) {
+  return kL1 || t.fb * 256 + 128 < a.rows_w;
 }
 
 // Four K steps of one row's UE8M0 scales (16 bytes); `avail` steps exist.
@@ -171,48 +190,12 @@ __global__ void __launch_bounds__(256, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // A prefetch cursor runs prefetch_stages K steps ahead of the loads and
-    // pulls the weight boxes into L2 (and, when it enters a tile, the lines
-    // holding that tile's weight scale rows), so the TMA loads that fill the
-    // shared-memory ring find their data in L2: the DRAM requests in flight
-    // are no longer limited by the ring's size.
-    int pf_tile = blockIdx.x, pf_kb = 0, pf_wrow = 0;
-    if (pf_tile < num_tiles) {
-      const Tile p = decode_tile(pf_tile, a, BN);
-      pf_wrow = p.e * a.rows_w + p.fb * C::BM;
-    }
-    auto prefetch_next = [&]() {
-      if (pf_tile >= num_tiles) return;
-      if (pf_kb == 0) {
-#pragma unroll
-        for (int op = 0; op < C::NA; ++op)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint8_t* row = a.w_sf + (size_t)(pf_wrow + op * a.I + 32 * i + lane) * sf_ld;
-            for (int off = 0; off < sf_ld; off += 128) prefetch_l2(row + off);
-            prefetch_l2(row + sf_ld - 1);
-          }
-      }
-      if (lane == 0) {
-        tma_prefetch_l2_2d(&tm_w, pf_kb * C::BK, pf_wrow);
-        if (kL1) tma_prefetch_l2_2d(&tm_w, pf_kb * C::BK, pf_wrow + a.I);
-      }
-      if (++pf_kb == kblocks) {
-        pf_kb = 0;
-        pf_tile += gridDim.x;
-        if (pf_tile < num_tiles) {
-          const Tile p = decode_tile(pf_tile, a, BN);
-          pf_wrow = p.e * a.rows_w + p.fb * C::BM;
-        }
-      }
-    };
-    for (int i = 0; i < a.prefetch_stages; ++i) prefetch_next();
-
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       const Tile t = decode_tile(tile, a, BN);
-      const int wrow = t.e * a.rows_w + t.fb * C::BM;
+      const int wrow = tile_wrow<kL1>(t, a);
+      const bool two = has_second<kL1>(t, a);
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
         const int s = (int)(it % STAGES);
         const uint32_t ph = (it / STAGES) & 1u;
@@ -221,12 +204,11 @@ __global__ void __launch_bounds__(256, 1)
         uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
         uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], C::NA * C::A_TX + C::B_BYTES);
+          mbar_arrive_expect_tx(&full[s], (two ? 2 : 1) * C::A_TX + C::B_BYTES);
           tma_load_2d(sA, &tm_w, &full[s], kb * C::BK, wrow);
-          if (kL1) tma_load_2d(sA + C::A_BYTES, &tm_w, &full[s], kb * C::BK, wrow + a.I);
+          if (two) tma_load_2d(sA + C::A_BYTES, &tm_w, &full[s], kb * C::BK, wrow + second_off<kL1>(a));
           tma_load_2d(sB, &tm_act, &full[s], kb * C::BK, t.row0);
         }
-        prefetch_next();
       }
     }
     if (!ok) {
@@ -251,7 +233,8 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       const Tile t = decode_tile(tile, a, BN);
-      const int wrow = t.e * a.rows_w + t.fb * C::BM;
+      const int wrow = tile_wrow<kL1>(t, a);
+      const bool two = has_second<kL1>(t, a);
       const int nb = (t.nrows + 31) / 32;
       for (int g = 0; g < kblocks && ok; g += 4) {
         const int avail = kblocks - g;
@@ -262,7 +245,10 @@ __global__ void __launch_bounds__(256, 1)
         for (int op = 0; op < C::NA; ++op)
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            wa[op][i] = load_sf4(a.w_sf + (size_t)(wrow + op * a.I + 32 * i + lane) * sf_ld + 4 * g, wvec, avail);
+            wa[op][i] = (op == 0 || two)
+                            ? load_sf4(a.w_sf + (size_t)(wrow + op * second_off<kL1>(a) + 32 * i + lane) * sf_ld + 4 * g,
+                                       wvec, avail)
+                            : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int j = 0; j < NB; ++j)
           wb[j] = j < nb ? load_sf4(a.act_sf + (size_t)(t.row0 + 32 * j + lane) * sf_ld + 4 * g, bvec, avail)
@@ -288,11 +274,12 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
     }
-  } else if (warp == 1 || (kL1 && warp == 2)) {
+  } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
-    // One thread per weight tile (L1: warp 1 gate, warp 2 up; L2: warp 1): the
+    // One thread per weight tile (warp 1: first tile, warp 2: second tile): the
     // tcgen05 instruction stream of a K step is split between them. Each
-    // copies its own scale factors to TMEM and commits its own work.
+    // copies its own scale factors to TMEM and commits its own work (a missing
+    // second L2 block still commits, so the barrier counts hold).
     if (lane == 0) {
       const int u = warp - 1;
       uint32_t it = 0, tcount = 0;
@@ -305,6 +292,7 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * C::ACC_COLS + u * BN);
         const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
+        const bool active = u == 0 || has_second<kL1>(t, a);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
@@ -313,19 +301,21 @@ __global__ void __launch_bounds__(256, 1)
           const uint8_t* sA = smem + C::A_OFF + (s * C::NA + u) * C::A_BYTES;
           const uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
           const uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
-          const uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + ((int)(it & 1u) * C::NI + u) * C::SF_ISSUER_COLS);
-          const uint32_t sfb = sfa + 4u;
-          tc_cp_32x128b_warpx4(sfa, sdesc_sf_32x16(smem_u32(sF + u * 512)));
+          if (active) {
+            const uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + ((int)(it & 1u) * C::NI + u) * C::SF_ISSUER_COLS);
+            const uint32_t sfb = sfa + 4u;
+            tc_cp_32x128b_warpx4(sfa, sdesc_sf_32x16(smem_u32(sF + u * 512)));
 #pragma unroll
-          for (int g = 0; g < C::SFB_ROWS / 128; ++g)
-            tc_cp_32x128b_warpx4(sfb + 4u * g, sdesc_sf_32x16(smem_u32(sF + C::NA * 512 + g * 512)));
-          const uint64_t da = sdesc_kmajor_sw128(smem_u32(sA));
-          const uint64_t db = sdesc_kmajor_sw128(smem_u32(sB));
+            for (int g = 0; g < C::SFB_ROWS / 128; ++g)
+              tc_cp_32x128b_warpx4(sfb + 4u * g, sdesc_sf_32x16(smem_u32(sF + C::NA * 512 + g * 512)));
+            const uint64_t da = sdesc_kmajor_sw128(smem_u32(sA));
+            const uint64_t db = sdesc_kmajor_sw128(smem_u32(sB));
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t id = idesc_mxf8f6f4(5u, 0u, n_mma, (uint32_t)k);
-            // +32 bytes of K per step inside the 128-byte swizzle atom (2 in 16-byte units)
-            tc_mma_mxf8f6f4(d, da + 2u * k, db + 2u * k, id, sfa, sfb, (kb > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t id = idesc_mxf8f6f4(5u, 0u, n_mma, (uint32_t)k);
+              // +32 bytes of K per step inside the 128-byte swizzle atom (2 in 16-byte units)
+              tc_mma_mxf8f6f4(d, da + 2u * k, db + 2u * k, id, sfa, sfb, (kb > 0 || k > 0) ? 1u : 0u);
+            }
           }
           tc_commit(&empty[s]);
         }
@@ -345,7 +335,9 @@ __global__ void __launch_bounds__(256, 1)
       if (!mbar_wait(&tfull[buf], bph, abort_flag, a.status, a.timeout_ns, site0 + 3)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::ACC_COLS);
-      const int feat = t.fb * C::BM + 32 * q + lane;  // L1: intermediate column; L2: hidden column
+      // L1: intermediate column of the gate/up pair; L2: hidden column of block 0 (block 1: +128)
+      const int feat = t.fb * (kL1 ? 128 : 256) + 32 * q + lane;
+      const bool two = has_second<kL1>(t, a);
       for (int c0 = 0; c0 < t.nrows; c0 += 16) {
         uint32_t g[16];
         tmem_ld_x16(tbase + (uint32_t)c0, g);
@@ -378,13 +370,17 @@ __global__ void __launch_bounds__(256, 1)
             }
           }
         } else {
+          uint32_t h[16];
+          tmem_ld_x16(tbase + (uint32_t)(BN + c0), h);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;
-            if (col < t.nrows)
-              a.out_z[(size_t)(t.row0 + col) * a.H + feat] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(g[j])));
+            if (col < t.nrows) {
+              uint16_t* zr = a.out_z + (size_t)(t.row0 + col) * a.H;
+              zr[feat] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(g[j])));
+              if (two) zr[feat + 128] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(h[j])));
+            }
           }
         }
       }
@@ -417,9 +413,9 @@ static int launch(const void* tw, const void* ta, const GemmArgs* a, int num_cta
   return (int)cudaGetLastError();
 }
 
-// Pipeline depths: as many stages as the 227 KB of shared memory allows (small L1:
+// Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
 // five, measured as fast as six).
-constexpr int kStagesL1Small = 5, kStagesL2Small = 8, kStagesL1Large = 4, kStagesL2Large = 4;
+constexpr int kStagesL1Small = 5, kStagesL2Small = 5, kStagesL1Large = 4, kStagesL2Large = 4;
 
 }  // namespace mm
 
@@ -428,8 +424,8 @@ extern "C" int mm_gemm_prepare(void) {
   int e = 0;
   if ((e = set_smem_attr<true, kBnSmall, kStagesL1Small>())) return e;
   if ((e = set_smem_attr<false, kBnSmall, kStagesL2Small>())) return e;
-  if ((e = set_smem_attr<true, kBnL1Large, kStagesL1Large>())) return e;
-  if ((e = set_smem_attr<false, kBnL2Large, kStagesL2Large>())) return e;
+  if ((e = set_smem_attr<true, kBnLarge, kStagesL1Large>())) return e;
+  if ((e = set_smem_attr<false, kBnLarge, kStagesL2Large>())) return e;
   return 0;
 }
 
@@ -439,8 +435,8 @@ extern "C" int mm_launch_gemm(int l1, int variant, const void* tmap_w, const voi
   cudaStream_t st = (cudaStream_t)stream;
   if (l1) {
     return variant == 0 ? launch<true, kBnSmall, kStagesL1Small>(tmap_w, tmap_act, a, num_ctas, st)
-                        : launch<true, kBnL1Large, kStagesL1Large>(tmap_w, tmap_act, a, num_ctas, st);
+                        : launch<true, kBnLarge, kStagesL1Large>(tmap_w, tmap_act, a, num_ctas, st);
   }
   return variant == 0 ? launch<false, kBnSmall, kStagesL2Small>(tmap_w, tmap_act, a, num_ctas, st)
-                      : launch<false, kBnL2Large, kStagesL2Large>(tmap_w, tmap_act, a, num_ctas, st);
+                      : launch<false, kBnLarge, kStagesL2Large>(tmap_w, tmap_act, a, num_ctas, st);
 }

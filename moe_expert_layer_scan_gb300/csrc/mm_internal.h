@@ -18,8 +18,7 @@ constexpr int kRowMargin = 256;    // pool rows beyond the last valid row that t
 // everything else; the N of each tile is the expert's remaining rows rounded up
 // to 16, so ragged tails never pay for a full tile.
 constexpr int kBnSmall = 16;
-constexpr int kBnL1Large = 112;
-constexpr int kBnL2Large = 224;
+constexpr int kBnLarge = 112;
 constexpr int kSmallMaxTokens = 16;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -68,7 +67,7 @@ struct RouteArgs {
   uint32_t* status;
   int T, E, k, S;
   int bn_l1, bn_l2;  // token-tile widths of the two GEMMs
-  int fb_l1, fb_l2;  // 128-row weight blocks per expert: I/128 and H/128
+  int fb_l1, fb_l2;  // weight tiles per expert: I/128 (gate/up pairs) and ceil(H/256)
 };
 
 struct GatherArgs {
@@ -94,7 +93,6 @@ struct GemmArgs {
   int Ep, K, rows_w, I, H;
   float clamp;
   int fast_math;
-  int prefetch_stages;  // weight boxes pulled into L2 this many K steps ahead of the loads
   int w_sf_vec, act_sf_vec;  // scale rows allow 16-byte loads (16-byte aligned base and row stride)
   unsigned long long timeout_ns;
 };

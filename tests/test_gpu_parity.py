@@ -26,6 +26,9 @@ SMALL_CASES = {
     "ragged": Workload("ragged", T=37, H=384, I=384, E=5, k=3, S=1, seed=105),
     "clamp_active": Workload("clamp_active", T=40, H=512, I=256, E=4, k=2, clamp=0.5, seed=106),
     "small_tiles": Workload("small_tiles", T=16, H=256, I=128, E=2, k=2, seed=107),
+    # H / 128 odd: the last L2 tile has a single 128-row block of W2
+    "odd_h_small": Workload("odd_h_small", T=8, H=384, I=256, E=4, k=2, seed=108),
+    "odd_h_large": Workload("odd_h_large", T=40, H=640, I=384, E=3, k=2, S=1, seed=109),
 }
 
 
