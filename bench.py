@@ -42,7 +42,12 @@ KERNEL_NAMES = ["route", "gather", "l1_gemm", "l2_gemm", "combine"]
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
 # capture, keyed by workload, valid only while mm_gemm.cu hashes to `src`.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # decode: E=64 capture (42 experts touched) scaled to the 61 experts one launch touches
+    "decode": {"src": "66163c8b27a38c06", "bytes": 969073189},
+    # prefill: T=2048/E=32 capture (16384 rows) scaled x8 to 131072 rows
+    "prefill": {"src": "66163c8b27a38c06", "bytes": 5231742976},
+}
 
 
 def gemm_source_hash() -> str:
