@@ -133,7 +133,8 @@ mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes) {
 
 mm_status_t mm_launches_per_run(mm_handle_t h, int T, int* launches) {
   if (!h || !launches || T < 0) return MM_ERR_INVALID_ARG;
-  *launches = T == 0 ? 1 : 5;
+  const int route = mm_route_launches(T * (h->k + h->S));
+  *launches = T == 0 ? route : route + 4;
   return MM_OK;
 }
 
@@ -170,6 +171,9 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ra.perm = reinterpret_cast<int32_t*>(base + L.perm);
   ra.pos = reinterpret_cast<int32_t*>(base + L.pos);
   ra.row_w = reinterpret_cast<float*>(base + L.row_w);
+  ra.chunk_cnt = reinterpret_cast<int32_t*>(base + L.chunk_cnt);
+  ra.chunk_base = reinterpret_cast<int32_t*>(base + L.chunk_base);
+  ra.chunk_bad = reinterpret_cast<int32_t*>(base + L.chunk_bad);
   ra.status = reinterpret_cast<uint32_t*>(base + L.status);
   ra.T = T; ra.E = h->E; ra.k = h->k; ra.S = h->S;
   ra.bn_l1 = bn1; ra.bn_l2 = bn2;

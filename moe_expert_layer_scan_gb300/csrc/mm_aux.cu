@@ -60,68 +60,15 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
   return excl;
 }
 
-// One CTA of 1024 threads (32 warps). Warp w owns a contiguous chunk of slots;
-// hist[w][e] first holds its per-expert counts, then its write cursors.
-__global__ void __launch_bounds__(1024, 1) route_kernel(RouteArgs a) {
-  extern __shared__ int sh[];
+// Stable placement of the slots [c0, c1) by one CTA of 1024 threads (32
+// warps). hist[w][e] must hold, for every warp w and expert e, the first pool
+// row warp w writes for expert e; warp w owns a contiguous sub-range and walks
+// it 32 slots at a time in order, ranking equal experts with __match_any_sync.
+__device__ void place_slots(const RouteArgs& a, long c0, long c1, int* hist) {
   const int Ep = a.E + a.S, Kp = a.k + a.S;
-  const long R = (long)a.T * Kp;
-  int* hist = sh;                 // [32][Ep]
-  int* scratch = sh + 32 * Ep;    // [72]
-  __shared__ int bad_any;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) bad_any = 0;
-  for (int i = tid; i < 32 * Ep; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-
-  const long chunk = (R + 31) / 32;
-  const long s0 = warp * chunk, s1 = (s0 + chunk < R) ? s0 + chunk : R;
-  bool bad = false;
-  for (long s = s0 + lane; s < s1; s += 32) {
-    int e = slot_expert(a, s, &bad);
-    if (e >= 0) atomicAdd(&hist[warp * Ep + e], 1);
-  }
-  if (bad) bad_any = 1;
-  __syncthreads();
-
-  // per-expert totals -> counts and offsets; per-warp write cursors
-  int tot = 0;
-  if (tid < Ep)
-    for (int w = 0; w < 32; ++w) tot += hist[w * Ep + tid];
-  int total_rows;
-  const int excl = block_exclusive_scan(tid < Ep ? tot : 0, scratch, &total_rows);
-  if (tid < Ep) {
-    a.counts[tid] = tot;
-    a.offsets[tid] = excl;
-    int run = excl;
-    for (int w = 0; w < 32; ++w) {
-      int c = hist[w * Ep + tid];
-      hist[w * Ep + tid] = run;
-      run += c;
-    }
-  }
-  if (tid == 0) a.offsets[Ep] = total_rows;
-
-  // tile tables: (ceil(count / BN) token tiles) x (weight row blocks) per expert
-  int t1 = 0, t2 = 0;
-  if (tid < Ep) {
-    t1 = (tot + a.bn_l1 - 1) / a.bn_l1 * a.fb_l1;
-    t2 = (tot + a.bn_l2 - 1) / a.bn_l2 * a.fb_l2;
-  }
-  int n1, n2;
-  const int e1 = block_exclusive_scan(t1, scratch, &n1);
-  const int e2 = block_exclusive_scan(t2, scratch, &n2);
-  if (tid < Ep) {
-    a.tiles_l1[tid] = e1;
-    a.tiles_l2[tid] = e2;
-  }
-  if (tid == 0) {
-    a.tiles_l1[Ep] = n1;
-    a.tiles_l2[Ep] = n2;
-  }
-  __syncthreads();
-
-  // stable scatter: each warp walks its chunk 32 slots at a time, in order
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long sub = (c1 - c0 + 31) / 32;
+  const long s0 = c0 + warp * sub, s1 = (s0 + sub < c1) ? s0 + sub : c1;
   const unsigned lt_mask = (1u << lane) - 1u;
   for (long base = s0; base < s1; base += 32) {
     const long s = base + lane;
@@ -144,8 +91,152 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(RouteArgs a) {
     if (e >= 0 && rank == 0) hist[warp * Ep + e] += __popc(peers);
     __syncwarp();
   }
+}
+
+// Per-warp expert histograms of the slots [c0, c1) (same split as place_slots).
+__device__ bool warp_histograms(const RouteArgs& a, long c0, long c1, int* hist) {
+  const int Ep = a.E + a.S;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 32 * Ep; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const long sub = (c1 - c0 + 31) / 32;
+  const long s0 = c0 + warp * sub, s1 = (s0 + sub < c1) ? s0 + sub : c1;
+  bool bad = false;
+  for (long s = s0 + lane; s < s1; s += 32) {
+    const int e = slot_expert(a, s, &bad);
+    if (e >= 0) atomicAdd(&hist[warp * Ep + e], 1);
+  }
+  __syncthreads();
+  return bad;
+}
+
+// Counts -> offsets (exclusive scan) and the two GEMM tile tables; thread e
+// holds expert e's total in `tot`. Called by all 1024 threads.
+__device__ int offsets_and_tiles(const RouteArgs& a, int tot, int* scratch) {
+  const int Ep = a.E + a.S;
+  const int tid = threadIdx.x;
+  int total_rows;
+  const int excl = block_exclusive_scan(tid < Ep ? tot : 0, scratch, &total_rows);
+  if (tid < Ep) {
+    a.counts[tid] = tot;
+    a.offsets[tid] = excl;
+  }
+  if (tid == 0) a.offsets[Ep] = total_rows;
+  int t1 = 0, t2 = 0;
+  if (tid < Ep) {
+    t1 = (tot + a.bn_l1 - 1) / a.bn_l1 * a.fb_l1;
+    t2 = (tot + a.bn_l2 - 1) / a.bn_l2 * a.fb_l2;
+  }
+  int n1, n2;
+  const int e1 = block_exclusive_scan(t1, scratch, &n1);
+  const int e2 = block_exclusive_scan(t2, scratch, &n2);
+  if (tid < Ep) {
+    a.tiles_l1[tid] = e1;
+    a.tiles_l2[tid] = e2;
+  }
+  if (tid == 0) {
+    a.tiles_l1[Ep] = n1;
+    a.tiles_l2[Ep] = n2;
+  }
+  return excl;
+}
+
+// Routing by one CTA (few slots): histograms, offsets, cursors, placement.
+__global__ void __launch_bounds__(1024, 1) route_kernel(RouteArgs a) {
+  extern __shared__ int sh[];
+  const int Ep = a.E + a.S, Kp = a.k + a.S;
+  const long R = (long)a.T * Kp;
+  int* hist = sh;               // [32][Ep]
+  int* scratch = sh + 32 * Ep;  // [72]
+  __shared__ int bad_any;
+  const int tid = threadIdx.x;
+  if (tid == 0) bad_any = 0;
+  const bool bad = warp_histograms(a, 0, R, hist);
+  if (bad) bad_any = 1;
+  int tot = 0;
+  if (tid < Ep)
+    for (int w = 0; w < 32; ++w) tot += hist[w * Ep + tid];
+  const int excl = offsets_and_tiles(a, tot, scratch);
+  if (tid < Ep) {
+    int run = excl;
+    for (int w = 0; w < 32; ++w) {
+      const int c = hist[w * Ep + tid];
+      hist[w * Ep + tid] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  place_slots(a, 0, R, hist);
   __syncthreads();
   if (tid == 0) *a.status = bad_any ? MM_DEV_BAD_ROUTING : 0u;
+}
+
+// Multi-CTA routing, pass 1: expert counts of each chunk of kRouteChunk slots.
+__global__ void __launch_bounds__(1024) route_count_kernel(RouteArgs a) {
+  extern __shared__ int hist[];  // [Ep]
+  __shared__ int bad_any;
+  const int Ep = a.E + a.S, Kp = a.k + a.S;
+  const long R = (long)a.T * Kp;
+  const long c0 = (long)blockIdx.x * kRouteChunk, c1 = (c0 + kRouteChunk < R) ? c0 + kRouteChunk : R;
+  if (threadIdx.x == 0) bad_any = 0;
+  for (int i = threadIdx.x; i < Ep; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (long s = c0 + threadIdx.x; s < c1; s += blockDim.x) {
+    const int e = slot_expert(a, s, &bad);
+    if (e >= 0) atomicAdd(&hist[e], 1);
+  }
+  if (bad) bad_any = 1;
+  __syncthreads();
+  for (int i = threadIdx.x; i < Ep; i += blockDim.x) a.chunk_cnt[(size_t)blockIdx.x * Ep + i] = hist[i];
+  if (threadIdx.x == 0) a.chunk_bad[blockIdx.x] = bad_any;
+}
+
+// Pass 2 (one CTA): totals, offsets, tile tables, each chunk's first row per
+// expert, and the status word.
+__global__ void __launch_bounds__(1024, 1) route_scan_kernel(RouteArgs a, int G) {
+  __shared__ int scratch[72];
+  __shared__ int bad_any;
+  const int Ep = a.E + a.S;
+  const int tid = threadIdx.x;
+  if (tid == 0) bad_any = 0;
+  __syncthreads();
+  int tot = 0;
+  if (tid < Ep)
+    for (int g = 0; g < G; ++g) tot += a.chunk_cnt[(size_t)g * Ep + tid];
+  for (int g = tid; g < G; g += blockDim.x)
+    if (a.chunk_bad[g]) bad_any = 1;
+  const int excl = offsets_and_tiles(a, tot, scratch);
+  if (tid < Ep) {
+    int run = excl;
+    for (int g = 0; g < G; ++g) {
+      const int c = a.chunk_cnt[(size_t)g * Ep + tid];
+      a.chunk_base[(size_t)g * Ep + tid] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) *a.status = bad_any ? MM_DEV_BAD_ROUTING : 0u;
+}
+
+// Pass 3: each CTA places its chunk's slots, starting at the chunk's first row
+// per expert.
+__global__ void __launch_bounds__(1024, 1) route_place_kernel(RouteArgs a) {
+  extern __shared__ int hist[];  // [32][Ep]
+  const int Ep = a.E + a.S, Kp = a.k + a.S;
+  const long R = (long)a.T * Kp;
+  const long c0 = (long)blockIdx.x * kRouteChunk, c1 = (c0 + kRouteChunk < R) ? c0 + kRouteChunk : R;
+  warp_histograms(a, c0, c1, hist);
+  if (threadIdx.x < Ep) {
+    int run = a.chunk_base[(size_t)blockIdx.x * Ep + threadIdx.x];
+    for (int w = 0; w < 32; ++w) {
+      const int c = hist[w * Ep + threadIdx.x];
+      hist[w * Ep + threadIdx.x] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  place_slots(a, c0, c1, hist);
 }
 
 // One warp per pool row: copies the token's FP8 row and its scale row into
@@ -224,17 +315,29 @@ __global__ void timeout_probe_kernel(uint32_t* status, unsigned long long timeou
 
 }  // namespace mm
 
+extern "C" int mm_route_launches(int slots) { return slots <= mm::kRouteSingleMax ? 1 : 3; }
+
 extern "C" int mm_launch_route(const mm::RouteArgs* a, void* stream) {
   const int Ep = a->E + a->S;
-  const size_t smem = sizeof(int) * (32 * (size_t)Ep + 72);
+  const long R = (long)a->T * (a->k + a->S);
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(mm::route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(int) * (32 * mm::kMaxExperts + 72)));
+    const int big = (int)(sizeof(int) * (32 * mm::kMaxExperts + 72));
+    cudaError_t e = cudaFuncSetAttribute(mm::route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(mm::route_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
     if (e != cudaSuccess) return (int)e;
     attr_set = true;
   }
-  mm::route_kernel<<<1, 1024, smem, (cudaStream_t)stream>>>(*a);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (R <= mm::kRouteSingleMax) {
+    mm::route_kernel<<<1, 1024, sizeof(int) * (32 * (size_t)Ep + 72), st>>>(*a);
+    return (int)cudaGetLastError();
+  }
+  const int G = (int)((R + mm::kRouteChunk - 1) / mm::kRouteChunk);
+  mm::route_count_kernel<<<G, 1024, sizeof(int) * (size_t)Ep, st>>>(*a);
+  mm::route_scan_kernel<<<1, 1024, 0, st>>>(*a, G);
+  mm::route_place_kernel<<<G, 1024, sizeof(int) * 32 * (size_t)Ep, st>>>(*a);
   return (int)cudaGetLastError();
 }
 

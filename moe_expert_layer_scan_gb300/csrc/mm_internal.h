@@ -12,6 +12,8 @@ namespace mm {
 constexpr int kMaxExperts = 1024;  // E + S
 constexpr int kMaxSlots = 16;      // topk + S
 constexpr int kRowMargin = 256;    // pool rows beyond the last valid row that tiles may touch
+constexpr int kRouteChunk = 8192;  // slots per CTA when routing runs on several CTAs
+constexpr int kRouteSingleMax = 16384;  // up to this many slots, one CTA routes everything
 
 // Token-tile widths (the MMA N dimension) and pipeline depths of the two GEMM
 // variants. "small" serves decode-like calls (few rows per expert), "large"
@@ -25,7 +27,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Byte offsets of every workspace region for one (shape, T).
 struct Layout {
-  size_t status, counts, offsets, tiles_l1, tiles_l2, perm, pos, row_w;
+  size_t status, counts, offsets, tiles_l1, tiles_l2, perm, pos, row_w, chunk_cnt, chunk_base, chunk_bad;
   size_t pool_x, pool_sf, l2a, l2a_sf, z, total;
   int rows_cap;
 };
@@ -45,6 +47,10 @@ inline Layout make_layout(int E, int S, int H, int I, int k, int T) {
   L.perm = take(sizeof(int32_t) * (R + 1), 256);
   L.pos = take(sizeof(int32_t) * (R + 1), 256);
   L.row_w = take(sizeof(float) * (R + 1), 256);
+  const size_t G = (R + kRouteChunk - 1) / kRouteChunk + 1;
+  L.chunk_cnt = take(sizeof(int32_t) * G * Ep, 256);
+  L.chunk_base = take(sizeof(int32_t) * G * Ep, 256);
+  L.chunk_bad = take(sizeof(int32_t) * G, 256);
   L.pool_x = take((size_t)L.rows_cap * H, 1024);
   L.pool_sf = take((size_t)L.rows_cap * (H / 32), 1024);
   L.l2a = take((size_t)L.rows_cap * I, 1024);
@@ -65,6 +71,9 @@ struct RouteArgs {
   int32_t* pos;
   float* row_w;
   uint32_t* status;
+  int32_t* chunk_cnt;   // [G][E+S] per-chunk expert counts (multi-CTA routing)
+  int32_t* chunk_base;  // [G][E+S] first pool row of each chunk's slots per expert
+  int32_t* chunk_bad;   // [G] out-of-range ids seen in the chunk
   int T, E, k, S;
   int bn_l1, bn_l2;  // token-tile widths of the two GEMMs
   int fb_l1, fb_l2;  // weight tiles per expert: I/128 (gate/up pairs) and ceil(H/256)
@@ -109,6 +118,7 @@ struct CombineArgs {
 // Kernel launchers (one translation unit each); return cudaError_t as int.
 extern "C" {
 int mm_launch_route(const mm::RouteArgs* a, void* stream);
+int mm_route_launches(int slots);  // kernels mm_launch_route enqueues for this many slots
 int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream);
 int mm_launch_combine(const mm::CombineArgs* a, void* stream);
 // variant: 0 = small tiles, 1 = large tiles. tmaps: two 128-byte CUtensorMap blobs (weights, activations).
