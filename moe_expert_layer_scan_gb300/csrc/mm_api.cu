@@ -177,7 +177,10 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ra.status = reinterpret_cast<uint32_t*>(base + L.status);
   ra.T = T; ra.E = h->E; ra.k = h->k; ra.S = h->S;
   ra.bn_l1 = bn1; ra.bn_l2 = bn2;
-  ra.fb_l1 = h->I / 128; ra.fb_l2 = (h->H + 255) / 256;
+  const int cs = mm_gemm_cluster(variant);
+  const int f1 = h->I / 128, f2 = (h->H + 255) / 256;  // weight tiles per expert
+  ra.fb_l1 = (f1 + cs - 1) / cs;                         // tile-table entries: groups of cs weight tiles
+  ra.fb_l2 = (f2 + cs - 1) / cs;
   int ev_i = 0;
   auto mark = [&]() {
     if (h->profile && ev_i < 6) cudaEventRecord(h->ev[ev_i++], (cudaStream_t)stream);
@@ -212,8 +215,11 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
     h->w2_key = w2;
   }
   CUtensorMap tm_x, tm_q;
-  if (!encode_2d(&tm_x, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, (uint32_t)bn1)) return MM_ERR_CUDA;
-  if (!encode_2d(&tm_q, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)bn2)) return MM_ERR_CUDA;
+  // token boxes: each CTA of a cluster loads (and multicasts) 1/cs of the token tile
+  if (!encode_2d(&tm_x, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, (uint32_t)(bn1 / cs)))
+    return MM_ERR_CUDA;
+  if (!encode_2d(&tm_q, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)(bn2 / cs)))
+    return MM_ERR_CUDA;
 
   GemmArgs g1;
   memset(&g1, 0, sizeof(g1));
@@ -225,7 +231,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g1.out_q = base + L.l2a;
   g1.out_sf = base + L.l2a_sf;
   g1.status = ra.status;
-  g1.Ep = Ep; g1.K = h->H; g1.rows_w = 2 * h->I; g1.I = h->I; g1.H = h->H;
+  g1.Ep = Ep; g1.K = h->H; g1.rows_w = 2 * h->I; g1.I = h->I; g1.H = h->H; g1.fb_total = f1;
   g1.clamp = h->clamp; g1.fast_math = h->fast_math; g1.timeout_ns = h->timeout_ns;
   g1.w_sf_vec = aligned(w1_sf, 16) && (h->H / 32) % 16 == 0;
   g1.act_sf_vec = (h->H / 32) % 16 == 0;
@@ -240,7 +246,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g2.out_q = nullptr;
   g2.out_sf = nullptr;
   g2.out_z = reinterpret_cast<uint16_t*>(base + L.z);
-  g2.K = h->I; g2.rows_w = h->H;
+  g2.K = h->I; g2.rows_w = h->H; g2.fb_total = f2;
   g2.w_sf_vec = aligned(w2_sf, 16) && (h->I / 32) % 16 == 0;
   g2.act_sf_vec = (h->I / 32) % 16 == 0;
   mark();

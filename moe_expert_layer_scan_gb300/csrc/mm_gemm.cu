@@ -17,10 +17,11 @@
 // the N operand (E4M3), N = the tile's rows rounded up to 16. One CTA per SM
 // walks a flat list of (expert, weight block, token tile) tiles.
 //
-// Warp roles (256 threads): warp 0 = TMA producer, warp 1 = MMA issuer (one
-// thread; L1: gate tile), warp 2 = TMEM allocator (L1: also the up tile's MMA
-// issuer), warp 3 = scale-factor producer, warps 4-7 = epilogue (warp w
-// reads TMEM lanes 32*(w%4) .. +31, i.e. 32 consecutive weight rows).
+// Warp roles (384 threads): warp 0 = TMA producer; warps 1 and 2 = the MMA
+// issuers of the tile's two weight blocks (one thread each; warp 2 also
+// allocates TMEM); warp 3 = scale-factor producer; warps 4-11 = epilogue (warp
+// w reads TMEM lanes 32*(w%4)..+31, i.e. 32 consecutive weight rows; the two
+// warps of a quadrant take alternate 16-column chunks of the token tile).
 // Pipelines: STAGES shared-memory stages (full/empty mbarriers) and two TMEM
 // accumulator buffers (tmem_full/tmem_empty) so the epilogue of one tile
 // overlaps the main loop of the next. Every wait is bounded.
@@ -34,7 +35,10 @@
 
 namespace mm {
 
-template <bool kL1, int BN, int STAGES>
+constexpr int kEpiWarps = 8;                      // two per TMEM lane quadrant
+constexpr int kThreads = 32 * (4 + kEpiWarps);   // producer, 2 issuers/allocator, scale warp, epilogue
+
+template <bool kL1, int BN, int STAGES, int CS>
 struct GemmCfg {
   static constexpr int BM = 128;                         // weight rows per MMA
   static constexpr int BK = 128;                         // K per stage
@@ -46,6 +50,7 @@ struct GemmCfg {
   static constexpr int A_BYTES = BM * BK;                // 16 KB in SMEM (4-bit codes padded to bytes)
   static constexpr int A_TX = BM * BK / 2;               // transaction bytes of one weight box (packed 4-bit size)
   static constexpr int B_BYTES = BN * BK;
+  static constexpr int B_PART_ROWS = BN / CS;            // token rows each CTA of a cluster loads (multicast)
   static constexpr int SFB_ROWS = BN <= 128 ? 128 : 256;
   static constexpr int SF_STAGE_BYTES = NA * 512 + SFB_ROWS * 4;
   static constexpr int A_OFF = 0;
@@ -66,13 +71,17 @@ struct GemmCfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(B_BYTES % 1024 == 0, "B tiles must keep 1024-byte alignment");
+  static_assert(BN % (8 * CS) == 0, "each multicast share must be whole 8-row swizzle atoms");
 };
 
 struct Tile {
   int e, fb, row0, nrows;
+  bool active;  // this CTA has a weight tile (fb < fb_total)
 };
 
-__device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a, int bn) {
+// Tile index -> expert, token tile and this CTA's weight tile: the table
+// counts weight-tile groups of cs tiles (one per CTA of a cluster).
+__device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a, int bn, int rank, int cs) {
   int lo = 0, hi = a.Ep - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -84,8 +93,10 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a, int bn)
   const int local = tile - a.tile_start[lo];
   const int cnt = a.offsets[lo + 1] - a.offsets[lo];
   const int ntt = (cnt + bn - 1) / bn;
-  t.fb = local / ntt;
-  const int tt = local - t.fb * ntt;
+  const int grp = local / ntt;
+  const int tt = local - grp * ntt;
+  t.fb = grp * cs + rank;
+  t.active = t.fb < a.fb_total;
   t.row0 = a.offsets[lo] + tt * bn;
   t.nrows = min(bn, cnt - tt * bn);
   return t;
@@ -103,7 +114,7 @@ __device__ __forceinline__ int second_off(const GemmArgs& a) {
 }
 template <bool kL1>
 __device__ __forceinline__ bool has_second(const Tile& t, const GemmArgs& a) {
-  return kL1 || t.fb * 256 + 128 < a.rows_w;
+  return t.active && (kL1 || t.fb * 256 + 128 < a.rows_w);
 }
 
 // Four K steps of one row's UE8M0 scales (16 bytes); `avail` steps exist.
@@ -143,11 +154,11 @@ __device__ __forceinline__ float inv_scale(uint32_t code) {
   return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(1u << (n + 149));
 }
 
-template <bool kL1, int BN, int STAGES>
-__global__ void __launch_bounds__(256, 1)
+template <bool kL1, int BN, int STAGES, int CS>
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_act,
                 const GemmArgs a) {
-  using C = GemmCfg<kL1, BN, STAGES>;
+  using C = GemmCfg<kL1, BN, STAGES, CS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -161,11 +172,11 @@ __global__ void __launch_bounds__(256, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1 + 32);  // TMA expect_tx arrival + one arrival per scale-factor lane
-      mbar_init(&empty[s], C::NI);  // one tcgen05.commit per issuing thread
+      mbar_init(&empty[s], C::NI * CS);  // one tcgen05.commit per issuing thread of every CTA of the cluster
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], C::NI);  // tcgen05.commit after the last K step, per issuing thread
-      mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+      mbar_init(&tempty[b], kEpiWarps);  // one arrival per epilogue warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -180,9 +191,13 @@ __global__ void __launch_bounds__(256, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (CS > 1) cluster_sync();  // barriers initialised cluster-wide before any multicast
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int num_tiles = a.tile_start[a.Ep];
+  const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
+  const int tile0 = blockIdx.x / CS, tile_step = gridDim.x / CS;
+  constexpr uint16_t kAllCtas = (uint16_t)((1u << CS) - 1u);
   // wait sites reported in the status word on expiry (L2 kernel: +8)
   const uint32_t site0 = kL1 ? 0u : 8u;
   const int kblocks = a.K / C::BK;
@@ -192,8 +207,8 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ producer
     uint32_t it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      const Tile t = decode_tile(tile, a, BN);
+    for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
+      const Tile t = decode_tile(tile, a, BN, rank, CS);
       const int wrow = tile_wrow<kL1>(t, a);
       const bool two = has_second<kL1>(t, a);
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
@@ -204,12 +219,24 @@ __global__ void __launch_bounds__(256, 1)
         uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
         uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], (two ? 2 : 1) * C::A_TX + C::B_BYTES);
-          tma_load_2d(sA, &tm_w, &full[s], kb * C::BK, wrow);
+          // the whole token tile lands here: this CTA's share and the others' multicasts
+          mbar_arrive_expect_tx(&full[s], (t.active ? (two ? 2 : 1) : 0) * C::A_TX + C::B_BYTES);
+          if (t.active) tma_load_2d(sA, &tm_w, &full[s], kb * C::BK, wrow);
           if (two) tma_load_2d(sA + C::A_BYTES, &tm_w, &full[s], kb * C::BK, wrow + second_off<kL1>(a));
-          tma_load_2d(sB, &tm_act, &full[s], kb * C::BK, t.row0);
+          if constexpr (CS == 1) {
+            tma_load_2d(sB, &tm_act, &full[s], kb * C::BK, t.row0);
+          } else {
+            tma_load_2d_multicast(sB + rank * C::B_PART_ROWS * C::BK, &tm_act, &full[s], kb * C::BK,
+                                  t.row0 + rank * C::B_PART_ROWS, kAllCtas);
+          }
         }
       }
+    }
+    if (ok && CS > 1) {
+      // Producer tail: wait until every CTA has released the last stages, so
+      // that no remote tcgen05.commit arrival targets this CTA after it exits.
+      for (uint32_t j = (it > (uint32_t)STAGES ? it - STAGES : 0u); j < it; ++j)
+        if (!mbar_wait(&empty[j % STAGES], (j / STAGES) & 1u, abort_flag, a.status, a.timeout_ns, site0 + 4)) break;
     }
     if (!ok) {
       // Let the copies already issued land before the CTA can exit (the
@@ -231,8 +258,8 @@ __global__ void __launch_bounds__(256, 1)
     constexpr int NB = C::SFB_ROWS / 32;  // 32-row blocks of the token operand
     uint32_t it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      const Tile t = decode_tile(tile, a, BN);
+    for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
+      const Tile t = decode_tile(tile, a, BN, rank, CS);
       const int wrow = tile_wrow<kL1>(t, a);
       const bool two = has_second<kL1>(t, a);
       const int nb = (t.nrows + 31) / 32;
@@ -245,7 +272,7 @@ __global__ void __launch_bounds__(256, 1)
         for (int op = 0; op < C::NA; ++op)
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            wa[op][i] = (op == 0 || two)
+            wa[op][i] = ((op == 0 && t.active) || two)
                             ? load_sf4(a.w_sf + (size_t)(wrow + op * second_off<kL1>(a) + 32 * i + lane) * sf_ld + 4 * g,
                                        wvec, avail)
                             : make_uint4(0u, 0u, 0u, 0u);
@@ -284,15 +311,15 @@ __global__ void __launch_bounds__(256, 1)
       const int u = warp - 1;
       uint32_t it = 0, tcount = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tcount) {
-        const Tile t = decode_tile(tile, a, BN);
+      for (int tile = tile0; tile < num_tiles && ok; tile += tile_step, ++tcount) {
+        const Tile t = decode_tile(tile, a, BN, rank, CS);
         const int buf = (int)(tcount & 1u);
         const uint32_t bph = (tcount >> 1) & 1u;
         if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, a.status, a.timeout_ns, site0 + 1)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * C::ACC_COLS + u * BN);
         const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
-        const bool active = u == 0 || has_second<kL1>(t, a);
+        const bool active = u == 0 ? t.active : has_second<kL1>(t, a);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
@@ -317,7 +344,9 @@ __global__ void __launch_bounds__(256, 1)
               tc_mma_mxf8f6f4(d, da + 2u * k, db + 2u * k, id, sfa, sfb, (kb > 0 || k > 0) ? 1u : 0u);
             }
           }
-          tc_commit(&empty[s]);
+          // the stage is free once every CTA the token tile was multicast to is done with it
+          if constexpr (CS == 1) tc_commit(&empty[s]);
+          else tc_commit_multicast(&empty[s], kAllCtas);
         }
         if (!ok) break;
         tc_commit(&tfull[buf]);
@@ -326,10 +355,13 @@ __global__ void __launch_bounds__(256, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
+    // Warp w reads TMEM lanes 32*(w%4)..+31 (hardware rule); the two warps of
+    // a quadrant take alternate 16-column chunks of the token tile.
     const int q = warp & 3;
+    const int half = (warp - 4) >> 2;
     uint32_t tcount = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
-      const Tile t = decode_tile(tile, a, BN);
+    for (int tile = tile0; tile < num_tiles; tile += tile_step, ++tcount) {
+      const Tile t = decode_tile(tile, a, BN, rank, CS);
       const int buf = (int)(tcount & 1u);
       const uint32_t bph = (tcount >> 1) & 1u;
       if (!mbar_wait(&tfull[buf], bph, abort_flag, a.status, a.timeout_ns, site0 + 3)) break;
@@ -338,7 +370,7 @@ __global__ void __launch_bounds__(256, 1)
       // L1: intermediate column of the gate/up pair; L2: hidden column of block 0 (block 1: +128)
       const int feat = t.fb * (kL1 ? 128 : 256) + 32 * q + lane;
       const bool two = has_second<kL1>(t, a);
-      for (int c0 = 0; c0 < t.nrows; c0 += 16) {
+      for (int c0 = 16 * half; t.active && c0 < t.nrows; c0 += 32) {
         uint32_t g[16];
         tmem_ld_x16(tbase + (uint32_t)c0, g);
         if constexpr (kL1) {
@@ -392,51 +424,94 @@ __global__ void __launch_bounds__(256, 1)
 
   tc_fence_before();
   __syncthreads();
+  // no CTA leaves while another may still multicast into it or arrive on its barriers
+  if constexpr (CS > 1) cluster_sync();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
-template <bool kL1, int BN, int STAGES>
-static int set_smem_attr() {
-  using C = GemmCfg<kL1, BN, STAGES>;
-  return (int)cudaFuncSetAttribute(gemm_kernel<kL1, BN, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   C::SMEM_BYTES);
+template <bool kL1, int BN, int STAGES, int CS>
+static int set_smem_attr(int* max_ctas) {
+  using C = GemmCfg<kL1, BN, STAGES, CS>;
+  auto k = gemm_kernel<kL1, BN, STAGES, CS>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return (int)e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  *max_ctas = sms;
+  if (CS > 1) {
+    // persistent grid: only as many clusters as can be resident at once
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(sms / CS * CS));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, k, &cfg);
+    if (e != cudaSuccess || clusters < 1) return e != cudaSuccess ? (int)e : (int)cudaErrorInvalidConfiguration;
+    *max_ctas = clusters * CS;
+  }
+  return 0;
 }
 
-template <bool kL1, int BN, int STAGES>
+template <bool kL1, int BN, int STAGES, int CS>
 static int launch(const void* tw, const void* ta, const GemmArgs* a, int num_ctas, cudaStream_t st) {
-  using C = GemmCfg<kL1, BN, STAGES>;
-  gemm_kernel<kL1, BN, STAGES><<<num_ctas, 256, C::SMEM_BYTES, st>>>(*static_cast<const CUtensorMap*>(tw),
-                                                                      *static_cast<const CUtensorMap*>(ta), *a);
-  return (int)cudaGetLastError();
+  using C = GemmCfg<kL1, BN, STAGES, CS>;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)num_ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = CS > 1 ? 1 : 0;
+  return (int)cudaLaunchKernelEx(&cfg, gemm_kernel<kL1, BN, STAGES, CS>, *static_cast<const CUtensorMap*>(tw),
+                                 *static_cast<const CUtensorMap*>(ta), *a);
 }
 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
 // five, measured as fast as six).
 constexpr int kStagesL1Small = 5, kStagesL2Small = 5, kStagesL1Large = 4, kStagesL2Large = 4;
+// CTAs per launch of each instantiation: [l1][variant]
+static int g_ctas[2][2];
 
 }  // namespace mm
 
 extern "C" int mm_gemm_prepare(void) {
   using namespace mm;
   int e = 0;
-  if ((e = set_smem_attr<true, kBnSmall, kStagesL1Small>())) return e;
-  if ((e = set_smem_attr<false, kBnSmall, kStagesL2Small>())) return e;
-  if ((e = set_smem_attr<true, kBnLarge, kStagesL1Large>())) return e;
-  if ((e = set_smem_attr<false, kBnLarge, kStagesL2Large>())) return e;
+  if ((e = set_smem_attr<true, kBnSmall, kStagesL1Small, 1>(&g_ctas[1][0]))) return e;
+  if ((e = set_smem_attr<false, kBnSmall, kStagesL2Small, 1>(&g_ctas[0][0]))) return e;
+  if ((e = set_smem_attr<true, kBnLarge, kStagesL1Large, kClusterLarge>(&g_ctas[1][1]))) return e;
+  if ((e = set_smem_attr<false, kBnLarge, kStagesL2Large, kClusterLarge>(&g_ctas[0][1]))) return e;
   return 0;
 }
+
+extern "C" int mm_gemm_cluster(int variant) { return variant == 0 ? 1 : mm::kClusterLarge; }
 
 extern "C" int mm_launch_gemm(int l1, int variant, const void* tmap_w, const void* tmap_act, const mm::GemmArgs* a,
                               int num_ctas, void* stream) {
   using namespace mm;
+  (void)num_ctas;
   cudaStream_t st = (cudaStream_t)stream;
+  const int n = g_ctas[l1 ? 1 : 0][variant];
   if (l1) {
-    return variant == 0 ? launch<true, kBnSmall, kStagesL1Small>(tmap_w, tmap_act, a, num_ctas, st)
-                        : launch<true, kBnLarge, kStagesL1Large>(tmap_w, tmap_act, a, num_ctas, st);
+    return variant == 0 ? launch<true, kBnSmall, kStagesL1Small, 1>(tmap_w, tmap_act, a, n, st)
+                        : launch<true, kBnLarge, kStagesL1Large, kClusterLarge>(tmap_w, tmap_act, a, n, st);
   }
-  return variant == 0 ? launch<false, kBnSmall, kStagesL2Small>(tmap_w, tmap_act, a, num_ctas, st)
-                      : launch<false, kBnLarge, kStagesL2Large>(tmap_w, tmap_act, a, num_ctas, st);
+  return variant == 0 ? launch<false, kBnSmall, kStagesL2Small, 1>(tmap_w, tmap_act, a, n, st)
+                      : launch<false, kBnLarge, kStagesL2Large, kClusterLarge>(tmap_w, tmap_act, a, n, st);
 }

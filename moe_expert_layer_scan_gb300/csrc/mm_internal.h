@@ -21,6 +21,10 @@ constexpr int kRouteSingleMax = 16384;  // up to this many slots, one CTA routes
 // to 16, so ragged tails never pay for a full tile.
 constexpr int kBnSmall = 16;
 constexpr int kBnLarge = 112;
+// Large tiles run as clusters of kClusterLarge CTAs: the CTAs take adjacent
+// weight tiles of the same (expert, token tile) and each multicasts its share
+// of the token tile to all of them.
+constexpr int kClusterLarge = 2;
 constexpr int kSmallMaxTokens = 16;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -100,6 +104,7 @@ struct GemmArgs {
   uint16_t* out_z;            // L2: [rows_cap][H] BF16
   uint32_t* status;
   int Ep, K, rows_w, I, H;
+  int fb_total;  // weight tiles per expert (L1: I/128 gate/up pairs, L2: ceil(H/256) block pairs)
   float clamp;
   int fast_math;
   int w_sf_vec, act_sf_vec;  // scale rows allow 16-byte loads (16-byte aligned base and row stride)
@@ -124,6 +129,7 @@ int mm_launch_combine(const mm::CombineArgs* a, void* stream);
 // variant: 0 = small tiles, 1 = large tiles. tmaps: two 128-byte CUtensorMap blobs (weights, activations).
 int mm_launch_gemm(int l1, int variant, const void* tmap_w, const void* tmap_act, const mm::GemmArgs* a,
                    int num_ctas, void* stream);
-int mm_gemm_prepare(void);  // sets the dynamic shared-memory limits once
+int mm_gemm_prepare(void);  // sets the dynamic shared-memory limits and the persistent grid sizes
+int mm_gemm_cluster(int variant);  // CTAs per cluster of the variant
 int mm_launch_timeout_probe(uint32_t* status, unsigned long long timeout_ns, void* stream);
 }
