@@ -35,8 +35,13 @@
 
 namespace mm {
 
-constexpr int kEpiWarps = 8;                      // two per TMEM lane quadrant
-constexpr int kThreads = 32 * (4 + kEpiWarps);   // producer, 2 issuers/allocator, scale warp, epilogue
+// Epilogue warps: two per TMEM lane quadrant for the large tiles (their L1
+// epilogue is as long as the main loop), one for the 16-column decode tiles.
+template <int BN>
+struct Warps {
+  static constexpr int EPI = BN > 16 ? 8 : 4;
+  static constexpr int THREADS = 32 * (4 + EPI);  // producer, 2 issuers/allocator, scale warp, epilogue
+};
 
 template <bool kL1, int BN, int STAGES, int CS>
 struct GemmCfg {
@@ -155,7 +160,7 @@ __device__ __forceinline__ float inv_scale(uint32_t code) {
 }
 
 template <bool kL1, int BN, int STAGES, int CS>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_act,
                 const GemmArgs a) {
   using C = GemmCfg<kL1, BN, STAGES, CS>;
@@ -176,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], C::NI);  // tcgen05.commit after the last K step, per issuing thread
-      mbar_init(&tempty[b], kEpiWarps);  // one arrival per epilogue warp
+      mbar_init(&tempty[b], Warps<BN>::EPI);  // one arrival per epilogue warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -358,51 +363,83 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Warp w reads TMEM lanes 32*(w%4)..+31 (hardware rule); the two warps of
     // a quadrant take alternate 16-column chunks of the token tile.
     const int q = warp & 3;
-    const int half = (warp - 4) >> 2;
+    const int half = (warp - 4) >> 2;  // 0 when there is one warp per quadrant
     uint32_t tcount = 0;
     for (int tile = tile0; tile < num_tiles; tile += tile_step, ++tcount) {
       const Tile t = decode_tile(tile, a, BN, rank, CS);
       const int buf = (int)(tcount & 1u);
       const uint32_t bph = (tcount >> 1) & 1u;
-      if (!mbar_wait(&tfull[buf], bph, abort_flag, a.status, a.timeout_ns, site0 + 3)) break;
+      if (!mbar_wait(&tfull[buf], bph, abort_flag, a.status, a.timeout_ns, site0 + 3, 256)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::ACC_COLS);
       // L1: intermediate column of the gate/up pair; L2: hidden column of block 0 (block 1: +128)
       const int feat = t.fb * (kL1 ? 128 : 256) + 32 * q + lane;
       const bool two = has_second<kL1>(t, a);
-      for (int c0 = 16 * half; t.active && c0 < t.nrows; c0 += 32) {
-        uint32_t g[16];
-        tmem_ld_x16(tbase + (uint32_t)c0, g);
-        if constexpr (kL1) {
-          uint32_t u[16];
-          tmem_ld_x16(tbase + (uint32_t)(BN + c0), u);
-          tmem_ld_wait();
-          const int wc = c0 + (lane & 15);
-          const float wl = wc < t.nrows ? a.row_w[t.row0 + wc] : 0.0f;
+      if constexpr (kL1) {
+        // The per-column amax over the warp's 32 features (one UE8M0 group) is
+        // a transpose-reduction: after the exchange steps lane c (32 columns)
+        // or lanes 2c, 2c+1 (16 columns) hold the maximum of column c, compute
+        // that column's scale once, and the inverse scales are broadcast back.
+        // NC = 32 columns per step (16 for the 16-row decode tiles).
+        constexpr int NC = BN > 16 ? 32 : 16;
+        constexpr int LOG2NC = NC == 32 ? 5 : 4;
+        for (int c0 = NC * half; t.active && c0 < t.nrows; c0 += NC * (Warps<BN>::EPI / 4)) {
+          const int ncol = min(NC, t.nrows - c0);
+          uint32_t g0[16], g1[16], u0[16], u1[16];
+          tmem_ld_x16(tbase + (uint32_t)c0, g0);
+          tmem_ld_x16(tbase + (uint32_t)(BN + c0), u0);
+          if (NC == 32 && ncol > 16) {
+            tmem_ld_x16(tbase + (uint32_t)(c0 + 16), g1);
+            tmem_ld_x16(tbase + (uint32_t)(BN + c0 + 16), u1);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < 16; ++j) g1[j] = u1[j] = 0u;
+          }
+          tmem_ld_wait();
+          const float wl = lane < ncol ? a.row_w[t.row0 + c0 + lane] : 0.0f;
+          float y[NC], v[NC];
+#pragma unroll
+          for (int j = 0; j < NC; ++j) {
             const float wj = __shfl_sync(0xffffffffu, wl, j);
-            float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
+            float gv = __uint_as_float(j < 16 ? g0[j] : g1[j - 16]);
+            float uv = __uint_as_float(j < 16 ? u0[j] : u1[j - 16]);
             if (a.clamp > 0.0f) {
               gv = fminf(fmaxf(gv, -a.clamp), a.clamp);
               uv = fminf(fmaxf(uv, -a.clamp), a.clamp);
             }
             const float ex = a.fast_math ? __expf(-gv) : expf(-gv);
             const float silu = __fdiv_rn(gv, __fadd_rn(1.0f, ex));
-            const float y = __fmul_rn(__fmul_rn(silu, uv), wj);
-            float am = fabsf(y);
+            y[j] = j < ncol ? __fmul_rn(__fmul_rn(silu, uv), wj) : 0.0f;
+            v[j] = fabsf(y[j]);
+          }
+          // halve the columns each lane holds at every exchange; with 16
+          // columns a last butterfly step pairs lanes 2c and 2c+1
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-            const uint32_t code = requant_code(am);
-            const uint8_t qb = (uint8_t)__nv_cvt_float_to_fp8(__fmul_rn(y, inv_scale(code)), __NV_SATFINITE, __NV_E4M3);
-            const int col = c0 + j;
-            if (col < t.nrows) {
-              a.out_q[(size_t)(t.row0 + col) * a.I + feat] = qb;
-              if (lane == 0) a.out_sf[(size_t)(t.row0 + col) * (a.I / 32) + t.fb * 4 + q] = (uint8_t)code;
+          for (int o = 16, n = NC; n > 1; o >>= 1, n >>= 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < n / 2; ++i) {
+              const float recv = __shfl_xor_sync(0xffffffffu, upper ? v[i] : v[i + n / 2], o);
+              v[i] = fmaxf(upper ? v[i + n / 2] : v[i], recv);
             }
           }
-        } else {
-          uint32_t h[16];
+          if (NC == 16) v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+          const int mycol = lane >> (5 - LOG2NC);
+          const uint32_t code = requant_code(v[0]);  // column c0 + mycol
+          const float inv = inv_scale(code);
+          if ((lane & ((1 << (5 - LOG2NC)) - 1)) == 0 && mycol < ncol)
+            a.out_sf[(size_t)(t.row0 + c0 + mycol) * (a.I / 32) + t.fb * 4 + q] = (uint8_t)code;
+#pragma unroll
+          for (int j = 0; j < NC; ++j) {
+            const float ij = __shfl_sync(0xffffffffu, inv, j << (5 - LOG2NC));
+            const uint8_t qb = (uint8_t)__nv_cvt_float_to_fp8(__fmul_rn(y[j], ij), __NV_SATFINITE, __NV_E4M3);
+            if (j < ncol) a.out_q[(size_t)(t.row0 + c0 + j) * a.I + feat] = qb;
+          }
+        }
+      } else {
+        for (int c0 = 16 * half; t.active && c0 < t.nrows; c0 += 16 * (Warps<BN>::EPI / 4)) {
+          uint32_t g[16], h[16];
+          tmem_ld_x16(tbase + (uint32_t)c0, g);
           tmem_ld_x16(tbase + (uint32_t)(BN + c0), h);
           tmem_ld_wait();
 #pragma unroll
@@ -451,7 +488,7 @@ static int set_smem_attr(int* max_ctas) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(sms / CS * CS));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Warps<BN>::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -473,7 +510,7 @@ static int launch(const void* tw, const void* ta, const GemmArgs* a, int num_cta
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3((unsigned)num_ctas);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(Warps<BN>::THREADS);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = st;
   cfg.attrs = attr;
