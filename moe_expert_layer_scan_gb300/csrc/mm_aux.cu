@@ -144,6 +144,7 @@ __device__ int offsets_and_tiles(const RouteArgs& a, int tot, int* scratch) {
 // Routing by one CTA (few slots): histograms, offsets, cursors, placement.
 __global__ void __launch_bounds__(1024, 1) route_kernel(RouteArgs a) {
   extern __shared__ int sh[];
+  pdl_trigger();
   const int Ep = a.E + a.S, Kp = a.k + a.S;
   const long R = (long)a.T * Kp;
   int* hist = sh;               // [32][Ep]
@@ -174,6 +175,7 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(RouteArgs a) {
 // Multi-CTA routing, pass 1: expert counts of each chunk of kRouteChunk slots.
 __global__ void __launch_bounds__(1024) route_count_kernel(RouteArgs a) {
   extern __shared__ int hist[];  // [Ep]
+  pdl_trigger();
   __shared__ int bad_any;
   const int Ep = a.E + a.S, Kp = a.k + a.S;
   const long R = (long)a.T * Kp;
@@ -197,6 +199,8 @@ __global__ void __launch_bounds__(1024) route_count_kernel(RouteArgs a) {
 __global__ void __launch_bounds__(1024, 1) route_scan_kernel(RouteArgs a, int G) {
   __shared__ int scratch[72];
   __shared__ int bad_any;
+  pdl_trigger();
+  pdl_wait();
   const int Ep = a.E + a.S;
   const int tid = threadIdx.x;
   if (tid == 0) bad_any = 0;
@@ -223,6 +227,8 @@ __global__ void __launch_bounds__(1024, 1) route_scan_kernel(RouteArgs a, int G)
 // per expert.
 __global__ void __launch_bounds__(1024, 1) route_place_kernel(RouteArgs a) {
   extern __shared__ int hist[];  // [32][Ep]
+  pdl_trigger();
+  pdl_wait();
   const int Ep = a.E + a.S, Kp = a.k + a.S;
   const long R = (long)a.T * Kp;
   const long c0 = (long)blockIdx.x * kRouteChunk, c1 = (c0 + kRouteChunk < R) ? c0 + kRouteChunk : R;
@@ -242,6 +248,8 @@ __global__ void __launch_bounds__(1024, 1) route_place_kernel(RouteArgs a) {
 // One warp per pool row: copies the token's FP8 row and its scale row into
 // expert-sorted pool order (the local form of the pages' L1 pool fill).
 __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int n = a.offsets[a.Ep];
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -262,6 +270,8 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
 // issues the loads of all the token's slot rows first, then sums them in FP32
 // in slot order and stores the BF16 result.
 __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int chunks = a.H / 8;
   const long total = (long)a.T * chunks;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
@@ -331,22 +341,24 @@ extern "C" int mm_launch_route(const mm::RouteArgs* a, void* stream) {
   }
   cudaStream_t st = (cudaStream_t)stream;
   if (R <= mm::kRouteSingleMax) {
-    mm::route_kernel<<<1, 1024, sizeof(int) * (32 * (size_t)Ep + 72), st>>>(*a);
-    return (int)cudaGetLastError();
+    // the first kernel of a forward: ordinary stream order behind the previous work
+    return (int)mm::launch_kernel(mm::route_kernel, dim3(1), dim3(1024), sizeof(int) * (32 * (size_t)Ep + 72), st,
+                                  false, 1, *a);
   }
   const int G = (int)((R + mm::kRouteChunk - 1) / mm::kRouteChunk);
-  mm::route_count_kernel<<<G, 1024, sizeof(int) * (size_t)Ep, st>>>(*a);
-  mm::route_scan_kernel<<<1, 1024, 0, st>>>(*a, G);
-  mm::route_place_kernel<<<G, 1024, sizeof(int) * 32 * (size_t)Ep, st>>>(*a);
-  return (int)cudaGetLastError();
+  cudaError_t e = mm::launch_kernel(mm::route_count_kernel, dim3(G), dim3(1024), sizeof(int) * (size_t)Ep, st, false,
+                                    1, *a);
+  if (e == cudaSuccess) e = mm::launch_kernel(mm::route_scan_kernel, dim3(1), dim3(1024), 0, st, true, 1, *a, G);
+  if (e == cudaSuccess)
+    e = mm::launch_kernel(mm::route_place_kernel, dim3(G), dim3(1024), sizeof(int) * 32 * (size_t)Ep, st, true, 1, *a);
+  return (int)e;
 }
 
 extern "C" int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream) {
   if (rows_upper_bound <= 0) return 0;
   int blocks = (rows_upper_bound + 7) / 8;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  mm::gather_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(*a);
-  return (int)cudaGetLastError();
+  return (int)mm::launch_kernel(mm::gather_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, true, 1, *a);
 }
 
 extern "C" int mm_launch_combine(const mm::CombineArgs* a, void* stream) {
@@ -354,8 +366,8 @@ extern "C" int mm_launch_combine(const mm::CombineArgs* a, void* stream) {
   const long threads = (long)a->T * (a->H / 8);
   long blocks = (threads + 127) / 128;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  mm::combine_kernel<<<(int)blocks, 128, 0, (cudaStream_t)stream>>>(*a);
-  return (int)cudaGetLastError();
+  return (int)mm::launch_kernel(mm::combine_kernel, dim3((unsigned)blocks), dim3(128), 0, (cudaStream_t)stream, true, 1,
+                                *a);
 }
 
 extern "C" int mm_launch_timeout_probe(uint32_t* status, unsigned long long timeout_ns, void* stream) {

@@ -198,6 +198,9 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
   __syncthreads();
   if constexpr (CS > 1) cluster_sync();  // barriers initialised cluster-wide before any multicast
   tc_fence_after();
+  // the prologue above overlaps the previous kernel; its outputs are read below
+  pdl_trigger();
+  pdl_wait();
   const uint32_t tmem = *tmem_slot;
   const int num_tiles = a.tile_start[a.Ep];
   const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
@@ -503,20 +506,9 @@ static int set_smem_attr(int* max_ctas) {
 template <bool kL1, int BN, int STAGES, int CS>
 static int launch(const void* tw, const void* ta, const GemmArgs* a, int num_ctas, cudaStream_t st) {
   using C = GemmCfg<kL1, BN, STAGES, CS>;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CS;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3((unsigned)num_ctas);
-  cfg.blockDim = dim3(Warps<BN>::THREADS);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = CS > 1 ? 1 : 0;
-  return (int)cudaLaunchKernelEx(&cfg, gemm_kernel<kL1, BN, STAGES, CS>, *static_cast<const CUtensorMap*>(tw),
-                                 *static_cast<const CUtensorMap*>(ta), *a);
+  return (int)launch_kernel(gemm_kernel<kL1, BN, STAGES, CS>, dim3((unsigned)num_ctas), dim3(Warps<BN>::THREADS),
+                            C::SMEM_BYTES, st, true, CS, *static_cast<const CUtensorMap*>(tw),
+                            *static_cast<const CUtensorMap*>(ta), *a);
 }
 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
