@@ -126,6 +126,15 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(dist, total_ms, e2e_ms, device):
+    """Slowest rank's elapsed times (the job's wall time): an all-reduce MAX of
+    (device-timed total, end-to-end total); e2e_ms None on every rank stays None."""
+    import torch
+    t = torch.tensor([total_ms, -1.0 if e2e_ms is None else e2e_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0]), (float(t[1]) if t[1] >= 0 else None)
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -264,9 +273,7 @@ def run_ours(args, world, rank, local):
     if not args.no_e2e:
         e2e_ms, h2d, d2h = measure_e2e(args, w, d, moe, out, flush, dist)
     if dist:
-        t = torch.tensor([total_ms, e2e_ms or 0.0], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), (float(t[1]) if e2e_ms is not None else None)
+        total_ms, e2e_ms = max_over_ranks(dist, total_ms, e2e_ms, device="cuda")
     if rank != 0:
         return
     report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk)
