@@ -38,15 +38,15 @@ import workloads  # noqa: E402
 METRIC = "MoE-layer tokens/s and TFLOP/s on 1 GB300; % of HBM or FP8xFP4 tensor roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
-KERNEL_NAMES = ["route", "gather", "l1_gemm", "l2_gemm", "combine"]
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
-# capture, keyed by workload, valid only while mm_gemm.cu hashes to `src`.
+# capture, keyed by workload, valid only while mm_gemm.cu hashes to `src` and
+# for the kernel named (fused "gemm" or "l1_gemm").
 NCU_TRAFFIC = {
     # decode: E=64 capture (42 experts touched) scaled to the 61 experts one launch touches
-    "decode": {"src": "66163c8b27a38c06", "bytes": 969073189},
+    "decode": {"src": "66163c8b27a38c06", "kernel": "l1_gemm", "bytes": 969073189},
     # prefill: T=2048/E=32 capture (16384 rows) scaled x8 to 131072 rows
-    "prefill": {"src": "66163c8b27a38c06", "bytes": 5231742976},
+    "prefill": {"src": "66163c8b27a38c06", "kernel": "l1_gemm", "bytes": 5231742976},
 }
 
 
@@ -218,7 +218,7 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl")
     w = workloads.CONFIGS[args.workload]
     d = workloads.device_inputs(w)
-    moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp)
+    moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp, fused=args.schedule == "fused")
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
     moe.workspace(w.T)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
@@ -257,7 +257,7 @@ def run_ours(args, world, rank, local):
     for i in range(args.steps):
         flush.zero_()
         moe.run(*ins, out=out)
-        per_kernel.append(mm.mm_profile_last(moe.h))
+        per_kernel.append(mm.mm_profile_stages(moe.h))
     torch.cuda.synchronize()
     mm.mm_profile_enable(moe.h, False)
     clk = clocks.stop() if clocks else None
@@ -321,35 +321,41 @@ def report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk
     ms = total_ms / args.steps
     tokens = w.T * world
     value = tokens / (ms / 1e3)
-    kern = {n: statistics.mean(p[i] for p in per_kernel) for i, n in enumerate(KERNEL_NAMES)
-            if all(len(p) > i for p in per_kernel)}
+    kern = {n: statistics.mean(p[n] for p in per_kernel) for n in per_kernel[0]}
     peaks, peak_src = load_peaks()
-    # the dominant kernel is the L1 grouped GEMM (W1 is two thirds of the weights and of the FLOPs)
-    l1_ms = kern.get("l1_gemm")
+    # the dominant kernel: the fused grouped GEMM (both linears in one launch)
+    # or, with one launch per linear, the L1 GEMM (two thirds of the weights and FLOPs)
+    fused = "gemm" in kern
+    k_name = "gemm" if fused else "l1_gemm"
+    k_ms = kern.get(k_name)
+    k_bytes = alg["l1_bytes"] + alg["l2_bytes"] if fused else alg["l1_bytes"]
+    k_flops = alg["flops"] if fused else alg["l1_flops"]
     hbm = float(peaks["hbm_gbs"])
     fp8_peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
     balance = fp8_peak * 1e12 / (hbm * 1e9)
-    intensity = alg["l1_flops"] / alg["l1_bytes"]
-    if intensity < balance:
-        achieved = alg["l1_bytes"] / (l1_ms / 1e3) / 1e9
+    if k_flops / k_bytes < balance:
+        achieved = k_bytes / (k_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                 "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"}
     else:
-        achieved = alg["l1_flops"] / (l1_ms / 1e3) / 1e12
+        achieved = k_flops / (k_ms / 1e3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                 "frac": achieved / fp8_peak,
                 "peak_source": f"{peak_src} bf16_tflops (burst) x {FP8_OVER_BF16} nominal FP8/BF16 ratio"}
     tr = NCU_TRAFFIC.get(w.name)
-    roof["traffic"] = tr["bytes"] if tr and tr.get("src") == gemm_source_hash() else None
-    roof["kernel"] = "gemm_kernel<L1> (mm_gemm.cu)"
-    roof["algorithmic_bytes_per_launch"] = alg["l1_bytes"]
-    roof["algorithmic_flops_per_launch"] = alg["l1_flops"]
-    roof["kernel_ms"] = l1_ms
+    roof["traffic"] = tr["bytes"] if tr and tr.get("src") == gemm_source_hash() and tr.get("kernel") == k_name \
+        else None
+    roof["kernel"] = ("gemm_kernel<fused> (mm_gemm.cu): L1 then L2 tiles in one launch" if fused
+                      else "gemm_kernel<L1> (mm_gemm.cu)")
+    roof["algorithmic_bytes_per_launch"] = k_bytes
+    roof["algorithmic_flops_per_launch"] = k_flops
+    roof["kernel_ms"] = k_ms
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8xfp4 (fp32 accumulate)", "data": "synthetic",
-            "config": dict(workload_config(w), parallelism=f"{world} independent replicas" if world > 1 else "1 GPU"),
+            "config": dict(workload_config(w), parallelism=f"{world} independent replicas" if world > 1 else "1 GPU",
+                           gemm_schedule=args.schedule),
             "tflops": alg["flops"] * world / (ms / 1e3) / 1e12,
             "hbm_gbs_whole_step": (alg["l1_bytes"] + alg["l2_bytes"]) / (ms / 1e3) / 1e9,
             "kernels_ms": kern,
@@ -380,6 +386,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
+    ap.add_argument("--schedule", default="fused", choices=["fused", "split"],
+                    help="both GEMMs in one persistent launch (default) or one launch per linear")
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (smaller cases for profiler captures; not a bench line)")
     ap.add_argument("--tokens", type=int, default=None,

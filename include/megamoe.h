@@ -66,8 +66,8 @@ typedef enum {
 /* With MM_DEV_TIMEOUT, bits 8..23 name the wait that expired (diagnostic):
  * bit 8 + s for the L1 GEMM and 16 + s for the L2 GEMM, s = 0 stage free,
  * 1 accumulator free, 2 stage loaded, 3 accumulator ready, 4 copy drain,
- * 5 stage free (scale-factor writer);
- * bit 15 for mm_debug_timeout_probe. */
+ * 5 stage free (scale-factor writer), 6 (L2 tiles of the fused schedule) token
+ * rows stored by the L1 epilogues; bit 15 for mm_debug_timeout_probe. */
 
 /* Human-readable name of a status code (static string). */
 MM_API const char* mm_status_string(mm_status_t s);
@@ -88,6 +88,15 @@ MM_API mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, in
  * [-c, c] before the SiLU, <= 0 disables the clamp; fast_math != 0 uses the
  * fast approximate exponential (__expf) in the SiLU. Defaults: no clamp, accurate exp. */
 MM_API mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_math);
+
+/* GEMM schedule ("MegaMoE research report" sec. 4.1, the Linear1 -> Linear2
+ * hand-off through per-row arrival flags). fused != 0 (the default) runs both
+ * grouped GEMMs in one persistent launch: every L1 tile, then every L2 tile,
+ * an L2 tile starting once the L1 epilogues of its token rows have stored
+ * them, so the weight stream of L2 follows that of L1 without a drain between
+ * them. fused == 0 launches one kernel per linear. The results are identical
+ * (the same tiles compute the same sums); only the timing differs. */
+MM_API mm_status_t mm_set_schedule(mm_handle_t h, int fused);
 
 /* Bytes of device workspace mm_run needs for T tokens (T >= 0). The
  * workspace holds the routing tables, the gathered FP8 L1 operand, the FP8 L2
@@ -156,11 +165,14 @@ MM_API mm_status_t mm_debug_timeout_probe(void* ws, uint64_t timeout_ns, mm_stre
 /* Per-launch timing for measurement: with profiling on, mm_run records a CUDA
  * event on its stream before each launch and after the last one. mm_profile_last
  * waits for the last recorded event and writes up to n durations in
- * milliseconds (route, gather, L1 GEMM, L2 GEMM, combine) into ms, returning the
- * count in *written. Events are created on the handle's device and freed by
+ * milliseconds into ms, one per launch of the last profiled mm_run (route,
+ * gather, then "l1_gemm", "l2_gemm" or the fused "gemm", then combine),
+ * returning the count in *written; mm_profile_name(h, i) names the i-th
+ * (NULL past the end). Events are created on the handle's device and freed by
  * mm_destroy or mm_profile_enable(h, 0). */
 MM_API mm_status_t mm_profile_enable(mm_handle_t h, int on);
 MM_API mm_status_t mm_profile_last(mm_handle_t h, float* ms, int n, int* written);
+MM_API const char* mm_profile_name(mm_handle_t h, int i);
 
 /* Allocation-free variant of mm_run (the pages have no counterpart; this is a
  * convenience of this library). Some callers cannot allocate device memory

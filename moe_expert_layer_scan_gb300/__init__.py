@@ -23,9 +23,9 @@ MM_DEV_BAD_ROUTING = 0x1
 MM_DEV_TIMEOUT = 0x2
 STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_WORKSPACE_TOO_SMALL",
                 4: "MM_ERR_CUDA", 5: "MM_ERR_DEVICE_TIMEOUT", 6: "MM_ERR_BAD_ROUTING", 7: "MM_ERR_ALIGNMENT"}
-EXPORTS = ["mm_status_string", "mm_create", "mm_set_options", "mm_workspace_bytes", "mm_run", "mm_get_status",
-           "mm_launches_per_run", "mm_debug_views", "mm_debug_timeout_probe", "mm_profile_enable", "mm_profile_last",
-           "mm_run_noalloc", "mm_destroy"]
+EXPORTS = ["mm_status_string", "mm_create", "mm_set_options", "mm_set_schedule", "mm_workspace_bytes", "mm_run",
+           "mm_get_status", "mm_launches_per_run", "mm_debug_views", "mm_debug_timeout_probe", "mm_profile_enable",
+           "mm_profile_last", "mm_profile_name", "mm_run_noalloc", "mm_destroy"]
 
 
 class MMError(RuntimeError):
@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
         L.mm_status_string.restype = ctypes.c_char_p
         L.mm_create.argtypes = [ctypes.POINTER(p), i32, i32, i32, i32, i32]
         L.mm_set_options.argtypes = [p, ctypes.c_float, i32]
+        L.mm_set_schedule.argtypes = [p, i32]
         L.mm_workspace_bytes.argtypes = [p, i32, ctypes.POINTER(ctypes.c_size_t)]
         L.mm_run.argtypes = [p, i32] + [p] * 10 + [ctypes.c_size_t, p]
         L.mm_get_status.argtypes = [p, p, p, u32p]
@@ -68,11 +69,13 @@ def lib() -> ctypes.CDLL:
         L.mm_debug_timeout_probe.argtypes = [p, ctypes.c_uint64, p]
         L.mm_profile_enable.argtypes = [p, i32]
         L.mm_profile_last.argtypes = [p, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(ctypes.c_int)]
+        L.mm_profile_name.argtypes = [p, i32]
+        L.mm_profile_name.restype = ctypes.c_char_p
         L.mm_run_noalloc.argtypes = [p, i32] + [p] * 9 + [p]
         L.mm_destroy.argtypes = [p]
         L.mm_destroy.restype = None
         for n in EXPORTS:
-            if n not in ("mm_status_string", "mm_destroy"):
+            if n not in ("mm_status_string", "mm_profile_name", "mm_destroy"):
                 getattr(L, n).restype = i32
         _lib = L
     return _lib
@@ -92,6 +95,10 @@ def mm_create(E: int, H: int, I: int, topk: int, num_shared: int = 0) -> int:
 
 def mm_set_options(h: int, swiglu_clamp: float = 0.0, fast_math: bool = False) -> None:
     _check(lib().mm_set_options(h, float(swiglu_clamp), int(bool(fast_math))), "mm_set_options")
+
+
+def mm_set_schedule(h: int, fused: bool = True) -> None:
+    _check(lib().mm_set_schedule(h, int(bool(fused))), "mm_set_schedule")
 
 
 def mm_workspace_bytes(h: int, T: int) -> int:
@@ -140,11 +147,23 @@ def mm_profile_enable(h: int, on: bool = True) -> None:
 
 
 def mm_profile_last(h: int) -> list:
-    """Per-launch milliseconds of the last mm_run (route, gather, L1, L2, combine)."""
+    """Per-launch milliseconds of the last profiled mm_run, in launch order."""
     buf = (ctypes.c_float * 8)()
     n = ctypes.c_int()
     _check(lib().mm_profile_last(h, buf, 8, ctypes.byref(n)), "mm_profile_last")
     return [float(buf[i]) for i in range(n.value)]
+
+
+def mm_profile_name(h: int, i: int):
+    """Stage name of the i-th interval of the last profiled mm_run (None past the end)."""
+    r = lib().mm_profile_name(h, i)
+    return None if r is None else r.decode()
+
+
+def mm_profile_stages(h: int) -> dict:
+    """{stage name: milliseconds} of the last profiled mm_run."""
+    ms = mm_profile_last(h)
+    return {mm_profile_name(h, i): v for i, v in enumerate(ms)}
 
 
 def mm_destroy(h: int) -> None:
@@ -161,10 +180,11 @@ class MegaMoE:
     """One layer shape bound to a handle; owns a reusable device workspace."""
 
     def __init__(self, E: int, H: int, I: int, topk: int, num_shared: int = 0, swiglu_clamp: float = 0.0,
-                 fast_math: bool = False):
+                 fast_math: bool = False, fused: bool = True):
         self.E, self.H, self.I, self.topk, self.S = E, H, I, topk, num_shared
         self.h = mm_create(E, H, I, topk, num_shared)
         mm_set_options(self.h, swiglu_clamp, fast_math)
+        mm_set_schedule(self.h, fused)
         self.ws = None
 
     def workspace(self, T: int, device=None):

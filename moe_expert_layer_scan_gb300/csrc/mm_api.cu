@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/megamoe.h: argument checks,
-// workspace carving, TMA tensor-map encoding and the five launches of one
-// forward (route -> gather -> L1 GEMM -> L2 GEMM -> combine).
+// workspace carving, TMA tensor-map encoding and the launches of one forward
+// (route -> gather -> L1 GEMM -> L2 GEMM -> combine, the two GEMMs in one
+// persistent launch by default).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -26,10 +27,14 @@ struct mm_handle {
   const void* w2_key;
   CUtensorMap tm_w1;
   CUtensorMap tm_w2;
-  // optional per-launch events (route, gather, L1, L2, combine, end)
+  // GEMM schedule: both linears in one persistent launch
+  int fused;
+  // optional per-launch events (route, gather, L1, L2, combine, end) and the
+  // stage name of each recorded interval
   bool profile;
   int n_recorded;
   cudaEvent_t ev[6];
+  const char* ev_name[6];
 };
 
 namespace {
@@ -112,6 +117,7 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
     if (ms > 0) h->timeout_ns = (unsigned long long)ms * 1000000ull;
   }
   h->w1_key = h->w2_key = nullptr;
+  h->fused = 1;
   h->profile = false;
   h->n_recorded = 0;
   *out = h;
@@ -125,6 +131,12 @@ mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_math) {
   return MM_OK;
 }
 
+mm_status_t mm_set_schedule(mm_handle_t h, int fused) {
+  if (!h) return MM_ERR_INVALID_ARG;
+  h->fused = fused ? 1 : 0;
+  return MM_OK;
+}
+
 mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes) {
   if (!h || !bytes || T < 0) return MM_ERR_INVALID_ARG;
   *bytes = make_layout(h->E, h->S, h->H, h->I, h->k, T).total;
@@ -134,7 +146,7 @@ mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes) {
 mm_status_t mm_launches_per_run(mm_handle_t h, int T, int* launches) {
   if (!h || !launches || T < 0) return MM_ERR_INVALID_ARG;
   const int route = mm_route_launches(T * (h->k + h->S));
-  *launches = T == 0 ? route : route + 4;
+  *launches = T == 0 ? route : route + (h->fused ? 3 : 4);
   return MM_OK;
 }
 
@@ -174,6 +186,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ra.chunk_cnt = reinterpret_cast<int32_t*>(base + L.chunk_cnt);
   ra.chunk_base = reinterpret_cast<int32_t*>(base + L.chunk_base);
   ra.chunk_bad = reinterpret_cast<int32_t*>(base + L.chunk_bad);
+  ra.ready = reinterpret_cast<int32_t*>(base + L.ready);
   ra.status = reinterpret_cast<uint32_t*>(base + L.status);
   ra.T = T; ra.E = h->E; ra.k = h->k; ra.S = h->S;
   ra.bn_l1 = bn1; ra.bn_l2 = bn2;
@@ -182,14 +195,18 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ra.fb_l1 = (f1 + cs - 1) / cs;                         // tile-table entries: groups of cs weight tiles
   ra.fb_l2 = (f2 + cs - 1) / cs;
   int ev_i = 0;
-  auto mark = [&]() {
-    if (h->profile && ev_i < 6) cudaEventRecord(h->ev[ev_i++], (cudaStream_t)stream);
+  // an event before each launch (named for it) and one after the last
+  auto mark = [&](const char* next) {
+    if (h->profile && ev_i < 6) {
+      h->ev_name[ev_i] = next;
+      cudaEventRecord(h->ev[ev_i++], (cudaStream_t)stream);
+    }
   };
   h->n_recorded = 0;
-  mark();
+  mark("route");
   if (mm_launch_route(&ra, stream) != 0) return MM_ERR_CUDA;
   if (T == 0) {
-    mark();
+    mark(nullptr);
     h->n_recorded = ev_i;
     return MM_OK;
   }
@@ -202,7 +219,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ga.pool_x = base + L.pool_x;
   ga.pool_sf = base + L.pool_sf;
   ga.H = h->H; ga.Kp = Kp; ga.Ep = Ep;
-  mark();
+  mark("gather");
   if (mm_launch_gather(&ga, T * Kp, stream) != 0) return MM_ERR_CUDA;
 
   // Tensor maps: weights are cached per base pointer, activations live in the workspace.
@@ -235,8 +252,8 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g1.clamp = h->clamp; g1.fast_math = h->fast_math; g1.timeout_ns = h->timeout_ns;
   g1.w_sf_vec = aligned(w1_sf, 16) && (h->H / 32) % 16 == 0;
   g1.act_sf_vec = (h->H / 32) % 16 == 0;
-  mark();
-  if (mm_launch_gemm(1, variant, &h->tm_w1, &tm_x, &g1, h->num_sms, stream) != 0) return MM_ERR_CUDA;
+  g1.ready = reinterpret_cast<int32_t*>(base + L.ready);
+  g1.ready_target = f1 * mm_gemm_epilogue_warps(variant);
 
   GemmArgs g2 = g1;
   g2.w_sf = static_cast<const uint8_t*>(w2_sf);
@@ -249,17 +266,25 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g2.K = h->I; g2.rows_w = h->H; g2.fb_total = f2;
   g2.w_sf_vec = aligned(w2_sf, 16) && (h->I / 32) % 16 == 0;
   g2.act_sf_vec = (h->I / 32) % 16 == 0;
-  mark();
-  if (mm_launch_gemm(0, variant, &h->tm_w2, &tm_q, &g2, h->num_sms, stream) != 0) return MM_ERR_CUDA;
+  if (h->fused) {
+    mark("gemm");
+    if (mm_launch_gemm_fused(variant, &h->tm_w1, &tm_x, &h->tm_w2, &tm_q, &g1, &g2, stream) != 0)
+      return MM_ERR_CUDA;
+  } else {
+    mark("l1_gemm");
+    if (mm_launch_gemm(1, variant, &h->tm_w1, &tm_x, &g1, h->num_sms, stream) != 0) return MM_ERR_CUDA;
+    mark("l2_gemm");
+    if (mm_launch_gemm(0, variant, &h->tm_w2, &tm_q, &g2, h->num_sms, stream) != 0) return MM_ERR_CUDA;
+  }
 
   CombineArgs ca;
   ca.z = g2.out_z;
   ca.pos = ra.pos;
   ca.out = static_cast<uint16_t*>(out_bf16);
   ca.T = T; ca.H = h->H; ca.Kp = Kp;
-  mark();
+  mark("combine");
   if (mm_launch_combine(&ca, stream) != 0) return MM_ERR_CUDA;
-  mark();
+  mark(nullptr);
   h->n_recorded = ev_i;
   return MM_OK;
 }
@@ -288,6 +313,11 @@ mm_status_t mm_profile_last(mm_handle_t h, float* ms, int n, int* written) {
     if (cudaEventElapsedTime(&ms[k], h->ev[i], h->ev[i + 1]) != cudaSuccess) return MM_ERR_CUDA;
   *written = k;
   return MM_OK;
+}
+
+const char* mm_profile_name(mm_handle_t h, int i) {
+  if (!h || i < 0 || i + 1 >= h->n_recorded) return nullptr;
+  return h->ev_name[i];
 }
 
 mm_status_t mm_get_status(mm_handle_t h, const void* ws, mm_stream_t stream, uint32_t* device_status) {

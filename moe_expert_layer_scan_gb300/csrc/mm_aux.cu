@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(RouteArgs a) {
   __shared__ int bad_any;
   const int tid = threadIdx.x;
   if (tid == 0) bad_any = 0;
+  for (long i = tid; i <= R; i += blockDim.x) a.ready[i] = 0;
   const bool bad = warp_histograms(a, 0, R, hist);
   if (bad) bad_any = 1;
   int tot = 0;
@@ -182,6 +183,8 @@ __global__ void __launch_bounds__(1024) route_count_kernel(RouteArgs a) {
   const long c0 = (long)blockIdx.x * kRouteChunk, c1 = (c0 + kRouteChunk < R) ? c0 + kRouteChunk : R;
   if (threadIdx.x == 0) bad_any = 0;
   for (int i = threadIdx.x; i < Ep; i += blockDim.x) hist[i] = 0;
+  for (long i = c0 + threadIdx.x; i < c1; i += blockDim.x) a.ready[i] = 0;
+  if (blockIdx.x == 0 && threadIdx.x == 0) a.ready[R] = 0;
   __syncthreads();
   bool bad = false;
   for (long s = c0 + threadIdx.x; s < c1; s += blockDim.x) {

@@ -25,6 +25,14 @@
 // Pipelines: STAGES shared-memory stages (full/empty mbarriers) and two TMEM
 // accumulator buffers (tmem_full/tmem_empty) so the epilogue of one tile
 // overlaps the main loop of the next. Every wait is bounded.
+//
+// Modes: one launch per linear (L1, L2), or both in one persistent launch
+// (fused, the arrival-mask scheme of the research report's Linear1 -> Linear2
+// hand-off): the tile list is every L1 tile followed by every L2 tile; each L1
+// epilogue warp publishes its stores and counts itself on its token tile's
+// arrival counter, and the loads of an L2 tile start once that counter is
+// complete. Every CTA finishes its own L1 tiles before its first L2 tile and
+// the persistent grid is co-resident, so the waits always end.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -43,7 +51,9 @@ struct Warps {
   static constexpr int THREADS = 32 * (4 + EPI);  // producer, 2 issuers/allocator, scale warp, epilogue
 };
 
-template <bool kL1, int BN, int STAGES, int CS>
+enum : int { kModeL2 = 0, kModeL1 = 1, kModeFused = 2 };
+
+template <int BN, int STAGES, int CS>
 struct GemmCfg {
   static constexpr int BM = 128;                         // weight rows per MMA
   static constexpr int BK = 128;                         // K per stage
@@ -108,28 +118,26 @@ __device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a, int bn,
 }
 
 // First weight row of a tile's first 128-row block, the offset of its second
-// block, and whether the second block exists.
-template <bool kL1>
-__device__ __forceinline__ int tile_wrow(const Tile& t, const GemmArgs& a) {
-  return t.e * a.rows_w + t.fb * (kL1 ? 128 : 256);
+// block, and whether the second block exists (l1: gate/up pair; else two W2 blocks).
+__device__ __forceinline__ int tile_wrow(bool l1, const Tile& t, const GemmArgs& a) {
+  return t.e * a.rows_w + t.fb * (l1 ? 128 : 256);
 }
-template <bool kL1>
-__device__ __forceinline__ int second_off(const GemmArgs& a) {
-  return kL1 ? a.I : 128;
-}
-template <bool kL1>
-__device__ __forceinline__ bool has_second(const Tile& t, const GemmArgs& a) {
-  return t.active && (kL1 || t.fb * 256 + 128 < a.rows_w);
+__device__ __forceinline__ int second_off(bool l1, const GemmArgs& a) { return l1 ? a.I : 128; }
+__device__ __forceinline__ bool has_second(bool l1, const Tile& t, const GemmArgs& a) {
+  return t.active && (l1 || t.fb * 256 + 128 < a.rows_w);
 }
 
 // Four K steps of one row's UE8M0 scales (16 bytes); `avail` steps exist.
-__device__ __forceinline__ uint4 load_sf4(const uint8_t* p, bool vec16, int avail) {
-  if (vec16) return __ldg(reinterpret_cast<const uint4*>(p));
+// fresh: the bytes were written by other CTAs during this launch, so the load
+// bypasses L1 (ld.global.cg) instead of using the read-only path.
+__device__ __forceinline__ uint4 load_sf4(const uint8_t* p, bool vec16, int avail, bool fresh) {
+  if (vec16) return fresh ? __ldcg(reinterpret_cast<const uint4*>(p)) : __ldg(reinterpret_cast<const uint4*>(p));
   const uint32_t* q = reinterpret_cast<const uint32_t*>(p);
-  uint4 r = make_uint4(__ldg(q), 0u, 0u, 0u);
-  if (avail > 1) r.y = __ldg(q + 1);
-  if (avail > 2) r.z = __ldg(q + 2);
-  if (avail > 3) r.w = __ldg(q + 3);
+  auto ld = [fresh](const uint32_t* x) { return fresh ? __ldcg(x) : __ldg(x); };
+  uint4 r = make_uint4(ld(q), 0u, 0u, 0u);
+  if (avail > 1) r.y = ld(q + 1);
+  if (avail > 2) r.z = ld(q + 2);
+  if (avail > 3) r.w = ld(q + 3);
   return r;
 }
 
@@ -159,11 +167,12 @@ __device__ __forceinline__ float inv_scale(uint32_t code) {
   return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(1u << (n + 149));
 }
 
-template <bool kL1, int BN, int STAGES, int CS>
+template <int MODE, int BN, int STAGES, int CS>
 __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_act,
-                const GemmArgs a) {
-  using C = GemmCfg<kL1, BN, STAGES, CS>;
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_a1,
+                const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_a2,
+                const __grid_constant__ GemmArgs g1, const __grid_constant__ GemmArgs g2) {
+  using C = GemmCfg<BN, STAGES, CS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -187,8 +196,14 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_w);
-    prefetch_tmap(&tm_act);
+    if (MODE != kModeL2) {
+      prefetch_tmap(&tm_w1);
+      prefetch_tmap(&tm_a1);
+    }
+    if (MODE != kModeL1) {
+      prefetch_tmap(&tm_w2);
+      prefetch_tmap(&tm_a2);
+    }
   }
   if (warp == 2) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -202,49 +217,62 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
   pdl_trigger();
   pdl_wait();
   const uint32_t tmem = *tmem_slot;
-  const int num_tiles = a.tile_start[a.Ep];
+  // tiles [0, n1) are L1 tiles, [n1, num_tiles) L2 tiles
+  const int n1 = MODE == kModeL2 ? 0 : g1.tile_start[g1.Ep];
+  const int num_tiles = MODE == kModeL1 ? n1 : n1 + g2.tile_start[g2.Ep];
+  auto is_l1 = [&](int tile) { return MODE == kModeL1 || (MODE == kModeFused && tile < n1); };
   const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
   const int tile0 = blockIdx.x / CS, tile_step = gridDim.x / CS;
   constexpr uint16_t kAllCtas = (uint16_t)((1u << CS) - 1u);
-  // wait sites reported in the status word on expiry (L2 kernel: +8)
-  const uint32_t site0 = kL1 ? 0u : 8u;
-  const int kblocks = a.K / C::BK;
-  const int sf_ld = a.K / 32;
+  // wait sites reported in the status word on expiry: L1 tiles s, L2 tiles 8 + s
+  constexpr uint32_t kSiteReady = 8u + 6u;  // an L2 tile waiting for its L1 rows (fused)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     uint32_t it = 0;
     bool ok = true;
     for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
-      const Tile t = decode_tile(tile, a, BN, rank, CS);
-      const int wrow = tile_wrow<kL1>(t, a);
-      const bool two = has_second<kL1>(t, a);
+      const bool l1 = is_l1(tile);
+      const GemmArgs& g = l1 ? g1 : g2;
+      const uint32_t site0 = l1 ? 0u : 8u;
+      const Tile t = decode_tile(l1 ? tile : tile - n1, g, BN, rank, CS);
+      const int wrow = tile_wrow(l1, t, g);
+      const bool two = has_second(l1, t, g);
+      const int kblocks = g.K / C::BK;
+      const CUtensorMap* tw = l1 ? &tm_w1 : &tm_w2;
+      const CUtensorMap* ta = l1 ? &tm_a1 : &tm_a2;
+      if (MODE == kModeFused && !l1 &&
+          !wait_counter(g1.ready + t.row0, g1.ready_target, abort_flag, g.status, g.timeout_ns, kSiteReady)) {
+        ok = false;
+        break;
+      }
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
         const int s = (int)(it % STAGES);
         const uint32_t ph = (it / STAGES) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status, a.timeout_ns, site0 + 0)) { ok = false; break; }
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g.status, g.timeout_ns, site0 + 0)) { ok = false; break; }
         uint8_t* sA = smem + C::A_OFF + s * C::NA * C::A_BYTES;
         uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
-        uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
         if (lane == 0) {
           // the whole token tile lands here: this CTA's share and the others' multicasts
           mbar_arrive_expect_tx(&full[s], (t.active ? (two ? 2 : 1) : 0) * C::A_TX + C::B_BYTES);
-          if (t.active) tma_load_2d(sA, &tm_w, &full[s], kb * C::BK, wrow);
-          if (two) tma_load_2d(sA + C::A_BYTES, &tm_w, &full[s], kb * C::BK, wrow + second_off<kL1>(a));
+          if (t.active) tma_load_2d(sA, tw, &full[s], kb * C::BK, wrow);
+          if (two) tma_load_2d(sA + C::A_BYTES, tw, &full[s], kb * C::BK, wrow + second_off(l1, g));
           if constexpr (CS == 1) {
-            tma_load_2d(sB, &tm_act, &full[s], kb * C::BK, t.row0);
+            tma_load_2d(sB, ta, &full[s], kb * C::BK, t.row0);
           } else {
-            tma_load_2d_multicast(sB + rank * C::B_PART_ROWS * C::BK, &tm_act, &full[s], kb * C::BK,
+            tma_load_2d_multicast(sB + rank * C::B_PART_ROWS * C::BK, ta, &full[s], kb * C::BK,
                                   t.row0 + rank * C::B_PART_ROWS, kAllCtas);
           }
         }
       }
     }
+    const GemmArgs& gl = MODE == kModeL1 ? g1 : g2;  // status word and limit (shared by both)
+    constexpr uint32_t kSiteTail = (MODE == kModeL1 ? 0u : 8u) + 4u;
     if (ok && CS > 1) {
       // Producer tail: wait until every CTA has released the last stages, so
       // that no remote tcgen05.commit arrival targets this CTA after it exits.
       for (uint32_t j = (it > (uint32_t)STAGES ? it - STAGES : 0u); j < it; ++j)
-        if (!mbar_wait(&empty[j % STAGES], (j / STAGES) & 1u, abort_flag, a.status, a.timeout_ns, site0 + 4)) break;
+        if (!mbar_wait(&empty[j % STAGES], (j / STAGES) & 1u, abort_flag, gl.status, gl.timeout_ns, kSiteTail)) break;
     }
     if (!ok) {
       // Let the copies already issued land before the CTA can exit (the
@@ -253,8 +281,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       const uint32_t issued = it;
       for (uint32_t j = (issued > (uint32_t)STAGES ? issued - STAGES : 0u); j < issued; ++j) {
         int dummy = 0;
-        mbar_wait(&full[j % STAGES], (j / STAGES) & 1u, reinterpret_cast<volatile int*>(&dummy), a.status,
-                  a.timeout_ns < 10000000ull ? a.timeout_ns : 10000000ull, site0 + 4);
+        mbar_wait(&full[j % STAGES], (j / STAGES) & 1u, reinterpret_cast<volatile int*>(&dummy), gl.status,
+                  gl.timeout_ns < 10000000ull ? gl.timeout_ns : 10000000ull, kSiteTail);
       }
     }
   } else if (warp == 3) {
@@ -267,13 +295,24 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     uint32_t it = 0;
     bool ok = true;
     for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
-      const Tile t = decode_tile(tile, a, BN, rank, CS);
-      const int wrow = tile_wrow<kL1>(t, a);
-      const bool two = has_second<kL1>(t, a);
+      const bool l1 = is_l1(tile);
+      const GemmArgs& g = l1 ? g1 : g2;
+      const uint32_t site0 = l1 ? 0u : 8u;
+      const Tile t = decode_tile(l1 ? tile : tile - n1, g, BN, rank, CS);
+      const int wrow = tile_wrow(l1, t, g);
+      const bool two = has_second(l1, t, g);
       const int nb = (t.nrows + 31) / 32;
-      for (int g = 0; g < kblocks && ok; g += 4) {
-        const int avail = kblocks - g;
-        const bool wvec = a.w_sf_vec && avail >= 4, bvec = a.act_sf_vec && avail >= 4;
+      const int kblocks = g.K / C::BK;
+      const int sf_ld = g.K / 32;
+      const bool fresh = MODE == kModeFused && !l1;  // token scales written by this launch's L1 tiles
+      if (fresh && !wait_counter(g1.ready + t.row0, g1.ready_target, abort_flag, g.status, g.timeout_ns,
+                                 kSiteReady)) {
+        ok = false;
+        break;
+      }
+      for (int kg = 0; kg < kblocks && ok; kg += 4) {
+        const int avail = kblocks - kg;
+        const bool wvec = g.w_sf_vec && avail >= 4, bvec = g.act_sf_vec && avail >= 4;
         uint4 wa[C::NA][4];
         uint4 wb[NB];
 #pragma unroll
@@ -281,19 +320,19 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             wa[op][i] = ((op == 0 && t.active) || two)
-                            ? load_sf4(a.w_sf + (size_t)(wrow + op * second_off<kL1>(a) + 32 * i + lane) * sf_ld + 4 * g,
-                                       wvec, avail)
+                            ? load_sf4(g.w_sf + (size_t)(wrow + op * second_off(l1, g) + 32 * i + lane) * sf_ld + 4 * kg,
+                                       wvec, avail, false)
                             : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int j = 0; j < NB; ++j)
-          wb[j] = j < nb ? load_sf4(a.act_sf + (size_t)(t.row0 + 32 * j + lane) * sf_ld + 4 * g, bvec, avail)
+          wb[j] = j < nb ? load_sf4(g.act_sf + (size_t)(t.row0 + 32 * j + lane) * sf_ld + 4 * kg, bvec, avail, fresh)
                          : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if (c >= avail) break;
           const int s = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, a.status, a.timeout_ns, site0 + 5)) { ok = false; break; }
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g.status, g.timeout_ns, site0 + 5)) { ok = false; break; }
           uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
 #pragma unroll
           for (int op = 0; op < C::NA; ++op)
@@ -320,18 +359,22 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       uint32_t it = 0, tcount = 0;
       bool ok = true;
       for (int tile = tile0; tile < num_tiles && ok; tile += tile_step, ++tcount) {
-        const Tile t = decode_tile(tile, a, BN, rank, CS);
+        const bool l1 = is_l1(tile);
+        const GemmArgs& g = l1 ? g1 : g2;
+        const uint32_t site0 = l1 ? 0u : 8u;
+        const Tile t = decode_tile(l1 ? tile : tile - n1, g, BN, rank, CS);
+        const int kblocks = g.K / C::BK;
         const int buf = (int)(tcount & 1u);
         const uint32_t bph = (tcount >> 1) & 1u;
-        if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, a.status, a.timeout_ns, site0 + 1)) break;
+        if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, g.status, g.timeout_ns, site0 + 1)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * C::ACC_COLS + u * BN);
         const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
-        const bool active = u == 0 ? t.active : has_second<kL1>(t, a);
+        const bool active = u == 0 ? t.active : has_second(l1, t, g);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&full[s], ph, abort_flag, a.status, a.timeout_ns, site0 + 2)) { ok = false; break; }
+          if (!mbar_wait(&full[s], ph, abort_flag, g.status, g.timeout_ns, site0 + 2)) { ok = false; break; }
           tc_fence_after();
           const uint8_t* sA = smem + C::A_OFF + (s * C::NA + u) * C::A_BYTES;
           const uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
@@ -341,8 +384,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
             const uint32_t sfb = sfa + 4u;
             tc_cp_32x128b_warpx4(sfa, sdesc_sf_32x16(smem_u32(sF + u * 512)));
 #pragma unroll
-            for (int g = 0; g < C::SFB_ROWS / 128; ++g)
-              tc_cp_32x128b_warpx4(sfb + 4u * g, sdesc_sf_32x16(smem_u32(sF + C::NA * 512 + g * 512)));
+            for (int gq = 0; gq < C::SFB_ROWS / 128; ++gq)
+              tc_cp_32x128b_warpx4(sfb + 4u * gq, sdesc_sf_32x16(smem_u32(sF + C::NA * 512 + gq * 512)));
             const uint64_t da = sdesc_kmajor_sw128(smem_u32(sA));
             const uint64_t db = sdesc_kmajor_sw128(smem_u32(sB));
 #pragma unroll
@@ -369,16 +412,18 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     const int half = (warp - 4) >> 2;  // 0 when there is one warp per quadrant
     uint32_t tcount = 0;
     for (int tile = tile0; tile < num_tiles; tile += tile_step, ++tcount) {
-      const Tile t = decode_tile(tile, a, BN, rank, CS);
+      const bool l1 = is_l1(tile);
+      const GemmArgs& g = l1 ? g1 : g2;
+      const uint32_t site0 = l1 ? 0u : 8u;
+      const Tile t = decode_tile(l1 ? tile : tile - n1, g, BN, rank, CS);
       const int buf = (int)(tcount & 1u);
       const uint32_t bph = (tcount >> 1) & 1u;
-      if (!mbar_wait(&tfull[buf], bph, abort_flag, a.status, a.timeout_ns, site0 + 3, 256)) break;
+      if (!mbar_wait(&tfull[buf], bph, abort_flag, g.status, g.timeout_ns, site0 + 3, 256)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::ACC_COLS);
       // L1: intermediate column of the gate/up pair; L2: hidden column of block 0 (block 1: +128)
-      const int feat = t.fb * (kL1 ? 128 : 256) + 32 * q + lane;
-      const bool two = has_second<kL1>(t, a);
-      if constexpr (kL1) {
+      const int feat = t.fb * (l1 ? 128 : 256) + 32 * q + lane;
+      if (MODE != kModeL2 && l1) {
         // The per-column amax over the warp's 32 features (one UE8M0 group) is
         // a transpose-reduction: after the exchange steps lane c (32 columns)
         // or lanes 2c, 2c+1 (16 columns) hold the maximum of column c, compute
@@ -388,29 +433,29 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
         constexpr int LOG2NC = NC == 32 ? 5 : 4;
         for (int c0 = NC * half; t.active && c0 < t.nrows; c0 += NC * (Warps<BN>::EPI / 4)) {
           const int ncol = min(NC, t.nrows - c0);
-          uint32_t g0[16], g1[16], u0[16], u1[16];
-          tmem_ld_x16(tbase + (uint32_t)c0, g0);
+          uint32_t gt0[16], gt1[16], u0[16], u1[16];
+          tmem_ld_x16(tbase + (uint32_t)c0, gt0);
           tmem_ld_x16(tbase + (uint32_t)(BN + c0), u0);
           if (NC == 32 && ncol > 16) {
-            tmem_ld_x16(tbase + (uint32_t)(c0 + 16), g1);
+            tmem_ld_x16(tbase + (uint32_t)(c0 + 16), gt1);
             tmem_ld_x16(tbase + (uint32_t)(BN + c0 + 16), u1);
           } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) g1[j] = u1[j] = 0u;
+            for (int j = 0; j < 16; ++j) gt1[j] = u1[j] = 0u;
           }
           tmem_ld_wait();
-          const float wl = lane < ncol ? a.row_w[t.row0 + c0 + lane] : 0.0f;
+          const float wl = lane < ncol ? g1.row_w[t.row0 + c0 + lane] : 0.0f;
           float y[NC], v[NC];
 #pragma unroll
           for (int j = 0; j < NC; ++j) {
             const float wj = __shfl_sync(0xffffffffu, wl, j);
-            float gv = __uint_as_float(j < 16 ? g0[j] : g1[j - 16]);
+            float gv = __uint_as_float(j < 16 ? gt0[j] : gt1[j - 16]);
             float uv = __uint_as_float(j < 16 ? u0[j] : u1[j - 16]);
-            if (a.clamp > 0.0f) {
-              gv = fminf(fmaxf(gv, -a.clamp), a.clamp);
-              uv = fminf(fmaxf(uv, -a.clamp), a.clamp);
+            if (g1.clamp > 0.0f) {
+              gv = fminf(fmaxf(gv, -g1.clamp), g1.clamp);
+              uv = fminf(fmaxf(uv, -g1.clamp), g1.clamp);
             }
-            const float ex = a.fast_math ? __expf(-gv) : expf(-gv);
+            const float ex = g1.fast_math ? __expf(-gv) : expf(-gv);
             const float silu = __fdiv_rn(gv, __fadd_rn(1.0f, ex));
             y[j] = j < ncol ? __fmul_rn(__fmul_rn(silu, uv), wj) : 0.0f;
             v[j] = fabsf(y[j]);
@@ -431,27 +476,30 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
           const uint32_t code = requant_code(v[0]);  // column c0 + mycol
           const float inv = inv_scale(code);
           if ((lane & ((1 << (5 - LOG2NC)) - 1)) == 0 && mycol < ncol)
-            a.out_sf[(size_t)(t.row0 + c0 + mycol) * (a.I / 32) + t.fb * 4 + q] = (uint8_t)code;
+            g1.out_sf[(size_t)(t.row0 + c0 + mycol) * (g1.I / 32) + t.fb * 4 + q] = (uint8_t)code;
 #pragma unroll
           for (int j = 0; j < NC; ++j) {
             const float ij = __shfl_sync(0xffffffffu, inv, j << (5 - LOG2NC));
             const uint8_t qb = (uint8_t)__nv_cvt_float_to_fp8(__fmul_rn(y[j], ij), __NV_SATFINITE, __NV_E4M3);
-            if (j < ncol) a.out_q[(size_t)(t.row0 + c0 + j) * a.I + feat] = qb;
+            if (j < ncol) g1.out_q[(size_t)(t.row0 + c0 + j) * g1.I + feat] = qb;
           }
         }
-      } else {
+        // fused: this warp's share of the token tile's L2 operand is stored
+        if (MODE == kModeFused && t.active) warp_signal(g1.ready + t.row0);
+      } else if (MODE != kModeL1) {
+        const bool two = has_second(false, t, g2);
         for (int c0 = 16 * half; t.active && c0 < t.nrows; c0 += 16 * (Warps<BN>::EPI / 4)) {
-          uint32_t g[16], h[16];
-          tmem_ld_x16(tbase + (uint32_t)c0, g);
-          tmem_ld_x16(tbase + (uint32_t)(BN + c0), h);
+          uint32_t gv[16], hv[16];
+          tmem_ld_x16(tbase + (uint32_t)c0, gv);
+          tmem_ld_x16(tbase + (uint32_t)(BN + c0), hv);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;
             if (col < t.nrows) {
-              uint16_t* zr = a.out_z + (size_t)(t.row0 + col) * a.H;
-              zr[feat] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(g[j])));
-              if (two) zr[feat + 128] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(h[j])));
+              uint16_t* zr = g2.out_z + (size_t)(t.row0 + col) * g2.H;
+              zr[feat] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(gv[j])));
+              if (two) zr[feat + 128] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(hv[j])));
             }
           }
         }
@@ -472,10 +520,10 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
   }
 }
 
-template <bool kL1, int BN, int STAGES, int CS>
+template <int MODE, int BN, int STAGES, int CS>
 static int set_smem_attr(int* max_ctas) {
-  using C = GemmCfg<kL1, BN, STAGES, CS>;
-  auto k = gemm_kernel<kL1, BN, STAGES, CS>;
+  using C = GemmCfg<BN, STAGES, CS>;
+  auto k = gemm_kernel<MODE, BN, STAGES, CS>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return (int)e;
   int dev = 0, sms = 0;
@@ -503,44 +551,68 @@ static int set_smem_attr(int* max_ctas) {
   return 0;
 }
 
-template <bool kL1, int BN, int STAGES, int CS>
-static int launch(const void* tw, const void* ta, const GemmArgs* a, int num_ctas, cudaStream_t st) {
-  using C = GemmCfg<kL1, BN, STAGES, CS>;
-  return (int)launch_kernel(gemm_kernel<kL1, BN, STAGES, CS>, dim3((unsigned)num_ctas), dim3(Warps<BN>::THREADS),
-                            C::SMEM_BYTES, st, true, CS, *static_cast<const CUtensorMap*>(tw),
-                            *static_cast<const CUtensorMap*>(ta), *a);
+template <int MODE, int BN, int STAGES, int CS>
+static int launch(const void* tw1, const void* ta1, const void* tw2, const void* ta2, const GemmArgs* g1,
+                  const GemmArgs* g2, int num_ctas, cudaStream_t st) {
+  using C = GemmCfg<BN, STAGES, CS>;
+  auto tm = [](const void* p) { return *static_cast<const CUtensorMap*>(p); };
+  return (int)launch_kernel(gemm_kernel<MODE, BN, STAGES, CS>, dim3((unsigned)num_ctas), dim3(Warps<BN>::THREADS),
+                            C::SMEM_BYTES, st, true, CS, tm(tw1), tm(ta1), tm(tw2), tm(ta2), *g1, *g2);
 }
 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
 // five, measured as fast as six).
-constexpr int kStagesL1Small = 5, kStagesL2Small = 5, kStagesL1Large = 4, kStagesL2Large = 4;
-// CTAs per launch of each instantiation: [l1][variant]
-static int g_ctas[2][2];
+constexpr int kStagesSmall = 5, kStagesLarge = 4;
+// CTAs per launch of each instantiation: [mode][variant]
+static int g_ctas[3][2];
 
 }  // namespace mm
 
 extern "C" int mm_gemm_prepare(void) {
   using namespace mm;
   int e = 0;
-  if ((e = set_smem_attr<true, kBnSmall, kStagesL1Small, 1>(&g_ctas[1][0]))) return e;
-  if ((e = set_smem_attr<false, kBnSmall, kStagesL2Small, 1>(&g_ctas[0][0]))) return e;
-  if ((e = set_smem_attr<true, kBnLarge, kStagesL1Large, kClusterLarge>(&g_ctas[1][1]))) return e;
-  if ((e = set_smem_attr<false, kBnLarge, kStagesL2Large, kClusterLarge>(&g_ctas[0][1]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesSmall, 1>(&g_ctas[kModeL1][0]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesSmall, 1>(&g_ctas[kModeL2][0]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesSmall, 1>(&g_ctas[kModeFused][0]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(&g_ctas[kModeL1][1]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(&g_ctas[kModeL2][1]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(&g_ctas[kModeFused][1]))) return e;
   return 0;
 }
 
 extern "C" int mm_gemm_cluster(int variant) { return variant == 0 ? 1 : mm::kClusterLarge; }
+
+extern "C" int mm_gemm_epilogue_warps(int variant) {
+  return variant == 0 ? mm::Warps<mm::kBnSmall>::EPI : mm::Warps<mm::kBnLarge>::EPI;
+}
 
 extern "C" int mm_launch_gemm(int l1, int variant, const void* tmap_w, const void* tmap_act, const mm::GemmArgs* a,
                               int num_ctas, void* stream) {
   using namespace mm;
   (void)num_ctas;
   cudaStream_t st = (cudaStream_t)stream;
-  const int n = g_ctas[l1 ? 1 : 0][variant];
+  const int mode = l1 ? kModeL1 : kModeL2;
+  const int n = g_ctas[mode][variant];
   if (l1) {
-    return variant == 0 ? launch<true, kBnSmall, kStagesL1Small, 1>(tmap_w, tmap_act, a, n, st)
-                        : launch<true, kBnLarge, kStagesL1Large, kClusterLarge>(tmap_w, tmap_act, a, n, st);
+    return variant == 0
+               ? launch<kModeL1, kBnSmall, kStagesSmall, 1>(tmap_w, tmap_act, tmap_w, tmap_act, a, a, n, st)
+               : launch<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(tmap_w, tmap_act, tmap_w, tmap_act, a, a, n,
+                                                                        st);
   }
-  return variant == 0 ? launch<false, kBnSmall, kStagesL2Small, 1>(tmap_w, tmap_act, a, n, st)
-                      : launch<false, kBnLarge, kStagesL2Large, kClusterLarge>(tmap_w, tmap_act, a, n, st);
+  return variant == 0
+             ? launch<kModeL2, kBnSmall, kStagesSmall, 1>(tmap_w, tmap_act, tmap_w, tmap_act, a, a, n, st)
+             : launch<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(tmap_w, tmap_act, tmap_w, tmap_act, a, a, n,
+                                                                      st);
+}
+
+extern "C" int mm_launch_gemm_fused(int variant, const void* tmap_w1, const void* tmap_x, const void* tmap_w2,
+                                    const void* tmap_q, const mm::GemmArgs* g1, const mm::GemmArgs* g2,
+                                    void* stream) {
+  using namespace mm;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int n = g_ctas[kModeFused][variant];
+  return variant == 0 ? launch<kModeFused, kBnSmall, kStagesSmall, 1>(tmap_w1, tmap_x, tmap_w2, tmap_q, g1, g2, n,
+                                                                       st)
+                      : launch<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(tmap_w1, tmap_x, tmap_w2, tmap_q,
+                                                                                  g1, g2, n, st);
 }

@@ -31,7 +31,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Byte offsets of every workspace region for one (shape, T).
 struct Layout {
-  size_t status, counts, offsets, tiles_l1, tiles_l2, perm, pos, row_w, chunk_cnt, chunk_base, chunk_bad;
+  size_t status, counts, offsets, tiles_l1, tiles_l2, perm, pos, row_w, chunk_cnt, chunk_base, chunk_bad, ready;
   size_t pool_x, pool_sf, l2a, l2a_sf, z, total;
   int rows_cap;
 };
@@ -55,6 +55,7 @@ inline Layout make_layout(int E, int S, int H, int I, int k, int T) {
   L.chunk_cnt = take(sizeof(int32_t) * G * Ep, 256);
   L.chunk_base = take(sizeof(int32_t) * G * Ep, 256);
   L.chunk_bad = take(sizeof(int32_t) * G, 256);
+  L.ready = take(sizeof(int32_t) * (R + 1), 256);
   L.pool_x = take((size_t)L.rows_cap * H, 1024);
   L.pool_sf = take((size_t)L.rows_cap * (H / 32), 1024);
   L.l2a = take((size_t)L.rows_cap * I, 1024);
@@ -78,6 +79,7 @@ struct RouteArgs {
   int32_t* chunk_cnt;   // [G][E+S] per-chunk expert counts (multi-CTA routing)
   int32_t* chunk_base;  // [G][E+S] first pool row of each chunk's slots per expert
   int32_t* chunk_bad;   // [G] out-of-range ids seen in the chunk
+  int32_t* ready;       // [R + 1] arrival counters of the fused GEMM, zeroed here
   int T, E, k, S;
   int bn_l1, bn_l2;  // token-tile widths of the two GEMMs
   int fb_l1, fb_l2;  // weight tiles per expert: I/128 (gate/up pairs) and ceil(H/256)
@@ -109,6 +111,11 @@ struct GemmArgs {
   int fast_math;
   int w_sf_vec, act_sf_vec;  // scale rows allow 16-byte loads (16-byte aligned base and row stride)
   unsigned long long timeout_ns;
+  // Fused L1 -> L2 launch: ready[row0] counts the L1 epilogue warps that have
+  // stored their part of the token tile starting at pool row row0; the L2
+  // tiles of that token tile wait for ready_target arrivals.
+  int32_t* ready;
+  int ready_target;
 };
 
 struct CombineArgs {
@@ -129,7 +136,13 @@ int mm_launch_combine(const mm::CombineArgs* a, void* stream);
 // variant: 0 = small tiles, 1 = large tiles. tmaps: two 128-byte CUtensorMap blobs (weights, activations).
 int mm_launch_gemm(int l1, int variant, const void* tmap_w, const void* tmap_act, const mm::GemmArgs* a,
                    int num_ctas, void* stream);
+// One persistent launch of both GEMMs: every L1 tile, then every L2 tile; an L2
+// tile starts once the L1 epilogues of its token tile have arrived on `ready`.
+// tmaps: W1, pool_x, W2, l2a.
+int mm_launch_gemm_fused(int variant, const void* tmap_w1, const void* tmap_x, const void* tmap_w2,
+                         const void* tmap_q, const mm::GemmArgs* g1, const mm::GemmArgs* g2, void* stream);
 int mm_gemm_prepare(void);  // sets the dynamic shared-memory limits and the persistent grid sizes
 int mm_gemm_cluster(int variant);  // CTAs per cluster of the variant
+int mm_gemm_epilogue_warps(int variant);  // epilogue warps per CTA (arrivals per L1 tile in the fused schedule)
 int mm_launch_timeout_probe(uint32_t* status, unsigned long long timeout_ns, void* stream);
 }

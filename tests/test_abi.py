@@ -59,3 +59,12 @@ def test_null_handle_calls_are_rejected(lib):
     assert lib.mm_set_options(None, 1.0, 0) == 1
     assert lib.mm_run(None, 1, *([None] * 10), 0, None) == 1
     lib.mm_destroy(None)
+
+
+def test_binding_return_types():
+    """Functions returning strings or nothing are not read back as status codes."""
+    L = mm.lib()
+    assert L.mm_status_string.restype is ctypes.c_char_p
+    assert L.mm_profile_name.restype is ctypes.c_char_p
+    assert L.mm_destroy.restype is None
+    assert L.mm_run.restype is ctypes.c_int

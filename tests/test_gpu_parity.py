@@ -53,12 +53,13 @@ def check_routing(inter, ref, n):
     assert np.array_equal(inter["pos"], ref["pos"])
 
 
+@pytest.mark.parametrize("schedule", ["fused", "split"])
 @pytest.mark.parametrize("name", list(SMALL_CASES))
-def test_parity_small(name, orc):
+def test_parity_small(name, schedule, orc):
     w = SMALL_CASES[name]
     h = workloads.host_inputs(w)
     ref = oracle_run(orc, w, h)
-    run = G.GpuRun(w, inputs=h)
+    run = G.GpuRun(w, inputs=h, fused=schedule == "fused")
     out = out_bits(run.run())
     inter = run.intermediates(w.T)
     assert inter["status"] == 0
@@ -103,3 +104,18 @@ def test_parity_full_size_sampled(name, orc):
     xsf_rows = np.concatenate([b for _, b in xs])
     ref = oracle.sampled_problem(w, tokens, idx, wt, x_rows, xsf_rows, _gen_weights(w))
     G.assert_out_close(out[tokens], ref["out"], f"{name} sampled tokens")
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill_t256", "skewed_t48"])
+def test_fused_schedule_equals_split_bit_for_bit(name):
+    """One persistent launch of both GEMMs computes the same tiles as one launch
+    per linear: outputs and intermediates are identical."""
+    w = CONFIGS.get(name) or SMALL_CASES[name]
+    a = G.GpuRun(w, device_weights=True, fused=True)
+    b = G.GpuRun(w, device_weights=True, fused=False)
+    oa, ob = out_bits(a.run()), out_bits(b.run())
+    ia, ib = a.intermediates(w.T), b.intermediates(w.T)
+    assert ia["status"] == 0 and ib["status"] == 0
+    assert np.array_equal(oa, ob)
+    for k in ("l2a", "l2a_sf", "z"):
+        assert np.array_equal(ia[k], ib[k]), k
