@@ -218,7 +218,7 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl")
     w = workloads.CONFIGS[args.workload]
     d = workloads.device_inputs(w)
-    moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp, fused=args.schedule == "fused")
+    moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp, schedule=args.schedule)
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
     moe.workspace(w.T)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
@@ -355,7 +355,8 @@ def report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "fp8xfp4 (fp32 accumulate)", "data": "synthetic",
             "config": dict(workload_config(w), parallelism=f"{world} independent replicas" if world > 1 else "1 GPU",
-                           gemm_schedule=args.schedule),
+                           gemm_schedule=("fused" if "gemm" in kern else "split")
+                           + (" (auto)" if args.schedule == "auto" else "")),
             "tflops": alg["flops"] * world / (ms / 1e3) / 1e12,
             "hbm_gbs_whole_step": (alg["l1_bytes"] + alg["l2_bytes"]) / (ms / 1e3) / 1e9,
             "kernels_ms": kern,
@@ -386,8 +387,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
-    ap.add_argument("--schedule", default="fused", choices=["fused", "split"],
-                    help="both GEMMs in one persistent launch (default) or one launch per linear")
+    ap.add_argument("--schedule", default="auto", choices=["auto", "fused", "split"],
+                    help="GEMM schedule: one persistent launch for both linears, one per linear, or the "
+                         "library's choice from the rows per expert (default)")
     ap.add_argument("--experts", type=int, default=None,
                     help="override E (smaller cases for profiler captures; not a bench line)")
     ap.add_argument("--tokens", type=int, default=None,

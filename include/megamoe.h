@@ -90,13 +90,22 @@ MM_API mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, in
 MM_API mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_math);
 
 /* GEMM schedule ("MegaMoE research report" sec. 4.1, the Linear1 -> Linear2
- * hand-off through per-row arrival flags). fused != 0 (the default) runs both
- * grouped GEMMs in one persistent launch: every L1 tile, then every L2 tile,
- * an L2 tile starting once the L1 epilogues of its token rows have stored
- * them, so the weight stream of L2 follows that of L1 without a drain between
- * them. fused == 0 launches one kernel per linear. The results are identical
- * (the same tiles compute the same sums); only the timing differs. */
-MM_API mm_status_t mm_set_schedule(mm_handle_t h, int fused);
+ * hand-off through per-row arrival flags).
+ *   MM_SCHEDULE_FUSED: both grouped GEMMs in one persistent launch: every L1
+ *     tile, then every L2 tile, an L2 tile starting once the L1 epilogues of
+ *     its token rows have stored them, so the weight stream of L2 follows that
+ *     of L1 without a drain between them (weight-bandwidth-bound calls).
+ *   MM_SCHEDULE_SPLIT: one launch per linear (compute-bound calls).
+ *   MM_SCHEDULE_AUTO (the default): fused when the call routes at most
+ *     MM_FUSED_MAX_ROWS_PER_EXPERT rows per expert on average (T*(topk+S)/(E+S)),
+ *     split above; the threshold is where the two measured equal on GB300.
+ * The results are identical (the same tiles compute the same sums); only the
+ * timing differs. Other values: MM_ERR_INVALID_ARG. */
+#define MM_SCHEDULE_AUTO (-1)
+#define MM_SCHEDULE_SPLIT 0
+#define MM_SCHEDULE_FUSED 1
+#define MM_FUSED_MAX_ROWS_PER_EXPERT 128
+MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
 
 /* Bytes of device workspace mm_run needs for T tokens (T >= 0). The
  * workspace holds the routing tables, the gathered FP8 L1 operand, the FP8 L2

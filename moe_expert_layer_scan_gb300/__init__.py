@@ -97,8 +97,14 @@ def mm_set_options(h: int, swiglu_clamp: float = 0.0, fast_math: bool = False) -
     _check(lib().mm_set_options(h, float(swiglu_clamp), int(bool(fast_math))), "mm_set_options")
 
 
-def mm_set_schedule(h: int, fused: bool = True) -> None:
-    _check(lib().mm_set_schedule(h, int(bool(fused))), "mm_set_schedule")
+MM_SCHEDULE_AUTO, MM_SCHEDULE_SPLIT, MM_SCHEDULE_FUSED = -1, 0, 1
+SCHEDULES = {"auto": MM_SCHEDULE_AUTO, "split": MM_SCHEDULE_SPLIT, "fused": MM_SCHEDULE_FUSED}
+
+
+def mm_set_schedule(h: int, schedule="auto") -> None:
+    """schedule: "auto" | "split" | "fused" (or the MM_SCHEDULE_* value)."""
+    v = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
+    _check(lib().mm_set_schedule(h, v), "mm_set_schedule")
 
 
 def mm_workspace_bytes(h: int, T: int) -> int:
@@ -180,11 +186,11 @@ class MegaMoE:
     """One layer shape bound to a handle; owns a reusable device workspace."""
 
     def __init__(self, E: int, H: int, I: int, topk: int, num_shared: int = 0, swiglu_clamp: float = 0.0,
-                 fast_math: bool = False, fused: bool = True):
+                 fast_math: bool = False, schedule="auto"):
         self.E, self.H, self.I, self.topk, self.S = E, H, I, topk, num_shared
         self.h = mm_create(E, H, I, topk, num_shared)
         mm_set_options(self.h, swiglu_clamp, fast_math)
-        mm_set_schedule(self.h, fused)
+        mm_set_schedule(self.h, schedule)
         self.ws = None
 
     def workspace(self, T: int, device=None):

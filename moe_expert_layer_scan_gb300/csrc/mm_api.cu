@@ -27,8 +27,8 @@ struct mm_handle {
   const void* w2_key;
   CUtensorMap tm_w1;
   CUtensorMap tm_w2;
-  // GEMM schedule: both linears in one persistent launch
-  int fused;
+  // GEMM schedule: MM_SCHEDULE_AUTO / _SPLIT / _FUSED
+  int schedule;
   // optional per-launch events (route, gather, L1, L2, combine, end) and the
   // stage name of each recorded interval
   bool profile;
@@ -117,7 +117,7 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
     if (ms > 0) h->timeout_ns = (unsigned long long)ms * 1000000ull;
   }
   h->w1_key = h->w2_key = nullptr;
-  h->fused = 1;
+  h->schedule = MM_SCHEDULE_AUTO;
   h->profile = false;
   h->n_recorded = 0;
   *out = h;
@@ -131,11 +131,20 @@ mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_math) {
   return MM_OK;
 }
 
-mm_status_t mm_set_schedule(mm_handle_t h, int fused) {
-  if (!h) return MM_ERR_INVALID_ARG;
-  h->fused = fused ? 1 : 0;
+mm_status_t mm_set_schedule(mm_handle_t h, int schedule) {
+  if (!h || schedule < MM_SCHEDULE_AUTO || schedule > MM_SCHEDULE_FUSED) return MM_ERR_INVALID_ARG;
+  h->schedule = schedule;
   return MM_OK;
 }
+
+namespace {
+// Whether a call of T tokens runs both GEMMs in one launch.
+bool use_fused(const mm_handle* h, int T) {
+  if (h->schedule != MM_SCHEDULE_AUTO) return h->schedule == MM_SCHEDULE_FUSED;
+  const long long rows = (long long)T * (h->k + h->S);
+  return rows <= (long long)MM_FUSED_MAX_ROWS_PER_EXPERT * (h->E + h->S);
+}
+}  // namespace
 
 mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes) {
   if (!h || !bytes || T < 0) return MM_ERR_INVALID_ARG;
@@ -146,7 +155,7 @@ mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes) {
 mm_status_t mm_launches_per_run(mm_handle_t h, int T, int* launches) {
   if (!h || !launches || T < 0) return MM_ERR_INVALID_ARG;
   const int route = mm_route_launches(T * (h->k + h->S));
-  *launches = T == 0 ? route : route + (h->fused ? 3 : 4);
+  *launches = T == 0 ? route : route + (use_fused(h, T) ? 3 : 4);
   return MM_OK;
 }
 
@@ -266,7 +275,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g2.K = h->I; g2.rows_w = h->H; g2.fb_total = f2;
   g2.w_sf_vec = aligned(w2_sf, 16) && (h->I / 32) % 16 == 0;
   g2.act_sf_vec = (h->I / 32) % 16 == 0;
-  if (h->fused) {
+  if (use_fused(h, T)) {
     mark("gemm");
     if (mm_launch_gemm_fused(variant, &h->tm_w1, &tm_x, &h->tm_w2, &tm_q, &g1, &g2, stream) != 0)
       return MM_ERR_CUDA;

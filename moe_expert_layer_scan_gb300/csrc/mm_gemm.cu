@@ -72,7 +72,12 @@ struct GemmCfg {
   static constexpr int B_OFF = A_OFF + STAGES * NA * A_BYTES;
   static constexpr int SF_OFF = B_OFF + STAGES * B_BYTES;
   static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+  // copies of the two tile tables and the row offsets ([kMaxExperts + 1] each)
+  static constexpr int TAB_OFF = BAR_OFF + 256;
+  static constexpr int TAB_INTS = kMaxExperts + 1;
+  // L2 tiles whose L1 rows the producer has seen stored (fused schedule)
+  static constexpr int L2RDY_OFF = TAB_OFF + 3 * TAB_INTS * 4;
+  static constexpr int SMEM_BYTES = L2RDY_OFF + 16 + 1024;  // + alignment slack
   // TMEM columns: two accumulator buffers, then two scale-factor slots per
   // issuing thread (weight scales: 4 columns, token scales: 4 or 8 columns;
   // every scale-factor address stays a multiple of 4 columns)
@@ -95,36 +100,58 @@ struct Tile {
 };
 
 // Tile index -> expert, token tile and this CTA's weight tile: the table
-// counts weight-tile groups of cs tiles (one per CTA of a cluster).
-__device__ __forceinline__ Tile decode_tile(int tile, const GemmArgs& a, int bn, int rank, int cs) {
-  int lo = 0, hi = a.Ep - 1;
+// counts weight-tile groups of cs tiles (one per CTA of a cluster). The tile
+// table and the row offsets are shared-memory copies.
+static __device__ __noinline__ Tile decode_tile(int tile, const int* tstart, const int* offs, int Ep, int fb_total,
+                                           int bn, int rank, int cs) {
+  int lo = 0, hi = Ep - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (a.tile_start[mid] <= tile) lo = mid;
+    if (tstart[mid] <= tile) lo = mid;
     else hi = mid - 1;
   }
   Tile t;
   t.e = lo;
-  const int local = tile - a.tile_start[lo];
-  const int cnt = a.offsets[lo + 1] - a.offsets[lo];
+  const int local = tile - tstart[lo];
+  const int cnt = offs[lo + 1] - offs[lo];
   const int ntt = (cnt + bn - 1) / bn;
   const int grp = local / ntt;
   const int tt = local - grp * ntt;
   t.fb = grp * cs + rank;
-  t.active = t.fb < a.fb_total;
-  t.row0 = a.offsets[lo] + tt * bn;
+  t.active = t.fb < fb_total;
+  t.row0 = offs[lo] + tt * bn;
   t.nrows = min(bn, cnt - tt * bn);
   return t;
 }
 
-// First weight row of a tile's first 128-row block, the offset of its second
-// block, and whether the second block exists (l1: gate/up pair; else two W2 blocks).
-__device__ __forceinline__ int tile_wrow(bool l1, const Tile& t, const GemmArgs& a) {
-  return t.e * a.rows_w + t.fb * (l1 ? 128 : 256);
+// The per-phase arguments a role needs for one tile, selected field by field
+// from the L1 or L2 argument block (each a constant-bank read).
+struct Phase {
+  const uint8_t* w_sf;
+  const uint8_t* act_sf;
+  int K, rows_w, second, w_sf_vec, act_sf_vec;
+  bool l1;
+};
+__device__ __forceinline__ Phase phase_of(bool l1, const GemmArgs& g1, const GemmArgs& g2) {
+  Phase p;
+  p.l1 = l1;
+  p.w_sf = l1 ? g1.w_sf : g2.w_sf;
+  p.act_sf = l1 ? g1.act_sf : g2.act_sf;
+  p.K = l1 ? g1.K : g2.K;
+  p.rows_w = l1 ? g1.rows_w : g2.rows_w;
+  p.second = l1 ? g1.I : 128;  // row offset of the tile's second 128-row block
+  p.w_sf_vec = l1 ? g1.w_sf_vec : g2.w_sf_vec;
+  p.act_sf_vec = l1 ? g1.act_sf_vec : g2.act_sf_vec;
+  return p;
 }
-__device__ __forceinline__ int second_off(bool l1, const GemmArgs& a) { return l1 ? a.I : 128; }
-__device__ __forceinline__ bool has_second(bool l1, const Tile& t, const GemmArgs& a) {
-  return t.active && (l1 || t.fb * 256 + 128 < a.rows_w);
+
+// First weight row of a tile's first 128-row block, and whether the second
+// block exists (L1: gate/up pair; L2: two W2 blocks, the last may be single).
+__device__ __forceinline__ int tile_wrow(const Phase& p, const Tile& t) {
+  return t.e * p.rows_w + t.fb * (p.l1 ? 128 : 256);
+}
+__device__ __forceinline__ bool has_second(const Phase& p, const Tile& t) {
+  return t.active && (p.l1 || t.fb * 256 + 128 < p.rows_w);
 }
 
 // Four K steps of one row's UE8M0 scales (16 bytes); `avail` steps exist.
@@ -193,6 +220,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       mbar_init(&tempty[b], Warps<BN>::EPI);  // one arrival per epilogue warp
     }
     *abort_flag = 0;
+    *reinterpret_cast<int*>(smem + C::L2RDY_OFF) = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -216,47 +244,79 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
   // the prologue above overlaps the previous kernel; its outputs are read below
   pdl_trigger();
   pdl_wait();
+  int* s_t1 = reinterpret_cast<int*>(smem + C::TAB_OFF);  // L1 tile table
+  int* s_t2 = s_t1 + C::TAB_INTS;                         // L2 tile table
+  int* s_off = s_t2 + C::TAB_INTS;                        // row offsets per expert
+  {
+    const GemmArgs& ga = MODE == kModeL2 ? g2 : g1;
+    for (int i = threadIdx.x; i <= ga.Ep; i += blockDim.x) {
+      if (MODE != kModeL2) s_t1[i] = g1.tile_start[i];
+      if (MODE != kModeL1) s_t2[i] = g2.tile_start[i];
+      s_off[i] = ga.offsets[i];
+    }
+  }
+  __syncthreads();
   const uint32_t tmem = *tmem_slot;
   // tiles [0, n1) are L1 tiles, [n1, num_tiles) L2 tiles
-  const int n1 = MODE == kModeL2 ? 0 : g1.tile_start[g1.Ep];
-  const int num_tiles = MODE == kModeL1 ? n1 : n1 + g2.tile_start[g2.Ep];
+  const int n1 = MODE == kModeL2 ? 0 : s_t1[g1.Ep];
+  const int num_tiles = MODE == kModeL1 ? n1 : n1 + s_t2[g2.Ep];
   auto is_l1 = [&](int tile) { return MODE == kModeL1 || (MODE == kModeFused && tile < n1); };
   const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
+  // flat tile index -> tile of its phase
+  auto tile_of = [&](int tile, bool l1) {
+    return decode_tile(l1 ? tile : tile - n1, l1 ? s_t1 : s_t2, s_off, g1.Ep, l1 ? g1.fb_total : g2.fb_total, BN,
+                       rank, CS);
+  };
   const int tile0 = blockIdx.x / CS, tile_step = gridDim.x / CS;
   constexpr uint16_t kAllCtas = (uint16_t)((1u << CS) - 1u);
   // wait sites reported in the status word on expiry: L1 tiles s, L2 tiles 8 + s
   constexpr uint32_t kSiteReady = 8u + 6u;  // an L2 tile waiting for its L1 rows (fused)
+  int* l2rdy = reinterpret_cast<int*>(smem + C::L2RDY_OFF);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // Fused: an L2 tile's loads start once its arrival counter is complete.
+    // The counter of the next L2 tile is peeked early (after the first stage of
+    // the current tile) so that the wait is usually over before the tile
+    // starts; every observation is handed on to the scale-factor warp
+    // (l2rdy counts this CTA's L2 tiles observed ready, in tile order).
     uint32_t it = 0;
     bool ok = true;
+    bool cur_ready = false;  // the current tile's counter was seen complete by a peek
     for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
       const bool l1 = is_l1(tile);
-      const GemmArgs& g = l1 ? g1 : g2;
+      const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
-      const Tile t = decode_tile(l1 ? tile : tile - n1, g, BN, rank, CS);
-      const int wrow = tile_wrow(l1, t, g);
-      const bool two = has_second(l1, t, g);
+      const Tile t = tile_of(tile, l1);
+      const int wrow = tile_wrow(g, t);
+      const bool two = has_second(g, t);
       const int kblocks = g.K / C::BK;
       const CUtensorMap* tw = l1 ? &tm_w1 : &tm_w2;
       const CUtensorMap* ta = l1 ? &tm_a1 : &tm_a2;
-      if (MODE == kModeFused && !l1 &&
-          !wait_counter(g1.ready + t.row0, g1.ready_target, abort_flag, g.status, g.timeout_ns, kSiteReady)) {
+      if (MODE == kModeFused && !l1 && !cur_ready &&
+          counter_ready_relay(g1.ready + t.row0, g1.ready_target, true, l2rdy, abort_flag, g1.status,
+                              g1.timeout_ns, kSiteReady) != 1) {
         ok = false;
         break;
       }
+      bool next_ready = false;
+      const int ntile = tile + tile_step;
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        if (MODE == kModeFused && kb == (kblocks > 1 ? 1 : 0) && ntile < num_tiles && !is_l1(ntile)) {
+          const Tile tn = tile_of(ntile, false);
+          next_ready = counter_ready_relay(g1.ready + tn.row0, g1.ready_target, false, l2rdy, abort_flag, g1.status,
+                                           g1.timeout_ns, kSiteReady) == 1;
+        }
         const int s = (int)(it % STAGES);
         const uint32_t ph = (it / STAGES) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g.status, g.timeout_ns, site0 + 0)) { ok = false; break; }
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 0)) { ok = false; break; }
         uint8_t* sA = smem + C::A_OFF + s * C::NA * C::A_BYTES;
         uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
         if (lane == 0) {
           // the whole token tile lands here: this CTA's share and the others' multicasts
           mbar_arrive_expect_tx(&full[s], (t.active ? (two ? 2 : 1) : 0) * C::A_TX + C::B_BYTES);
           if (t.active) tma_load_2d(sA, tw, &full[s], kb * C::BK, wrow);
-          if (two) tma_load_2d(sA + C::A_BYTES, tw, &full[s], kb * C::BK, wrow + second_off(l1, g));
+          if (two) tma_load_2d(sA + C::A_BYTES, tw, &full[s], kb * C::BK, wrow + g.second);
           if constexpr (CS == 1) {
             tma_load_2d(sB, ta, &full[s], kb * C::BK, t.row0);
           } else {
@@ -265,6 +325,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
           }
         }
       }
+      cur_ready = next_ready;
     }
     const GemmArgs& gl = MODE == kModeL1 ? g1 : g2;  // status word and limit (shared by both)
     constexpr uint32_t kSiteTail = (MODE == kModeL1 ? 0u : 8u) + 4u;
@@ -287,66 +348,110 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ scale-factor producer
-    // Loads each row's UE8M0 bytes for four K steps at once (one 16-byte
-    // request per row per four steps) and, per K step, writes the layout
+    // Loads each row's UE8M0 bytes for a group of four K steps at once (one
+    // 16-byte request per row) and, per K step, writes the layout
     // tcgen05.cp.32x128b.warpx4 reads: 16 bytes per lane l holding the step's
     // four scale bytes of rows l, l+32, l+64, l+96 of each 128-row group.
+    // The warp walks the flattened (tile, group) sequence and issues the loads
+    // of the next group before it stores the current one, so their latency
+    // overlaps four pipeline stages instead of stalling the ring.
     constexpr int NB = C::SFB_ROWS / 32;  // 32-row blocks of the token operand
+    uint4 ca[C::NA][4], cb[NB];           // current group
+    uint4 xa[C::NA][4], xb[NB];           // next group
+    auto load_group = [&](int tile, int kg, uint4(&wa)[C::NA][4], uint4(&wb)[NB]) {
+      const bool l1 = is_l1(tile);
+      const Phase g = phase_of(l1, g1, g2);
+      const Tile t = tile_of(tile, l1);
+      const int wrow = tile_wrow(g, t);
+      const bool two = has_second(g, t);
+      const int nb = (t.nrows + 31) / 32;
+      const int sf_ld = g.K / 32;
+      const int avail = g.K / C::BK - kg;
+      const bool fresh = MODE == kModeFused && !l1;  // token scales written by this launch's L1 tiles
+      const bool wvec = g.w_sf_vec && avail >= 4, bvec = g.act_sf_vec && avail >= 4;
+#pragma unroll
+      for (int op = 0; op < C::NA; ++op)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          wa[op][i] = ((op == 0 && t.active) || two)
+                          ? load_sf4(g.w_sf + (size_t)(wrow + op * g.second + 32 * i + lane) * sf_ld + 4 * kg,
+                                     wvec, avail, false)
+                          : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+        wb[j] = j < nb ? load_sf4(g.act_sf + (size_t)(t.row0 + 32 * j + lane) * sf_ld + 4 * kg, bvec, avail, fresh)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    };
+    // fused: an L2 tile's token scales are read only once the producer has
+    // seen its L1 rows stored (the producer counts its L2 tiles in l2rdy;
+    // both warps walk the same tiles, so this warp's n-th L2 tile waits for n)
+    int l2seen = 0;
+    auto ready_wait = [&](int tile) {
+      if (MODE != kModeFused || is_l1(tile)) return true;
+      return wait_shared_counter(l2rdy, ++l2seen, abort_flag, g1.status, g1.timeout_ns, kSiteReady);
+    };
     uint32_t it = 0;
     bool ok = true;
-    for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
+    int tile = tile0, kg = 0;
+    if (tile < num_tiles) {
+      ok = ready_wait(tile);
+      if (ok) load_group(tile, kg, ca, cb);
+    }
+    while (ok && tile < num_tiles) {
       const bool l1 = is_l1(tile);
-      const GemmArgs& g = l1 ? g1 : g2;
+      const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
-      const Tile t = decode_tile(l1 ? tile : tile - n1, g, BN, rank, CS);
-      const int wrow = tile_wrow(l1, t, g);
-      const bool two = has_second(l1, t, g);
-      const int nb = (t.nrows + 31) / 32;
       const int kblocks = g.K / C::BK;
-      const int sf_ld = g.K / 32;
-      const bool fresh = MODE == kModeFused && !l1;  // token scales written by this launch's L1 tiles
-      if (fresh && !wait_counter(g1.ready + t.row0, g1.ready_target, abort_flag, g.status, g.timeout_ns,
-                                 kSiteReady)) {
-        ok = false;
-        break;
+      const int avail = kblocks - kg;
+      int ntile = tile, nkg = kg + 4;
+      if (nkg >= kblocks) {
+        ntile = tile + tile_step;
+        nkg = 0;
       }
-      for (int kg = 0; kg < kblocks && ok; kg += 4) {
-        const int avail = kblocks - kg;
-        const bool wvec = g.w_sf_vec && avail >= 4, bvec = g.act_sf_vec && avail >= 4;
-        uint4 wa[C::NA][4];
-        uint4 wb[NB];
+      const bool has_next = ntile < num_tiles;
+      // a next group whose L1 rows are not all stored yet is loaded after this
+      // group is stored (its rows may come from this CTA's own tile in flight)
+      bool next_waits = false;
+      if (MODE == kModeFused && has_next && nkg == 0 && !is_l1(ntile)) {
+        int done = 0;
+        if (lane == 0) done = ld_acquire_cta_shared(l2rdy) > l2seen;
+        next_waits = !__shfl_sync(0xffffffffu, done, 0);
+        __syncwarp();
+        if (!next_waits) ++l2seen;
+      }
+      if (has_next && !next_waits) load_group(ntile, nkg, xa, xb);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (c >= avail) break;
+        const int s = (int)(it % STAGES);
+        const uint32_t ph = (it / STAGES) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 5)) { ok = false; break; }
+        uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
 #pragma unroll
         for (int op = 0; op < C::NA; ++op)
+          st_shared_v4(sF + op * 512 + lane * 16, word(ca[op][0], c), word(ca[op][1], c), word(ca[op][2], c),
+                       word(ca[op][3], c));
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            wa[op][i] = ((op == 0 && t.active) || two)
-                            ? load_sf4(g.w_sf + (size_t)(wrow + op * second_off(l1, g) + 32 * i + lane) * sf_ld + 4 * kg,
-                                       wvec, avail, false)
-                            : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int j = 0; j < NB; ++j)
-          wb[j] = j < nb ? load_sf4(g.act_sf + (size_t)(t.row0 + 32 * j + lane) * sf_ld + 4 * kg, bvec, avail, fresh)
-                         : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (c >= avail) break;
-          const int s = (int)(it % STAGES);
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g.status, g.timeout_ns, site0 + 5)) { ok = false; break; }
-          uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
-#pragma unroll
-          for (int op = 0; op < C::NA; ++op)
-            st_shared_v4(sF + op * 512 + lane * 16, word(wa[op][0], c), word(wa[op][1], c), word(wa[op][2], c),
-                         word(wa[op][3], c));
-#pragma unroll
-          for (int q = 0; q < NB / 4; ++q)
-            st_shared_v4(sF + C::NA * 512 + q * 512 + lane * 16, word(wb[4 * q], c), word(wb[4 * q + 1], c),
-                         word(wb[4 * q + 2], c), word(wb[4 * q + 3], c));
-          fence_proxy_async_smem();  // generic-proxy writes, read next by tcgen05.cp
-          mbar_arrive(&full[s]);
-          ++it;
-        }
+        for (int q = 0; q < NB / 4; ++q)
+          st_shared_v4(sF + C::NA * 512 + q * 512 + lane * 16, word(cb[4 * q], c), word(cb[4 * q + 1], c),
+                       word(cb[4 * q + 2], c), word(cb[4 * q + 3], c));
+        fence_proxy_async_smem();  // generic-proxy writes, read next by tcgen05.cp
+        mbar_arrive(&full[s]);
+        ++it;
       }
+      if (!ok || !has_next) break;
+      if (next_waits) {
+        if (!ready_wait(ntile)) break;
+        load_group(ntile, nkg, xa, xb);
+      }
+#pragma unroll
+      for (int op = 0; op < C::NA; ++op)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ca[op][i] = xa[op][i];
+#pragma unroll
+      for (int j = 0; j < NB; ++j) cb[j] = xb[j];
+      tile = ntile;
+      kg = nkg;
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------ MMA issuers
@@ -360,21 +465,21 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       bool ok = true;
       for (int tile = tile0; tile < num_tiles && ok; tile += tile_step, ++tcount) {
         const bool l1 = is_l1(tile);
-        const GemmArgs& g = l1 ? g1 : g2;
+        const Phase g = phase_of(l1, g1, g2);
         const uint32_t site0 = l1 ? 0u : 8u;
-        const Tile t = decode_tile(l1 ? tile : tile - n1, g, BN, rank, CS);
+        const Tile t = tile_of(tile, l1);
         const int kblocks = g.K / C::BK;
         const int buf = (int)(tcount & 1u);
         const uint32_t bph = (tcount >> 1) & 1u;
-        if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, g.status, g.timeout_ns, site0 + 1)) break;
+        if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 1)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * C::ACC_COLS + u * BN);
         const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
-        const bool active = u == 0 ? t.active : has_second(l1, t, g);
+        const bool active = u == 0 ? t.active : has_second(g, t);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&full[s], ph, abort_flag, g.status, g.timeout_ns, site0 + 2)) { ok = false; break; }
+          if (!mbar_wait(&full[s], ph, abort_flag, g1.status, g1.timeout_ns, site0 + 2)) { ok = false; break; }
           tc_fence_after();
           const uint8_t* sA = smem + C::A_OFF + (s * C::NA + u) * C::A_BYTES;
           const uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
@@ -413,12 +518,12 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     uint32_t tcount = 0;
     for (int tile = tile0; tile < num_tiles; tile += tile_step, ++tcount) {
       const bool l1 = is_l1(tile);
-      const GemmArgs& g = l1 ? g1 : g2;
+      const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
-      const Tile t = decode_tile(l1 ? tile : tile - n1, g, BN, rank, CS);
+      const Tile t = tile_of(tile, l1);
       const int buf = (int)(tcount & 1u);
       const uint32_t bph = (tcount >> 1) & 1u;
-      if (!mbar_wait(&tfull[buf], bph, abort_flag, g.status, g.timeout_ns, site0 + 3, 256)) break;
+      if (!mbar_wait(&tfull[buf], bph, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 256)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::ACC_COLS);
       // L1: intermediate column of the gate/up pair; L2: hidden column of block 0 (block 1: +128)
@@ -487,7 +592,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
         // fused: this warp's share of the token tile's L2 operand is stored
         if (MODE == kModeFused && t.active) warp_signal(g1.ready + t.row0);
       } else if (MODE != kModeL1) {
-        const bool two = has_second(false, t, g2);
+        const bool two = has_second(phase_of(false, g1, g2), t);
         for (int c0 = 16 * half; t.active && c0 < t.nrows; c0 += 16 * (Warps<BN>::EPI / 4)) {
           uint32_t gv[16], hv[16];
           tmem_ld_x16(tbase + (uint32_t)c0, gv);

@@ -52,13 +52,13 @@ class GpuRun:
     """Owns a handle, device inputs and a workspace for one workload."""
 
     def __init__(self, w: workloads.Workload, inputs: dict | None = None, fast_math=False, device_weights=False,
-                 clamp=None, fused=True):
+                 clamp=None, schedule="auto"):
         import torch
         import moe_expert_layer_scan_gb300 as mm
         self.w = w
         self.mm = mm
         self.moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp if clamp is None else clamp,
-                              fast_math=fast_math, fused=fused)
+                              fast_math=fast_math, schedule=schedule)
         if inputs is None:
             if device_weights:
                 self.d = workloads.device_inputs(w)

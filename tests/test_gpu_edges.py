@@ -121,3 +121,25 @@ def test_bounded_wait_reports_timeout_and_gpu_stays_usable(orc):
     h = workloads.host_inputs(w)
     run = G.GpuRun(w, inputs=h)
     G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
+
+
+def test_schedule_choice_and_validation():
+    """AUTO runs both GEMMs in one launch up to 128 routed rows per expert on
+    average and one launch per linear above; explicit choices are honoured and
+    out-of-range values rejected."""
+    import moe_expert_layer_scan_gb300 as mm
+    moe = mm.MegaMoE(256, 7168, 2048, 8, 0)
+    small = mm.mm_launches_per_run(moe.h, 8)          # 64 rows over 256 experts: fused
+    at = mm.mm_launches_per_run(moe.h, 4096)          # 128 rows per expert: still fused
+    above = mm.mm_launches_per_run(moe.h, 4097)       # just above: split (same routing launches)
+    assert above == at + 1
+    n_big = mm.mm_launches_per_run(moe.h, 16384)      # 512 rows per expert: split
+    mm.mm_set_schedule(moe.h, "fused")
+    assert mm.mm_launches_per_run(moe.h, 16384) == n_big - 1
+    assert mm.mm_launches_per_run(moe.h, 8) == small
+    mm.mm_set_schedule(moe.h, "split")
+    assert mm.mm_launches_per_run(moe.h, 8) == small + 1
+    with pytest.raises(mm.MMError):
+        mm.mm_set_schedule(moe.h, 2)
+    with pytest.raises(mm.MMError):
+        mm.mm_set_schedule(moe.h, -2)

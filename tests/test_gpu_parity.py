@@ -59,7 +59,7 @@ def test_parity_small(name, schedule, orc):
     w = SMALL_CASES[name]
     h = workloads.host_inputs(w)
     ref = oracle_run(orc, w, h)
-    run = G.GpuRun(w, inputs=h, fused=schedule == "fused")
+    run = G.GpuRun(w, inputs=h, schedule=schedule)
     out = out_bits(run.run())
     inter = run.intermediates(w.T)
     assert inter["status"] == 0
@@ -111,8 +111,8 @@ def test_fused_schedule_equals_split_bit_for_bit(name):
     """One persistent launch of both GEMMs computes the same tiles as one launch
     per linear: outputs and intermediates are identical."""
     w = CONFIGS.get(name) or SMALL_CASES[name]
-    a = G.GpuRun(w, device_weights=True, fused=True)
-    b = G.GpuRun(w, device_weights=True, fused=False)
+    a = G.GpuRun(w, device_weights=True, schedule="fused")
+    b = G.GpuRun(w, device_weights=True, schedule="split")
     oa, ob = out_bits(a.run()), out_bits(b.run())
     ia, ib = a.intermediates(w.T), b.intermediates(w.T)
     assert ia["status"] == 0 and ib["status"] == 0
