@@ -107,6 +107,29 @@ MM_API mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_ma
 #define MM_FUSED_MAX_ROWS_PER_EXPERT 128
 MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
 
+/* Expert-parallel-ready routing outputs ("MegaMoE research report", the
+ * dispatch step of the expert-parallel layer and its per-rank receive
+ * statistics; here every expert is local and nothing is sent).
+ *
+ * mm_set_ep_ranks: the routed experts are owned by num_ranks destination
+ * ranks in contiguous blocks of E / num_ranks (rank g owns experts
+ * [g*E/num_ranks, (g+1)*E/num_ranks)); E % num_ranks must be 0
+ * (MM_ERR_UNSUPPORTED otherwise), 1 <= num_ranks <= E (MM_ERR_INVALID_ARG
+ * otherwise). Default 1. Because the routing order is expert-major with the
+ * experts of a rank contiguous, it is also ordered by destination rank: after
+ * each mm_run, the workspace holds rank_offsets[num_ranks + 1] (see
+ * mm_debug_views_t) with rows [rank_offsets[g], rank_offsets[g+1]) of the
+ * sorted order bound for rank g; rank_offsets[num_ranks] is the number of
+ * routed rows, the shared experts' rows (replicated on every rank) follow.
+ *
+ * mm_set_expert_stats: a caller-owned device array of E + S int32 (4-byte
+ * aligned; NULL disables). Every mm_run adds each expert's routed row count of
+ * that call to it on the device, in stream order after routing; the library
+ * never reads it otherwise, never clears it and never frees it. The pointer
+ * must stay valid while calls that use it are in flight. */
+MM_API mm_status_t mm_set_ep_ranks(mm_handle_t h, int num_ranks);
+MM_API mm_status_t mm_set_expert_stats(mm_handle_t h, int32_t* cumulative_counts);
+
 /* Bytes of device workspace mm_run needs for T tokens (T >= 0). The
  * workspace holds the routing tables, the gathered FP8 L1 operand, the FP8 L2
  * operand, the BF16 per-slot L2 output and a status word. */
@@ -161,6 +184,7 @@ typedef struct {
   uint16_t* z;
   uint32_t* status;
   int rows_capacity;
+  int32_t* rank_offsets; /* [ep_ranks + 1], see mm_set_ep_ranks */
 } mm_debug_views_t;
 
 MM_API mm_status_t mm_debug_views(mm_handle_t h, void* ws, int T, mm_debug_views_t* views);

@@ -23,7 +23,8 @@ MM_DEV_BAD_ROUTING = 0x1
 MM_DEV_TIMEOUT = 0x2
 STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_WORKSPACE_TOO_SMALL",
                 4: "MM_ERR_CUDA", 5: "MM_ERR_DEVICE_TIMEOUT", 6: "MM_ERR_BAD_ROUTING", 7: "MM_ERR_ALIGNMENT"}
-EXPORTS = ["mm_status_string", "mm_create", "mm_set_options", "mm_set_schedule", "mm_workspace_bytes", "mm_run",
+EXPORTS = ["mm_status_string", "mm_create", "mm_set_options", "mm_set_schedule", "mm_set_ep_ranks",
+           "mm_set_expert_stats", "mm_workspace_bytes", "mm_run",
            "mm_get_status", "mm_launches_per_run", "mm_debug_views", "mm_debug_timeout_probe", "mm_profile_enable",
            "mm_profile_last", "mm_profile_name", "mm_run_noalloc", "mm_destroy"]
 
@@ -36,7 +37,8 @@ class MMError(RuntimeError):
 
 class DebugViews(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("counts", "offsets", "perm", "pos", "row_w", "pool_x", "pool_sf", "l2a",
-                                                "l2a_sf", "z", "status")] + [("rows_capacity", ctypes.c_int)]
+                                                "l2a_sf", "z", "status")] + [("rows_capacity", ctypes.c_int),
+                                                                             ("rank_offsets", ctypes.c_void_p)]
 
 
 _lib = None
@@ -61,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.mm_create.argtypes = [ctypes.POINTER(p), i32, i32, i32, i32, i32]
         L.mm_set_options.argtypes = [p, ctypes.c_float, i32]
         L.mm_set_schedule.argtypes = [p, i32]
+        L.mm_set_ep_ranks.argtypes = [p, i32]
+        L.mm_set_expert_stats.argtypes = [p, p]
         L.mm_workspace_bytes.argtypes = [p, i32, ctypes.POINTER(ctypes.c_size_t)]
         L.mm_run.argtypes = [p, i32] + [p] * 10 + [ctypes.c_size_t, p]
         L.mm_get_status.argtypes = [p, p, p, u32p]
@@ -105,6 +109,15 @@ def mm_set_schedule(h: int, schedule="auto") -> None:
     """schedule: "auto" | "split" | "fused" (or the MM_SCHEDULE_* value)."""
     v = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
     _check(lib().mm_set_schedule(h, v), "mm_set_schedule")
+
+
+def mm_set_ep_ranks(h: int, num_ranks: int) -> None:
+    _check(lib().mm_set_ep_ranks(h, int(num_ranks)), "mm_set_ep_ranks")
+
+
+def mm_set_expert_stats(h: int, cumulative_counts_ptr) -> None:
+    """Device pointer to E + S int32 counters (or None to disable)."""
+    _check(lib().mm_set_expert_stats(h, cumulative_counts_ptr or None), "mm_set_expert_stats")
 
 
 def mm_workspace_bytes(h: int, T: int) -> int:

@@ -29,6 +29,10 @@ struct mm_handle {
   CUtensorMap tm_w2;
   // GEMM schedule: MM_SCHEDULE_AUTO / _SPLIT / _FUSED
   int schedule;
+  // expert-parallel-ready routing: destination ranks and the caller's
+  // cumulative per-expert row counts (device, may be null)
+  int ep_ranks;
+  int32_t* expert_stats;
   // optional per-launch events (route, gather, L1, L2, combine, end) and the
   // stage name of each recorded interval
   bool profile;
@@ -118,6 +122,8 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
   }
   h->w1_key = h->w2_key = nullptr;
   h->schedule = MM_SCHEDULE_AUTO;
+  h->ep_ranks = 1;
+  h->expert_stats = nullptr;
   h->profile = false;
   h->n_recorded = 0;
   *out = h;
@@ -134,6 +140,20 @@ mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_math) {
 mm_status_t mm_set_schedule(mm_handle_t h, int schedule) {
   if (!h || schedule < MM_SCHEDULE_AUTO || schedule > MM_SCHEDULE_FUSED) return MM_ERR_INVALID_ARG;
   h->schedule = schedule;
+  return MM_OK;
+}
+
+mm_status_t mm_set_ep_ranks(mm_handle_t h, int num_ranks) {
+  if (!h || num_ranks < 1 || num_ranks > h->E) return MM_ERR_INVALID_ARG;
+  if (h->E % num_ranks != 0) return MM_ERR_UNSUPPORTED;
+  h->ep_ranks = num_ranks;
+  return MM_OK;
+}
+
+mm_status_t mm_set_expert_stats(mm_handle_t h, int32_t* cumulative_counts) {
+  if (!h) return MM_ERR_INVALID_ARG;
+  if (cumulative_counts && !aligned(cumulative_counts, 4)) return MM_ERR_ALIGNMENT;
+  h->expert_stats = cumulative_counts;
   return MM_OK;
 }
 
@@ -196,6 +216,9 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ra.chunk_base = reinterpret_cast<int32_t*>(base + L.chunk_base);
   ra.chunk_bad = reinterpret_cast<int32_t*>(base + L.chunk_bad);
   ra.ready = reinterpret_cast<int32_t*>(base + L.ready);
+  ra.rank_offsets = reinterpret_cast<int32_t*>(base + L.rank_offsets);
+  ra.stats = h->expert_stats;
+  ra.ep_ranks = h->ep_ranks;
   ra.status = reinterpret_cast<uint32_t*>(base + L.status);
   ra.T = T; ra.E = h->E; ra.k = h->k; ra.S = h->S;
   ra.bn_l1 = bn1; ra.bn_l2 = bn2;
@@ -355,6 +378,7 @@ mm_status_t mm_debug_views(mm_handle_t h, void* ws, int T, mm_debug_views_t* v) 
   v->z = reinterpret_cast<uint16_t*>(b + L.z);
   v->status = reinterpret_cast<uint32_t*>(b + L.status);
   v->rows_capacity = L.rows_cap;
+  v->rank_offsets = reinterpret_cast<int32_t*>(b + L.rank_offsets);
   return MM_OK;
 }
 

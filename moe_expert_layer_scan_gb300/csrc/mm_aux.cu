@@ -138,6 +138,16 @@ __device__ int offsets_and_tiles(const RouteArgs& a, int tot, int* scratch) {
     a.tiles_l1[Ep] = n1;
     a.tiles_l2[Ep] = n2;
   }
+  // Expert-parallel-ready outputs. With the routed experts split over ranks in
+  // contiguous blocks, the expert-major order is also rank-major, so each
+  // destination rank's rows are one range of the sorted order. The shared
+  // experts (replicated on every rank) follow the last routed rank.
+  const int per_rank = a.E / a.ep_ranks;
+  if (tid < a.E && tid % per_rank == 0) a.rank_offsets[tid / per_rank] = excl;
+  if (a.S > 0 && tid == a.E) a.rank_offsets[a.ep_ranks] = excl;
+  if (a.S == 0 && tid == 0) a.rank_offsets[a.ep_ranks] = total_rows;
+  // cumulative per-expert receive statistics (never cleared here)
+  if (a.stats && tid < Ep && tot > 0) atomicAdd(&a.stats[tid], tot);
   return excl;
 }
 

@@ -31,7 +31,8 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Byte offsets of every workspace region for one (shape, T).
 struct Layout {
-  size_t status, counts, offsets, tiles_l1, tiles_l2, perm, pos, row_w, chunk_cnt, chunk_base, chunk_bad, ready;
+  size_t status, counts, offsets, tiles_l1, tiles_l2, rank_offsets, perm, pos, row_w, chunk_cnt, chunk_base,
+      chunk_bad, ready;
   size_t pool_x, pool_sf, l2a, l2a_sf, z, total;
   int rows_cap;
 };
@@ -48,6 +49,7 @@ inline Layout make_layout(int E, int S, int H, int I, int k, int T) {
   L.offsets = take(sizeof(int32_t) * (Ep + 1), 256);
   L.tiles_l1 = take(sizeof(int32_t) * (Ep + 1), 256);
   L.tiles_l2 = take(sizeof(int32_t) * (Ep + 1), 256);
+  L.rank_offsets = take(sizeof(int32_t) * (E + 1), 256);
   L.perm = take(sizeof(int32_t) * (R + 1), 256);
   L.pos = take(sizeof(int32_t) * (R + 1), 256);
   L.row_w = take(sizeof(float) * (R + 1), 256);
@@ -83,6 +85,13 @@ struct RouteArgs {
   int T, E, k, S;
   int bn_l1, bn_l2;  // token-tile widths of the two GEMMs
   int fb_l1, fb_l2;  // weight tiles per expert: I/128 (gate/up pairs) and ceil(H/256)
+  // expert-parallel-ready outputs: the routed experts split over ep_ranks
+  // destination ranks in contiguous blocks; rank_offsets[g] = first sorted row
+  // bound for rank g ([ep_ranks + 1]); stats (optional, caller-owned [E + S])
+  // accumulates every call's rows per expert
+  int32_t* rank_offsets;
+  int32_t* stats;
+  int ep_ranks;
 };
 
 struct GatherArgs {
