@@ -40,7 +40,7 @@ def build(mutant: int = 0, verbose: bool = False) -> str:
 class _Dims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int), ("E", ctypes.c_int),
                 ("k", ctypes.c_int), ("S", ctypes.c_int), ("clamp", ctypes.c_float),
-                ("weight_in_combine", ctypes.c_int)]
+                ("weight_in_combine", ctypes.c_int), ("w_fmt", ctypes.c_int)]
 
 
 def _p(a):
@@ -67,7 +67,7 @@ class Oracle:
         lib.orc_route.restype = i32
         lib.orc_forward.argtypes = [ctypes.POINTER(_Dims)] + [p] * 13 + [i32]
         lib.orc_forward.restype = i32
-        lib.orc_l2_rows.argtypes = [i32, i32, i32, p, p, p, p, p, p]
+        lib.orc_l2_rows.argtypes = [i32, i32, i32, i32, p, p, p, p, p, p]
         lib.orc_l2_rows.restype = None
         self.lib = lib
         self.mutant = mutant
@@ -114,7 +114,9 @@ class Oracle:
                 nthreads: int | None = None, weight_in_combine: bool = False):
         """Run the path. dims: T,H,I,E,k,S,clamp. Returns dict(out=uint16 [T,H], ...)."""
         T, H, I, E, k, S = (int(dims[n]) for n in ("T", "H", "I", "E", "k", "S"))
-        d = _Dims(T, H, I, E, k, S, float(dims.get("clamp", 0.0)), int(weight_in_combine))
+        w_fmt = int(dims.get("w_fmt", 0))  # 0: E2M1 weights (MXFP4), 1: E4M3 weights (MXFP8)
+        d = _Dims(T, H, I, E, k, S, float(dims.get("clamp", 0.0)), int(weight_in_combine), w_fmt)
+        wb = 1 if w_fmt else 2  # weight elements per byte is 2 for E2M1
         R = T * (k + S)
         c = np.ascontiguousarray
         x, x_sf = c(x, np.uint8), c(x_sf, np.uint8)
@@ -122,8 +124,8 @@ class Oracle:
         w1, w1_sf, w2, w2_sf = c(w1, np.uint8), c(w1_sf, np.uint8), c(w2, np.uint8), c(w2_sf, np.uint8)
         assert x.shape == (T, H) and x_sf.shape == (T, H // 32)
         assert topk_idx.shape == (T, k) and topk_w.shape == (T, k)
-        assert w1.size == (E + S) * 2 * I * H // 2 and w1_sf.size == (E + S) * 2 * I * H // 32
-        assert w2.size == (E + S) * H * I // 2 and w2_sf.size == (E + S) * H * I // 32
+        assert w1.size == (E + S) * 2 * I * H // wb and w1_sf.size == (E + S) * 2 * I * H // 32
+        assert w2.size == (E + S) * H * I // wb and w2_sf.size == (E + S) * H * I // 32
         out = np.zeros((T, H), np.uint16)
         res = dict(out=out)
         acc1 = q = qsf = None
@@ -143,11 +145,11 @@ class Oracle:
         res.update(self.route(topk_idx, E, S))
         return res
 
-    def l2_rows(self, expert_of_row, q, q_sf, w2, w2_sf, H: int, I: int):
+    def l2_rows(self, expert_of_row, q, q_sf, w2, w2_sf, H: int, I: int, w_fmt: int = 0):
         expert_of_row = np.ascontiguousarray(expert_of_row, np.int32)
         R = expert_of_row.size
         acc2 = np.zeros((R, H), np.float32)
-        self.lib.orc_l2_rows(R, H, I, _p(expert_of_row), _p(np.ascontiguousarray(q, np.uint8)),
+        self.lib.orc_l2_rows(R, H, I, int(w_fmt), _p(expert_of_row), _p(np.ascontiguousarray(q, np.uint8)),
                              _p(np.ascontiguousarray(q_sf, np.uint8)), _p(np.ascontiguousarray(w2, np.uint8)),
                              _p(np.ascontiguousarray(w2_sf, np.uint8)), _p(acc2))
         return acc2
@@ -187,5 +189,6 @@ def sampled_problem(w, tokens, topk_idx, topk_w, x_rows, x_sf_rows, gen_weights)
     experts = routed + list(range(w.E, w.E + w.S))
     w1, w1sf = gen_weights(2, experts)
     w2, w2sf = gen_weights(3, experts)
-    dims = dict(T=len(tokens), H=w.H, I=w.I, E=len(routed), k=w.k, S=w.S, clamp=w.clamp)
+    dims = dict(T=len(tokens), H=w.H, I=w.I, E=len(routed), k=w.k, S=w.S, clamp=w.clamp,
+                w_fmt=getattr(w, "w_fmt", 0))
     return get().forward(dims, x_rows, x_sf_rows, new_idx, np.ascontiguousarray(topk_w[tokens]), w1, w1sf, w2, w2sf)

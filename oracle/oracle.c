@@ -23,7 +23,9 @@
  *  - the E4M3 cast rounds to nearest even and saturates at +-448;
  *  - the clamp is symmetric on both gate and up, before the SiLU;
  *  - W1 rows [0, I) are gate and [I, 2I) are up; E2M1 codes are packed two per
- *    byte with the even K index in the low nibble;
+ *    byte with the even K index in the low nibble; E4M3 weights (the FP8
+ *    weight variant) are one byte per element; both carry one UE8M0 scale per
+ *    32 along K (OCP MX: MXFP4 / MXFP8);
  *  - within one expert, rows are in ascending source-slot order;
  *  - shared experts sit at expert indices E..E+S-1, slot k+s of every token,
  *    with weight 1; a topk_idx of -1 disables its slot.
@@ -164,6 +166,20 @@ static long orc_sf_index(long kk) {
 #endif
 }
 
+/* Element kk of a weight row (format fmt), before its block scale. Rows are
+ * K/2 bytes for E2M1 and K bytes for E4M3. */
+static float orc_weight(const uint8_t* row, long kk, int fmt) {
+#if MUT(13)
+  (void)fmt;
+  return orc_e2m1_to_float(orc_nibble(row, kk)); /* mistake: every weight read as E2M1 */
+#else
+  return fmt ? orc_e4m3_to_float(row[kk]) : orc_e2m1_to_float(orc_nibble(row, kk));
+#endif
+}
+
+/* Bytes per weight row of K elements. */
+static long orc_row_bytes(long K, int fmt) { return fmt ? K : K / 2; }
+
 /* ------------------------------------------------------------------ routing */
 
 static int orc_slot_expert(int T, int k, int S, int E, const int32_t* topk_idx, long s, int* bad) {
@@ -240,11 +256,11 @@ static void orc_one_row(const orc_job* J, long r, float* xh, float* a1, float* y
   }
   /* L1: acc1[n] = sum_k x[k] * W1[e][n][k], FP32, ascending k */
   for (long n = 0; n < 2L * I; ++n) {
-    const uint8_t* wr = J->w1 + ((long)e * 2 * I + n) * (H / 2);
+    const uint8_t* wr = J->w1 + ((long)e * 2 * I + n) * orc_row_bytes(H, d->w_fmt);
     const uint8_t* sr = J->w1_sf + ((long)e * 2 * I + n) * (H / 32);
     float acc = 0.0f;
     for (long kk = 0; kk < H; ++kk) {
-      float wv = orc_e2m1_to_float(orc_nibble(wr, kk)) * orc_ue8m0_to_float(sr[orc_sf_index(kk)]);
+      float wv = orc_weight(wr, kk, d->w_fmt) * orc_ue8m0_to_float(sr[orc_sf_index(kk)]);
       acc += xh[kk] * wv;
     }
     a1[n] = acc;
@@ -290,19 +306,19 @@ static void orc_one_row(const orc_job* J, long r, float* xh, float* a1, float* y
   }
   /* L2: z[h] = bf16(sum_i q[i] * W2[e][h][i]), FP32, ascending i */
   for (long h = 0; h < H; ++h) {
-    const uint8_t* wr = J->w2 + ((long)e * H + h) * (I / 2);
+    const uint8_t* wr = J->w2 + ((long)e * H + h) * orc_row_bytes(I, d->w_fmt);
     const uint8_t* sr = J->w2_sf + ((long)e * H + h) * (I / 32);
     float acc = 0.0f;
     for (long i = 0; i < I; ++i) {
 #if MUT(5)
       /* mistake: W2 read transposed ([I][H] instead of [H][I]) */
       long flat = i * H + h;
-      const uint8_t* wt = J->w2 + (long)e * H * (I / 2);
+      const uint8_t* wt = J->w2 + (long)e * H * orc_row_bytes(I, d->w_fmt);
       const uint8_t* st = J->w2_sf + (long)e * H * (I / 32);
-      float wv = orc_e2m1_to_float(orc_nibble(wt, flat)) * orc_ue8m0_to_float(st[flat / 32]);
+      float wv = orc_weight(wt, flat, d->w_fmt) * orc_ue8m0_to_float(st[flat / 32]);
       (void)wr; (void)sr;
 #else
-      float wv = orc_e2m1_to_float(orc_nibble(wr, i)) * orc_ue8m0_to_float(sr[orc_sf_index(i)]);
+      float wv = orc_weight(wr, i, d->w_fmt) * orc_ue8m0_to_float(sr[orc_sf_index(i)]);
 #endif
       acc += qh[i] * wv;
     }
@@ -327,6 +343,7 @@ int orc_forward(const orc_dims* d, const uint8_t* x, const uint8_t* x_sf, const 
                 const uint8_t* w2_sf, uint16_t* out, float* acc1, uint8_t* q, uint8_t* qsf, uint16_t* z,
                 int nthreads) {
   if (!d || d->T < 0 || d->H % 32 || d->I % 32 || d->E < 1 || d->k < 1 || d->S < 0) return -1;
+  if (d->w_fmt != 0 && d->w_fmt != 1) return -1;
   const int T = d->T, H = d->H, k = d->k, Kp = d->k + d->S, Ep = d->E + d->S;
   long R = (long)T * Kp;
   int32_t* counts = (int32_t*)malloc(sizeof(int32_t) * ((size_t)Ep + 1));
@@ -374,17 +391,17 @@ int orc_forward(const orc_dims* d, const uint8_t* x, const uint8_t* x_sf, const 
   return bad;
 }
 
-void orc_l2_rows(int R, int H, int I, const int32_t* expert_of_row, const uint8_t* q, const uint8_t* qsf,
-                 const uint8_t* w2, const uint8_t* w2_sf, float* acc2) {
+void orc_l2_rows(int R, int H, int I, int w_fmt, const int32_t* expert_of_row, const uint8_t* q,
+                 const uint8_t* qsf, const uint8_t* w2, const uint8_t* w2_sf, float* acc2) {
   for (long r = 0; r < R; ++r) {
     long e = expert_of_row[r];
     for (long h = 0; h < H; ++h) {
-      const uint8_t* wr = w2 + (e * H + h) * (I / 2);
+      const uint8_t* wr = w2 + (e * H + h) * orc_row_bytes(I, w_fmt);
       const uint8_t* sr = w2_sf + (e * H + h) * (I / 32);
       float acc = 0.0f;
       for (long i = 0; i < I; ++i) {
         float a = orc_e4m3_to_float(q[r * I + i]) * orc_ue8m0_to_float(qsf[r * (I / 32) + i / 32]);
-        acc += a * (orc_e2m1_to_float(orc_nibble(wr, i)) * orc_ue8m0_to_float(sr[orc_sf_index(i)]));
+        acc += a * (orc_weight(wr, i, w_fmt) * orc_ue8m0_to_float(sr[orc_sf_index(i)]));
       }
       acc2[r * H + h] = acc;
     }

@@ -22,6 +22,8 @@ typedef struct {
   int S;          /* shared experts (0 or more), weight 1    */
   float clamp;    /* SwiGLU clamp c (<= 0: off)              */
   int weight_in_combine; /* diagnosis only: apply top-k weight in the combine instead of L1 */
+  int w_fmt;      /* weight elements: 0 = E2M1 packed two per byte (MXFP4),
+                     1 = E4M3 one per byte (MXFP8); both with UE8M0 per 32 along K */
 } orc_dims;
 
 /* Format decoders / encoders (OCP Microscaling v1.0, OCP FP8, bfloat16). */
@@ -59,9 +61,10 @@ int orc_forward(const orc_dims* d, const uint8_t* x, const uint8_t* x_sf, const 
                 int nthreads);
 
 /* L2 alone from given E4M3 activations (used to pin the L2 contraction):
- * acc2[r][h] = sum_i deq(q[r][i]) * deq(W2[e_r][h][i]), float, ascending i. */
-void orc_l2_rows(int R, int H, int I, const int32_t* expert_of_row, const uint8_t* q, const uint8_t* qsf,
-                 const uint8_t* w2, const uint8_t* w2_sf, float* acc2);
+ * acc2[r][h] = sum_i deq(q[r][i]) * deq(W2[e_r][h][i]), float, ascending i;
+ * w_fmt as in orc_dims. */
+void orc_l2_rows(int R, int H, int I, int w_fmt, const int32_t* expert_of_row, const uint8_t* q,
+                 const uint8_t* qsf, const uint8_t* w2, const uint8_t* w2_sf, float* acc2);
 
 #ifdef __cplusplus
 }

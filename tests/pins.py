@@ -56,8 +56,11 @@ def unpack_e2m1(packed) -> np.ndarray:
     return out
 
 
-def deq_w(packed, sf) -> np.ndarray:
-    return e2m1_table()[unpack_e2m1(packed)] * np.repeat(deq_ue8m0(sf), 32, axis=-1)
+def deq_w(codes, sf, fmt: int = 0) -> np.ndarray:
+    """Weights from their codes: E2M1 packed two per byte (fmt 0, OCP MXFP4) or
+    E4M3 one per byte (fmt 1, OCP MXFP8), times the UE8M0 scale of each 32."""
+    vals = deq_e4m3(codes) if fmt else e2m1_table()[unpack_e2m1(codes)]
+    return vals * np.repeat(deq_ue8m0(sf), 32, axis=-1)
 
 
 def deq_x(x, sf) -> np.ndarray:
@@ -208,6 +211,8 @@ def pin_route(o):
 PIN_WORKLOADS = [
     workloads.CONFIGS["tiny"],
     workloads.Workload("pin_shared", T=12, H=256, I=128, E=5, k=3, S=1, clamp=0.75, zipf=1.2, seed=21),
+    # FP8 (MXFP8) weights
+    workloads.Workload("pin_fp8w", T=10, H=256, I=128, E=4, k=2, S=1, seed=22, w_fmt=1),
 ]
 
 
@@ -215,7 +220,7 @@ def run_case(o, w, topk_idx=None, topk_w=None):
     d = workloads.host_inputs(w)
     if topk_idx is not None:
         d["topk_idx"], d["topk_w"] = topk_idx, topk_w
-    dims = dict(T=w.T, H=w.H, I=w.I, E=w.E, k=w.k, S=w.S, clamp=w.clamp)
+    dims = dict(T=w.T, H=w.H, I=w.I, E=w.E, k=w.k, S=w.S, clamp=w.clamp, w_fmt=w.w_fmt)
     res = o.forward(dims, d["x"], d["x_sf"], d["topk_idx"], d["topk_w"], d["w1"], d["w1_sf"], d["w2"], d["w2_sf"],
                     intermediates=True, nthreads=4)
     return d, res
@@ -234,7 +239,7 @@ def pin_l1(o, w, d, res):
     x = deq_x(d["x"], d["x_sf"])
     fails = []
     for r in range(len(tok)):
-        W1 = deq_w(d["w1"][ex[r]], d["w1_sf"][ex[r]])  # [2I, H]
+        W1 = deq_w(d["w1"][ex[r]], d["w1_sf"][ex[r]], w.w_fmt)  # [2I, H]
         ref = W1 @ x[tok[r]]
         bound = gamma(w.H) * (np.abs(W1) @ np.abs(x[tok[r]])) + 1e-30
         err = np.abs(res["acc1"][r].astype(np.float64) - ref)
@@ -312,7 +317,7 @@ def pin_l2(o, w, d, res):
     z = bf16_bits_to_f64(res["z"][:n])
     fails = []
     for r in range(n):
-        W2 = deq_w(d["w2"][ex[r]], d["w2_sf"][ex[r]])  # [H, I]
+        W2 = deq_w(d["w2"][ex[r]], d["w2_sf"][ex[r]], w.w_fmt)  # [H, I]
         ref = W2 @ qv[r]
         tot = np.abs(W2) @ np.abs(qv[r])
         bound = gamma(w.I) * tot * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(ref) + 1e-30
@@ -383,8 +388,8 @@ def pin_f64_model(o, w, d, res):
     ex = slot_experts(d["topk_idx"], w.E, w.S).reshape(w.T, w.Kp)
     wt = slot_weights(d["topk_w"], w.S).reshape(w.T, w.Kp)
     ref = np.zeros((w.T, w.H))
-    W1 = {e: deq_w(d["w1"][e], d["w1_sf"][e]) for e in range(w.Ep)}
-    W2 = {e: deq_w(d["w2"][e], d["w2_sf"][e]) for e in range(w.Ep)}
+    W1 = {e: deq_w(d["w1"][e], d["w1_sf"][e], w.w_fmt) for e in range(w.Ep)}
+    W2 = {e: deq_w(d["w2"][e], d["w2_sf"][e], w.w_fmt) for e in range(w.Ep)}
     for t in range(w.T):
         for j in range(w.Kp):
             e = ex[t, j]

@@ -36,3 +36,23 @@ def test_normal_moments():
     key = lib.syn_key(7, 1)
     v = np.array([lib.syn_normal_at(key, i) for i in range(200000)])
     assert abs(v.mean()) < 0.01 and abs(v.std() - 1.0) < 0.01
+
+
+def test_fp8_weights_quantise_the_same_values():
+    """The MXFP8 weight variant draws the same N(0, 1/K) values as MXFP4 and
+    quantises each 32-group to E4M3 with the smallest power-of-two scale >=
+    amax/448: dequantised FP8 weights agree with the FP4 ones to FP4's error."""
+    import pins
+    w4 = workloads.Workload("g4", T=4, H=256, I=128, E=2, k=1, seed=9)
+    w8 = w4.replace(name="g8", w_fmt=1)
+    c4, s4 = workloads.w_host(w4, workloads.TAG_W1)
+    c8, s8 = workloads.w_host(w8, workloads.TAG_W1)
+    assert c8.shape == (2, 256, 256) and c4.shape == (2, 256, 128)
+    v4, v8 = pins.deq_w(c4, s4, 0), pins.deq_w(c8, s8, 1)
+    # FP8: relative error of E4M3 (<= 2^-4 of the value above the subnormal range)
+    amax = np.abs(v8).reshape(-1, 32).max(axis=1)
+    sc = pins.deq_ue8m0(s8.reshape(-1))
+    assert (amax <= 448 * sc).all() and (amax >= 224 * sc).all()
+    err = np.abs(v8 - v4).max()
+    assert err <= 0.5 * np.abs(v4).max()   # same draws (FP4 is the coarse one)
+    assert np.corrcoef(v4.ravel(), v8.ravel())[0, 1] > 0.98

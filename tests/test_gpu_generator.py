@@ -23,7 +23,7 @@ def test_device_generator_matches_host(name):
     for which in (workloads.TAG_W1, workloads.TAG_W2):
         rows_w, K = workloads.weight_shape(w, which)
         for e in sorted({0, w.Ep - 1}):
-            c = torch.empty((1, rows_w, K // 2), dtype=torch.uint8, device="cuda")
+            c = torch.empty((1, rows_w, workloads.code_bytes(w, K)), dtype=torch.uint8, device="cuda")
             s = torch.empty((1, rows_w, K // 32), dtype=torch.uint8, device="cuda")
             workloads.w_device(w, which, c, s, e, e + 1)
             hc, hs = workloads.w_host(w, which, e, e + 1)

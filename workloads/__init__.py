@@ -16,6 +16,10 @@ Value recipe (identical bytes from the host and the device builds):
   W2  : [E+S, H, I], N(0, 1/I) -> E2M1 + UE8M0 per 32 along I
   topk: uniform without replacement (or Zipf for "skewed"), weights = softmax of N(0,1) logits
 
+The FP8-weight variants (w_fmt = 1: decode_fp8w, prefill_fp8w) draw the same
+weight values and quantise them to E4M3 + UE8M0 per 32 (MXFP8, one byte per
+element) instead of E2M1.
+
 This module holds no step of the expert computation; it only produces inputs.
 """
 from __future__ import annotations
@@ -48,6 +52,7 @@ class Workload:
     clamp: float = 0.0
     zipf: float = 0.0
     seed: int = 0
+    w_fmt: int = 0  # weights: 0 = E2M1 (MXFP4, two per byte), 1 = E4M3 (MXFP8, one per byte)
 
     @property
     def Ep(self) -> int:
@@ -80,9 +85,14 @@ class Workload:
         n = self.rows if n_rows is None else n_rows
         return 6.0 * self.H * self.I * n
 
+    @property
+    def w_elem_bytes(self) -> float:
+        """Bytes per weight element: 1/2 (E2M1) or 1 (E4M3)."""
+        return 1.0 if self.w_fmt else 0.5
+
     def expert_bytes(self) -> float:
-        """Weight bytes one expert streams: W1 + W2 codes (1/2 B) and scales (1/32 B)."""
-        return 3.0 * self.H * self.I * (0.5 + 1.0 / 32.0)
+        """Weight bytes one expert streams: W1 + W2 codes and scales (1/32 B per element)."""
+        return 3.0 * self.H * self.I * (self.w_elem_bytes + 1.0 / 32.0)
 
 
 CONFIGS = {
@@ -91,6 +101,9 @@ CONFIGS = {
     "mid": Workload("mid", T=1024, H=4096, I=1536, E=128, k=8, clamp=7.0, seed=2),
     "skewed": Workload("skewed", T=4096, H=7168, I=2048, E=256, k=8, S=1, zipf=1.2, seed=3),
     "prefill": Workload("prefill", T=16384, H=7168, I=2048, E=256, k=8, seed=4),
+    # FP8 (MXFP8) weight variants of the decode and prefill shapes
+    "decode_fp8w": Workload("decode_fp8w", T=8, H=7168, I=2048, E=256, k=8, seed=5, w_fmt=1),
+    "prefill_fp8w": Workload("prefill_fp8w", T=16384, H=7168, I=2048, E=256, k=8, seed=6, w_fmt=1),
 }
 
 
@@ -124,6 +137,8 @@ def _lib_host():
         lib.syn_gen_x.restype = None
         lib.syn_gen_w.argtypes = [u64, i32, i32, i32, i32, i32, f32, p, p, i32]
         lib.syn_gen_w.restype = None
+        lib.syn_gen_w8.argtypes = [u64, i32, i32, i32, i32, i32, f32, p, p, i32]
+        lib.syn_gen_w8.restype = None
         lib.syn_gen_routing.argtypes = [u64, i32, i32, i32, ctypes.c_double, p, p]
         lib.syn_gen_routing.restype = i32
         lib.syn_u64_at.argtypes = [u64, u64]
@@ -147,6 +162,8 @@ def _lib_dev():
         lib.syn_dev_gen_x.restype = i32
         lib.syn_dev_gen_w.argtypes = [u64, i32, i32, i32, i32, i32, f32, p, p, p]
         lib.syn_dev_gen_w.restype = i32
+        lib.syn_dev_gen_w8.argtypes = [u64, i32, i32, i32, i32, i32, f32, p, p, p]
+        lib.syn_dev_gen_w8.restype = i32
         _dev = lib
     return _dev
 
@@ -188,17 +205,23 @@ def weight_shape(w: Workload, which: int):
     return (2 * w.I, w.H) if which == TAG_W1 else (w.H, w.I)
 
 
+def code_bytes(w: Workload, K: int) -> int:
+    """Bytes of one weight row of K elements."""
+    return K if w.w_fmt else K // 2
+
+
 def w_host(w: Workload, which: int, e0: int = 0, e1: int | None = None, nthreads: int | None = None):
-    """Weights of experts [e0, e1): (codes uint8 [n,rows,K/2], scales uint8 [n,rows,K/32])."""
+    """Weights of experts [e0, e1): (codes uint8 [n,rows,K/2] (E2M1) or [n,rows,K] (E4M3),
+    scales uint8 [n,rows,K/32])."""
     e1 = w.Ep if e1 is None else e1
     rows, K = weight_shape(w, which)
     n = max(0, e1 - e0)
-    codes = np.zeros((n, rows, K // 2), np.uint8)
+    codes = np.zeros((n, rows, code_bytes(w, K)), np.uint8)
     sf = np.zeros((n, rows, K // 32), np.uint8)
     std = w.std1 if which == TAG_W1 else w.std2
     if n:
-        _lib_host().syn_gen_w(w.seed, which, rows, K, e0, e1, std, _ptr(codes), _ptr(sf),
-                              nthreads or _nthreads())
+        gen = _lib_host().syn_gen_w8 if w.w_fmt else _lib_host().syn_gen_w
+        gen(w.seed, which, rows, K, e0, e1, std, _ptr(codes), _ptr(sf), nthreads or _nthreads())
     return codes, sf
 
 
@@ -228,8 +251,8 @@ def w_device(w: Workload, which: int, codes, sf, e0: int = 0, e1: int | None = N
     rows, K = weight_shape(w, which)
     std = w.std1 if which == TAG_W1 else w.std2
     s = stream if stream is not None else torch.cuda.current_stream()
-    rc = _lib_dev().syn_dev_gen_w(w.seed, which, rows, K, e0, e1, std, codes.data_ptr(), sf.data_ptr(),
-                                  s.cuda_stream)
+    gen = _lib_dev().syn_dev_gen_w8 if w.w_fmt else _lib_dev().syn_dev_gen_w
+    rc = gen(w.seed, which, rows, K, e0, e1, std, codes.data_ptr(), sf.data_ptr(), s.cuda_stream)
     if rc != 0:
         raise RuntimeError(f"device weight generator failed ({rc})")
 
@@ -246,7 +269,7 @@ def device_inputs(w: Workload, device="cuda"):
     out.update(x=x, x_sf=xsf)
     for which, name in ((TAG_W1, "w1"), (TAG_W2, "w2")):
         rows, K = weight_shape(w, which)
-        c = torch.empty((w.Ep, rows, K // 2), dtype=torch.uint8, device=device)
+        c = torch.empty((w.Ep, rows, code_bytes(w, K)), dtype=torch.uint8, device=device)
         s = torch.empty((w.Ep, rows, K // 32), dtype=torch.uint8, device=device)
         w_device(w, which, c, s)
         out[name] = c

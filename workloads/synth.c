@@ -19,7 +19,7 @@ void syn_gen_x(uint64_t seed, int H, int t0, int t1, uint8_t* x, uint8_t* x_sf) 
 
 typedef struct {
   uint64_t key;
-  int rows, K, e0, e1, th, nth;
+  int rows, K, e0, e1, th, nth, fp8;
   float std_;
   uint8_t *w, *w_sf;
 } syn_wjob;
@@ -31,9 +31,14 @@ static void* syn_w_worker(void* arg) {
   for (long r = j->th; r < total; r += j->nth) {
     long e = j->e0 + r / j->rows, n = r % j->rows;
     uint64_t base = ((uint64_t)e * (uint64_t)j->rows + (uint64_t)n) * (uint64_t)j->K;
-    for (int g = 0; g < G; ++g)
-      syn_group_w(j->key, base + (uint64_t)g * 32u, j->std_,
-                  j->w + (size_t)r * (j->K / 2) + (size_t)g * 16, j->w_sf + (size_t)r * G + g);
+    for (int g = 0; g < G; ++g) {
+      if (j->fp8)
+        syn_group_w8(j->key, base + (uint64_t)g * 32u, j->std_, j->w + (size_t)r * j->K + (size_t)g * 32,
+                     j->w_sf + (size_t)r * G + g);
+      else
+        syn_group_w(j->key, base + (uint64_t)g * 32u, j->std_,
+                    j->w + (size_t)r * (j->K / 2) + (size_t)g * 16, j->w_sf + (size_t)r * G + g);
+    }
   }
   return NULL;
 }
@@ -41,8 +46,8 @@ static void* syn_w_worker(void* arg) {
 /* Weight tensor `which` (SYN_TAG_W1 or SYN_TAG_W2) for experts [e0, e1):
  * rows_per_expert rows of K elements each, E2M1 packed + UE8M0 per 32 along K.
  * Output buffers hold only the requested experts, expert e0 first. */
-void syn_gen_w(uint64_t seed, int which, int rows_per_expert, int K, int e0, int e1,
-               float std_, uint8_t* w, uint8_t* w_sf, int nthreads) {
+static void syn_gen_w_any(uint64_t seed, int which, int rows_per_expert, int K, int e0, int e1,
+                          float std_, uint8_t* w, uint8_t* w_sf, int nthreads, int fp8) {
   if (nthreads < 1) nthreads = 1;
   if (nthreads > 256) nthreads = 256;
   syn_wjob jobs[256];
@@ -51,10 +56,22 @@ void syn_gen_w(uint64_t seed, int which, int rows_per_expert, int K, int e0, int
     jobs[i].key = syn_stream_key(seed, (uint64_t)which);
     jobs[i].rows = rows_per_expert; jobs[i].K = K; jobs[i].e0 = e0; jobs[i].e1 = e1;
     jobs[i].th = i; jobs[i].nth = nthreads; jobs[i].std_ = std_; jobs[i].w = w; jobs[i].w_sf = w_sf;
+    jobs[i].fp8 = fp8;
   }
   for (int i = 1; i < nthreads; ++i) pthread_create(&tid[i], NULL, syn_w_worker, &jobs[i]);
   syn_w_worker(&jobs[0]);
   for (int i = 1; i < nthreads; ++i) pthread_join(tid[i], NULL);
+}
+
+void syn_gen_w(uint64_t seed, int which, int rows_per_expert, int K, int e0, int e1,
+               float std_, uint8_t* w, uint8_t* w_sf, int nthreads) {
+  syn_gen_w_any(seed, which, rows_per_expert, K, e0, e1, std_, w, w_sf, nthreads, 0);
+}
+
+/* Same weights quantised to E4M3 + UE8M0 (one byte per element, K bytes per row). */
+void syn_gen_w8(uint64_t seed, int which, int rows_per_expert, int K, int e0, int e1,
+                float std_, uint8_t* w, uint8_t* w_sf, int nthreads) {
+  syn_gen_w_any(seed, which, rows_per_expert, K, e0, e1, std_, w, w_sf, nthreads, 1);
 }
 
 /* Routing for T tokens over E experts, k distinct experts per token.

@@ -20,7 +20,8 @@
  *   so the sum is an integer multiple of 2^-17 and is exact in float32.
  *
  *   Block quantisation (OCP Microscaling formats v1.0): one shared UE8M0
- *   exponent per 32 consecutive elements along the reduction dimension,
+ *   exponent per 32 consecutive elements along the reduction dimension
+ *   (weights in E2M1 (MXFP4) or, for the FP8 weight variant, E4M3 (MXFP8)),
  *   chosen as the smallest power of two s with amax / qmax <= s (qmax = 448
  *   for E4M3, 6 for E2M1), elements rounded to nearest-even in the element
  *   format after division by s.
@@ -195,6 +196,22 @@ SYN_FN void syn_group_w(uint64_t key, uint64_t idx0, float std_, uint8_t* packed
     uint8_t hi = syn_e2m1_encode(v[2 * j + 1] * inv);
     packed16[j] = (uint8_t)(lo | (hi << 4));
   }
+  *sf = code;
+}
+
+/* One 32-element group of FP8 weights: N(0, std^2) -> E4M3 + UE8M0 (the MXFP8
+ * weight variant), one byte per element. Same stream elements as syn_group_w. */
+SYN_FN void syn_group_w8(uint64_t key, uint64_t idx0, float std_, uint8_t* q32, uint8_t* sf) {
+  float v[32];
+  float amax = 0.0f;
+  for (int j = 0; j < 32; ++j) {
+    v[j] = syn_normal(key, idx0 + (uint64_t)j) * std_;
+    float a = v[j] < 0.0f ? -v[j] : v[j];
+    if (a > amax) amax = a;
+  }
+  uint8_t code = syn_scale_code(amax, 448.0f);
+  float inv = syn_pow2(127 - (int)code);
+  for (int j = 0; j < 32; ++j) q32[j] = syn_e4m3_encode(v[j] * inv);
   *sf = code;
 }
 

@@ -42,6 +42,27 @@ __global__ void syn_w_kernel(uint64_t key, int rows, int K, int e0, long long gr
   }
 }
 
+__global__ void syn_w8_kernel(uint64_t key, int rows, int K, int e0, long long groups, float std_,
+                              uint8_t* w, uint8_t* w_sf) {
+  const int G = K / 32;
+  for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < groups;
+       g += (long long)gridDim.x * blockDim.x) {
+    long long r = g / G, gg = g % G;
+    long long e = e0 + r / rows, n = r % rows;
+    uint64_t base = ((uint64_t)e * (uint64_t)rows + (uint64_t)n) * (uint64_t)K + (uint64_t)gg * 32u;
+    uint8_t q[32];
+    uint8_t sf;
+    syn_group_w8(key, base, std_, q, &sf);
+    uint4 a, b;
+    memcpy(&a, q, 16);
+    memcpy(&b, q + 16, 16);
+    uint4* dst = reinterpret_cast<uint4*>(w + (size_t)r * K + (size_t)gg * 32);
+    dst[0] = a;
+    dst[1] = b;
+    w_sf[(size_t)r * G + gg] = sf;
+  }
+}
+
 static int syn_grid(long long groups) {
   long long b = (groups + 255) / 256;
   if (b > 152 * 64) b = 152 * 64;
@@ -64,6 +85,16 @@ extern "C" int syn_dev_gen_w(uint64_t seed, int which, int rows_per_expert, int 
   if (K % 32) return -1;
   long long groups = (long long)(e1 - e0) * rows_per_expert * (K / 32);
   syn_w_kernel<<<syn_grid(groups), 256, 0, (cudaStream_t)stream>>>(
+      syn_stream_key(seed, (uint64_t)which), rows_per_expert, K, e0, groups, std_, (uint8_t*)w, (uint8_t*)w_sf);
+  return (int)cudaGetLastError();
+}
+
+extern "C" int syn_dev_gen_w8(uint64_t seed, int which, int rows_per_expert, int K, int e0, int e1,
+                              float std_, void* w, void* w_sf, void* stream) {
+  if (e1 <= e0) return 0;
+  if (K % 32) return -1;
+  long long groups = (long long)(e1 - e0) * rows_per_expert * (K / 32);
+  syn_w8_kernel<<<syn_grid(groups), 256, 0, (cudaStream_t)stream>>>(
       syn_stream_key(seed, (uint64_t)which), rows_per_expert, K, e0, groups, std_, (uint8_t*)w, (uint8_t*)w_sf);
   return (int)cudaGetLastError();
 }
