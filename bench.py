@@ -70,8 +70,8 @@ def algorithmic(w, counts):
     R = int(counts.sum())
     touched = int((counts > 0).sum())
     sf = 1.0 / 32.0
-    w1 = touched * 2 * w.I * w.H * (0.5 + sf)
-    w2 = touched * w.H * w.I * (0.5 + sf)
+    w1 = touched * 2 * w.I * w.H * (w.w_elem_bytes + sf)
+    w2 = touched * w.H * w.I * (w.w_elem_bytes + sf)
     l1_act = R * w.H * (1 + sf) + R * w.I * (1 + sf)          # pool rows in, FP8 L2 operand out
     l2_act = R * w.I * (1 + sf) + R * w.H * 2                  # FP8 L2 operand in, BF16 slot rows out
     return dict(rows=R, touched=touched, flops=6.0 * w.H * w.I * R, l1_flops=4.0 * w.H * w.I * R,
@@ -156,7 +156,7 @@ def oracle_sample(w, n_tokens):
     parts1 = [workloads.w_host(w, workloads.TAG_W1, e, e + 1) for e in experts]
     parts2 = [workloads.w_host(w, workloads.TAG_W2, e, e + 1) for e in experts]
     cat = lambda ps, i: np.ascontiguousarray(np.concatenate([p[i] for p in ps]))
-    dims = dict(T=len(tokens), H=w.H, I=w.I, E=len(routed), k=w.k, S=w.S, clamp=w.clamp)
+    dims = dict(T=len(tokens), H=w.H, I=w.I, E=len(routed), k=w.k, S=w.S, clamp=w.clamp, w_fmt=w.w_fmt)
     args = (np.concatenate([a for a, _ in xs]), np.concatenate([b for _, b in xs]), sub_idx,
             np.ascontiguousarray(wt[tokens]), cat(parts1, 0), cat(parts1, 1), cat(parts2, 0), cat(parts2, 1))
     return dims, args, len(tokens), len(experts)
@@ -193,16 +193,21 @@ def run_reference(args, world, rank):
     sample = f"first {nt} of {w.T} tokens of the {w.name} workload ({nt * w.Kp} slot rows, {ne} experts), per step"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "fp8xfp4 (fp32 accumulate)", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic",
             "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+def dtype_of(w):
+    return ("fp8xfp8" if w.w_fmt else "fp8xfp4") + " (fp32 accumulate)"
+
+
 def workload_config(w):
     return {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "topk": w.k, "shared": w.S,
             "swiglu_clamp": w.clamp, "routing": f"zipf({w.zipf})" if w.zipf else "uniform", "seed": w.seed,
+            "weights": "MXFP8 (E4M3 + UE8M0/32)" if w.w_fmt else "MXFP4 (E2M1 + UE8M0/32)",
             "l2": "flushed between steps (256 MB write outside the timed events)"}
 
 
@@ -218,7 +223,7 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl")
     w = workloads.CONFIGS[args.workload]
     d = workloads.device_inputs(w)
-    moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp, schedule=args.schedule)
+    moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp, schedule=args.schedule, weight_format=w.w_fmt)
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
     moe.workspace(w.T)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
@@ -353,7 +358,7 @@ def report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp8xfp4 (fp32 accumulate)", "data": "synthetic",
+            "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic",
             "config": dict(workload_config(w), parallelism=f"{world} independent replicas" if world > 1 else "1 GPU",
                            gemm_schedule=("fused" if "gemm" in kern else "split")
                            + (" (auto)" if args.schedule == "auto" else "")),

@@ -107,6 +107,17 @@ MM_API mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_ma
 #define MM_FUSED_MAX_ROWS_PER_EXPERT 128
 MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
 
+/* Weight element format (both linears). MM_WEIGHTS_MXFP4 (the default): E2M1
+ * codes packed two per byte, the even K index in the low nibble (OCP MXFP4).
+ * MM_WEIGHTS_MXFP8: E4M3 codes, one byte per element (OCP MXFP8; the FP8 x FP8
+ * variant of the pages' SM90 recipe, with the UE8M0-per-32 block scales the
+ * block-scaled tensor-core MMA reads instead of float scales per 128). Either
+ * way one UE8M0 scale per 32 elements along K. Other values:
+ * MM_ERR_INVALID_ARG. */
+#define MM_WEIGHTS_MXFP4 0
+#define MM_WEIGHTS_MXFP8 1
+MM_API mm_status_t mm_set_weight_format(mm_handle_t h, int format);
+
 /* Expert-parallel-ready routing outputs ("MegaMoE research report", the
  * dispatch step of the expert-parallel layer and its per-rank receive
  * statistics; here every expert is local and nothing is sent).
@@ -142,8 +153,10 @@ MM_API mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes);
  *            other values disable the slot and set MM_DEV_BAD_ROUTING
  *   topk_w   device, [T][topk] float32 (need not sum to 1)
  *   w1       device, [E+S][2I][H/2] E2M1 packed; rows [0,I) gate, [I,2I) up   (32-byte aligned)
+ *            (MM_WEIGHTS_MXFP8: [E+S][2I][H] E4M3)
  *   w1_sf    device, [E+S][2I][H/32] UE8M0                                     (4-byte aligned)
  *   w2       device, [E+S][H][I/2] E2M1 packed                                  (32-byte aligned)
+ *            (MM_WEIGHTS_MXFP8: [E+S][H][I] E4M3)
  *   w2_sf    device, [E+S][H][I/32] UE8M0                                      (4-byte aligned)
  *   out_bf16 device, [T][H] bfloat16, fully overwritten               (16-byte aligned)
  *   ws       device workspace of ws_bytes >= mm_workspace_bytes(T) (256-byte aligned),

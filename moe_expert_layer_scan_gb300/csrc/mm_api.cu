@@ -33,6 +33,8 @@ struct mm_handle {
   // cumulative per-expert row counts (device, may be null)
   int ep_ranks;
   int32_t* expert_stats;
+  // weight format: MM_WEIGHTS_MXFP4 / MM_WEIGHTS_MXFP8
+  int w_fmt;
   // optional per-launch events (route, gather, L1, L2, combine, end) and the
   // stage name of each recorded interval
   bool profile;
@@ -124,6 +126,7 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
   h->schedule = MM_SCHEDULE_AUTO;
   h->ep_ranks = 1;
   h->expert_stats = nullptr;
+  h->w_fmt = MM_WEIGHTS_MXFP4;
   h->profile = false;
   h->n_recorded = 0;
   *out = h;
@@ -140,6 +143,13 @@ mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_math) {
 mm_status_t mm_set_schedule(mm_handle_t h, int schedule) {
   if (!h || schedule < MM_SCHEDULE_AUTO || schedule > MM_SCHEDULE_FUSED) return MM_ERR_INVALID_ARG;
   h->schedule = schedule;
+  return MM_OK;
+}
+
+mm_status_t mm_set_weight_format(mm_handle_t h, int format) {
+  if (!h || (format != MM_WEIGHTS_MXFP4 && format != MM_WEIGHTS_MXFP8)) return MM_ERR_INVALID_ARG;
+  if (format != h->w_fmt) h->w1_key = h->w2_key = nullptr;  // cached weight maps describe the old layout
+  h->w_fmt = format;
   return MM_OK;
 }
 
@@ -255,12 +265,13 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   if (mm_launch_gather(&ga, T * Kp, stream) != 0) return MM_ERR_CUDA;
 
   // Tensor maps: weights are cached per base pointer, activations live in the workspace.
+  const bool fp4 = h->w_fmt == MM_WEIGHTS_MXFP4;
   if (h->w1_key != w1) {
-    if (!encode_2d(&h->tm_w1, w1, true, (uint64_t)h->H, (uint64_t)Ep * 2 * h->I, 128)) return MM_ERR_CUDA;
+    if (!encode_2d(&h->tm_w1, w1, fp4, (uint64_t)h->H, (uint64_t)Ep * 2 * h->I, 128)) return MM_ERR_CUDA;
     h->w1_key = w1;
   }
   if (h->w2_key != w2) {
-    if (!encode_2d(&h->tm_w2, w2, true, (uint64_t)h->I, (uint64_t)Ep * h->H, 128)) return MM_ERR_CUDA;
+    if (!encode_2d(&h->tm_w2, w2, fp4, (uint64_t)h->I, (uint64_t)Ep * h->H, 128)) return MM_ERR_CUDA;
     h->w2_key = w2;
   }
   CUtensorMap tm_x, tm_q;
@@ -284,6 +295,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g1.clamp = h->clamp; g1.fast_math = h->fast_math; g1.timeout_ns = h->timeout_ns;
   g1.w_sf_vec = aligned(w1_sf, 16) && (h->H / 32) % 16 == 0;
   g1.act_sf_vec = (h->H / 32) % 16 == 0;
+  g1.w_fp8 = fp4 ? 0 : 1;
   g1.ready = reinterpret_cast<int32_t*>(base + L.ready);
   g1.ready_target = f1 * mm_gemm_epilogue_warps(variant);
 

@@ -13,7 +13,8 @@
 //     per-slot row r.
 //
 // Orientation: the weights are the MMA's M=128 operand (E2M1, read by TMA as
-// 16 x 4-bit groups padded to 16 bytes in SMEM) and the expert's token rows are
+// 16 x 4-bit groups padded to 16 bytes in SMEM; or E4M3 weights, one byte per
+// element, the same 128-byte SMEM rows) and the expert's token rows are
 // the N operand (E4M3), N = the tile's rows rounded up to 16. One CTA per SM
 // walks a flat list of (expert, weight block, token tile) tiles.
 //
@@ -283,6 +284,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     uint32_t it = 0;
     bool ok = true;
     bool cur_ready = false;  // the current tile's counter was seen complete by a peek
+    // transaction bytes of one 128x128 weight box: packed E2M1 or E4M3
+    const uint32_t a_tx = g1.w_fp8 ? (uint32_t)(C::BM * C::BK) : (uint32_t)C::A_TX;
     for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
       const bool l1 = is_l1(tile);
       const Phase g = phase_of(l1, g1, g2);
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
         uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
         if (lane == 0) {
           // the whole token tile lands here: this CTA's share and the others' multicasts
-          mbar_arrive_expect_tx(&full[s], (t.active ? (two ? 2 : 1) : 0) * C::A_TX + C::B_BYTES);
+          mbar_arrive_expect_tx(&full[s], (t.active ? (two ? 2 : 1) : 0) * a_tx + C::B_BYTES);
           if (t.active) tma_load_2d(sA, tw, &full[s], kb * C::BK, wrow);
           if (two) tma_load_2d(sA + C::A_BYTES, tw, &full[s], kb * C::BK, wrow + g.second);
           if constexpr (CS == 1) {
@@ -461,6 +464,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     // second L2 block still commits, so the barrier counts hold).
     if (lane == 0) {
       const int u = warp - 1;
+      // A (weights): E2M1 (format 5) or E4M3 (format 0); B (tokens): E4M3
+      const uint32_t a_fmt = g1.w_fp8 ? 0u : 5u;
       uint32_t it = 0, tcount = 0;
       bool ok = true;
       for (int tile = tile0; tile < num_tiles && ok; tile += tile_step, ++tcount) {
@@ -495,7 +500,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
             const uint64_t db = sdesc_kmajor_sw128(smem_u32(sB));
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint32_t id = idesc_mxf8f6f4(5u, 0u, n_mma, (uint32_t)k);
+              const uint32_t id = idesc_mxf8f6f4(a_fmt, 0u, n_mma, (uint32_t)k);
               // +32 bytes of K per step inside the 128-byte swizzle atom (2 in 16-byte units)
               tc_mma_mxf8f6f4(d, da + 2u * k, db + 2u * k, id, sfa, sfb, (kb > 0 || k > 0) ? 1u : 0u);
             }

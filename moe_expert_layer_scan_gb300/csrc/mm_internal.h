@@ -125,6 +125,7 @@ struct GemmArgs {
   // tiles of that token tile wait for ready_target arrivals.
   int32_t* ready;
   int ready_target;
+  int w_fp8;  // weights are E4M3 (one byte per element) instead of packed E2M1
 };
 
 struct CombineArgs {

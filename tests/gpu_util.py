@@ -58,7 +58,7 @@ class GpuRun:
         self.w = w
         self.mm = mm
         self.moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp if clamp is None else clamp,
-                              fast_math=fast_math, schedule=schedule)
+                              fast_math=fast_math, schedule=schedule, weight_format=w.w_fmt)
         if inputs is None:
             if device_weights:
                 self.d = workloads.device_inputs(w)

@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 
 
 def dims(w):
-    return dict(T=w.T, H=w.H, I=w.I, E=w.E, k=w.k, S=w.S, clamp=w.clamp)
+    return dict(T=w.T, H=w.H, I=w.I, E=w.E, k=w.k, S=w.S, clamp=w.clamp, w_fmt=w.w_fmt)
 
 
 def bits(t):
@@ -143,3 +143,22 @@ def test_schedule_choice_and_validation():
         mm.mm_set_schedule(moe.h, 2)
     with pytest.raises(mm.MMError):
         mm.mm_set_schedule(moe.h, -2)
+
+
+def test_weight_format_validation_and_switch(orc):
+    """Switching the weight format re-describes the cached weight layout: the
+    same handle runs an MXFP4 and then an MXFP8 problem correctly."""
+    import torch
+    import moe_expert_layer_scan_gb300 as mm
+    w4 = Workload("fmt4", T=6, H=256, I=128, E=4, k=2, seed=305)
+    w8 = w4.replace(name="fmt8", w_fmt=1)
+    run = G.GpuRun(w4)
+    out4 = bits(run.run())
+    G.assert_out_close(out4, ref_out(orc, w4, workloads.host_inputs(w4))["out"])
+    h8 = workloads.host_inputs(w8)
+    mm.mm_set_weight_format(run.moe.h, mm.MM_WEIGHTS_MXFP8)
+    d8 = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in h8.items()}
+    out8 = bits(run.run(**d8))
+    G.assert_out_close(out8, ref_out(orc, w8, h8)["out"])
+    with pytest.raises(mm.MMError):
+        mm.mm_set_weight_format(run.moe.h, 2)

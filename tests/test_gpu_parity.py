@@ -29,11 +29,14 @@ SMALL_CASES = {
     # H / 128 odd: the last L2 tile has a single 128-row block of W2
     "odd_h_small": Workload("odd_h_small", T=8, H=384, I=256, E=4, k=2, seed=108),
     "odd_h_large": Workload("odd_h_large", T=40, H=640, I=384, E=3, k=2, S=1, seed=109),
+    # FP8 (MXFP8) weights, 16-token and 112-token tiles
+    "fp8w_small": Workload("fp8w_small", T=8, H=1024, I=512, E=8, k=4, seed=110, w_fmt=1),
+    "fp8w_large": Workload("fp8w_large", T=48, H=640, I=384, E=4, k=2, S=1, clamp=3.0, seed=111, w_fmt=1),
 }
 
 
 def dims(w):
-    return dict(T=w.T, H=w.H, I=w.I, E=w.E, k=w.k, S=w.S, clamp=w.clamp)
+    return dict(T=w.T, H=w.H, I=w.I, E=w.E, k=w.k, S=w.S, clamp=w.clamp, w_fmt=w.w_fmt)
 
 
 def oracle_run(orc, w, h):
@@ -84,7 +87,7 @@ def _gen_weights(w):
     return gen
 
 
-@pytest.mark.parametrize("name", ["decode", "mid", "skewed", "prefill"])
+@pytest.mark.parametrize("name", ["decode", "mid", "skewed", "prefill", "decode_fp8w", "prefill_fp8w"])
 def test_parity_full_size_sampled(name, orc):
     """Full workload in the benchmark's launch configuration (weights generated
     in HBM); routing compared in full, outputs on sampled tokens that the oracle
