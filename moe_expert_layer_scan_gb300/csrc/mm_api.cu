@@ -25,8 +25,12 @@ struct mm_handle {
   // cached weight tensor maps (keyed by base pointer)
   const void* w1_key;
   const void* w2_key;
+  const void* w1sf_key;
+  const void* w2sf_key;
   CUtensorMap tm_w1;
   CUtensorMap tm_w2;
+  CUtensorMap tm_w1sf;  // scale rows, 16-byte x 128-row boxes
+  CUtensorMap tm_w2sf;
   // GEMM schedule: MM_SCHEDULE_AUTO / _SPLIT / _FUSED
   int schedule;
   // expert-parallel-ready routing: destination ranks and the caller's
@@ -72,6 +76,21 @@ bool encode_2d(CUtensorMap* m, const void* base, bool fp4, uint64_t k_elems, uin
   CUresult r = fn(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Scale rows [rows][cols] bytes, boxes of 16 bytes (four K steps) x 128 rows,
+// no swizzle (the scale warp reads them with plain 16-byte loads).
+bool encode_sf(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {16, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -122,7 +141,7 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
     long ms = atol(t);
     if (ms > 0) h->timeout_ns = (unsigned long long)ms * 1000000ull;
   }
-  h->w1_key = h->w2_key = nullptr;
+  h->w1_key = h->w2_key = h->w1sf_key = h->w2sf_key = nullptr;
   h->schedule = MM_SCHEDULE_AUTO;
   h->ep_ranks = 1;
   h->expert_stats = nullptr;
@@ -274,12 +293,33 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
     if (!encode_2d(&h->tm_w2, w2, fp4, (uint64_t)h->I, (uint64_t)Ep * h->H, 128)) return MM_ERR_CUDA;
     h->w2_key = w2;
   }
-  CUtensorMap tm_x, tm_q;
+  GemmMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  maps.w1 = h->tm_w1;
+  maps.w2 = h->tm_w2;
   // token boxes: each CTA of a cluster loads (and multicasts) 1/cs of the token tile
-  if (!encode_2d(&tm_x, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, (uint32_t)(bn1 / cs)))
+  if (!encode_2d(&maps.a1, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, (uint32_t)(bn1 / cs)))
     return MM_ERR_CUDA;
-  if (!encode_2d(&tm_q, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)(bn2 / cs)))
+  if (!encode_2d(&maps.a2, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)(bn2 / cs)))
     return MM_ERR_CUDA;
+  // Scale rows by TMA when every scale row is a whole number of 16-byte groups
+  // (K a multiple of 512) and the weight scale tensors are 16-byte aligned;
+  // otherwise the scale warp loads them itself.
+  const bool sf_tma = h->H % 512 == 0 && h->I % 512 == 0 && aligned(w1_sf, 16) && aligned(w2_sf, 16);
+  if (sf_tma) {
+    if (h->w1sf_key != w1_sf) {
+      if (!encode_sf(&h->tm_w1sf, w1_sf, (uint64_t)h->H / 32, (uint64_t)Ep * 2 * h->I)) return MM_ERR_CUDA;
+      h->w1sf_key = w1_sf;
+    }
+    if (h->w2sf_key != w2_sf) {
+      if (!encode_sf(&h->tm_w2sf, w2_sf, (uint64_t)h->I / 32, (uint64_t)Ep * h->H)) return MM_ERR_CUDA;
+      h->w2sf_key = w2_sf;
+    }
+    maps.wsf1 = h->tm_w1sf;
+    maps.wsf2 = h->tm_w2sf;
+    if (!encode_sf(&maps.asf1, base + L.pool_sf, (uint64_t)h->H / 32, (uint64_t)L.rows_cap)) return MM_ERR_CUDA;
+    if (!encode_sf(&maps.asf2, base + L.l2a_sf, (uint64_t)h->I / 32, (uint64_t)L.rows_cap)) return MM_ERR_CUDA;
+  }
 
   GemmArgs g1;
   memset(&g1, 0, sizeof(g1));
@@ -296,6 +336,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g1.w_sf_vec = aligned(w1_sf, 16) && (h->H / 32) % 16 == 0;
   g1.act_sf_vec = (h->H / 32) % 16 == 0;
   g1.w_fp8 = fp4 ? 0 : 1;
+  g1.sf_tma = sf_tma ? 1 : 0;
   g1.ready = reinterpret_cast<int32_t*>(base + L.ready);
   g1.ready_target = f1 * mm_gemm_epilogue_warps(variant);
 
@@ -312,13 +353,13 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g2.act_sf_vec = (h->I / 32) % 16 == 0;
   if (use_fused(h, T)) {
     mark("gemm");
-    if (mm_launch_gemm_fused(variant, &h->tm_w1, &tm_x, &h->tm_w2, &tm_q, &g1, &g2, stream) != 0)
+    if (mm_launch_gemm_fused(variant, &maps, &g1, &g2, stream) != 0)
       return MM_ERR_CUDA;
   } else {
     mark("l1_gemm");
-    if (mm_launch_gemm(1, variant, &h->tm_w1, &tm_x, &g1, h->num_sms, stream) != 0) return MM_ERR_CUDA;
+    if (mm_launch_gemm(1, variant, &maps, &g1, h->num_sms, stream) != 0) return MM_ERR_CUDA;
     mark("l2_gemm");
-    if (mm_launch_gemm(0, variant, &h->tm_w2, &tm_q, &g2, h->num_sms, stream) != 0) return MM_ERR_CUDA;
+    if (mm_launch_gemm(0, variant, &maps, &g2, h->num_sms, stream) != 0) return MM_ERR_CUDA;
   }
 
   CombineArgs ca;

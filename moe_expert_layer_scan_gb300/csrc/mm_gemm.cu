@@ -78,7 +78,13 @@ struct GemmCfg {
   static constexpr int TAB_INTS = kMaxExperts + 1;
   // L2 tiles whose L1 rows the producer has seen stored (fused schedule)
   static constexpr int L2RDY_OFF = TAB_OFF + 3 * TAB_INTS * 4;
-  static constexpr int SMEM_BYTES = L2RDY_OFF + 16 + 1024;  // + alignment slack
+  // TMA-loaded scale rows: RAW_G groups of four K steps; per group 16 bytes of
+  // each of 128 rows for each weight block and for the token rows
+  static constexpr int RAW_G = 3;
+  static constexpr int RAW_ROWS_BYTES = 128 * 16;
+  static constexpr int RAW_GROUP_BYTES = (NA + 1) * RAW_ROWS_BYTES;
+  static constexpr int RAW_OFF = (L2RDY_OFF + 16 + 127) / 128 * 128;
+  static constexpr int SMEM_BYTES = RAW_OFF + RAW_G * RAW_GROUP_BYTES + 1024;  // + alignment slack
   // TMEM columns: two accumulator buffers, then two scale-factor slots per
   // issuing thread (weight scales: 4 columns, token scales: 4 or 8 columns;
   // every scale-factor address stays a multiple of 4 columns)
@@ -197,9 +203,8 @@ __device__ __forceinline__ float inv_scale(uint32_t code) {
 
 template <int MODE, int BN, int STAGES, int CS>
 __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_a1,
-                const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_a2,
-                const __grid_constant__ GemmArgs g1, const __grid_constant__ GemmArgs g2) {
+    gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g1,
+                const __grid_constant__ GemmArgs g2) {
   using C = GemmCfg<BN, STAGES, CS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -207,7 +212,9 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* rfull = tempty + 2;        // [RAW_G] TMA scale rows landed
+  uint64_t* rempty = rfull + C::RAW_G;  // [RAW_G] scale warp done with a group
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + C::RAW_G);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -220,18 +227,22 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       mbar_init(&tfull[b], C::NI);  // tcgen05.commit after the last K step, per issuing thread
       mbar_init(&tempty[b], Warps<BN>::EPI);  // one arrival per epilogue warp
     }
+    for (int b = 0; b < C::RAW_G; ++b) {
+      mbar_init(&rfull[b], 1);   // producer's expect_tx arrival
+      mbar_init(&rempty[b], 1);  // scale warp, lane 0
+    }
     *abort_flag = 0;
     *reinterpret_cast<int*>(smem + C::L2RDY_OFF) = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     if (MODE != kModeL2) {
-      prefetch_tmap(&tm_w1);
-      prefetch_tmap(&tm_a1);
+      prefetch_tmap(&maps.w1);
+      prefetch_tmap(&maps.a1);
     }
     if (MODE != kModeL1) {
-      prefetch_tmap(&tm_w2);
-      prefetch_tmap(&tm_a2);
+      prefetch_tmap(&maps.w2);
+      prefetch_tmap(&maps.a2);
     }
   }
   if (warp == 2) {
@@ -273,6 +284,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
   // wait sites reported in the status word on expiry: L1 tiles s, L2 tiles 8 + s
   constexpr uint32_t kSiteReady = 8u + 6u;  // an L2 tile waiting for its L1 rows (fused)
   int* l2rdy = reinterpret_cast<int*>(smem + C::L2RDY_OFF);
+  // scale rows by TMA (else the scale warp loads them from global memory)
+  const bool sf_tma = g1.sf_tma != 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -281,7 +294,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     // the current tile) so that the wait is usually over before the tile
     // starts; every observation is handed on to the scale-factor warp
     // (l2rdy counts this CTA's L2 tiles observed ready, in tile order).
-    uint32_t it = 0;
+    uint32_t it = 0, gi = 0;  // stages and scale groups issued
     bool ok = true;
     bool cur_ready = false;  // the current tile's counter was seen complete by a peek
     // transaction bytes of one 128x128 weight box: packed E2M1 or E4M3
@@ -294,8 +307,10 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       const int wrow = tile_wrow(g, t);
       const bool two = has_second(g, t);
       const int kblocks = g.K / C::BK;
-      const CUtensorMap* tw = l1 ? &tm_w1 : &tm_w2;
-      const CUtensorMap* ta = l1 ? &tm_a1 : &tm_a2;
+      const CUtensorMap* tw = l1 ? &maps.w1 : &maps.w2;
+      const CUtensorMap* ta = l1 ? &maps.a1 : &maps.a2;
+      const CUtensorMap* twsf = l1 ? &maps.wsf1 : &maps.wsf2;
+      const CUtensorMap* tasf = l1 ? &maps.asf1 : &maps.asf2;
       if (MODE == kModeFused && !l1 && !cur_ready &&
           counter_ready_relay(g1.ready + t.row0, g1.ready_target, true, l2rdy, abort_flag, g1.status,
                               g1.timeout_ns, kSiteReady) != 1) {
@@ -305,6 +320,23 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       bool next_ready = false;
       const int ntile = tile + tile_step;
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        if (sf_tma && (kb & 3) == 0) {
+          // this group's scale rows (16 bytes = four K steps per row) into a raw slot
+          const int gslot = (int)(gi % C::RAW_G);
+          const uint32_t gph = (gi / C::RAW_G) & 1u;
+          if (!mbar_wait(&rempty[gslot], gph ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 0)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            uint8_t* raw = smem + C::RAW_OFF + gslot * C::RAW_GROUP_BYTES;
+            mbar_arrive_expect_tx(&rfull[gslot], ((t.active ? 1 : 0) + (two ? 1 : 0) + 1) * C::RAW_ROWS_BYTES);
+            if (t.active) tma_load_2d(raw, twsf, &rfull[gslot], kb * 4, wrow);
+            if (two) tma_load_2d(raw + C::RAW_ROWS_BYTES, twsf, &rfull[gslot], kb * 4, wrow + g.second);
+            tma_load_2d(raw + C::NA * C::RAW_ROWS_BYTES, tasf, &rfull[gslot], kb * 4, t.row0);
+          }
+          ++gi;
+        }
         if (MODE == kModeFused && kb == (kblocks > 1 ? 1 : 0) && ntile < num_tiles && !is_l1(ntile)) {
           const Tile tn = tile_of(ntile, false);
           next_ready = counter_ready_relay(g1.ready + tn.row0, g1.ready_target, false, l2rdy, abort_flag, g1.status,
@@ -347,6 +379,62 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
         int dummy = 0;
         mbar_wait(&full[j % STAGES], (j / STAGES) & 1u, reinterpret_cast<volatile int*>(&dummy), gl.status,
                   gl.timeout_ns < 10000000ull ? gl.timeout_ns : 10000000ull, kSiteTail);
+      }
+    }
+  } else if (warp == 3 && sf_tma) {
+    // ------------------------------------------------------------ scale-factor transposer
+    // The producer TMA-loads each group's scale rows (16 bytes = four K steps
+    // per row) into a raw slot; per K step this warp writes the layout
+    // tcgen05.cp.32x128b.warpx4 reads: 16 bytes per lane l holding the step's
+    // four scale bytes of rows l, l+32, l+64, l+96 of each 128-row group.
+    constexpr int NB = C::SFB_ROWS / 32;
+    uint32_t it = 0, gi = 0;
+    bool ok = true;
+    for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
+      const bool l1 = is_l1(tile);
+      const Phase g = phase_of(l1, g1, g2);
+      const uint32_t site0 = l1 ? 0u : 8u;
+      const Tile t = tile_of(tile, l1);
+      const bool two = has_second(g, t);
+      const int nb = (t.nrows + 31) / 32;
+      const int kblocks = g.K / C::BK;
+      for (int kg = 0; kg < kblocks && ok; kg += 4, ++gi) {
+        const int gslot = (int)(gi % C::RAW_G);
+        const uint32_t gph = (gi / C::RAW_G) & 1u;
+        if (!mbar_wait(&rfull[gslot], gph, abort_flag, g1.status, g1.timeout_ns, site0 + 5)) { ok = false; break; }
+        const uint8_t* raw = smem + C::RAW_OFF + gslot * C::RAW_GROUP_BYTES;
+        uint4 wa[C::NA][4], wb[NB];
+#pragma unroll
+        for (int op = 0; op < C::NA; ++op)
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            wa[op][i] = ((op == 0 && t.active) || two)
+                            ? *reinterpret_cast<const uint4*>(raw + op * C::RAW_ROWS_BYTES + (32 * i + lane) * 16)
+                            : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+          wb[j] = j < nb ? *reinterpret_cast<const uint4*>(raw + C::NA * C::RAW_ROWS_BYTES + (32 * j + lane) * 16)
+                         : make_uint4(0u, 0u, 0u, 0u);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rempty[gslot]);  // the raw slot may be refilled
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int s = (int)(it % STAGES);
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 5)) { ok = false; break; }
+          uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
+#pragma unroll
+          for (int op = 0; op < C::NA; ++op)
+            st_shared_v4(sF + op * 512 + lane * 16, word(wa[op][0], c), word(wa[op][1], c), word(wa[op][2], c),
+                         word(wa[op][3], c));
+#pragma unroll
+          for (int q = 0; q < NB / 4; ++q)
+            st_shared_v4(sF + C::NA * 512 + q * 512 + lane * 16, word(wb[4 * q], c), word(wb[4 * q + 1], c),
+                         word(wb[4 * q + 2], c), word(wb[4 * q + 3], c));
+          fence_proxy_async_smem();  // generic-proxy writes, read next by tcgen05.cp
+          mbar_arrive(&full[s]);
+          ++it;
+        }
       }
     }
   } else if (warp == 3) {
@@ -662,12 +750,10 @@ static int set_smem_attr(int* max_ctas) {
 }
 
 template <int MODE, int BN, int STAGES, int CS>
-static int launch(const void* tw1, const void* ta1, const void* tw2, const void* ta2, const GemmArgs* g1,
-                  const GemmArgs* g2, int num_ctas, cudaStream_t st) {
+static int launch(const GemmMaps* maps, const GemmArgs* g1, const GemmArgs* g2, int num_ctas, cudaStream_t st) {
   using C = GemmCfg<BN, STAGES, CS>;
-  auto tm = [](const void* p) { return *static_cast<const CUtensorMap*>(p); };
   return (int)launch_kernel(gemm_kernel<MODE, BN, STAGES, CS>, dim3((unsigned)num_ctas), dim3(Warps<BN>::THREADS),
-                            C::SMEM_BYTES, st, true, CS, tm(tw1), tm(ta1), tm(tw2), tm(ta2), *g1, *g2);
+                            C::SMEM_BYTES, st, true, CS, *maps, *g1, *g2);
 }
 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
@@ -696,33 +782,26 @@ extern "C" int mm_gemm_epilogue_warps(int variant) {
   return variant == 0 ? mm::Warps<mm::kBnSmall>::EPI : mm::Warps<mm::kBnLarge>::EPI;
 }
 
-extern "C" int mm_launch_gemm(int l1, int variant, const void* tmap_w, const void* tmap_act, const mm::GemmArgs* a,
-                              int num_ctas, void* stream) {
+extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a, int num_ctas,
+                              void* stream) {
   using namespace mm;
   (void)num_ctas;
   cudaStream_t st = (cudaStream_t)stream;
   const int mode = l1 ? kModeL1 : kModeL2;
   const int n = g_ctas[mode][variant];
   if (l1) {
-    return variant == 0
-               ? launch<kModeL1, kBnSmall, kStagesSmall, 1>(tmap_w, tmap_act, tmap_w, tmap_act, a, a, n, st)
-               : launch<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(tmap_w, tmap_act, tmap_w, tmap_act, a, a, n,
-                                                                        st);
+    return variant == 0 ? launch<kModeL1, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
+                        : launch<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
   }
-  return variant == 0
-             ? launch<kModeL2, kBnSmall, kStagesSmall, 1>(tmap_w, tmap_act, tmap_w, tmap_act, a, a, n, st)
-             : launch<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(tmap_w, tmap_act, tmap_w, tmap_act, a, a, n,
-                                                                      st);
+  return variant == 0 ? launch<kModeL2, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
+                      : launch<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
 }
 
-extern "C" int mm_launch_gemm_fused(int variant, const void* tmap_w1, const void* tmap_x, const void* tmap_w2,
-                                    const void* tmap_q, const mm::GemmArgs* g1, const mm::GemmArgs* g2,
-                                    void* stream) {
+extern "C" int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const mm::GemmArgs* g1,
+                                    const mm::GemmArgs* g2, void* stream) {
   using namespace mm;
   cudaStream_t st = (cudaStream_t)stream;
   const int n = g_ctas[kModeFused][variant];
-  return variant == 0 ? launch<kModeFused, kBnSmall, kStagesSmall, 1>(tmap_w1, tmap_x, tmap_w2, tmap_q, g1, g2, n,
-                                                                       st)
-                      : launch<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(tmap_w1, tmap_x, tmap_w2, tmap_q,
-                                                                                  g1, g2, n, st);
+  return variant == 0 ? launch<kModeFused, kBnSmall, kStagesSmall, 1>(maps, g1, g2, n, st)
+                      : launch<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(maps, g1, g2, n, st);
 }

@@ -2,6 +2,8 @@
 // workspace layout, kernel argument blocks and tile-shape constants.
 #pragma once
 
+#include <cuda.h>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -126,6 +128,14 @@ struct GemmArgs {
   int32_t* ready;
   int ready_target;
   int w_fp8;  // weights are E4M3 (one byte per element) instead of packed E2M1
+  int sf_tma;  // scale rows are loaded by TMA (every K a multiple of 512, 16-byte aligned scale tensors)
+};
+
+// Tensor maps of one GEMM launch (L1 and L2; a single-linear launch repeats its
+// own): weights, activations, weight scales, activation scales.
+struct GemmMaps {
+  CUtensorMap w1, a1, w2, a2;
+  CUtensorMap wsf1, asf1, wsf2, asf2;
 };
 
 struct CombineArgs {
@@ -143,14 +153,13 @@ int mm_launch_route(const mm::RouteArgs* a, void* stream);
 int mm_route_launches(int slots);  // kernels mm_launch_route enqueues for this many slots
 int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream);
 int mm_launch_combine(const mm::CombineArgs* a, void* stream);
-// variant: 0 = small tiles, 1 = large tiles. tmaps: two 128-byte CUtensorMap blobs (weights, activations).
-int mm_launch_gemm(int l1, int variant, const void* tmap_w, const void* tmap_act, const mm::GemmArgs* a,
-                   int num_ctas, void* stream);
+// variant: 0 = small tiles, 1 = large tiles. maps: the launch's tensor maps (a
+// single-linear launch reads w1/a1/wsf1/asf1 for L1 and w2/a2/wsf2/asf2 for L2).
+int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a, int num_ctas, void* stream);
 // One persistent launch of both GEMMs: every L1 tile, then every L2 tile; an L2
 // tile starts once the L1 epilogues of its token tile have arrived on `ready`.
-// tmaps: W1, pool_x, W2, l2a.
-int mm_launch_gemm_fused(int variant, const void* tmap_w1, const void* tmap_x, const void* tmap_w2,
-                         const void* tmap_q, const mm::GemmArgs* g1, const mm::GemmArgs* g2, void* stream);
+int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const mm::GemmArgs* g1, const mm::GemmArgs* g2,
+                         void* stream);
 int mm_gemm_prepare(void);  // sets the dynamic shared-memory limits and the persistent grid sizes
 int mm_gemm_cluster(int variant);  // CTAs per cluster of the variant
 int mm_gemm_epilogue_warps(int variant);  // epilogue warps per CTA (arrivals per L1 tile in the fused schedule)
