@@ -223,7 +223,8 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl")
     w = workloads.CONFIGS[args.workload]
     d = workloads.device_inputs(w)
-    moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp, schedule=args.schedule, weight_format=w.w_fmt)
+    moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp, schedule=args.schedule, weight_format=w.w_fmt,
+                     tiles=args.tiles)
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")
     moe.workspace(w.T)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
@@ -392,6 +393,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
+    ap.add_argument("--tiles", type=int, default=-1, choices=[-1, 16, 112],
+                    help="token-tile width (-1: the library's choice)")
     ap.add_argument("--schedule", default="auto", choices=["auto", "fused", "split"],
                     help="GEMM schedule: one persistent launch for both linears, one per linear, or the "
                          "library's choice from the rows per expert (default)")

@@ -107,6 +107,25 @@ MM_API mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_ma
 #define MM_FUSED_MAX_ROWS_PER_EXPERT 128
 MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
 
+/* Token-tile width of the grouped GEMMs ("tuned expert-load buckets").
+ *   MM_TILES_16: 16-token tiles pairing two 128-row weight blocks, one MMA
+ *     stream per block, no cluster (weight-stream bound calls);
+ *   MM_TILES_112: 112-token tiles in 2-CTA clusters sharing the token tile by
+ *     multicast, eight epilogue warps (compute bound calls);
+ *   MM_TILES_AUTO (the default): MM_TILES_16 while the call routes at most
+ *     MM_TILES16_MAX_ROWS_PER_EXPERT rows per expert on average
+ *     (T*(topk+S) <= 12*(E+S)), MM_TILES_112 above: the crossover measured on
+ *     GB300 at H = 7168, I = 2048, 256 experts, top-8 and at H = 4096,
+ *     I = 1536, 128 experts, top-8 (16-token tiles faster up to 12 rows per
+ *     expert, 112-token tiles from 14; moe_expert_layer_scan_gb300/tune_tiles.py).
+ * Either width computes the same tiles' sums; the results are identical.
+ * Other values: MM_ERR_INVALID_ARG. */
+#define MM_TILES_AUTO (-1)
+#define MM_TILES_16 16
+#define MM_TILES_112 112
+#define MM_TILES16_MAX_ROWS_PER_EXPERT 12
+MM_API mm_status_t mm_set_tile_policy(mm_handle_t h, int policy);
+
 /* Weight element format (both linears). MM_WEIGHTS_MXFP4 (the default): E2M1
  * codes packed two per byte, the even K index in the low nibble (OCP MXFP4).
  * MM_WEIGHTS_MXFP8: E4M3 codes, one byte per element (OCP MXFP8; the FP8 x FP8

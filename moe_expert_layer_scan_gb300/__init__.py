@@ -23,7 +23,8 @@ MM_DEV_BAD_ROUTING = 0x1
 MM_DEV_TIMEOUT = 0x2
 STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_WORKSPACE_TOO_SMALL",
                 4: "MM_ERR_CUDA", 5: "MM_ERR_DEVICE_TIMEOUT", 6: "MM_ERR_BAD_ROUTING", 7: "MM_ERR_ALIGNMENT"}
-EXPORTS = ["mm_status_string", "mm_create", "mm_set_options", "mm_set_schedule", "mm_set_weight_format",
+EXPORTS = ["mm_status_string", "mm_create", "mm_set_options", "mm_set_schedule", "mm_set_tile_policy",
+           "mm_set_weight_format",
            "mm_set_ep_ranks",
            "mm_set_expert_stats", "mm_workspace_bytes", "mm_run",
            "mm_get_status", "mm_launches_per_run", "mm_debug_views", "mm_debug_timeout_probe", "mm_profile_enable",
@@ -66,6 +67,7 @@ def lib() -> ctypes.CDLL:
         L.mm_set_schedule.argtypes = [p, i32]
         L.mm_set_ep_ranks.argtypes = [p, i32]
         L.mm_set_weight_format.argtypes = [p, i32]
+        L.mm_set_tile_policy.argtypes = [p, i32]
         L.mm_set_expert_stats.argtypes = [p, p]
         L.mm_workspace_bytes.argtypes = [p, i32, ctypes.POINTER(ctypes.c_size_t)]
         L.mm_run.argtypes = [p, i32] + [p] * 10 + [ctypes.c_size_t, p]
@@ -111,6 +113,14 @@ def mm_set_schedule(h: int, schedule="auto") -> None:
     """schedule: "auto" | "split" | "fused" (or the MM_SCHEDULE_* value)."""
     v = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
     _check(lib().mm_set_schedule(h, v), "mm_set_schedule")
+
+
+MM_TILES_AUTO, MM_TILES_16, MM_TILES_112 = -1, 16, 112
+
+
+def mm_set_tile_policy(h: int, policy: int = MM_TILES_AUTO) -> None:
+    """Token-tile width: MM_TILES_AUTO, MM_TILES_16 or MM_TILES_112."""
+    _check(lib().mm_set_tile_policy(h, int(policy)), "mm_set_tile_policy")
 
 
 MM_WEIGHTS_MXFP4, MM_WEIGHTS_MXFP8 = 0, 1
@@ -209,12 +219,14 @@ class MegaMoE:
     """One layer shape bound to a handle; owns a reusable device workspace."""
 
     def __init__(self, E: int, H: int, I: int, topk: int, num_shared: int = 0, swiglu_clamp: float = 0.0,
-                 fast_math: bool = False, schedule="auto", weight_format: int = MM_WEIGHTS_MXFP4):
+                 fast_math: bool = False, schedule="auto", weight_format: int = MM_WEIGHTS_MXFP4,
+                 tiles: int = MM_TILES_AUTO):
         self.E, self.H, self.I, self.topk, self.S = E, H, I, topk, num_shared
         self.h = mm_create(E, H, I, topk, num_shared)
         mm_set_options(self.h, swiglu_clamp, fast_math)
         mm_set_schedule(self.h, schedule)
         mm_set_weight_format(self.h, weight_format)
+        mm_set_tile_policy(self.h, tiles)
         self.ws = None
 
     def workspace(self, T: int, device=None):

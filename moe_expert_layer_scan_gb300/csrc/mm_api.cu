@@ -39,6 +39,8 @@ struct mm_handle {
   int32_t* expert_stats;
   // weight format: MM_WEIGHTS_MXFP4 / MM_WEIGHTS_MXFP8
   int w_fmt;
+  // token-tile width: MM_TILES_AUTO / _16 / _112
+  int tiles;
   // optional per-launch events (route, gather, L1, L2, combine, end) and the
   // stage name of each recorded interval
   bool profile;
@@ -96,7 +98,12 @@ bool encode_sf(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int variant_for(int T) { return T <= kSmallMaxTokens ? 0 : 1; }
+// Tile variant of a call: 0 = 16-token tiles, 1 = 112-token tiles.
+int variant_for(const mm_handle* h, int T) {
+  if (h->tiles == MM_TILES_16) return 0;
+  if (h->tiles == MM_TILES_112) return 1;
+  return (long long)T * (h->k + h->S) <= (long long)MM_TILES16_MAX_ROWS_PER_EXPERT * (h->E + h->S) ? 0 : 1;
+}
 
 }  // namespace
 
@@ -146,6 +153,7 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
   h->ep_ranks = 1;
   h->expert_stats = nullptr;
   h->w_fmt = MM_WEIGHTS_MXFP4;
+  h->tiles = MM_TILES_AUTO;
   h->profile = false;
   h->n_recorded = 0;
   *out = h;
@@ -162,6 +170,12 @@ mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_math) {
 mm_status_t mm_set_schedule(mm_handle_t h, int schedule) {
   if (!h || schedule < MM_SCHEDULE_AUTO || schedule > MM_SCHEDULE_FUSED) return MM_ERR_INVALID_ARG;
   h->schedule = schedule;
+  return MM_OK;
+}
+
+mm_status_t mm_set_tile_policy(mm_handle_t h, int policy) {
+  if (!h || (policy != MM_TILES_AUTO && policy != MM_TILES_16 && policy != MM_TILES_112)) return MM_ERR_INVALID_ARG;
+  h->tiles = policy;
   return MM_OK;
 }
 
@@ -227,7 +241,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
 
   uint8_t* base = static_cast<uint8_t*>(ws);
   const int Ep = h->E + h->S, Kp = h->k + h->S;
-  const int variant = variant_for(T);
+  const int variant = variant_for(h, T);
   const int bn1 = variant == 0 ? kBnSmall : kBnLarge;
   const int bn2 = bn1;
 

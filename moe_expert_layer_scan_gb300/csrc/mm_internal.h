@@ -27,7 +27,6 @@ constexpr int kBnLarge = 112;
 // weight tiles of the same (expert, token tile) and each multicasts its share
 // of the token tile to all of them.
 constexpr int kClusterLarge = 2;
-constexpr int kSmallMaxTokens = 16;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

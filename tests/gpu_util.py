@@ -52,13 +52,13 @@ class GpuRun:
     """Owns a handle, device inputs and a workspace for one workload."""
 
     def __init__(self, w: workloads.Workload, inputs: dict | None = None, fast_math=False, device_weights=False,
-                 clamp=None, schedule="auto"):
+                 clamp=None, schedule="auto", tiles=-1):
         import torch
         import moe_expert_layer_scan_gb300 as mm
         self.w = w
         self.mm = mm
         self.moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp if clamp is None else clamp,
-                              fast_math=fast_math, schedule=schedule, weight_format=w.w_fmt)
+                              fast_math=fast_math, schedule=schedule, weight_format=w.w_fmt, tiles=tiles)
         if inputs is None:
             if device_weights:
                 self.d = workloads.device_inputs(w)

@@ -69,11 +69,11 @@ def test_all_slots_disabled_gives_zero():
 
 
 def test_duplicate_experts_small_variant(orc):
-    """T <= 16 with every slot on one expert: 64 rows over 16-wide token tiles."""
+    """Every slot on one expert: 64 rows over four 16-token tiles."""
     w = Workload("dup", T=16, H=512, I=256, E=4, k=4, seed=205)
     h = workloads.host_inputs(w)
     h["topk_idx"] = np.full_like(h["topk_idx"], 2)
-    run = G.GpuRun(w, inputs=h)
+    run = G.GpuRun(w, inputs=h, tiles=16)
     G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
 
 

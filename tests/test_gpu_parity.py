@@ -16,7 +16,8 @@ from workloads import CONFIGS, Workload
 pytestmark = pytest.mark.gpu
 
 # Several tiles and ragged tails at sizes the oracle finishes in seconds,
-# covering both GEMM variants (<= 16 tokens: 16-wide token tiles).
+# covering both token-tile widths (16-token tiles up to 12 routed rows per
+# expert on average, 112-token tiles above).
 SMALL_CASES = {
     "tiny": CONFIGS["tiny"],
     "decode_e16": Workload("decode_e16", T=8, H=7168, I=2048, E=16, k=8, seed=101),
@@ -122,3 +123,19 @@ def test_fused_schedule_equals_split_bit_for_bit(name):
     assert np.array_equal(oa, ob)
     for k in ("l2a", "l2a_sf", "z"):
         assert np.array_equal(ia[k], ib[k]), k
+
+
+@pytest.mark.parametrize("name,tiles", [("decode_e16", 112), ("small_tiles", 112), ("mid_t32", 16),
+                                        ("skewed_t48", 16), ("fp8w_small", 112)])
+def test_parity_with_the_other_tile_width(name, tiles, orc):
+    """Each token-tile width is correct on the token counts the automatic policy
+    gives to the other one."""
+    w = SMALL_CASES[name]
+    h = workloads.host_inputs(w)
+    ref = oracle_run(orc, w, h)
+    for schedule in ("fused", "split"):
+        run = G.GpuRun(w, inputs=h, schedule=schedule, tiles=tiles)
+        out = out_bits(run.run())
+        inter = run.intermediates(w.T)
+        assert inter["status"] == 0
+        G.assert_out_close(out, ref["out"])
