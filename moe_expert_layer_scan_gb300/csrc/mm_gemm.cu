@@ -85,13 +85,14 @@ struct GemmCfg {
   static constexpr int RAW_GROUP_BYTES = (NA + 1) * RAW_ROWS_BYTES;
   static constexpr int RAW_OFF = (L2RDY_OFF + 16 + 127) / 128 * 128;
   static constexpr int SMEM_BYTES = RAW_OFF + RAW_G * RAW_GROUP_BYTES + 1024;  // + alignment slack
-  // TMEM columns: two accumulator buffers, then two scale-factor slots per
-  // issuing thread (weight scales: 4 columns, token scales: 4 or 8 columns;
-  // every scale-factor address stays a multiple of 4 columns)
+  // TMEM columns: two accumulator buffers, then one scale-factor slot per
+  // stage (every scale-factor address stays a multiple of 4 columns)
   static constexpr int ACC_COLS = NA * BN;
-  static constexpr int SF_ISSUER_COLS = 4 + SFB_ROWS / 32;
+  // per stage: 4 columns of scales per weight block, then the token tile's
+  // (4 per 128 rows), shared by both MMA streams
+  static constexpr int SF_STAGE_COLS = 4 * NA + SFB_ROWS / 32;
   static constexpr int SF_BASE = 2 * ACC_COLS;
-  static constexpr int TMEM_USED = SF_BASE + 2 * NI * SF_ISSUER_COLS;
+  static constexpr int TMEM_USED = SF_BASE + STAGES * SF_STAGE_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
   static_assert(TMEM_USED <= 512, "TMEM budget");
@@ -212,7 +213,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
-  uint64_t* rfull = tempty + 2;        // [RAW_G] TMA scale rows landed
+  uint64_t* sfready = tempty + 2;      // [STAGES] a stage's scales are in TMEM (tcgen05.commit of the copies)
+  uint64_t* rfull = sfready + STAGES;  // [RAW_G] TMA scale rows landed
   uint64_t* rempty = rfull + C::RAW_G;  // [RAW_G] scale warp done with a group
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + C::RAW_G);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -220,7 +222,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1 + 32);  // TMA expect_tx arrival + one arrival per scale-factor lane
+      mbar_init(&full[s], 1);     // TMA expect_tx arrival
+      mbar_init(&sfready[s], 1);  // the scale warp's tcgen05.commit
       mbar_init(&empty[s], C::NI * CS);  // one tcgen05.commit per issuing thread of every CTA of the cluster
     }
     for (int b = 0; b < 2; ++b) {
@@ -286,6 +289,20 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
   int* l2rdy = reinterpret_cast<int*>(smem + C::L2RDY_OFF);
   // scale rows by TMA (else the scale warp loads them from global memory)
   const bool sf_tma = g1.sf_tma != 0;
+  // The scale warp's lane 0 copies a stage's scales from the SMEM layout into
+  // the stage's TMEM slot (the weight blocks' and the token tile's, the latter
+  // shared by both MMA streams) and commits the copies to sfready[s]; the MMA
+  // threads then issue only MMAs. The slot is free once empty[s] completed.
+  auto copy_scales = [&](int s, bool a0, bool a1, const uint8_t* sF) {
+    tc_fence_after();
+    const uint32_t slot = tmem + (uint32_t)(C::SF_BASE + s * C::SF_STAGE_COLS);
+    if (a0) tc_cp_32x128b_warpx4(slot, sdesc_sf_32x16(smem_u32(sF)));
+    if (a1 && C::NA > 1) tc_cp_32x128b_warpx4(slot + 4u, sdesc_sf_32x16(smem_u32(sF + 512)));
+#pragma unroll
+    for (int gq = 0; gq < C::SFB_ROWS / 128; ++gq)
+      tc_cp_32x128b_warpx4(slot + 4u * C::NA + 4u * gq, sdesc_sf_32x16(smem_u32(sF + C::NA * 512 + gq * 512)));
+    tc_commit(&sfready[s]);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -432,7 +449,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
             st_shared_v4(sF + C::NA * 512 + q * 512 + lane * 16, word(wb[4 * q], c), word(wb[4 * q + 1], c),
                          word(wb[4 * q + 2], c), word(wb[4 * q + 3], c));
           fence_proxy_async_smem();  // generic-proxy writes, read next by tcgen05.cp
-          mbar_arrive(&full[s]);
+          __syncwarp();
+          if (lane == 0) copy_scales(s, t.active, two, sF);
           ++it;
         }
       }
@@ -494,6 +512,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       const uint32_t site0 = l1 ? 0u : 8u;
       const int kblocks = g.K / C::BK;
       const int avail = kblocks - kg;
+      const Tile tc = tile_of(tile, l1);
+      const bool cur_active = tc.active, cur_two = has_second(g, tc);
       int ntile = tile, nkg = kg + 4;
       if (nkg >= kblocks) {
         ntile = tile + tile_step;
@@ -527,7 +547,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
           st_shared_v4(sF + C::NA * 512 + q * 512 + lane * 16, word(cb[4 * q], c), word(cb[4 * q + 1], c),
                        word(cb[4 * q + 2], c), word(cb[4 * q + 3], c));
         fence_proxy_async_smem();  // generic-proxy writes, read next by tcgen05.cp
-        mbar_arrive(&full[s]);
+        __syncwarp();
+        if (lane == 0) copy_scales(s, cur_active, cur_two, sF);
         ++it;
       }
       if (!ok || !has_next) break;
@@ -573,17 +594,14 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
           const int s = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait(&full[s], ph, abort_flag, g1.status, g1.timeout_ns, site0 + 2)) { ok = false; break; }
+          if (!mbar_wait(&sfready[s], ph, abort_flag, g1.status, g1.timeout_ns, site0 + 2)) { ok = false; break; }
           tc_fence_after();
           const uint8_t* sA = smem + C::A_OFF + (s * C::NA + u) * C::A_BYTES;
           const uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
-          const uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
           if (active) {
-            const uint32_t sfa = tmem + (uint32_t)(C::SF_BASE + ((int)(it & 1u) * C::NI + u) * C::SF_ISSUER_COLS);
-            const uint32_t sfb = sfa + 4u;
-            tc_cp_32x128b_warpx4(sfa, sdesc_sf_32x16(smem_u32(sF + u * 512)));
-#pragma unroll
-            for (int gq = 0; gq < C::SFB_ROWS / 128; ++gq)
-              tc_cp_32x128b_warpx4(sfb + 4u * gq, sdesc_sf_32x16(smem_u32(sF + C::NA * 512 + gq * 512)));
+            const uint32_t slot = tmem + (uint32_t)(C::SF_BASE + s * C::SF_STAGE_COLS);
+            const uint32_t sfa = slot + 4u * (uint32_t)u;
+            const uint32_t sfb = slot + 4u * C::NA;
             const uint64_t da = sdesc_kmajor_sw128(smem_u32(sA));
             const uint64_t db = sdesc_kmajor_sw128(smem_u32(sB));
 #pragma unroll
