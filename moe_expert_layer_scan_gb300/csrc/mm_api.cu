@@ -83,12 +83,12 @@ bool encode_2d(CUtensorMap* m, const void* base, bool fp4, uint64_t k_elems, uin
 
 // Scale rows [rows][cols] bytes, boxes of 16 bytes (four K steps) x 128 rows,
 // no swizzle (the scale warp reads them with plain 16-byte loads).
-bool encode_sf(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+bool encode_sf(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols};
-  cuuint32_t box[2] = {16, 128};
+  cuuint32_t box[2] = {16, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -98,11 +98,24 @@ bool encode_sf(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Tile variant of a call: 0 = 16-token tiles, 1 = 112-token tiles.
+// MM_DEEP=0 keeps 16-token tiles at five stages (measurement only).
+bool deep_disabled() {
+  static const bool off = [] {
+    const char* e = getenv("MM_DEEP");
+    return e && e[0] == '0';
+  }();
+  return off;
+}
+
+// Kernel variant of a call: 0 = 16-token tiles, 2 = 16-token tiles with six
+// stages (at most kDeepMaxExperts experts), 1 = 112-token tiles.
 int variant_for(const mm_handle* h, int T) {
-  if (h->tiles == MM_TILES_16) return 0;
-  if (h->tiles == MM_TILES_112) return 1;
-  return (long long)T * (h->k + h->S) <= (long long)MM_TILES16_MAX_ROWS_PER_EXPERT * (h->E + h->S) ? 0 : 1;
+  bool small;
+  if (h->tiles == MM_TILES_16) small = true;
+  else if (h->tiles == MM_TILES_112) small = false;
+  else small = (long long)T * (h->k + h->S) <= (long long)MM_TILES16_MAX_ROWS_PER_EXPERT * (h->E + h->S);
+  if (!small) return 1;
+  return (h->E + h->S <= kDeepMaxExperts && !deep_disabled()) ? 2 : 0;
 }
 
 }  // namespace
@@ -242,7 +255,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   uint8_t* base = static_cast<uint8_t*>(ws);
   const int Ep = h->E + h->S, Kp = h->k + h->S;
   const int variant = variant_for(h, T);
-  const int bn1 = variant == 0 ? kBnSmall : kBnLarge;
+  const int bn1 = variant == 1 ? kBnLarge : kBnSmall;
   const int bn2 = bn1;
 
   RouteArgs ra;
@@ -331,8 +344,9 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
     }
     maps.wsf1 = h->tm_w1sf;
     maps.wsf2 = h->tm_w2sf;
-    if (!encode_sf(&maps.asf1, base + L.pool_sf, (uint64_t)h->H / 32, (uint64_t)L.rows_cap)) return MM_ERR_CUDA;
-    if (!encode_sf(&maps.asf2, base + L.l2a_sf, (uint64_t)h->I / 32, (uint64_t)L.rows_cap)) return MM_ERR_CUDA;
+    const uint32_t tb = (uint32_t)mm_gemm_token_scale_box_rows(variant);
+    if (!encode_sf(&maps.asf1, base + L.pool_sf, (uint64_t)h->H / 32, (uint64_t)L.rows_cap, tb)) return MM_ERR_CUDA;
+    if (!encode_sf(&maps.asf2, base + L.l2a_sf, (uint64_t)h->I / 32, (uint64_t)L.rows_cap, tb)) return MM_ERR_CUDA;
   }
 
   GemmArgs g1;

@@ -73,16 +73,21 @@ struct GemmCfg {
   static constexpr int B_OFF = A_OFF + STAGES * NA * A_BYTES;
   static constexpr int SF_OFF = B_OFF + STAGES * B_BYTES;
   static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE_BYTES;
-  // copies of the two tile tables and the row offsets ([kMaxExperts + 1] each)
+  // The deep 16-token configuration (six stages) keeps room for them by
+  // supporting at most kDeepMaxExperts experts and two scale groups in flight.
+  static constexpr bool DEEP = BN == 16 && STAGES > 5;
+  // copies of the two tile tables and the row offsets ([experts + 1] each)
   static constexpr int TAB_OFF = BAR_OFF + 256;
-  static constexpr int TAB_INTS = kMaxExperts + 1;
+  static constexpr int TAB_INTS = DEEP ? kDeepMaxExperts + 1 : kMaxExperts + 1;
   // L2 tiles whose L1 rows the producer has seen stored (fused schedule)
   static constexpr int L2RDY_OFF = TAB_OFF + 3 * TAB_INTS * 4;
   // TMA-loaded scale rows: RAW_G groups of four K steps; per group 16 bytes of
-  // each of 128 rows for each weight block and for the token rows
-  static constexpr int RAW_G = 3;
+  // each of 128 rows for each weight block and of RAW_B_ROWS token rows
+  static constexpr int RAW_G = DEEP ? 2 : 3;
   static constexpr int RAW_ROWS_BYTES = 128 * 16;
-  static constexpr int RAW_GROUP_BYTES = (NA + 1) * RAW_ROWS_BYTES;
+  static constexpr int RAW_B_ROWS = BN <= 32 ? 32 : 128;
+  static constexpr int RAW_B_BYTES = RAW_B_ROWS * 16;
+  static constexpr int RAW_GROUP_BYTES = NA * RAW_ROWS_BYTES + RAW_B_BYTES;
   static constexpr int RAW_OFF = (L2RDY_OFF + 16 + 127) / 128 * 128;
   static constexpr int SMEM_BYTES = RAW_OFF + RAW_G * RAW_GROUP_BYTES + 1024;  // + alignment slack
   // TMEM columns: two accumulator buffers, then one scale-factor slot per
@@ -98,6 +103,7 @@ struct GemmCfg {
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(BN <= RAW_B_ROWS, "every token row of a tile has its scale row in the raw group");
   static_assert(B_BYTES % 1024 == 0, "B tiles must keep 1024-byte alignment");
   static_assert(BN % (8 * CS) == 0, "each multicast share must be whole 8-row swizzle atoms");
 };
@@ -347,7 +353,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
           }
           if (lane == 0) {
             uint8_t* raw = smem + C::RAW_OFF + gslot * C::RAW_GROUP_BYTES;
-            mbar_arrive_expect_tx(&rfull[gslot], ((t.active ? 1 : 0) + (two ? 1 : 0) + 1) * C::RAW_ROWS_BYTES);
+            mbar_arrive_expect_tx(&rfull[gslot], ((t.active ? 1 : 0) + (two ? 1 : 0)) * C::RAW_ROWS_BYTES +
+                                                     C::RAW_B_BYTES);
             if (t.active) tma_load_2d(raw, twsf, &rfull[gslot], kb * 4, wrow);
             if (two) tma_load_2d(raw + C::RAW_ROWS_BYTES, twsf, &rfull[gslot], kb * 4, wrow + g.second);
             tma_load_2d(raw + C::NA * C::RAW_ROWS_BYTES, tasf, &rfull[gslot], kb * 4, t.row0);
@@ -430,8 +437,9 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
                             : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int j = 0; j < NB; ++j)
-          wb[j] = j < nb ? *reinterpret_cast<const uint4*>(raw + C::NA * C::RAW_ROWS_BYTES + (32 * j + lane) * 16)
-                         : make_uint4(0u, 0u, 0u, 0u);
+          wb[j] = (j < nb && 32 * j < C::RAW_B_ROWS)
+                      ? *reinterpret_cast<const uint4*>(raw + C::NA * C::RAW_ROWS_BYTES + (32 * j + lane) * 16)
+                      : make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
         if (lane == 0) mbar_arrive(&rempty[gslot]);  // the raw slot may be refilled
 #pragma unroll
@@ -776,9 +784,10 @@ static int launch(const GemmMaps* maps, const GemmArgs* g1, const GemmArgs* g2, 
 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
 // five, measured as fast as six).
-constexpr int kStagesSmall = 5, kStagesLarge = 4;
-// CTAs per launch of each instantiation: [mode][variant]
-static int g_ctas[3][2];
+constexpr int kStagesSmall = 5, kStagesSmallDeep = 6, kStagesLarge = 4;
+// CTAs per launch of each instantiation: [mode][variant] (variant 2: 16-token
+// tiles with six stages, for at most kDeepMaxExperts experts)
+static int g_ctas[3][3];
 
 }  // namespace mm
 
@@ -791,13 +800,21 @@ extern "C" int mm_gemm_prepare(void) {
   if ((e = set_smem_attr<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(&g_ctas[kModeL1][1]))) return e;
   if ((e = set_smem_attr<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(&g_ctas[kModeL2][1]))) return e;
   if ((e = set_smem_attr<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(&g_ctas[kModeFused][1]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesSmallDeep, 1>(&g_ctas[kModeL1][2]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesSmallDeep, 1>(&g_ctas[kModeL2][2]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesSmallDeep, 1>(&g_ctas[kModeFused][2]))) return e;
   return 0;
 }
 
-extern "C" int mm_gemm_cluster(int variant) { return variant == 0 ? 1 : mm::kClusterLarge; }
+extern "C" int mm_gemm_cluster(int variant) { return variant == 1 ? mm::kClusterLarge : 1; }
 
 extern "C" int mm_gemm_epilogue_warps(int variant) {
-  return variant == 0 ? mm::Warps<mm::kBnSmall>::EPI : mm::Warps<mm::kBnLarge>::EPI;
+  return variant == 1 ? mm::Warps<mm::kBnLarge>::EPI : mm::Warps<mm::kBnSmall>::EPI;
+}
+
+extern "C" int mm_gemm_token_scale_box_rows(int variant) {
+  return variant == 1 ? mm::GemmCfg<mm::kBnLarge, mm::kStagesLarge, mm::kClusterLarge>::RAW_B_ROWS
+                      : mm::GemmCfg<mm::kBnSmall, mm::kStagesSmall, 1>::RAW_B_ROWS;
 }
 
 extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a, int num_ctas,
@@ -808,11 +825,13 @@ extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, con
   const int mode = l1 ? kModeL1 : kModeL2;
   const int n = g_ctas[mode][variant];
   if (l1) {
-    return variant == 0 ? launch<kModeL1, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
-                        : launch<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
+    return variant == 0   ? launch<kModeL1, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
+           : variant == 2 ? launch<kModeL1, kBnSmall, kStagesSmallDeep, 1>(maps, a, a, n, st)
+                          : launch<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
   }
-  return variant == 0 ? launch<kModeL2, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
-                      : launch<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
+  return variant == 0   ? launch<kModeL2, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
+         : variant == 2 ? launch<kModeL2, kBnSmall, kStagesSmallDeep, 1>(maps, a, a, n, st)
+                        : launch<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
 }
 
 extern "C" int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const mm::GemmArgs* g1,
@@ -820,6 +839,7 @@ extern "C" int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const
   using namespace mm;
   cudaStream_t st = (cudaStream_t)stream;
   const int n = g_ctas[kModeFused][variant];
-  return variant == 0 ? launch<kModeFused, kBnSmall, kStagesSmall, 1>(maps, g1, g2, n, st)
-                      : launch<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(maps, g1, g2, n, st);
+  return variant == 0   ? launch<kModeFused, kBnSmall, kStagesSmall, 1>(maps, g1, g2, n, st)
+         : variant == 2 ? launch<kModeFused, kBnSmall, kStagesSmallDeep, 1>(maps, g1, g2, n, st)
+                        : launch<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(maps, g1, g2, n, st);
 }

@@ -27,6 +27,9 @@ constexpr int kBnLarge = 112;
 // weight tiles of the same (expert, token tile) and each multicasts its share
 // of the token tile to all of them.
 constexpr int kClusterLarge = 2;
+// 16-token tiles run six pipeline stages (instead of five) when the call has
+// at most this many experts (E + S): the smaller tile tables make room.
+constexpr int kDeepMaxExperts = 300;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -152,7 +155,8 @@ int mm_launch_route(const mm::RouteArgs* a, void* stream);
 int mm_route_launches(int slots);  // kernels mm_launch_route enqueues for this many slots
 int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream);
 int mm_launch_combine(const mm::CombineArgs* a, void* stream);
-// variant: 0 = small tiles, 1 = large tiles. maps: the launch's tensor maps (a
+// variant: 0 = small tiles, 1 = large tiles, 2 = small tiles with six stages
+// (E + S <= kDeepMaxExperts). maps: the launch's tensor maps (a
 // single-linear launch reads w1/a1/wsf1/asf1 for L1 and w2/a2/wsf2/asf2 for L2).
 int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a, int num_ctas, void* stream);
 // One persistent launch of both GEMMs: every L1 tile, then every L2 tile; an L2
@@ -162,5 +166,6 @@ int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const mm::GemmAr
 int mm_gemm_prepare(void);  // sets the dynamic shared-memory limits and the persistent grid sizes
 int mm_gemm_cluster(int variant);  // CTAs per cluster of the variant
 int mm_gemm_epilogue_warps(int variant);  // epilogue warps per CTA (arrivals per L1 tile in the fused schedule)
+int mm_gemm_token_scale_box_rows(int variant);  // token rows per TMA box of the token scale rows
 int mm_launch_timeout_probe(uint32_t* status, unsigned long long timeout_ns, void* stream);
 }
