@@ -16,6 +16,16 @@
 
 namespace mm {
 
+// MM_ROUTE_SMALL=0 routes small calls with the general one-CTA kernel
+// (measurement only).
+inline bool route_small_disabled() {
+  static const bool off = [] {
+    const char* e = getenv("MM_ROUTE_SMALL");
+    return e && e[0] == '0';
+  }();
+  return off;
+}
+
 __device__ __forceinline__ int slot_expert(const RouteArgs& a, long s, bool* bad) {
   const int Kp = a.k + a.S;
   const long t = s / Kp;
@@ -149,6 +159,53 @@ __device__ int offsets_and_tiles(const RouteArgs& a, int tot, int* scratch) {
   // cumulative per-expert receive statistics (never cleared here)
   if (a.stats && tid < Ep && tot > 0) atomicAdd(&a.stats[tid], tot);
   return excl;
+}
+
+// Routing of at most kRouteSmallMax slots (decode-sized calls) by one CTA:
+// every slot's expert is read once into shared memory and counted with
+// shared atomics; a slot's rank within its expert is the number of earlier
+// slots of the same expert, counted from the shared list, which keeps the
+// placement stable (ascending slot order within each expert).
+__global__ void __launch_bounds__(1024, 1) route_small_kernel(RouteArgs a) {
+  __shared__ int es[kRouteSmallMax];
+  __shared__ int cnt[kMaxExperts];
+  __shared__ int first[kMaxExperts];
+  __shared__ int scratch[72];
+  __shared__ int bad_any;
+  pdl_trigger();
+  const int Ep = a.E + a.S, Kp = a.k + a.S;
+  const int R = a.T * Kp;
+  const int tid = threadIdx.x;
+  if (tid == 0) bad_any = 0;
+  if (tid < Ep) cnt[tid] = 0;
+  for (int i = tid; i <= R; i += blockDim.x) a.ready[i] = 0;
+  __syncthreads();
+  bool bad = false;
+  int e = -1;
+  if (tid < R) {
+    e = slot_expert(a, tid, &bad);
+    es[tid] = e;
+    if (e >= 0) atomicAdd(&cnt[e], 1);
+  }
+  if (bad) bad_any = 1;
+  __syncthreads();
+  const int excl = offsets_and_tiles(a, tid < Ep ? cnt[tid] : 0, scratch);
+  if (tid < Ep) first[tid] = excl;
+  __syncthreads();
+  if (tid < R) {
+    if (e >= 0) {
+      int rank = 0;
+      for (int s2 = 0; s2 < tid; ++s2) rank += es[s2] == e ? 1 : 0;
+      const int p = first[e] + rank;
+      a.perm[p] = tid;
+      a.pos[tid] = p;
+      const int t = tid / Kp, j = tid - t * Kp;
+      a.row_w[p] = (j < a.k) ? a.topk_w[t * a.k + j] : 1.0f;
+    } else {
+      a.pos[tid] = -1;
+    }
+  }
+  if (tid == 0) *a.status = bad_any ? MM_DEV_BAD_ROUTING : 0u;
 }
 
 // Routing by one CTA (few slots): histograms, offsets, cursors, placement.
@@ -353,6 +410,10 @@ extern "C" int mm_launch_route(const mm::RouteArgs* a, void* stream) {
     attr_set = true;
   }
   cudaStream_t st = (cudaStream_t)stream;
+  if (R <= mm::kRouteSmallMax && !mm::route_small_disabled()) {
+    // the first kernel of a forward: ordinary stream order behind the previous work
+    return (int)mm::launch_kernel(mm::route_small_kernel, dim3(1), dim3(1024), 0, st, false, 1, *a);
+  }
   if (R <= mm::kRouteSingleMax) {
     // the first kernel of a forward: ordinary stream order behind the previous work
     return (int)mm::launch_kernel(mm::route_kernel, dim3(1), dim3(1024), sizeof(int) * (32 * (size_t)Ep + 72), st,

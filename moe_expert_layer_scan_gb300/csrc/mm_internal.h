@@ -16,6 +16,7 @@ constexpr int kMaxSlots = 16;      // topk + S
 constexpr int kRowMargin = 256;    // pool rows beyond the last valid row that tiles may touch
 constexpr int kRouteChunk = 8192;  // slots per CTA when routing runs on several CTAs
 constexpr int kRouteSingleMax = 16384;  // up to this many slots, one CTA routes everything
+constexpr int kRouteSmallMax = 512;     // up to this many slots, the lean one-CTA routing kernel
 
 // Token-tile widths (the MMA N dimension) and pipeline depths of the two GEMM
 // variants. "small" serves decode-like calls (few rows per expert), "large"
