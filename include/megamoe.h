@@ -18,7 +18,14 @@
  *
  * Activations are FP8 E4M3 with one UE8M0 scale per 32 along K; expert
  * weights are MXFP4: E2M1 codes packed two per byte (even K index in the low
- * nibble) with one UE8M0 scale per 32 along K. Accumulation is FP32.
+ * nibble) with one UE8M0 scale per 32 along K, or, after
+ * mm_set_weight_format(h, MM_WEIGHTS_MXFP8), E4M3 codes one per byte with the
+ * same scales. Accumulation is FP32.
+ *
+ * Call order: mm_create, optionally mm_set_options / mm_set_schedule /
+ * mm_set_tile_policy / mm_set_weight_format / mm_set_ep_ranks /
+ * mm_set_expert_stats, mm_workspace_bytes, then any number of mm_run calls,
+ * then mm_destroy. Options may change between calls.
  * Shared experts (num_shared = S) are stacked after the E routed experts in
  * W1/W2 (indices E..E+S-1) and applied to every token with weight 1.
  *
