@@ -393,7 +393,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
-    ap.add_argument("--tiles", type=int, default=-1, choices=[-1, 16, 112],
+    ap.add_argument("--tiles", type=int, default=-1, choices=[-1, 16, 112, 224],
                     help="token-tile width (-1: the library's choice)")
     ap.add_argument("--schedule", default="auto", choices=["auto", "fused", "split"],
                     help="GEMM schedule: one persistent launch for both linears, one per linear, or the "

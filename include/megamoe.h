@@ -93,7 +93,9 @@ MM_API mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, in
 /* SwiGLU options (the SM90 design's activation_clamp / fast_math arguments,
  * "MEGAMOE_SM90_DESIGN" sec. 10.1): swiglu_clamp > 0 clamps gate and up to
  * [-c, c] before the SiLU, <= 0 disables the clamp; fast_math != 0 uses the
- * fast approximate exponential (__expf) in the SiLU. Defaults: no clamp, accurate exp. */
+ * fast approximate exponential (__expf) and the approximate reciprocal in the
+ * SiLU (the pages' fast path). Defaults: no clamp, accurate exp and a correctly
+ * rounded division (see mm_debug_div_check). */
 MM_API mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_math);
 
 /* GEMM schedule ("MegaMoE research report" sec. 4.1, the Linear1 -> Linear2
@@ -118,19 +120,28 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
  *   MM_TILES_16: 16-token tiles pairing two 128-row weight blocks, one MMA
  *     stream per block, no cluster (weight-stream bound calls);
  *   MM_TILES_112: 112-token tiles in 2-CTA clusters sharing the token tile by
- *     multicast, eight epilogue warps (compute bound calls);
+ *     multicast, eight epilogue warps, two TMEM accumulator buffers so that a
+ *     tile's epilogue overlaps the next tile's MMAs;
+ *   MM_TILES_224: 224-token tiles, otherwise as MM_TILES_112 but with one
+ *     accumulator buffer (two 224-column accumulators fill TMEM) and three
+ *     pipeline stages: one MMA per K step and weight block does twice the
+ *     work of a 112-token MMA for one instruction issue (compute-bound calls
+ *     with many rows per expert);
  *   MM_TILES_AUTO (the default): MM_TILES_16 while the call routes at most
  *     MM_TILES16_MAX_ROWS_PER_EXPERT rows per expert on average
- *     (T*(topk+S) <= 12*(E+S)), MM_TILES_112 above: the crossover measured on
- *     GB300 at H = 7168, I = 2048, 256 experts, top-8 and at H = 4096,
- *     I = 1536, 128 experts, top-8 (16-token tiles faster up to 12 rows per
- *     expert, 112-token tiles from 14; moe_expert_layer_scan_gb300/tune_tiles.py).
- * Either width computes the same tiles' sums; the results are identical.
+ *     (T*(topk+S) <= 12*(E+S)), MM_TILES_224 from
+ *     MM_TILES224_MIN_ROWS_PER_EXPERT rows per expert, MM_TILES_112 between:
+ *     the crossovers measured on GB300 at H = 7168, I = 2048, 256 experts,
+ *     top-8 and at H = 4096, I = 1536, 128 experts, top-8
+ *     (moe_expert_layer_scan_gb300/tune_tiles.py).
+ * Every width computes the same tiles' sums; the results are identical.
  * Other values: MM_ERR_INVALID_ARG. */
 #define MM_TILES_AUTO (-1)
 #define MM_TILES_16 16
 #define MM_TILES_112 112
+#define MM_TILES_224 224
 #define MM_TILES16_MAX_ROWS_PER_EXPERT 12
+#define MM_TILES224_MIN_ROWS_PER_EXPERT 192
 MM_API mm_status_t mm_set_tile_policy(mm_handle_t h, int policy);
 
 /* Weight element format (both linears). MM_WEIGHTS_MXFP4 (the default): E2M1
@@ -233,6 +244,21 @@ MM_API mm_status_t mm_debug_views(mm_handle_t h, void* ws, int T, mm_debug_views
  * sets MM_DEV_TIMEOUT in the workspace status word and returns. The GPU stays
  * usable. ws must hold at least 256 bytes. */
 MM_API mm_status_t mm_debug_timeout_probe(void* ws, uint64_t timeout_ns, mm_stream_t stream);
+
+/* Test hook for the SiLU division: the L1 epilogue divides the gate by
+ * 1 + exp(-gate) with a branch-free Newton-Raphson reciprocal and Markstein's
+ * residual correction instead of the IEEE division routine. This compares it
+ * with __frcp_rn / __fdiv_rn on the GPU. counts: device memory, 5 x uint64,
+ * 8-byte aligned, zeroed here, then
+ *   [0] significands of y in [1, 2) (all 2^23) whose refined reciprocal is not
+ *       the correctly rounded one,
+ *   [1] of `pairs` pseudo-random (x, y >= 1) pairs (splitmix64 stream `seed`),
+ *       those with a normal IEEE quotient where the two differ,
+ *   [2] those with a subnormal or zero IEEE quotient where they differ,
+ *   [3] pairs checked,
+ *   [4] pairs where they differ by more than one unit in the last place.
+ * pairs <= 2^40. Asynchronous on `stream`. */
+MM_API mm_status_t mm_debug_div_check(uint64_t pairs, uint64_t seed, unsigned long long* counts, mm_stream_t stream);
 
 /* Per-launch timing for measurement: with profiling on, mm_run records a CUDA
  * event on its stream before each launch and after the last one. mm_profile_last

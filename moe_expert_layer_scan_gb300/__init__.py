@@ -27,7 +27,8 @@ EXPORTS = ["mm_status_string", "mm_create", "mm_set_options", "mm_set_schedule",
            "mm_set_weight_format",
            "mm_set_ep_ranks",
            "mm_set_expert_stats", "mm_workspace_bytes", "mm_run",
-           "mm_get_status", "mm_launches_per_run", "mm_debug_views", "mm_debug_timeout_probe", "mm_profile_enable",
+           "mm_get_status", "mm_launches_per_run", "mm_debug_views", "mm_debug_timeout_probe", "mm_debug_div_check",
+           "mm_profile_enable",
            "mm_profile_last", "mm_profile_name", "mm_run_noalloc", "mm_destroy"]
 
 
@@ -75,6 +76,7 @@ def lib() -> ctypes.CDLL:
         L.mm_launches_per_run.argtypes = [p, i32, ctypes.POINTER(ctypes.c_int)]
         L.mm_debug_views.argtypes = [p, p, i32, ctypes.POINTER(DebugViews)]
         L.mm_debug_timeout_probe.argtypes = [p, ctypes.c_uint64, p]
+        L.mm_debug_div_check.argtypes = [ctypes.c_uint64, ctypes.c_uint64, p, p]
         L.mm_profile_enable.argtypes = [p, i32]
         L.mm_profile_last.argtypes = [p, ctypes.POINTER(ctypes.c_float), i32, ctypes.POINTER(ctypes.c_int)]
         L.mm_profile_name.argtypes = [p, i32]
@@ -115,11 +117,11 @@ def mm_set_schedule(h: int, schedule="auto") -> None:
     _check(lib().mm_set_schedule(h, v), "mm_set_schedule")
 
 
-MM_TILES_AUTO, MM_TILES_16, MM_TILES_112 = -1, 16, 112
+MM_TILES_AUTO, MM_TILES_16, MM_TILES_112, MM_TILES_224 = -1, 16, 112, 224
 
 
 def mm_set_tile_policy(h: int, policy: int = MM_TILES_AUTO) -> None:
-    """Token-tile width: MM_TILES_AUTO, MM_TILES_16 or MM_TILES_112."""
+    """Token-tile width: MM_TILES_AUTO, MM_TILES_16, MM_TILES_112 or MM_TILES_224."""
     _check(lib().mm_set_tile_policy(h, int(policy)), "mm_set_tile_policy")
 
 
@@ -179,6 +181,11 @@ def mm_debug_views(h: int, ws: int, T: int) -> DebugViews:
 
 def mm_debug_timeout_probe(ws: int, timeout_ns: int, stream: int) -> None:
     _check(lib().mm_debug_timeout_probe(ws, int(timeout_ns), stream), "mm_debug_timeout_probe")
+
+
+def mm_debug_div_check(pairs: int, seed: int, counts: int, stream: int) -> None:
+    """counts: device address of 5 uint64 (see include/megamoe.h)."""
+    _check(lib().mm_debug_div_check(int(pairs), int(seed), counts, stream), "mm_debug_div_check")
 
 
 def mm_profile_enable(h: int, on: bool = True) -> None:

@@ -39,7 +39,7 @@ struct mm_handle {
   int32_t* expert_stats;
   // weight format: MM_WEIGHTS_MXFP4 / MM_WEIGHTS_MXFP8
   int w_fmt;
-  // token-tile width: MM_TILES_AUTO / _16 / _112
+  // token-tile width: MM_TILES_AUTO / _16 / _112 / _224
   int tiles;
   // optional per-launch events (route, gather, L1, L2, combine, end) and the
   // stage name of each recorded interval
@@ -108,15 +108,21 @@ bool deep_disabled() {
 }
 
 // Kernel variant of a call: 0 = 16-token tiles, 2 = 16-token tiles with six
-// stages (at most kDeepMaxExperts experts), 1 = 112-token tiles.
+// stages (at most kDeepMaxExperts experts), 1 = 112-token tiles, 3 = 224-token
+// tiles.
 int variant_for(const mm_handle* h, int T) {
-  bool small;
-  if (h->tiles == MM_TILES_16) small = true;
-  else if (h->tiles == MM_TILES_112) small = false;
-  else small = (long long)T * (h->k + h->S) <= (long long)MM_TILES16_MAX_ROWS_PER_EXPERT * (h->E + h->S);
-  if (!small) return 1;
+  const long long rows = (long long)T * (h->k + h->S), ep = h->E + h->S;
+  int width = h->tiles;
+  if (width == MM_TILES_AUTO)
+    width = rows <= MM_TILES16_MAX_ROWS_PER_EXPERT * ep    ? MM_TILES_16
+            : rows >= MM_TILES224_MIN_ROWS_PER_EXPERT * ep ? MM_TILES_224
+                                                            : MM_TILES_112;
+  if (width == MM_TILES_112) return 1;
+  if (width == MM_TILES_224) return 3;
   return (h->E + h->S <= kDeepMaxExperts && !deep_disabled()) ? 2 : 0;
 }
+
+int tile_width(int variant) { return variant == 1 ? kBnLarge : variant == 3 ? kBnWide : kBnSmall; }
 
 }  // namespace
 
@@ -187,7 +193,8 @@ mm_status_t mm_set_schedule(mm_handle_t h, int schedule) {
 }
 
 mm_status_t mm_set_tile_policy(mm_handle_t h, int policy) {
-  if (!h || (policy != MM_TILES_AUTO && policy != MM_TILES_16 && policy != MM_TILES_112)) return MM_ERR_INVALID_ARG;
+  if (!h || (policy != MM_TILES_AUTO && policy != MM_TILES_16 && policy != MM_TILES_112 && policy != MM_TILES_224))
+    return MM_ERR_INVALID_ARG;
   h->tiles = policy;
   return MM_OK;
 }
@@ -255,7 +262,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   uint8_t* base = static_cast<uint8_t*>(ws);
   const int Ep = h->E + h->S, Kp = h->k + h->S;
   const int variant = variant_for(h, T);
-  const int bn1 = variant == 1 ? kBnLarge : kBnSmall;
+  const int bn1 = tile_width(variant);
   const int bn2 = bn1;
 
   RouteArgs ra;
@@ -460,6 +467,14 @@ mm_status_t mm_debug_views(mm_handle_t h, void* ws, int T, mm_debug_views_t* v) 
   v->status = reinterpret_cast<uint32_t*>(b + L.status);
   v->rows_capacity = L.rows_cap;
   v->rank_offsets = reinterpret_cast<int32_t*>(b + L.rank_offsets);
+  return MM_OK;
+}
+
+mm_status_t mm_debug_div_check(uint64_t pairs, uint64_t seed, unsigned long long* counts, mm_stream_t stream) {
+  if (!counts || pairs > (1ull << 40) || !aligned(counts, 8)) return MM_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(counts, 0, 5 * sizeof(unsigned long long), (cudaStream_t)stream) != cudaSuccess)
+    return MM_ERR_CUDA;
+  if (mm_launch_div_check(pairs, seed, counts, stream) != 0) return MM_ERR_CUDA;
   return MM_OK;
 }
 

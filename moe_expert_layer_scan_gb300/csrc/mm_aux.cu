@@ -378,6 +378,65 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
   }
 }
 
+// splitmix64 (G. Steele, D. Lea, C. Flood, "Fast splittable pseudorandom
+// number generators", OOPSLA 2014): the i-th output of the stream `seed`.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t seed, uint64_t i) {
+  uint64_t z = seed + (i + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// Checks the SiLU division against the IEEE operations on this GPU.
+// counts[0]: significands of y in [1, 2) (all 2^23) whose refined reciprocal
+//            differs from __frcp_rn(y);
+// counts[1]: pairs with a normal IEEE quotient where div_ge1 differs from
+//            __fdiv_rn;
+// counts[2]: pairs with a subnormal or zero IEEE quotient where they differ;
+// counts[3]: pairs checked;
+// counts[4]: pairs where they differ by more than one unit in the last place.
+// x: any finite float (random sign, exponent field 0..254 and significand);
+// y: half the pairs a random significand times 2^(0..127) (so [1, 2^128)),
+// half 1 + e with e = a random significand times 2^(-40..129) (up to +inf).
+__global__ void div_check_kernel(unsigned long long n, unsigned long long seed, unsigned long long* counts) {
+  const unsigned long long tid = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const unsigned long long nth = (unsigned long long)gridDim.x * blockDim.x;
+  unsigned long long c0 = 0, c1 = 0, c2 = 0, c3 = 0, c4 = 0;
+  for (unsigned long long m = tid; m < (1ull << 23); m += nth) {
+    const float y = __uint_as_float(0x3F800000u | (uint32_t)m);
+    if (__float_as_uint(rcp_newton(y)) != __float_as_uint(__frcp_rn(y))) ++c0;
+  }
+  for (unsigned long long i = tid; i < n; i += nth) {
+    const uint64_t h = splitmix64(seed, i);
+    const uint32_t hx = (uint32_t)h, hy = (uint32_t)(h >> 32);
+    uint32_t xe = (hx >> 23) & 0xFFu;
+    if (xe == 0xFFu) xe = 0xFEu;
+    const float x = __uint_as_float((hx & 0x807FFFFFu) | (xe << 23));
+    const float sig = __uint_as_float(0x3F800000u | (hy & 0x7FFFFFu));
+    float y;
+    if (hy >> 31) {
+      y = ldexpf(sig, (int)((hy >> 23) & 0x7Fu));
+    } else {
+      const int k = (int)((hy >> 23) & 0xFFu) % 170 - 40;  // 128, 129: 1 + e = +inf
+      y = __fadd_rn(1.0f, ldexpf(sig, k));
+    }
+    const float a = div_ge1(x, y), b = __fdiv_rn(x, y);
+    const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+    ++c3;
+    if (ua != ub) {
+      if (fabsf(b) >= 0x1p-126f) ++c1;
+      else ++c2;
+      const uint32_t d = ua > ub ? ua - ub : ub - ua;
+      if (((ua ^ ub) >> 31) != 0u ? (ua & 0x7FFFFFFFu) + (ub & 0x7FFFFFFFu) > 1u : d > 1u) ++c4;
+    }
+  }
+  if (c0) atomicAdd(&counts[0], c0);
+  if (c1) atomicAdd(&counts[1], c1);
+  if (c2) atomicAdd(&counts[2], c2);
+  atomicAdd(&counts[3], c3);
+  if (c4) atomicAdd(&counts[4], c4);
+}
+
 // Waits on an mbarrier nobody arrives on, with the same bounded wait the GEMM
 // pipeline uses, and records the expiry in the status word.
 __global__ void timeout_probe_kernel(uint32_t* status, unsigned long long timeout_ns) {
@@ -442,6 +501,12 @@ extern "C" int mm_launch_combine(const mm::CombineArgs* a, void* stream) {
   if (blocks > 152 * 16) blocks = 152 * 16;
   return (int)mm::launch_kernel(mm::combine_kernel, dim3((unsigned)blocks), dim3(128), 0, (cudaStream_t)stream, true, 1,
                                 *a);
+}
+
+extern "C" int mm_launch_div_check(unsigned long long pairs, unsigned long long seed, unsigned long long* counts,
+                                   void* stream) {
+  mm::div_check_kernel<<<152 * 4, 256, 0, (cudaStream_t)stream>>>(pairs, seed, counts);
+  return (int)cudaGetLastError();
 }
 
 extern "C" int mm_launch_timeout_probe(uint32_t* status, unsigned long long timeout_ns, void* stream) {

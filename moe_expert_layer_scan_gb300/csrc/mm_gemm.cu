@@ -85,18 +85,22 @@ struct GemmCfg {
   // each of 128 rows for each weight block and of RAW_B_ROWS token rows
   static constexpr int RAW_G = DEEP ? 2 : 3;
   static constexpr int RAW_ROWS_BYTES = 128 * 16;
-  static constexpr int RAW_B_ROWS = BN <= 32 ? 32 : 128;
+  static constexpr int RAW_B_ROWS = BN <= 32 ? 32 : (BN <= 128 ? 128 : 256);
   static constexpr int RAW_B_BYTES = RAW_B_ROWS * 16;
   static constexpr int RAW_GROUP_BYTES = NA * RAW_ROWS_BYTES + RAW_B_BYTES;
   static constexpr int RAW_OFF = (L2RDY_OFF + 16 + 127) / 128 * 128;
   static constexpr int SMEM_BYTES = RAW_OFF + RAW_G * RAW_GROUP_BYTES + 1024;  // + alignment slack
-  // TMEM columns: two accumulator buffers, then one scale-factor slot per
+  // TMEM columns: the accumulator buffers, then one scale-factor slot per
   // stage (every scale-factor address stays a multiple of 4 columns)
   static constexpr int ACC_COLS = NA * BN;
   // per stage: 4 columns of scales per weight block, then the token tile's
   // (4 per 128 rows), shared by both MMA streams
   static constexpr int SF_STAGE_COLS = 4 * NA + SFB_ROWS / 32;
-  static constexpr int SF_BASE = 2 * ACC_COLS;
+  // Two accumulator buffers (the epilogue of one tile overlaps the main loop
+  // of the next) where TMEM holds them; the 224-token tiles fill TMEM with one
+  // and the epilogue drains it between tiles.
+  static constexpr int ACC_BUFS = 2 * ACC_COLS + STAGES * SF_STAGE_COLS <= 512 ? 2 : 1;
+  static constexpr int SF_BASE = ACC_BUFS * ACC_COLS;
   static constexpr int TMEM_USED = SF_BASE + STAGES * SF_STAGE_COLS;
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
@@ -591,8 +595,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
         const uint32_t site0 = l1 ? 0u : 8u;
         const Tile t = tile_of(tile, l1);
         const int kblocks = g.K / C::BK;
-        const int buf = (int)(tcount & 1u);
-        const uint32_t bph = (tcount >> 1) & 1u;
+        const int buf = C::ACC_BUFS == 2 ? (int)(tcount & 1u) : 0;
+        const uint32_t bph = (C::ACC_BUFS == 2 ? tcount >> 1 : tcount) & 1u;
         if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 1)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * C::ACC_COLS + u * BN);
@@ -640,8 +644,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
       const Tile t = tile_of(tile, l1);
-      const int buf = (int)(tcount & 1u);
-      const uint32_t bph = (tcount >> 1) & 1u;
+      const int buf = C::ACC_BUFS == 2 ? (int)(tcount & 1u) : 0;
+      const uint32_t bph = (C::ACC_BUFS == 2 ? tcount >> 1 : tcount) & 1u;
       if (!mbar_wait(&tfull[buf], bph, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 256)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::ACC_COLS);
@@ -652,8 +656,10 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
         // a transpose-reduction: after the exchange steps lane c (32 columns)
         // or lanes 2c, 2c+1 (16 columns) hold the maximum of column c, compute
         // that column's scale once, and the inverse scales are broadcast back.
-        // NC = 32 columns per step (16 for the 16-row decode tiles).
-        constexpr int NC = BN > 16 ? 32 : 16;
+        // NC = 32 columns per step; 16 for the 16-row decode tiles, and for
+        // the 224-row tiles, whose 14 chunks of 16 split evenly between the
+        // two warps of a quadrant (7 chunks of 32 would not).
+        constexpr int NC = (BN > 16 && BN != 224) ? 32 : 16;
         constexpr int LOG2NC = NC == 32 ? 5 : 4;
         for (int c0 = NC * half; t.active && c0 < t.nrows; c0 += NC * (Warps<BN>::EPI / 4)) {
           const int ncol = min(NC, t.nrows - c0);
@@ -679,8 +685,10 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
               gv = fminf(fmaxf(gv, -g1.clamp), g1.clamp);
               uv = fminf(fmaxf(uv, -g1.clamp), g1.clamp);
             }
-            const float ex = g1.fast_math ? __expf(-gv) : expf(-gv);
-            const float silu = __fdiv_rn(gv, __fadd_rn(1.0f, ex));
+            // silu(g) = g / (1 + exp(-g)); the fast path: __expf and the
+            // approximate reciprocal
+            const float silu = g1.fast_math ? __fmul_rn(gv, rcp_approx(__fadd_rn(1.0f, __expf(-gv))))
+                                            : div_ge1(gv, __fadd_rn(1.0f, expf(-gv)));
             y[j] = j < ncol ? __fmul_rn(__fmul_rn(silu, uv), wj) : 0.0f;
             v[j] = fabsf(y[j]);
           }
@@ -784,10 +792,11 @@ static int launch(const GemmMaps* maps, const GemmArgs* g1, const GemmArgs* g2, 
 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
 // five, measured as fast as six).
-constexpr int kStagesSmall = 5, kStagesSmallDeep = 6, kStagesLarge = 4;
+constexpr int kStagesSmall = 5, kStagesSmallDeep = 6, kStagesLarge = 4, kStagesWide = 3;
 // CTAs per launch of each instantiation: [mode][variant] (variant 2: 16-token
-// tiles with six stages, for at most kDeepMaxExperts experts)
-static int g_ctas[3][3];
+// tiles with six stages, for at most kDeepMaxExperts experts; variant 3:
+// 224-token tiles)
+static int g_ctas[3][4];
 
 }  // namespace mm
 
@@ -803,18 +812,24 @@ extern "C" int mm_gemm_prepare(void) {
   if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesSmallDeep, 1>(&g_ctas[kModeL1][2]))) return e;
   if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesSmallDeep, 1>(&g_ctas[kModeL2][2]))) return e;
   if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesSmallDeep, 1>(&g_ctas[kModeFused][2]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnWide, kStagesWide, kClusterLarge>(&g_ctas[kModeL1][3]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnWide, kStagesWide, kClusterLarge>(&g_ctas[kModeL2][3]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnWide, kStagesWide, kClusterLarge>(&g_ctas[kModeFused][3]))) return e;
   return 0;
 }
 
-extern "C" int mm_gemm_cluster(int variant) { return variant == 1 ? mm::kClusterLarge : 1; }
+extern "C" int mm_gemm_cluster(int variant) { return variant == 1 || variant == 3 ? mm::kClusterLarge : 1; }
 
 extern "C" int mm_gemm_epilogue_warps(int variant) {
-  return variant == 1 ? mm::Warps<mm::kBnLarge>::EPI : mm::Warps<mm::kBnSmall>::EPI;
+  return variant == 1   ? mm::Warps<mm::kBnLarge>::EPI
+         : variant == 3 ? mm::Warps<mm::kBnWide>::EPI
+                        : mm::Warps<mm::kBnSmall>::EPI;
 }
 
 extern "C" int mm_gemm_token_scale_box_rows(int variant) {
-  return variant == 1 ? mm::GemmCfg<mm::kBnLarge, mm::kStagesLarge, mm::kClusterLarge>::RAW_B_ROWS
-                      : mm::GemmCfg<mm::kBnSmall, mm::kStagesSmall, 1>::RAW_B_ROWS;
+  return variant == 1   ? mm::GemmCfg<mm::kBnLarge, mm::kStagesLarge, mm::kClusterLarge>::RAW_B_ROWS
+         : variant == 3 ? mm::GemmCfg<mm::kBnWide, mm::kStagesWide, mm::kClusterLarge>::RAW_B_ROWS
+                        : mm::GemmCfg<mm::kBnSmall, mm::kStagesSmall, 1>::RAW_B_ROWS;
 }
 
 extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a, int num_ctas,
@@ -827,10 +842,12 @@ extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, con
   if (l1) {
     return variant == 0   ? launch<kModeL1, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
            : variant == 2 ? launch<kModeL1, kBnSmall, kStagesSmallDeep, 1>(maps, a, a, n, st)
+           : variant == 3 ? launch<kModeL1, kBnWide, kStagesWide, kClusterLarge>(maps, a, a, n, st)
                           : launch<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
   }
   return variant == 0   ? launch<kModeL2, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
          : variant == 2 ? launch<kModeL2, kBnSmall, kStagesSmallDeep, 1>(maps, a, a, n, st)
+         : variant == 3 ? launch<kModeL2, kBnWide, kStagesWide, kClusterLarge>(maps, a, a, n, st)
                         : launch<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
 }
 
@@ -841,5 +858,6 @@ extern "C" int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const
   const int n = g_ctas[kModeFused][variant];
   return variant == 0   ? launch<kModeFused, kBnSmall, kStagesSmall, 1>(maps, g1, g2, n, st)
          : variant == 2 ? launch<kModeFused, kBnSmall, kStagesSmallDeep, 1>(maps, g1, g2, n, st)
+         : variant == 3 ? launch<kModeFused, kBnWide, kStagesWide, kClusterLarge>(maps, g1, g2, n, st)
                         : launch<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(maps, g1, g2, n, st);
 }

@@ -24,6 +24,11 @@ constexpr int kRouteSmallMax = 512;     // up to this many slots, the lean one-C
 // to 16, so ragged tails never pay for a full tile.
 constexpr int kBnSmall = 16;
 constexpr int kBnLarge = 112;
+// 224-token tiles: one MMA of N up to 224 per K step and weight block keeps
+// the tensor pipe busy (two 112-wide MMAs cost two instruction issues for the
+// same work); their two 224-column accumulators fill TMEM, so there is one
+// accumulator buffer. For the compute-bound calls with many rows per expert.
+constexpr int kBnWide = 224;
 // Large tiles run as clusters of kClusterLarge CTAs: the CTAs take adjacent
 // weight tiles of the same (expert, token tile) and each multicasts its share
 // of the token tile to all of them.
@@ -157,7 +162,7 @@ int mm_route_launches(int slots);  // kernels mm_launch_route enqueues for this 
 int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream);
 int mm_launch_combine(const mm::CombineArgs* a, void* stream);
 // variant: 0 = small tiles, 1 = large tiles, 2 = small tiles with six stages
-// (E + S <= kDeepMaxExperts). maps: the launch's tensor maps (a
+// (E + S <= kDeepMaxExperts), 3 = 224-token tiles. maps: the launch's tensor maps (a
 // single-linear launch reads w1/a1/wsf1/asf1 for L1 and w2/a2/wsf2/asf2 for L2).
 int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a, int num_ctas, void* stream);
 // One persistent launch of both GEMMs: every L1 tile, then every L2 tile; an L2
@@ -169,4 +174,5 @@ int mm_gemm_cluster(int variant);  // CTAs per cluster of the variant
 int mm_gemm_epilogue_warps(int variant);  // epilogue warps per CTA (arrivals per L1 tile in the fused schedule)
 int mm_gemm_token_scale_box_rows(int variant);  // token rows per TMA box of the token scale rows
 int mm_launch_timeout_probe(uint32_t* status, unsigned long long timeout_ns, void* stream);
+int mm_launch_div_check(unsigned long long pairs, unsigned long long seed, unsigned long long* counts, void* stream);
 }

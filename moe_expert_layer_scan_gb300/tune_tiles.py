@@ -1,14 +1,15 @@
-"""Measures the token-tile crossover of the grouped GEMMs on this GPU.
+"""Measures the token-tile crossovers of the grouped GEMMs on this GPU.
 
     python -m moe_expert_layer_scan_gb300.tune_tiles [--workload prefill] [--tokens 64,128,256,384,512]
+                                                     [--widths 16,112,224]
 
-For each token count, runs the whole forward with 16-token and with
-112-token tiles (schedule chosen by the library) on seeded synthetic inputs
-of the workload's shape (weights generated in device memory), L2 flushed
-between steps, and prints the median step time of each and the mean routed
-rows per expert. The library's automatic policy switches from 16- to
-112-token tiles above MM_TILES16_MAX_ROWS_PER_EXPERT rows per expert, the
-crossover this measures.
+For each token count, runs the whole forward with each token-tile width
+(schedule chosen by the library) on seeded synthetic inputs of the workload's
+shape (weights generated in device memory), L2 flushed between steps, and
+prints the median step time of each and the mean routed rows per expert. The
+library's automatic policy switches from 16- to 112-token tiles above
+MM_TILES16_MAX_ROWS_PER_EXPERT rows per expert and from 112- to 224-token
+tiles at MM_TILES224_MIN_ROWS_PER_EXPERT, the crossovers this measures.
 """
 from __future__ import annotations
 
@@ -50,13 +51,15 @@ def main():
     ap.add_argument("--workload", default="prefill", choices=list(workloads.CONFIGS))
     ap.add_argument("--tokens", default="64,128,256,320,384,448,512,1024")
     ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--widths", default="16,112")
     a = ap.parse_args()
     base = workloads.CONFIGS[a.workload]
     Ts = [int(t) for t in a.tokens.split(",")]
+    widths = [int(x) for x in a.widths.split(",")]
     d = workloads.device_inputs(base.replace(T=max(Ts)))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     print(f"# {base.name} shape: H={base.H} I={base.I} E={base.E} top-{base.k} shared={base.S}")
-    print("tokens  rows/expert  ms(16-token tiles)  ms(112-token tiles)  faster")
+    print("tokens  rows/expert  " + "  ".join(f"ms({b}-token tiles)" for b in widths) + "  faster")
     for T in Ts:
         w = base.replace(T=T, name=f"{base.name}_T{T}")
         idx, wt = workloads.routing(w)
@@ -64,13 +67,14 @@ def main():
                 d["w1"], d["w1_sf"], d["w2"], d["w2_sf"])
         out = torch.empty((T, w.H), dtype=torch.bfloat16, device="cuda")
         ms = {}
-        for tiles in (mm.MM_TILES_16, mm.MM_TILES_112):
+        for tiles in widths:
             moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp, weight_format=w.w_fmt, tiles=tiles)
             ms[tiles] = measure(moe, args, out, flush, steps=a.steps)
             del moe
         rows = T * w.Kp / w.Ep
-        print(f"{T:6d}  {rows:11.2f}  {ms[16]:18.4f}  {ms[112]:19.4f}  {16 if ms[16] <= ms[112] else 112}")
-        print(json.dumps({"T": T, "rows_per_expert": rows, "ms16": ms[16], "ms112": ms[112]}), file=sys.stderr)
+        best = min(widths, key=lambda b: ms[b])
+        print(f"{T:6d}  {rows:11.2f}  " + "  ".join(f"{ms[b]:18.4f}" for b in widths) + f"  {best}")
+        print(json.dumps({"T": T, "rows_per_expert": rows, **{f"ms{b}": ms[b] for b in widths}}), file=sys.stderr)
 
 
 if __name__ == "__main__":

@@ -77,12 +77,14 @@ def test_duplicate_experts_small_variant(orc):
     G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
 
 
-def test_hot_expert_many_tiles(orc):
-    """One expert receives every token: several full token tiles plus a ragged tail."""
+@pytest.mark.parametrize("tiles", [-1, 224])
+def test_hot_expert_many_tiles(orc, tiles):
+    """One expert receives every token: several full token tiles plus a ragged
+    tail (112-token tiles by the automatic policy, or 224-token tiles)."""
     w = Workload("hot", T=300, H=256, I=256, E=4, k=1, seed=206)
     h = workloads.host_inputs(w)
     h["topk_idx"] = np.zeros_like(h["topk_idx"])
-    run = G.GpuRun(w, inputs=h)
+    run = G.GpuRun(w, inputs=h, tiles=tiles)
     G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
 
 
@@ -162,3 +164,14 @@ def test_weight_format_validation_and_switch(orc):
     G.assert_out_close(out8, ref_out(orc, w8, h8)["out"])
     with pytest.raises(mm.MMError):
         mm.mm_set_weight_format(run.moe.h, 2)
+
+
+def test_tile_policy_validation():
+    """The three widths and the automatic policy are accepted, anything else rejected."""
+    import moe_expert_layer_scan_gb300 as mm
+    moe = mm.MegaMoE(8, 512, 256, 2, 0)
+    for t in (mm.MM_TILES_16, mm.MM_TILES_112, mm.MM_TILES_224, mm.MM_TILES_AUTO):
+        mm.mm_set_tile_policy(moe.h, t)
+    for bad in (0, 32, 128, 200, 256):
+        with pytest.raises(mm.MMError):
+            mm.mm_set_tile_policy(moe.h, bad)

@@ -16,8 +16,8 @@ from workloads import CONFIGS, Workload
 pytestmark = pytest.mark.gpu
 
 # Several tiles and ragged tails at sizes the oracle finishes in seconds,
-# covering both token-tile widths (16-token tiles up to 12 routed rows per
-# expert on average, 112-token tiles above).
+# covering the three token-tile widths (16-token tiles up to 12 routed rows
+# per expert on average, 224-token tiles from 192, 112-token tiles between).
 SMALL_CASES = {
     "tiny": CONFIGS["tiny"],
     "decode_e16": Workload("decode_e16", T=8, H=7168, I=2048, E=16, k=8, seed=101),
@@ -33,6 +33,11 @@ SMALL_CASES = {
     # FP8 (MXFP8) weights, 16-token and 112-token tiles
     "fp8w_small": Workload("fp8w_small", T=8, H=1024, I=512, E=8, k=4, seed=110, w_fmt=1),
     "fp8w_large": Workload("fp8w_large", T=48, H=640, I=384, E=4, k=2, S=1, clamp=3.0, seed=111, w_fmt=1),
+    # 224-token tiles: one full tile and a 16-row tail per expert on average;
+    # several full tiles, a shared expert and an odd number of W2 blocks; MXFP8
+    "wide_t480": Workload("wide_t480", T=480, H=512, I=256, E=4, k=2, seed=112),
+    "wide_shared": Workload("wide_shared", T=600, H=384, I=384, E=3, k=2, S=1, clamp=2.0, seed=113),
+    "fp8w_wide": Workload("fp8w_wide", T=300, H=512, I=256, E=2, k=2, seed=114, w_fmt=1),
 }
 
 
@@ -110,7 +115,7 @@ def test_parity_full_size_sampled(name, orc):
     G.assert_out_close(out[tokens], ref["out"], f"{name} sampled tokens")
 
 
-@pytest.mark.parametrize("name", ["decode", "prefill_t256", "skewed_t48"])
+@pytest.mark.parametrize("name", ["decode", "prefill_t256", "skewed_t48", "wide_shared"])
 def test_fused_schedule_equals_split_bit_for_bit(name):
     """One persistent launch of both GEMMs computes the same tiles as one launch
     per linear: outputs and intermediates are identical."""
@@ -126,7 +131,9 @@ def test_fused_schedule_equals_split_bit_for_bit(name):
 
 
 @pytest.mark.parametrize("name,tiles", [("decode_e16", 112), ("small_tiles", 112), ("mid_t32", 16),
-                                        ("skewed_t48", 16), ("fp8w_small", 112)])
+                                        ("skewed_t48", 16), ("fp8w_small", 112), ("decode_e16", 224),
+                                        ("prefill_t256", 224), ("ragged", 224), ("fp8w_large", 224),
+                                        ("wide_t480", 112), ("wide_t480", 16)])
 def test_parity_with_the_other_tile_width(name, tiles, orc):
     """Each token-tile width is correct on the token counts the automatic policy
     gives to the other one."""
@@ -139,3 +146,18 @@ def test_parity_with_the_other_tile_width(name, tiles, orc):
         inter = run.intermediates(w.T)
         assert inter["status"] == 0
         G.assert_out_close(out, ref["out"])
+
+
+@pytest.mark.parametrize("name", ["wide_shared", "prefill_t256"])
+def test_tile_widths_agree_bit_for_bit(name):
+    """Every token-tile width runs each output element's K loop in the same
+    order: the outputs and intermediates of the three widths are identical."""
+    w = SMALL_CASES[name]
+    runs = [G.GpuRun(w, device_weights=True, tiles=t) for t in (16, 112, 224)]
+    outs = [out_bits(r.run()) for r in runs]
+    inters = [r.intermediates(w.T) for r in runs]
+    for o, i in zip(outs[1:], inters[1:]):
+        assert i["status"] == 0
+        assert np.array_equal(o, outs[0])
+        for k in ("l2a", "l2a_sf", "z"):
+            assert np.array_equal(i[k], inters[0][k]), k
