@@ -119,7 +119,11 @@ struct Tile {
 
 // Tile index -> expert, token tile and this CTA's weight tile: the table
 // counts weight-tile groups of cs tiles (one per CTA of a cluster). The tile
-// table and the row offsets are shared-memory copies.
+// table and the row offsets are shared-memory copies. An expert's rows are
+// split into the fewest token tiles of at most bn rows, all of one size
+// rounded up to 16 (the last takes the rest): 256 rows with bn = 224 give two
+// tiles of 128, not 224 + 32 (a tile costs its weight stream and a per-K-step
+// instruction floor whatever its row count).
 static __device__ __noinline__ Tile decode_tile(int tile, const int* tstart, const int* offs, int Ep, int fb_total,
                                            int bn, int rank, int cs) {
   int lo = 0, hi = Ep - 1;
@@ -137,8 +141,9 @@ static __device__ __noinline__ Tile decode_tile(int tile, const int* tstart, con
   const int tt = local - grp * ntt;
   t.fb = grp * cs + rank;
   t.active = t.fb < fb_total;
-  t.row0 = offs[lo] + tt * bn;
-  t.nrows = min(bn, cnt - tt * bn);
+  const int per = ((cnt + ntt - 1) / ntt + 15) & ~15;  // <= bn, and (ntt - 1) * per < cnt
+  t.row0 = offs[lo] + tt * per;
+  t.nrows = min(per, cnt - tt * per);
   return t;
 }
 

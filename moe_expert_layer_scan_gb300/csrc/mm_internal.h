@@ -18,10 +18,11 @@ constexpr int kRouteChunk = 8192;  // slots per CTA when routing runs on several
 constexpr int kRouteSingleMax = 16384;  // up to this many slots, one CTA routes everything
 constexpr int kRouteSmallMax = 512;     // up to this many slots, the lean one-CTA routing kernel
 
-// Token-tile widths (the MMA N dimension) and pipeline depths of the two GEMM
-// variants. "small" serves decode-like calls (few rows per expert), "large"
-// everything else; the N of each tile is the expert's remaining rows rounded up
-// to 16, so ragged tails never pay for a full tile.
+// Token-tile widths (the largest MMA N) of the GEMM variants. "small" serves
+// decode-like calls (few rows per expert), "large" and "wide" everything else;
+// an expert's rows are split into equal tiles (rounded up to 16 rows) and the
+// MMA N of a tile is its rows rounded up to 16, so ragged tails never pay for
+// a full tile.
 constexpr int kBnSmall = 16;
 constexpr int kBnLarge = 112;
 // 224-token tiles: one MMA of N up to 224 per K step and weight block keeps
