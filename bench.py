@@ -44,9 +44,10 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 # for the kernel named (fused "gemm" or "l1_gemm").
 NCU_TRAFFIC = {
     # decode (fused GEMM): E=64 capture (42 experts touched) scaled to the 61 experts one launch touches
-    "decode": {"src": "4a1244e6000d0dff", "kernel": "gemm", "bytes": 1442289670},
-    # prefill (L1 GEMM of the split schedule): T=2048/E=32 capture (16384 rows) scaled x8 to 131072 rows
-    "prefill": {"src": "4a1244e6000d0dff", "kernel": "l1_gemm", "bytes": 5240934400},
+    "decode": {"src": "96d4a1c2f1ef7675", "kernel": "gemm", "bytes": 1442342839},
+    # prefill (L1 GEMM of the split schedule, 224-token tiles): T=2048/E=32 capture (16384 rows)
+    # scaled x8 to 131072 rows
+    "prefill": {"src": "96d4a1c2f1ef7675", "kernel": "l1_gemm", "bytes": 5359276032},
 }
 
 
@@ -324,6 +325,7 @@ def measure_e2e(args, w, d, moe, out, flush, dist):
 
 
 def report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk):
+    import moe_expert_layer_scan_gb300 as mm
     ms = total_ms / args.steps
     tokens = w.T * world
     value = tokens / (ms / 1e3)
@@ -362,7 +364,9 @@ def report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk
             "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic",
             "config": dict(workload_config(w), parallelism=f"{world} independent replicas" if world > 1 else "1 GPU",
                            gemm_schedule=("fused" if "gemm" in kern else "split")
-                           + (" (auto)" if args.schedule == "auto" else "")),
+                           + (" (auto)" if args.schedule == "auto" else ""),
+                           token_tiles=f"{mm.mm_token_tile_width(moe.h, w.T)}"
+                           + (" (auto)" if args.tiles == -1 else "")),
             "tflops": alg["flops"] * world / (ms / 1e3) / 1e12,
             "hbm_gbs_whole_step": (alg["l1_bytes"] + alg["l2_bytes"]) / (ms / 1e3) / 1e9,
             "kernels_ms": kern,

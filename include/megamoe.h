@@ -144,6 +144,10 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
 #define MM_TILES224_MIN_ROWS_PER_EXPERT 192
 MM_API mm_status_t mm_set_tile_policy(mm_handle_t h, int policy);
 
+/* The token-tile width (16, 112 or 224) a call of T tokens runs with under the
+ * handle's current policy. Host only. */
+MM_API mm_status_t mm_token_tile_width(mm_handle_t h, int T, int* width);
+
 /* Weight element format (both linears). MM_WEIGHTS_MXFP4 (the default): E2M1
  * codes packed two per byte, the even K index in the low nibble (OCP MXFP4).
  * MM_WEIGHTS_MXFP8: E4M3 codes, one byte per element (OCP MXFP8; the FP8 x FP8

@@ -24,6 +24,7 @@ MM_DEV_TIMEOUT = 0x2
 STATUS_NAMES = {0: "MM_OK", 1: "MM_ERR_INVALID_ARG", 2: "MM_ERR_UNSUPPORTED", 3: "MM_ERR_WORKSPACE_TOO_SMALL",
                 4: "MM_ERR_CUDA", 5: "MM_ERR_DEVICE_TIMEOUT", 6: "MM_ERR_BAD_ROUTING", 7: "MM_ERR_ALIGNMENT"}
 EXPORTS = ["mm_status_string", "mm_create", "mm_set_options", "mm_set_schedule", "mm_set_tile_policy",
+           "mm_token_tile_width",
            "mm_set_weight_format",
            "mm_set_ep_ranks",
            "mm_set_expert_stats", "mm_workspace_bytes", "mm_run",
@@ -69,6 +70,7 @@ def lib() -> ctypes.CDLL:
         L.mm_set_ep_ranks.argtypes = [p, i32]
         L.mm_set_weight_format.argtypes = [p, i32]
         L.mm_set_tile_policy.argtypes = [p, i32]
+        L.mm_token_tile_width.argtypes = [p, i32, ctypes.POINTER(ctypes.c_int)]
         L.mm_set_expert_stats.argtypes = [p, p]
         L.mm_workspace_bytes.argtypes = [p, i32, ctypes.POINTER(ctypes.c_size_t)]
         L.mm_run.argtypes = [p, i32] + [p] * 10 + [ctypes.c_size_t, p]
@@ -118,6 +120,13 @@ def mm_set_schedule(h: int, schedule="auto") -> None:
 
 
 MM_TILES_AUTO, MM_TILES_16, MM_TILES_112, MM_TILES_224 = -1, 16, 112, 224
+
+
+def mm_token_tile_width(h: int, T: int) -> int:
+    """Token-tile width a call of T tokens runs with under the handle's policy."""
+    v = ctypes.c_int(0)
+    _check(lib().mm_token_tile_width(h, int(T), ctypes.byref(v)), "mm_token_tile_width")
+    return v.value
 
 
 def mm_set_tile_policy(h: int, policy: int = MM_TILES_AUTO) -> None:

@@ -235,6 +235,12 @@ mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes) {
   return MM_OK;
 }
 
+mm_status_t mm_token_tile_width(mm_handle_t h, int T, int* width) {
+  if (!h || !width || T < 0) return MM_ERR_INVALID_ARG;
+  *width = tile_width(variant_for(h, T));
+  return MM_OK;
+}
+
 mm_status_t mm_launches_per_run(mm_handle_t h, int T, int* launches) {
   if (!h || !launches || T < 0) return MM_ERR_INVALID_ARG;
   const int route = mm_route_launches(T * (h->k + h->S));
