@@ -297,7 +297,41 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     return decode_tile(l1 ? tile : tile - n1, l1 ? s_t1 : s_t2, s_off, g1.Ep, l1 ? g1.fb_total : g2.fb_total, BN,
                        rank, CS);
   };
-  const int tile0 = blockIdx.x / CS, tile_step = gridDim.x / CS;
+  // This CTA's (cluster's) tile sequence: tiles g, g + G, ... (concurrent
+  // CTAs work on adjacent tiles, so their weight streams stay close in HBM).
+  // Fused: the L1 tiles that way; the r = n1 mod G CTAs that hold one L1 tile
+  // more are still busy with it when the others reach the L2 tiles, so the
+  // first A = (G - r) * round(K1 / K2) L2 tiles go round-robin to the other
+  // G - r CTAs only (about one L1 tile's worth each), the rest to all G.
+  const int G = gridDim.x / CS, g = blockIdx.x / CS;
+  int r_l1 = 0, n_early = 0;
+  if (MODE == kModeFused) {
+    r_l1 = n1 % G;
+    const int s1 = g1.K / 128, s2 = g2.K / 128;
+    const long long a = (long long)(G - r_l1) * ((s1 + s2 / 2) / s2);
+    n_early = r_l1 == 0 ? 0 : (int)(a < num_tiles - n1 ? a : num_tiles - n1);
+  }
+  // first L2 tile (index past the L1 tiles) of this CTA, and the one after j
+  auto l2_first = [&]() {
+    const int j = g >= r_l1 && g - r_l1 < n_early ? g - r_l1 : n_early + g;
+    return n1 + j < num_tiles ? n1 + j : num_tiles;
+  };
+  auto l2_next = [&](int j) {
+    int jn;
+    if (j < n_early) {
+      jn = j + (G - r_l1);
+      if (jn >= n_early) jn = n_early + g;
+    } else {
+      jn = j + G;
+    }
+    return n1 + jn < num_tiles ? n1 + jn : num_tiles;
+  };
+  const int tile0 = MODE != kModeFused || g < n1 ? g : l2_first();
+  auto next_tile = [&](int t) {
+    if (MODE != kModeFused) return t + G;
+    if (t < n1) return t + G < n1 ? t + G : l2_first();
+    return l2_next(t - n1);
+  };
   constexpr uint16_t kAllCtas = (uint16_t)((1u << CS) - 1u);
   // wait sites reported in the status word on expiry: L1 tiles s, L2 tiles 8 + s
   constexpr uint32_t kSiteReady = 8u + 6u;  // an L2 tile waiting for its L1 rows (fused)
@@ -331,7 +365,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     bool cur_ready = false;  // the current tile's counter was seen complete by a peek
     // transaction bytes of one 128x128 weight box: packed E2M1 or E4M3
     const uint32_t a_tx = g1.w_fp8 ? (uint32_t)(C::BM * C::BK) : (uint32_t)C::A_TX;
-    for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
+    for (int tile = tile0; tile < num_tiles && ok; tile = next_tile(tile)) {
       const bool l1 = is_l1(tile);
       const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
@@ -350,7 +384,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
         break;
       }
       bool next_ready = false;
-      const int ntile = tile + tile_step;
+      const int ntile = next_tile(tile);
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
         if (sf_tma && (kb & 3) == 0) {
           // this group's scale rows (16 bytes = four K steps per row) into a raw slot
@@ -423,7 +457,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     constexpr int NB = C::SFB_ROWS / 32;
     uint32_t it = 0, gi = 0;
     bool ok = true;
-    for (int tile = tile0; tile < num_tiles && ok; tile += tile_step) {
+    for (int tile = tile0; tile < num_tiles && ok; tile = next_tile(tile)) {
       const bool l1 = is_l1(tile);
       const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
@@ -533,7 +567,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       const bool cur_active = tc.active, cur_two = has_second(g, tc);
       int ntile = tile, nkg = kg + 4;
       if (nkg >= kblocks) {
-        ntile = tile + tile_step;
+        ntile = next_tile(tile);
         nkg = 0;
       }
       const bool has_next = ntile < num_tiles;
@@ -594,7 +628,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       const uint32_t a_fmt = g1.w_fp8 ? 0u : 5u;
       uint32_t it = 0, tcount = 0;
       bool ok = true;
-      for (int tile = tile0; tile < num_tiles && ok; tile += tile_step, ++tcount) {
+      for (int tile = tile0; tile < num_tiles && ok; tile = next_tile(tile), ++tcount) {
         const bool l1 = is_l1(tile);
         const Phase g = phase_of(l1, g1, g2);
         const uint32_t site0 = l1 ? 0u : 8u;
@@ -644,7 +678,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     const int q = warp & 3;
     const int half = (warp - 4) >> 2;  // 0 when there is one warp per quadrant
     uint32_t tcount = 0;
-    for (int tile = tile0; tile < num_tiles; tile += tile_step, ++tcount) {
+    for (int tile = tile0; tile < num_tiles; tile = next_tile(tile), ++tcount) {
       const bool l1 = is_l1(tile);
       const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
