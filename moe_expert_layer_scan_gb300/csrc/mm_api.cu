@@ -107,9 +107,20 @@ bool deep_disabled() {
   return off;
 }
 
+// MM_QUAD=0 keeps 16-token tiles at two weight blocks (measurement only).
+bool quad_disabled() {
+  static const bool off = [] {
+    const char* e = getenv("MM_QUAD");
+    return e && e[0] == '0';
+  }();
+  return off;
+}
+
 // Kernel variant of a call: 0 = 16-token tiles, 2 = 16-token tiles with six
-// stages (at most kDeepMaxExperts experts), 1 = 112-token tiles, 3 = 224-token
-// tiles.
+// stages (at most kDeepMaxExperts experts), 4 = 16-token tiles with four weight
+// blocks (E4M3 weights, at most kQuadMaxExperts experts, I a multiple of 256:
+// measured 97% -> 100% of the copy bandwidth at decode; with E2M1 weights it
+// was 2% slower than variant 2), 1 = 112-token tiles, 3 = 224-token tiles.
 int variant_for(const mm_handle* h, int T) {
   const long long rows = (long long)T * (h->k + h->S), ep = h->E + h->S;
   int width = h->tiles;
@@ -119,6 +130,8 @@ int variant_for(const mm_handle* h, int T) {
                                                             : MM_TILES_112;
   if (width == MM_TILES_112) return 1;
   if (width == MM_TILES_224) return 3;
+  if (h->w_fmt == MM_WEIGHTS_MXFP8 && h->E + h->S <= kQuadMaxExperts && h->I % 256 == 0 && !quad_disabled())
+    return 4;
   return (h->E + h->S <= kDeepMaxExperts && !deep_disabled()) ? 2 : 0;
 }
 
@@ -267,7 +280,12 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
 
   uint8_t* base = static_cast<uint8_t*>(ws);
   const int Ep = h->E + h->S, Kp = h->k + h->S;
-  const int variant = variant_for(h, T);
+  // Scale rows by TMA when every scale row is a whole number of 16-byte groups
+  // (K a multiple of 512) and the weight scale tensors are 16-byte aligned;
+  // otherwise the scale warp loads them itself (two-block tiles only).
+  const bool sf_tma = h->H % 512 == 0 && h->I % 512 == 0 && aligned(w1_sf, 16) && aligned(w2_sf, 16);
+  int variant = variant_for(h, T);
+  if (variant == 4 && !sf_tma) variant = (h->E + h->S <= kDeepMaxExperts && !deep_disabled()) ? 2 : 0;
   const int bn1 = tile_width(variant);
   const int bn2 = bn1;
 
@@ -292,7 +310,8 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ra.T = T; ra.E = h->E; ra.k = h->k; ra.S = h->S;
   ra.bn_l1 = bn1; ra.bn_l2 = bn2;
   const int cs = mm_gemm_cluster(variant);
-  const int f1 = h->I / 128, f2 = (h->H + 255) / 256;  // weight tiles per expert
+  const int na = mm_gemm_blocks(variant);                 // 128-row weight blocks per tile
+  const int f1 = h->I / (64 * na), f2 = (h->H + 128 * na - 1) / (128 * na);  // weight tiles per expert
   ra.fb_l1 = (f1 + cs - 1) / cs;                         // tile-table entries: groups of cs weight tiles
   ra.fb_l2 = (f2 + cs - 1) / cs;
   int ev_i = 0;
@@ -342,10 +361,6 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
     return MM_ERR_CUDA;
   if (!encode_2d(&maps.a2, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)(bn2 / cs)))
     return MM_ERR_CUDA;
-  // Scale rows by TMA when every scale row is a whole number of 16-byte groups
-  // (K a multiple of 512) and the weight scale tensors are 16-byte aligned;
-  // otherwise the scale warp loads them itself.
-  const bool sf_tma = h->H % 512 == 0 && h->I % 512 == 0 && aligned(w1_sf, 16) && aligned(w2_sf, 16);
   if (sf_tma) {
     if (h->w1sf_key != w1_sf) {
       if (!encode_sf(&h->tm_w1sf, w1_sf, (uint64_t)h->H / 32, (uint64_t)Ep * 2 * h->I)) return MM_ERR_CUDA;

@@ -46,22 +46,26 @@ namespace mm {
 
 // Epilogue warps: two per TMEM lane quadrant for the large tiles (their L1
 // epilogue is as long as the main loop), one for the 16-column decode tiles.
-template <int BN>
+// One MMA-issuing warp per weight block of a tile (NA of them): warp 0 is the
+// producer, warps 1 and 2 issue for blocks 0 and 1 (warp 2 also allocates
+// TMEM), warp 3 handles the scales, warps 4 .. 4 + EPI - 1 are the epilogue
+// and warps 4 + EPI .. issue for blocks 2 .. NA - 1.
+template <int BN, int NA>
 struct Warps {
   static constexpr int EPI = BN > 16 ? 8 : 4;
-  static constexpr int THREADS = 32 * (4 + EPI);  // producer, 2 issuers/allocator, scale warp, epilogue
+  static constexpr int THREADS = 32 * (2 + NA + EPI);
 };
 
 enum : int { kModeL2 = 0, kModeL1 = 1, kModeFused = 2 };
 
-template <int BN, int STAGES, int CS>
+template <int BN, int STAGES, int CS, int NA_ = 2>
 struct GemmCfg {
   static constexpr int BM = 128;                         // weight rows per MMA
   static constexpr int BK = 128;                         // K per stage
-  // Two 128-row weight tiles per stage: L1 the gate rows and the matching up
-  // rows; L2 two consecutive 128-row blocks of W2 (the second may be absent
-  // when H / 128 is odd).
-  static constexpr int NA = 2;
+  // NA 128-row weight blocks per stage (2 or 4): L1 the gate rows of NA / 2
+  // feature blocks and the matching up rows; L2 NA consecutive 128-row blocks
+  // of W2 (the last ones may be absent at the end of H).
+  static constexpr int NA = NA_;
   static constexpr int NI = NA;                          // MMA-issuing threads, one per weight tile
   static constexpr int A_BYTES = BM * BK;                // 16 KB in SMEM (4-bit codes padded to bytes)
   static constexpr int A_TX = BM * BK / 2;               // transaction bytes of one weight box (packed 4-bit size)
@@ -78,12 +82,12 @@ struct GemmCfg {
   static constexpr bool DEEP = BN == 16 && STAGES > 5;
   // copies of the two tile tables and the row offsets ([experts + 1] each)
   static constexpr int TAB_OFF = BAR_OFF + 256;
-  static constexpr int TAB_INTS = DEEP ? kDeepMaxExperts + 1 : kMaxExperts + 1;
+  static constexpr int TAB_INTS = (NA > 2 ? kQuadMaxExperts : DEEP ? kDeepMaxExperts : kMaxExperts) + 1;
   // L2 tiles whose L1 rows the producer has seen stored (fused schedule)
   static constexpr int L2RDY_OFF = TAB_OFF + 3 * TAB_INTS * 4;
   // TMA-loaded scale rows: RAW_G groups of four K steps; per group 16 bytes of
   // each of 128 rows for each weight block and of RAW_B_ROWS token rows
-  static constexpr int RAW_G = DEEP ? 2 : 3;
+  static constexpr int RAW_G = DEEP || NA > 2 ? 2 : 3;
   static constexpr int RAW_ROWS_BYTES = 128 * 16;
   static constexpr int RAW_B_ROWS = BN <= 32 ? 32 : (BN <= 128 ? 128 : 256);
   static constexpr int RAW_B_BYTES = RAW_B_ROWS * 16;
@@ -162,19 +166,22 @@ __device__ __forceinline__ Phase phase_of(bool l1, const GemmArgs& g1, const Gem
   p.act_sf = l1 ? g1.act_sf : g2.act_sf;
   p.K = l1 ? g1.K : g2.K;
   p.rows_w = l1 ? g1.rows_w : g2.rows_w;
-  p.second = l1 ? g1.I : 128;  // row offset of the tile's second 128-row block
+  p.second = g1.I;  // L1: row offset of the up rows from the gate rows
   p.w_sf_vec = l1 ? g1.w_sf_vec : g2.w_sf_vec;
   p.act_sf_vec = l1 ? g1.act_sf_vec : g2.act_sf_vec;
   return p;
 }
 
-// First weight row of a tile's first 128-row block, and whether the second
-// block exists (L1: gate/up pair; L2: two W2 blocks, the last may be single).
-__device__ __forceinline__ int tile_wrow(const Phase& p, const Tile& t) {
-  return t.e * p.rows_w + t.fb * (p.l1 ? 128 : 256);
+// First weight row of weight block u of a tile with na blocks, and whether it
+// exists. L1: block 2j holds the gate rows of the tile's j-th 128-row feature
+// block, block 2j + 1 the matching up rows (I rows further); L2: na
+// consecutive 128-row blocks of W2, the last ones absent at the end of H.
+__device__ __forceinline__ int block_wrow(const Phase& p, const Tile& t, int u, int na) {
+  return p.l1 ? t.e * p.rows_w + (t.fb * (na / 2) + (u >> 1)) * 128 + (u & 1) * p.second
+              : t.e * p.rows_w + (t.fb * na + u) * 128;
 }
-__device__ __forceinline__ bool has_second(const Phase& p, const Tile& t) {
-  return t.active && (p.l1 || t.fb * 256 + 128 < p.rows_w);
+__device__ __forceinline__ bool block_active(const Phase& p, const Tile& t, int u, int na) {
+  return t.active && (p.l1 || (t.fb * na + u) * 128 < p.rows_w);
 }
 
 // Four K steps of one row's UE8M0 scales (16 bytes); `avail` steps exist.
@@ -217,11 +224,12 @@ __device__ __forceinline__ float inv_scale(uint32_t code) {
   return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(1u << (n + 149));
 }
 
-template <int MODE, int BN, int STAGES, int CS>
-__global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
+template <int MODE, int BN, int STAGES, int CS, int NA>
+__global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g1,
                 const __grid_constant__ GemmArgs g2) {
-  using C = GemmCfg<BN, STAGES, CS>;
+  using C = GemmCfg<BN, STAGES, CS, NA>;
+  using W = Warps<BN, NA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -243,7 +251,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], C::NI);  // tcgen05.commit after the last K step, per issuing thread
-      mbar_init(&tempty[b], Warps<BN>::EPI);  // one arrival per epilogue warp
+      mbar_init(&tempty[b], W::EPI);  // one arrival per epilogue warp
     }
     for (int b = 0; b < C::RAW_G; ++b) {
       mbar_init(&rfull[b], 1);   // producer's expect_tx arrival
@@ -342,15 +350,25 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
   // the stage's TMEM slot (the weight blocks' and the token tile's, the latter
   // shared by both MMA streams) and commits the copies to sfready[s]; the MMA
   // threads then issue only MMAs. The slot is free once empty[s] completed.
-  auto copy_scales = [&](int s, bool a0, bool a1, const uint8_t* sF) {
+  auto copy_scales = [&](int s, uint32_t amask, const uint8_t* sF) {
     tc_fence_after();
     const uint32_t slot = tmem + (uint32_t)(C::SF_BASE + s * C::SF_STAGE_COLS);
-    if (a0) tc_cp_32x128b_warpx4(slot, sdesc_sf_32x16(smem_u32(sF)));
-    if (a1 && C::NA > 1) tc_cp_32x128b_warpx4(slot + 4u, sdesc_sf_32x16(smem_u32(sF + 512)));
+#pragma unroll
+    for (int u = 0; u < C::NA; ++u)
+      if ((amask >> u) & 1u) tc_cp_32x128b_warpx4(slot + 4u * u, sdesc_sf_32x16(smem_u32(sF + 512 * u)));
 #pragma unroll
     for (int gq = 0; gq < C::SFB_ROWS / 128; ++gq)
       tc_cp_32x128b_warpx4(slot + 4u * C::NA + 4u * gq, sdesc_sf_32x16(smem_u32(sF + C::NA * 512 + gq * 512)));
     tc_commit(&sfready[s]);
+  };
+
+  // the tile's existing weight blocks (bit u) and their first rows
+  auto block_mask = [&](const Phase& ph, const Tile& t) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int u = 0; u < C::NA; ++u)
+      if (block_active(ph, t, u, C::NA)) m |= 1u << u;
+    return m;
   };
 
   if (warp == 0) {
@@ -370,8 +388,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
       const Tile t = tile_of(tile, l1);
-      const int wrow = tile_wrow(g, t);
-      const bool two = has_second(g, t);
+      const uint32_t amask = block_mask(g, t);
+      const int nact = __popc(amask);
       const int kblocks = g.K / C::BK;
       const CUtensorMap* tw = l1 ? &maps.w1 : &maps.w2;
       const CUtensorMap* ta = l1 ? &maps.a1 : &maps.a2;
@@ -396,10 +414,11 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
           }
           if (lane == 0) {
             uint8_t* raw = smem + C::RAW_OFF + gslot * C::RAW_GROUP_BYTES;
-            mbar_arrive_expect_tx(&rfull[gslot], ((t.active ? 1 : 0) + (two ? 1 : 0)) * C::RAW_ROWS_BYTES +
-                                                     C::RAW_B_BYTES);
-            if (t.active) tma_load_2d(raw, twsf, &rfull[gslot], kb * 4, wrow);
-            if (two) tma_load_2d(raw + C::RAW_ROWS_BYTES, twsf, &rfull[gslot], kb * 4, wrow + g.second);
+            mbar_arrive_expect_tx(&rfull[gslot], nact * C::RAW_ROWS_BYTES + C::RAW_B_BYTES);
+#pragma unroll
+            for (int u = 0; u < C::NA; ++u)
+              if ((amask >> u) & 1u)
+                tma_load_2d(raw + u * C::RAW_ROWS_BYTES, twsf, &rfull[gslot], kb * 4, block_wrow(g, t, u, C::NA));
             tma_load_2d(raw + C::NA * C::RAW_ROWS_BYTES, tasf, &rfull[gslot], kb * 4, t.row0);
           }
           ++gi;
@@ -416,9 +435,10 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
         uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
         if (lane == 0) {
           // the whole token tile lands here: this CTA's share and the others' multicasts
-          mbar_arrive_expect_tx(&full[s], (t.active ? (two ? 2 : 1) : 0) * a_tx + C::B_BYTES);
-          if (t.active) tma_load_2d(sA, tw, &full[s], kb * C::BK, wrow);
-          if (two) tma_load_2d(sA + C::A_BYTES, tw, &full[s], kb * C::BK, wrow + g.second);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)nact * a_tx + C::B_BYTES);
+#pragma unroll
+          for (int u = 0; u < C::NA; ++u)
+            if ((amask >> u) & 1u) tma_load_2d(sA + u * C::A_BYTES, tw, &full[s], kb * C::BK, block_wrow(g, t, u, C::NA));
           if constexpr (CS == 1) {
             tma_load_2d(sB, ta, &full[s], kb * C::BK, t.row0);
           } else {
@@ -462,7 +482,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
       const Tile t = tile_of(tile, l1);
-      const bool two = has_second(g, t);
+      const uint32_t amask = block_mask(g, t);
       const int nb = (t.nrows + 31) / 32;
       const int kblocks = g.K / C::BK;
       for (int kg = 0; kg < kblocks && ok; kg += 4, ++gi) {
@@ -475,7 +495,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
         for (int op = 0; op < C::NA; ++op)
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            wa[op][i] = ((op == 0 && t.active) || two)
+            wa[op][i] = ((amask >> op) & 1u)
                             ? *reinterpret_cast<const uint4*>(raw + op * C::RAW_ROWS_BYTES + (32 * i + lane) * 16)
                             : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -501,13 +521,15 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
                          word(wb[4 * q + 2], c), word(wb[4 * q + 3], c));
           fence_proxy_async_smem();  // generic-proxy writes, read next by tcgen05.cp
           __syncwarp();
-          if (lane == 0) copy_scales(s, t.active, two, sF);
+          if (lane == 0) copy_scales(s, amask, sF);
           ++it;
         }
       }
     }
-  } else if (warp == 3) {
+  } else if (warp == 3 && C::NA == 2) {
     // ------------------------------------------------------------ scale-factor producer
+    // (tiles of two weight blocks only: the host runs four-block tiles only
+    // with TMA-loaded scale rows)
     // Loads each row's UE8M0 bytes for a group of four K steps at once (one
     // 16-byte request per row) and, per K step, writes the layout
     // tcgen05.cp.32x128b.warpx4 reads: 16 bytes per lane l holding the step's
@@ -522,8 +544,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       const bool l1 = is_l1(tile);
       const Phase g = phase_of(l1, g1, g2);
       const Tile t = tile_of(tile, l1);
-      const int wrow = tile_wrow(g, t);
-      const bool two = has_second(g, t);
+      const uint32_t amask = block_mask(g, t);
       const int nb = (t.nrows + 31) / 32;
       const int sf_ld = g.K / 32;
       const int avail = g.K / C::BK - kg;
@@ -533,8 +554,8 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       for (int op = 0; op < C::NA; ++op)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          wa[op][i] = ((op == 0 && t.active) || two)
-                          ? load_sf4(g.w_sf + (size_t)(wrow + op * g.second + 32 * i + lane) * sf_ld + 4 * kg,
+          wa[op][i] = ((amask >> op) & 1u)
+                          ? load_sf4(g.w_sf + (size_t)(block_wrow(g, t, op, C::NA) + 32 * i + lane) * sf_ld + 4 * kg,
                                      wvec, avail, false)
                           : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -564,7 +585,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       const int kblocks = g.K / C::BK;
       const int avail = kblocks - kg;
       const Tile tc = tile_of(tile, l1);
-      const bool cur_active = tc.active, cur_two = has_second(g, tc);
+      const uint32_t cur_mask = block_mask(g, tc);
       int ntile = tile, nkg = kg + 4;
       if (nkg >= kblocks) {
         ntile = next_tile(tile);
@@ -599,7 +620,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
                        word(cb[4 * q + 2], c), word(cb[4 * q + 3], c));
         fence_proxy_async_smem();  // generic-proxy writes, read next by tcgen05.cp
         __syncwarp();
-        if (lane == 0) copy_scales(s, cur_active, cur_two, sF);
+        if (lane == 0) copy_scales(s, cur_mask, sF);
         ++it;
       }
       if (!ok || !has_next) break;
@@ -616,14 +637,14 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       tile = ntile;
       kg = nkg;
     }
-  } else if (warp == 1 || warp == 2) {
+  } else if (warp == 1 || warp == 2 || warp >= 4 + W::EPI) {
     // ------------------------------------------------------------ MMA issuers
-    // One thread per weight tile (warp 1: first tile, warp 2: second tile): the
-    // tcgen05 instruction stream of a K step is split between them. Each
-    // copies its own scale factors to TMEM and commits its own work (a missing
-    // second L2 block still commits, so the barrier counts hold).
+    // One thread per weight block (warps 1, 2, then 4 + EPI ...): one warp
+    // issues about one block-scaled MMA per 125 cycles, so the instruction
+    // stream of a K step is split between them. Each commits its own work (a
+    // missing last L2 block still commits, so the barrier counts hold).
     if (lane == 0) {
-      const int u = warp - 1;
+      const int u = warp <= 2 ? warp - 1 : warp - (4 + W::EPI) + 2;
       // A (weights): E2M1 (format 5) or E4M3 (format 0); B (tokens): E4M3
       const uint32_t a_fmt = g1.w_fp8 ? 0u : 5u;
       uint32_t it = 0, tcount = 0;
@@ -640,7 +661,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(buf * C::ACC_COLS + u * BN);
         const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
-        const bool active = u == 0 ? t.active : has_second(g, t);
+        const bool active = block_active(g, t, u, C::NA);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
@@ -671,7 +692,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 4 + W::EPI) {
     // ------------------------------------------------------------ epilogue
     // Warp w reads TMEM lanes 32*(w%4)..+31 (hardware rule); the two warps of
     // a quadrant take alternate 16-column chunks of the token tile.
@@ -688,8 +709,6 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
       if (!mbar_wait(&tfull[buf], bph, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 256)) break;
       tc_fence_after();
       const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::ACC_COLS);
-      // L1: intermediate column of the gate/up pair; L2: hidden column of block 0 (block 1: +128)
-      const int feat = t.fb * (l1 ? 128 : 256) + 32 * q + lane;
       if (MODE != kModeL2 && l1) {
         // The per-column amax over the warp's 32 features (one UE8M0 group) is
         // a transpose-reduction: after the exchange steps lane c (32 columns)
@@ -700,14 +719,19 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
         // two warps of a quadrant (7 chunks of 32 would not).
         constexpr int NC = (BN > 16 && BN != 224) ? 32 : 16;
         constexpr int LOG2NC = NC == 32 ? 5 : 4;
-        for (int c0 = NC * half; t.active && c0 < t.nrows; c0 += NC * (Warps<BN>::EPI / 4)) {
+        // feature block j of the tile: gate accumulator 2j, up accumulator 2j + 1
+        for (int jb = 0; jb < C::NA / 2; ++jb) {
+        const uint32_t tg = tbase + (uint32_t)(2 * jb * BN), tu = tg + (uint32_t)BN;
+        const int fblk = t.fb * (C::NA / 2) + jb;  // 128-feature block of the intermediate
+        const int feat = fblk * 128 + 32 * q + lane;
+        for (int c0 = NC * half; t.active && c0 < t.nrows; c0 += NC * (W::EPI / 4)) {
           const int ncol = min(NC, t.nrows - c0);
           uint32_t gt0[16], gt1[16], u0[16], u1[16];
-          tmem_ld_x16(tbase + (uint32_t)c0, gt0);
-          tmem_ld_x16(tbase + (uint32_t)(BN + c0), u0);
+          tmem_ld_x16(tg + (uint32_t)c0, gt0);
+          tmem_ld_x16(tu + (uint32_t)c0, u0);
           if (NC == 32 && ncol > 16) {
-            tmem_ld_x16(tbase + (uint32_t)(c0 + 16), gt1);
-            tmem_ld_x16(tbase + (uint32_t)(BN + c0 + 16), u1);
+            tmem_ld_x16(tg + (uint32_t)(c0 + 16), gt1);
+            tmem_ld_x16(tu + (uint32_t)(c0 + 16), u1);
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) gt1[j] = u1[j] = 0u;
@@ -747,7 +771,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
           const uint32_t code = requant_code(v[0]);  // column c0 + mycol
           const float inv = inv_scale(code);
           if ((lane & ((1 << (5 - LOG2NC)) - 1)) == 0 && mycol < ncol)
-            g1.out_sf[(size_t)(t.row0 + c0 + mycol) * (g1.I / 32) + t.fb * 4 + q] = (uint8_t)code;
+            g1.out_sf[(size_t)(t.row0 + c0 + mycol) * (g1.I / 32) + fblk * 4 + q] = (uint8_t)code;
 #pragma unroll
           for (int j = 0; j < NC; ++j) {
             const float ij = __shfl_sync(0xffffffffu, inv, j << (5 - LOG2NC));
@@ -755,14 +779,21 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
             if (j < ncol) g1.out_q[(size_t)(t.row0 + c0 + j) * g1.I + feat] = qb;
           }
         }
+        }
         // fused: this warp's share of the token tile's L2 operand is stored
         if (MODE == kModeFused && t.active) warp_signal(g1.ready + t.row0);
       } else if (MODE != kModeL1) {
-        const bool two = has_second(phase_of(false, g1, g2), t);
-        for (int c0 = 16 * half; t.active && c0 < t.nrows; c0 += 16 * (Warps<BN>::EPI / 4)) {
+        // W2 blocks 2j and 2j + 1 of the tile: hidden columns feat and feat + 128
+        const Phase g2p = phase_of(false, g1, g2);
+        for (int jb = 0; jb < C::NA / 2; ++jb) {
+        if (!block_active(g2p, t, 2 * jb, C::NA)) break;
+        const bool two = block_active(g2p, t, 2 * jb + 1, C::NA);
+        const int feat = (t.fb * C::NA + 2 * jb) * 128 + 32 * q + lane;
+        const uint32_t tg = tbase + (uint32_t)(2 * jb * BN), th = tg + (uint32_t)BN;
+        for (int c0 = 16 * half; c0 < t.nrows; c0 += 16 * (W::EPI / 4)) {
           uint32_t gv[16], hv[16];
-          tmem_ld_x16(tbase + (uint32_t)c0, gv);
-          tmem_ld_x16(tbase + (uint32_t)(BN + c0), hv);
+          tmem_ld_x16(tg + (uint32_t)c0, gv);
+          tmem_ld_x16(th + (uint32_t)c0, hv);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -773,6 +804,7 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
               if (two) zr[feat + 128] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(hv[j])));
             }
           }
+        }
         }
       }
       tc_fence_before();
@@ -791,10 +823,10 @@ __global__ void __launch_bounds__(Warps<BN>::THREADS, 1)
   }
 }
 
-template <int MODE, int BN, int STAGES, int CS>
+template <int MODE, int BN, int STAGES, int CS, int NA = 2>
 static int set_smem_attr(int* max_ctas) {
-  using C = GemmCfg<BN, STAGES, CS>;
-  auto k = gemm_kernel<MODE, BN, STAGES, CS>;
+  using C = GemmCfg<BN, STAGES, CS, NA>;
+  auto k = gemm_kernel<MODE, BN, STAGES, CS, NA>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return (int)e;
   int dev = 0, sms = 0;
@@ -810,7 +842,7 @@ static int set_smem_attr(int* max_ctas) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3((unsigned)(sms / CS * CS));
-    cfg.blockDim = dim3(Warps<BN>::THREADS);
+    cfg.blockDim = dim3(Warps<BN, NA>::THREADS);
     cfg.dynamicSmemBytes = C::SMEM_BYTES;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -822,20 +854,21 @@ static int set_smem_attr(int* max_ctas) {
   return 0;
 }
 
-template <int MODE, int BN, int STAGES, int CS>
+template <int MODE, int BN, int STAGES, int CS, int NA = 2>
 static int launch(const GemmMaps* maps, const GemmArgs* g1, const GemmArgs* g2, int num_ctas, cudaStream_t st) {
-  using C = GemmCfg<BN, STAGES, CS>;
-  return (int)launch_kernel(gemm_kernel<MODE, BN, STAGES, CS>, dim3((unsigned)num_ctas), dim3(Warps<BN>::THREADS),
-                            C::SMEM_BYTES, st, true, CS, *maps, *g1, *g2);
+  using C = GemmCfg<BN, STAGES, CS, NA>;
+  return (int)launch_kernel(gemm_kernel<MODE, BN, STAGES, CS, NA>, dim3((unsigned)num_ctas),
+                            dim3(Warps<BN, NA>::THREADS), C::SMEM_BYTES, st, true, CS, *maps, *g1, *g2);
 }
 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
 // five, measured as fast as six).
-constexpr int kStagesSmall = 5, kStagesSmallDeep = 6, kStagesLarge = 4, kStagesWide = 3;
+constexpr int kStagesSmall = 5, kStagesSmallDeep = 6, kStagesLarge = 4, kStagesWide = 3, kStagesQuad = 3;
 // CTAs per launch of each instantiation: [mode][variant] (variant 2: 16-token
 // tiles with six stages, for at most kDeepMaxExperts experts; variant 3:
-// 224-token tiles)
-static int g_ctas[3][4];
+// 224-token tiles; variant 4: 16-token tiles with four weight blocks, for at
+// most kQuadMaxExperts experts)
+static int g_ctas[3][5];
 
 }  // namespace mm
 
@@ -854,20 +887,27 @@ extern "C" int mm_gemm_prepare(void) {
   if ((e = set_smem_attr<kModeL1, kBnWide, kStagesWide, kClusterLarge>(&g_ctas[kModeL1][3]))) return e;
   if ((e = set_smem_attr<kModeL2, kBnWide, kStagesWide, kClusterLarge>(&g_ctas[kModeL2][3]))) return e;
   if ((e = set_smem_attr<kModeFused, kBnWide, kStagesWide, kClusterLarge>(&g_ctas[kModeFused][3]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesQuad, 1, 4>(&g_ctas[kModeL1][4]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesQuad, 1, 4>(&g_ctas[kModeL2][4]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesQuad, 1, 4>(&g_ctas[kModeFused][4]))) return e;
   return 0;
 }
+
+extern "C" int mm_gemm_blocks(int variant) { return variant == 4 ? 4 : 2; }
 
 extern "C" int mm_gemm_cluster(int variant) { return variant == 1 || variant == 3 ? mm::kClusterLarge : 1; }
 
 extern "C" int mm_gemm_epilogue_warps(int variant) {
-  return variant == 1   ? mm::Warps<mm::kBnLarge>::EPI
-         : variant == 3 ? mm::Warps<mm::kBnWide>::EPI
-                        : mm::Warps<mm::kBnSmall>::EPI;
+  return variant == 1   ? mm::Warps<mm::kBnLarge, 2>::EPI
+         : variant == 3 ? mm::Warps<mm::kBnWide, 2>::EPI
+         : variant == 4 ? mm::Warps<mm::kBnSmall, 4>::EPI
+                        : mm::Warps<mm::kBnSmall, 2>::EPI;
 }
 
 extern "C" int mm_gemm_token_scale_box_rows(int variant) {
   return variant == 1   ? mm::GemmCfg<mm::kBnLarge, mm::kStagesLarge, mm::kClusterLarge>::RAW_B_ROWS
          : variant == 3 ? mm::GemmCfg<mm::kBnWide, mm::kStagesWide, mm::kClusterLarge>::RAW_B_ROWS
+         : variant == 4 ? mm::GemmCfg<mm::kBnSmall, mm::kStagesQuad, 1, 4>::RAW_B_ROWS
                         : mm::GemmCfg<mm::kBnSmall, mm::kStagesSmall, 1>::RAW_B_ROWS;
 }
 
@@ -882,11 +922,13 @@ extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, con
     return variant == 0   ? launch<kModeL1, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
            : variant == 2 ? launch<kModeL1, kBnSmall, kStagesSmallDeep, 1>(maps, a, a, n, st)
            : variant == 3 ? launch<kModeL1, kBnWide, kStagesWide, kClusterLarge>(maps, a, a, n, st)
+           : variant == 4 ? launch<kModeL1, kBnSmall, kStagesQuad, 1, 4>(maps, a, a, n, st)
                           : launch<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
   }
   return variant == 0   ? launch<kModeL2, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
          : variant == 2 ? launch<kModeL2, kBnSmall, kStagesSmallDeep, 1>(maps, a, a, n, st)
          : variant == 3 ? launch<kModeL2, kBnWide, kStagesWide, kClusterLarge>(maps, a, a, n, st)
+         : variant == 4 ? launch<kModeL2, kBnSmall, kStagesQuad, 1, 4>(maps, a, a, n, st)
                         : launch<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
 }
 
@@ -898,5 +940,6 @@ extern "C" int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const
   return variant == 0   ? launch<kModeFused, kBnSmall, kStagesSmall, 1>(maps, g1, g2, n, st)
          : variant == 2 ? launch<kModeFused, kBnSmall, kStagesSmallDeep, 1>(maps, g1, g2, n, st)
          : variant == 3 ? launch<kModeFused, kBnWide, kStagesWide, kClusterLarge>(maps, g1, g2, n, st)
+         : variant == 4 ? launch<kModeFused, kBnSmall, kStagesQuad, 1, 4>(maps, g1, g2, n, st)
                         : launch<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(maps, g1, g2, n, st);
 }

@@ -37,6 +37,12 @@ constexpr int kClusterLarge = 2;
 // 16-token tiles run six pipeline stages (instead of five) when the call has
 // at most this many experts (E + S): the smaller tile tables make room.
 constexpr int kDeepMaxExperts = 300;
+// 16-token tiles with four 128-row weight blocks per tile (two gate/up pairs in
+// L1, four W2 blocks in L2) and four MMA-issuing warps: twice the MMA issue
+// capacity per weight byte, which is what limits the two-block tiles when they
+// stream E4M3 weights. Three 66 KB stages; the tile tables fit for at most
+// this many experts (E + S), and I must be a multiple of 256.
+constexpr int kQuadMaxExperts = 264;
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -163,7 +169,8 @@ int mm_route_launches(int slots);  // kernels mm_launch_route enqueues for this 
 int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream);
 int mm_launch_combine(const mm::CombineArgs* a, void* stream);
 // variant: 0 = small tiles, 1 = large tiles, 2 = small tiles with six stages
-// (E + S <= kDeepMaxExperts), 3 = 224-token tiles. maps: the launch's tensor maps (a
+// (E + S <= kDeepMaxExperts), 3 = 224-token tiles, 4 = small tiles with four
+// weight blocks (E + S <= kQuadMaxExperts, I % 256 == 0). maps: the launch's tensor maps (a
 // single-linear launch reads w1/a1/wsf1/asf1 for L1 and w2/a2/wsf2/asf2 for L2).
 int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a, int num_ctas, void* stream);
 // One persistent launch of both GEMMs: every L1 tile, then every L2 tile; an L2
@@ -172,6 +179,7 @@ int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const mm::GemmAr
                          void* stream);
 int mm_gemm_prepare(void);  // sets the dynamic shared-memory limits and the persistent grid sizes
 int mm_gemm_cluster(int variant);  // CTAs per cluster of the variant
+int mm_gemm_blocks(int variant);   // 128-row weight blocks per tile (2 or 4)
 int mm_gemm_epilogue_warps(int variant);  // epilogue warps per CTA (arrivals per L1 tile in the fused schedule)
 int mm_gemm_token_scale_box_rows(int variant);  // token rows per TMA box of the token scale rows
 int mm_launch_timeout_probe(uint32_t* status, unsigned long long timeout_ns, void* stream);

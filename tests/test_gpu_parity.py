@@ -115,7 +115,7 @@ def test_parity_full_size_sampled(name, orc):
     G.assert_out_close(out[tokens], ref["out"], f"{name} sampled tokens")
 
 
-@pytest.mark.parametrize("name", ["decode", "prefill_t256", "skewed_t48", "wide_shared"])
+@pytest.mark.parametrize("name", ["decode", "prefill_t256", "skewed_t48", "wide_shared", "fp8w_small"])
 def test_fused_schedule_equals_split_bit_for_bit(name):
     """One persistent launch of both GEMMs computes the same tiles as one launch
     per linear: outputs and intermediates are identical."""
@@ -148,10 +148,11 @@ def test_parity_with_the_other_tile_width(name, tiles, orc):
         G.assert_out_close(out, ref["out"])
 
 
-@pytest.mark.parametrize("name", ["wide_shared", "prefill_t256"])
+@pytest.mark.parametrize("name", ["wide_shared", "prefill_t256", "fp8w_wide", "fp8w_small"])
 def test_tile_widths_agree_bit_for_bit(name):
     """Every token-tile width runs each output element's K loop in the same
-    order: the outputs and intermediates of the three widths are identical."""
+    order: the outputs and intermediates of the three widths are identical
+    (with E4M3 weights the 16-token tiles hold four weight blocks)."""
     w = SMALL_CASES[name]
     runs = [G.GpuRun(w, device_weights=True, tiles=t) for t in (16, 112, 224)]
     outs = [out_bits(r.run()) for r in runs]
