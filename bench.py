@@ -44,10 +44,10 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 # for the kernel named (fused "gemm" or "l1_gemm").
 NCU_TRAFFIC = {
     # decode (fused GEMM): E=64 capture (42 experts touched) scaled to the 61 experts one launch touches
-    "decode": {"src": "96d4a1c2f1ef7675", "kernel": "gemm", "bytes": 1442342839},
+    "decode": {"src": "289b20f263387efc", "kernel": "gemm", "bytes": 1442267733},
     # prefill (L1 GEMM of the split schedule, 224-token tiles): T=2048/E=32 capture (16384 rows)
     # scaled x8 to 131072 rows
-    "prefill": {"src": "96d4a1c2f1ef7675", "kernel": "l1_gemm", "bytes": 5359276032},
+    "prefill": {"src": "289b20f263387efc", "kernel": "l1_gemm", "bytes": 5358245888},
 }
 
 
