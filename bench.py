@@ -40,20 +40,24 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
-# capture, keyed by workload, valid only while mm_gemm.cu hashes to `src` and
-# for the kernel named (fused "gemm" or "l1_gemm").
+# capture, keyed by workload, valid only while the GEMM sources hash to `src`
+# (gemm_source_hash) and for the kernel named (fused "gemm" or "l1_gemm").
 NCU_TRAFFIC = {
     # decode (fused GEMM): E=64 capture (42 experts touched) scaled to the 61 experts one launch touches
-    "decode": {"src": "289b20f263387efc", "kernel": "gemm", "bytes": 1442267733},
-    # prefill (L1 GEMM of the split schedule, 224-token tiles): T=2048/E=32 capture (16384 rows)
-    # scaled x8 to 131072 rows
-    "prefill": {"src": "289b20f263387efc", "kernel": "l1_gemm", "bytes": 5358245888},
+    "decode": {"src": "ab1551256eaf10f5", "kernel": "gemm", "bytes": 1442267733},
+    # prefill (L1 GEMM of the split schedule, 224-token tiles, one CTA per tile): T=2048/E=32
+    # capture (16384 rows) scaled x8 to 131072 rows
+    "prefill": {"src": "ab1551256eaf10f5", "kernel": "l1_gemm", "bytes": 5245456384},
 }
 
 
 def gemm_source_hash() -> str:
-    with open(os.path.join(ROOT, "moe_expert_layer_scan_gb300", "csrc", "mm_gemm.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 prefix of the GEMM kernel's sources (kernel, constants, PTX helpers)."""
+    h = hashlib.sha256()
+    for name in ("mm_gemm.cu", "mm_internal.h", "mm_ptx.cuh"):
+        with open(os.path.join(ROOT, "moe_expert_layer_scan_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_peaks():

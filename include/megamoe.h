@@ -119,9 +119,9 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
 /* Token-tile width of the grouped GEMMs ("tuned expert-load buckets").
  *   MM_TILES_16: 16-token tiles pairing two 128-row weight blocks, one MMA
  *     stream per block, no cluster (weight-stream bound calls);
- *   MM_TILES_112: 112-token tiles in 2-CTA clusters sharing the token tile by
- *     multicast, eight epilogue warps, two TMEM accumulator buffers so that a
- *     tile's epilogue overlaps the next tile's MMAs;
+ *   MM_TILES_112: 112-token tiles, eight epilogue warps, two TMEM
+ *     accumulator buffers so that a tile's epilogue overlaps the next tile's
+ *     MMAs;
  *   MM_TILES_224: 224-token tiles, otherwise as MM_TILES_112 but with one
  *     accumulator buffer (two 224-column accumulators fill TMEM) and three
  *     pipeline stages: one MMA per K step and weight block does twice the

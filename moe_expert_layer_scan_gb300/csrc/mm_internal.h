@@ -30,10 +30,13 @@ constexpr int kBnLarge = 112;
 // same work); their two 224-column accumulators fill TMEM, so there is one
 // accumulator buffer. For the compute-bound calls with many rows per expert.
 constexpr int kBnWide = 224;
-// Large tiles run as clusters of kClusterLarge CTAs: the CTAs take adjacent
-// weight tiles of the same (expert, token tile) and each multicasts its share
-// of the token tile to all of them.
-constexpr int kClusterLarge = 2;
+// CTAs per cluster of the 112- and 224-token tiles. With 2, the CTAs of a
+// cluster take adjacent weight tiles of the same (expert, token tile) and each
+// multicasts its share of the token tile to both, halving the token tile's L2
+// reads; a stage is then released only when both CTAs are done with it, and
+// that lock-step measured 0.7-1% slower than single CTAs (mid, skewed,
+// prefill), so the kernels run without clusters.
+constexpr int kClusterLarge = 1;
 // 16-token tiles run six pipeline stages (instead of five) when the call has
 // at most this many experts (E + S): the smaller tile tables make room.
 constexpr int kDeepMaxExperts = 300;
