@@ -4,28 +4,33 @@
 //
 //   L1 ("MegaMoE research report" sec. 4.1, Linear1 phase):
 //     acc[n, r] = sum_k W1[e, n, k] * x[r, k] for the gate rows n and the
-//     matching up rows I + n of one 128-row block, then the fused epilogue
-//     y = silu(clamp(gate)) * clamp(up) * w_r, per (row, 32 columns) amax ->
-//     UE8M0 scale (smallest power of two >= amax/448) -> E4M3
+//     matching up rows I + n of the tile's 128-row feature blocks, then the
+//     fused epilogue y = silu(clamp(gate)) * clamp(up) * w_r, per (row, 32
+//     columns) amax -> UE8M0 scale (smallest power of two >= amax/448) -> E4M3
 //     ("MEGAMOE_SM90_DESIGN" sec. 10.1, steps 2-5; UE8M0 per the SM100 kernel).
 //   L2 (Linear2 phase; sec. 11.1): acc[h, r] = sum_i W2[e, h, i] * q[r, i]
-//     for two consecutive 128-row blocks of W2, written as BF16 into the
-//     per-slot row r.
+//     for the tile's consecutive 128-row blocks of W2, written as BF16 into
+//     the per-slot row r.
 //
 // Orientation: the weights are the MMA's M=128 operand (E2M1, read by TMA as
 // 16 x 4-bit groups padded to 16 bytes in SMEM; or E4M3 weights, one byte per
 // element, the same 128-byte SMEM rows) and the expert's token rows are
 // the N operand (E4M3), N = the tile's rows rounded up to 16. One CTA per SM
-// walks a flat list of (expert, weight block, token tile) tiles.
+// walks a flat list of (expert, weight blocks, token tile) tiles; an expert's
+// rows are split into equal token tiles of at most BN (16, 112 or 224) rows.
 //
-// Warp roles (384 threads): warp 0 = TMA producer; warps 1 and 2 = the MMA
-// issuers of the tile's two weight blocks (one thread each; warp 2 also
-// allocates TMEM); warp 3 = scale-factor producer; warps 4-11 = epilogue (warp
-// w reads TMEM lanes 32*(w%4)..+31, i.e. 32 consecutive weight rows; the two
-// warps of a quadrant take alternate 16-column chunks of the token tile).
+// Warp roles: warp 0 = TMA producer; one MMA-issuing warp per weight block of
+// a tile (NA = 2: warps 1 and 2; NA = 4 adds warps 4 + EPI and 5 + EPI), one
+// thread each, since one warp issues only about one block-scaled MMA per 125
+// cycles (warp 2 also allocates TMEM); warp 3 = scale rows into the
+// tcgen05.cp layout and their copies into TMEM; warps 4 .. 4 + EPI - 1 =
+// epilogue (warp w reads TMEM lanes 32*(w%4)..+31, i.e. 32 consecutive weight
+// rows; with eight of them the two warps of a quadrant take alternate column
+// chunks of the token tile).
 // Pipelines: STAGES shared-memory stages (full/empty mbarriers) and two TMEM
 // accumulator buffers (tmem_full/tmem_empty) so the epilogue of one tile
-// overlaps the main loop of the next. Every wait is bounded.
+// overlaps the main loop of the next; the 224-token tiles fill TMEM with one
+// buffer. Every wait is bounded.
 //
 // Modes: one launch per linear (L1, L2), or both in one persistent launch
 // (fused, the arrival-mask scheme of the research report's Linear1 -> Linear2
