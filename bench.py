@@ -44,10 +44,10 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 # (gemm_source_hash) and for the kernel named (fused "gemm" or "l1_gemm").
 NCU_TRAFFIC = {
     # decode (fused GEMM): E=64 capture (42 experts touched) scaled to the 61 experts one launch touches
-    "decode": {"src": "fa9bd50c1ded483e", "kernel": "gemm", "bytes": 1442267733},
+    "decode": {"src": "088ba0c1e54361e5", "kernel": "gemm", "bytes": 1442267733},
     # prefill (L1 GEMM of the split schedule, 224-token tiles, one CTA per tile): T=2048/E=32
     # capture (16384 rows) scaled x8 to 131072 rows
-    "prefill": {"src": "fa9bd50c1ded483e", "kernel": "l1_gemm", "bytes": 5245456384},
+    "prefill": {"src": "088ba0c1e54361e5", "kernel": "l1_gemm", "bytes": 5257148416},
 }
 
 

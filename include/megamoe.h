@@ -123,8 +123,8 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
  *     accumulator buffers so that a tile's epilogue overlaps the next tile's
  *     MMAs;
  *   MM_TILES_224: 224-token tiles, otherwise as MM_TILES_112 but with one
- *     accumulator buffer (two 224-column accumulators fill TMEM) and three
- *     pipeline stages: one MMA per K step and weight block does twice the
+ *     accumulator buffer (two 224-column accumulators fill TMEM), twelve
+ *     epilogue warps and three pipeline stages: one MMA per K step and weight block does twice the
  *     work of a 112-token MMA for one instruction issue (compute-bound calls
  *     with many rows per expert);
  *   MM_TILES_AUTO (the default): MM_TILES_16 while the call routes at most

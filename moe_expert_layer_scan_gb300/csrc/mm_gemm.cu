@@ -25,8 +25,8 @@
 // cycles (warp 2 also allocates TMEM); warp 3 = scale rows into the
 // tcgen05.cp layout and their copies into TMEM; warps 4 .. 4 + EPI - 1 =
 // epilogue (warp w reads TMEM lanes 32*(w%4)..+31, i.e. 32 consecutive weight
-// rows; with eight of them the two warps of a quadrant take alternate column
-// chunks of the token tile).
+// rows; with eight or twelve of them the warps of a quadrant take turns over
+// the column chunks of the token tile).
 // Pipelines: STAGES shared-memory stages (full/empty mbarriers) and two TMEM
 // accumulator buffers (tmem_full/tmem_empty) so the epilogue of one tile
 // overlaps the main loop of the next; the 224-token tiles fill TMEM with one
@@ -49,15 +49,18 @@
 
 namespace mm {
 
-// Epilogue warps: two per TMEM lane quadrant for the large tiles (their L1
-// epilogue is as long as the main loop), one for the 16-column decode tiles.
+// Epilogue warps: one per TMEM lane quadrant for the 16-column decode tiles,
+// two for the 112-token tiles (their L1 epilogue is as long as the main
+// loop), three for the 224-token tiles, whose epilogue runs between tiles
+// (measured against two: prefill L2 GEMM 1.69 -> 1.61 ms; four were slower,
+// at 96 registers a thread).
 // One MMA-issuing warp per weight block of a tile (NA of them): warp 0 is the
 // producer, warps 1 and 2 issue for blocks 0 and 1 (warp 2 also allocates
 // TMEM), warp 3 handles the scales, warps 4 .. 4 + EPI - 1 are the epilogue
 // and warps 4 + EPI .. issue for blocks 2 .. NA - 1.
 template <int BN, int NA>
 struct Warps {
-  static constexpr int EPI = BN > 16 ? 8 : 4;
+  static constexpr int EPI = BN > 112 ? 12 : BN > 16 ? 8 : 4;
   static constexpr int THREADS = 32 * (2 + NA + EPI);
 };
 
