@@ -130,7 +130,10 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
  *   MM_TILES_AUTO (the default): MM_TILES_16 while the call routes at most
  *     MM_TILES16_MAX_ROWS_PER_EXPERT rows per expert on average
  *     (T*(topk+S) <= 12*(E+S)), MM_TILES_224 from
- *     MM_TILES224_MIN_ROWS_PER_EXPERT rows per expert, MM_TILES_112 between:
+ *     MM_TILES224_MIN_ROWS_PER_EXPERT rows per expert, and above
+ *     MM_TILES224_MIN_ROWS_PER_EXPERT_FUSED when the call runs fused (there an
+ *     expert's 113-128 rows take one 224-token tile instead of two 112-token
+ *     tiles), MM_TILES_112 between:
  *     the crossovers measured on GB300 at H = 7168, I = 2048, 256 experts,
  *     top-8 and at H = 4096, I = 1536, 128 experts, top-8
  *     (moe_expert_layer_scan_gb300/tune_tiles.py).
@@ -142,6 +145,7 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
 #define MM_TILES_224 224
 #define MM_TILES16_MAX_ROWS_PER_EXPERT 12
 #define MM_TILES224_MIN_ROWS_PER_EXPERT 192
+#define MM_TILES224_MIN_ROWS_PER_EXPERT_FUSED 112
 MM_API mm_status_t mm_set_tile_policy(mm_handle_t h, int policy);
 
 /* The token-tile width (16, 112 or 224) a call of T tokens runs with under the

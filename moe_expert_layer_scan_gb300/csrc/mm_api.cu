@@ -116,6 +116,13 @@ bool quad_disabled() {
   return off;
 }
 
+// Whether a call of T tokens runs both GEMMs in one launch.
+bool use_fused(const mm_handle* h, int T) {
+  if (h->schedule != MM_SCHEDULE_AUTO) return h->schedule == MM_SCHEDULE_FUSED;
+  const long long rows = (long long)T * (h->k + h->S);
+  return rows <= (long long)MM_FUSED_MAX_ROWS_PER_EXPERT * (h->E + h->S);
+}
+
 // Kernel variant of a call: 0 = 16-token tiles, 2 = 16-token tiles with six
 // stages (at most kDeepMaxExperts experts), 4 = 16-token tiles with four weight
 // blocks (E4M3 weights, at most kQuadMaxExperts experts, I a multiple of 256:
@@ -127,7 +134,8 @@ int variant_for(const mm_handle* h, int T) {
   if (width == MM_TILES_AUTO)
     width = rows <= MM_TILES16_MAX_ROWS_PER_EXPERT * ep    ? MM_TILES_16
             : rows >= MM_TILES224_MIN_ROWS_PER_EXPERT * ep ? MM_TILES_224
-                                                            : MM_TILES_112;
+            : rows > MM_TILES224_MIN_ROWS_PER_EXPERT_FUSED * ep && use_fused(h, T) ? MM_TILES_224
+                                                                                   : MM_TILES_112;
   if (width == MM_TILES_112) return 1;
   if (width == MM_TILES_224) return 3;
   if (h->w_fmt == MM_WEIGHTS_MXFP8 && h->E + h->S <= kQuadMaxExperts && h->I % 256 == 0 && !quad_disabled())
@@ -232,15 +240,6 @@ mm_status_t mm_set_expert_stats(mm_handle_t h, int32_t* cumulative_counts) {
   h->expert_stats = cumulative_counts;
   return MM_OK;
 }
-
-namespace {
-// Whether a call of T tokens runs both GEMMs in one launch.
-bool use_fused(const mm_handle* h, int T) {
-  if (h->schedule != MM_SCHEDULE_AUTO) return h->schedule == MM_SCHEDULE_FUSED;
-  const long long rows = (long long)T * (h->k + h->S);
-  return rows <= (long long)MM_FUSED_MAX_ROWS_PER_EXPERT * (h->E + h->S);
-}
-}  // namespace
 
 mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes) {
   if (!h || !bytes || T < 0) return MM_ERR_INVALID_ARG;

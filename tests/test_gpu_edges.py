@@ -179,17 +179,25 @@ def test_tile_policy_validation():
 
 def test_token_tile_width_policy():
     """AUTO: 16-token tiles up to 12 routed rows per expert on average, 224 from
-    192, 112 between; a fixed policy is reported as set."""
+    192 (or above 112 when the call runs fused), 112 between; a fixed policy
+    is reported as set."""
     import moe_expert_layer_scan_gb300 as mm
     moe = mm.MegaMoE(256, 7168, 2048, 8, 0)
     assert mm.mm_token_tile_width(moe.h, 8) == 16          # decode: 0.25 rows per expert
     assert mm.mm_token_tile_width(moe.h, 384) == 16        # 12 rows per expert
     assert mm.mm_token_tile_width(moe.h, 385) == 112
+    assert mm.mm_token_tile_width(moe.h, 3584) == 112      # 112 rows per expert
+    assert mm.mm_token_tile_width(moe.h, 3585) == 224      # fused, above 112
+    assert mm.mm_token_tile_width(moe.h, 4096) == 224      # 128: still fused
+    assert mm.mm_token_tile_width(moe.h, 4097) == 112      # split from here
     assert mm.mm_token_tile_width(moe.h, 6143) == 112      # just under 192 rows per expert
     assert mm.mm_token_tile_width(moe.h, 6144) == 224
     assert mm.mm_token_tile_width(moe.h, 16384) == 224     # prefill: 512 rows per expert
     skewed = mm.MegaMoE(256, 7168, 2048, 8, 1)
     assert mm.mm_token_tile_width(skewed.h, 4096) == 112   # 143 rows per expert
+    mm.mm_set_schedule(moe.h, "split")
+    assert mm.mm_token_tile_width(moe.h, 4096) == 112      # split below 192 rows per expert
+    mm.mm_set_schedule(moe.h, "auto")
     mm.mm_set_tile_policy(moe.h, mm.MM_TILES_112)
     assert mm.mm_token_tile_width(moe.h, 16384) == 112
     mm.mm_set_tile_policy(moe.h, mm.MM_TILES_16)
