@@ -48,7 +48,7 @@ def assert_l2a_close(q_gpu, sf_gpu, q_ref, sf_ref, what="L2 activations"):
     assert sdiff <= 2e-3, f"{what}: {sdiff:.3%} of UE8M0 scales differ"
 
 
-class GpuRun:
+class DeviceRun:
     """Owns a handle, device inputs and a workspace for one workload."""
 
     def __init__(self, w: workloads.Workload, inputs: dict | None = None, fast_math=False, device_weights=False,

@@ -28,7 +28,7 @@ def ref_out(orc, w, h):
 def test_zero_tokens():
     import torch
     w = Workload("t0", T=0, H=256, I=128, E=4, k=2, seed=201)
-    run = G.GpuRun(w)
+    run = G.DeviceRun(w)
     out = run.run()
     assert out.shape == (0, 256)
     assert run.status() == 0
@@ -39,7 +39,7 @@ def test_zero_tokens():
 def test_single_and_boundary_token_counts(orc, T):
     w = Workload(f"t{T}", T=T, H=512, I=256, E=8, k=2, S=1, seed=202)
     h = workloads.host_inputs(w)
-    run = G.GpuRun(w, inputs=h)
+    run = G.DeviceRun(w, inputs=h)
     G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
 
 
@@ -53,7 +53,7 @@ def test_disabled_and_out_of_range_slots(orc):
     h["topk_idx"] = idx
     ref = ref_out(orc, w, h)
     assert ref["bad"] == 2
-    run = G.GpuRun(w, inputs=h)
+    run = G.DeviceRun(w, inputs=h)
     out = bits(run.run())
     assert run.status() & 0x1
     G.assert_out_close(out, ref["out"])
@@ -63,7 +63,7 @@ def test_all_slots_disabled_gives_zero():
     w = Workload("none", T=5, H=256, I=128, E=3, k=2, seed=204)
     h = workloads.host_inputs(w)
     h["topk_idx"] = np.full_like(h["topk_idx"], -1)
-    run = G.GpuRun(w, inputs=h)
+    run = G.DeviceRun(w, inputs=h)
     out = bits(run.run())
     assert (out == 0).all() and run.status() == 0
 
@@ -73,7 +73,7 @@ def test_duplicate_experts_small_variant(orc):
     w = Workload("dup", T=16, H=512, I=256, E=4, k=4, seed=205)
     h = workloads.host_inputs(w)
     h["topk_idx"] = np.full_like(h["topk_idx"], 2)
-    run = G.GpuRun(w, inputs=h, tiles=16)
+    run = G.DeviceRun(w, inputs=h, tiles=16)
     G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
 
 
@@ -84,7 +84,7 @@ def test_hot_expert_many_tiles(orc, tiles):
     w = Workload("hot", T=300, H=256, I=256, E=4, k=1, seed=206)
     h = workloads.host_inputs(w)
     h["topk_idx"] = np.zeros_like(h["topk_idx"])
-    run = G.GpuRun(w, inputs=h, tiles=tiles)
+    run = G.DeviceRun(w, inputs=h, tiles=tiles)
     G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
 
 
@@ -92,21 +92,21 @@ def test_workspace_reuse_and_determinism():
     w = Workload("reuse", T=40, H=512, I=256, E=6, k=2, S=1, seed=207)
     a = workloads.host_inputs(w)
     b = workloads.host_inputs(w.replace(seed=208))
-    run = G.GpuRun(w, inputs=a)
+    run = G.DeviceRun(w, inputs=a)
     first = bits(run.run())
     import torch
     bd = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in b.items()}
     other = bits(run.run(**bd))
     again = bits(run.run())
     assert np.array_equal(first, again)          # no pollution from the previous call, deterministic
-    fresh = G.GpuRun(w, inputs=b)
+    fresh = G.DeviceRun(w, inputs=b)
     assert np.array_equal(other, bits(fresh.run()))
 
 
 def test_fast_math_silu(orc):
     w = Workload("fast", T=24, H=512, I=256, E=4, k=2, seed=209)
     h = workloads.host_inputs(w)
-    run = G.GpuRun(w, inputs=h, fast_math=True)
+    run = G.DeviceRun(w, inputs=h, fast_math=True)
     G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
 
 
@@ -121,7 +121,7 @@ def test_bounded_wait_reports_timeout_and_gpu_stays_usable(orc):
     assert status & 0x2
     w = Workload("after", T=8, H=256, I=128, E=4, k=2, seed=210)
     h = workloads.host_inputs(w)
-    run = G.GpuRun(w, inputs=h)
+    run = G.DeviceRun(w, inputs=h)
     G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
 
 
@@ -154,7 +154,7 @@ def test_weight_format_validation_and_switch(orc):
     import moe_expert_layer_scan_gb300 as mm
     w4 = Workload("fmt4", T=6, H=256, I=128, E=4, k=2, seed=305)
     w8 = w4.replace(name="fmt8", w_fmt=1)
-    run = G.GpuRun(w4)
+    run = G.DeviceRun(w4)
     out4 = bits(run.run())
     G.assert_out_close(out4, ref_out(orc, w4, workloads.host_inputs(w4))["out"])
     h8 = workloads.host_inputs(w8)

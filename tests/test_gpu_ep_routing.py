@@ -23,7 +23,7 @@ def _grab(run, ptr, n, dtype):
                                         ("skewed_small", 16)])
 def test_rank_offsets_follow_expert_blocks(orc, name, ranks):
     w = CONFIGS.get(name) or Workload("skewed_small", T=48, H=1024, I=512, E=16, k=8, S=1, zipf=1.2, seed=103)
-    run = G.GpuRun(w, device_weights=True)
+    run = G.DeviceRun(w, device_weights=True)
     run.mm.mm_set_ep_ranks(run.moe.h, ranks)
     run.run()
     v = run.moe.views(w.T)
@@ -45,7 +45,7 @@ def test_rank_offsets_follow_expert_blocks(orc, name, ranks):
 def test_expert_stats_accumulate_over_calls(orc):
     import torch
     w = Workload("stats", T=40, H=512, I=256, E=8, k=2, S=1, seed=301)
-    run = G.GpuRun(w)
+    run = G.DeviceRun(w)
     stats = torch.full((w.Ep,), 5, dtype=torch.int32, device="cuda")
     run.mm.mm_set_expert_stats(run.moe.h, stats.data_ptr())
     for _ in range(3):
@@ -67,7 +67,7 @@ def test_expert_stats_skip_disabled_slots(orc):
     idx = h["topk_idx"].copy()
     idx[::3, 1] = -1
     h["topk_idx"] = idx
-    run = G.GpuRun(w, inputs=h)
+    run = G.DeviceRun(w, inputs=h)
     stats = torch.zeros(w.Ep, dtype=torch.int32, device="cuda")
     run.mm.mm_set_expert_stats(run.moe.h, stats.data_ptr())
     run.run()

@@ -30,7 +30,7 @@ def test_most_experts_and_slots(orc):
     """E + S = 1024 experts (4 shared) and topk + S = 16 slots per token."""
     w = Workload("max_experts", T=24, H=256, I=128, E=1020, k=12, S=4, seed=401)
     h = workloads.host_inputs(w)
-    run = G.GpuRun(w, inputs=h)
+    run = G.DeviceRun(w, inputs=h)
     out = bits(run.run())
     ref = oracle_out(orc, w, h)
     inter = run.intermediates(w.T)
@@ -45,7 +45,7 @@ def test_routing_boundary_single_and_multi_cta(orc, T):
     routing: both bit-exact, both outputs within tolerance."""
     w = Workload(f"route_{T}", T=T, H=256, I=128, E=64, k=8, seed=402)
     h = workloads.host_inputs(w)
-    run = G.GpuRun(w, inputs=h)
+    run = G.DeviceRun(w, inputs=h)
     out = bits(run.run())
     ref = oracle_out(orc, w, h)
     inter = run.intermediates(w.T)
@@ -62,7 +62,7 @@ def test_routing_boundary_single_and_multi_cta(orc, T):
 def test_largest_hidden_and_intermediate(orc, H, I):
     w = Workload(f"big_{H}_{I}", T=5, H=H, I=I, E=2, k=1, S=1, seed=403)
     h = workloads.host_inputs(w)
-    run = G.GpuRun(w, inputs=h)
+    run = G.DeviceRun(w, inputs=h)
     G.assert_out_close(bits(run.run()), oracle_out(orc, w, h)["out"])
 
 
@@ -75,7 +75,7 @@ def test_cuda_graph_capture_and_replay(orc, T):
     w = Workload(f"graph_{T}", T=T, H=1024, I=512, E=16, k=4, seed=404)
     a = workloads.host_inputs(w)
     b = workloads.host_inputs(w.replace(seed=405))
-    run = G.GpuRun(w, inputs=a)
+    run = G.DeviceRun(w, inputs=a)
     eager_a = bits(run.run())
     static = run.d
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device="cuda")

@@ -68,7 +68,7 @@ def test_parity_small(name, schedule, orc):
     w = SMALL_CASES[name]
     h = workloads.host_inputs(w)
     ref = oracle_run(orc, w, h)
-    run = G.GpuRun(w, inputs=h, schedule=schedule)
+    run = G.DeviceRun(w, inputs=h, schedule=schedule)
     out = out_bits(run.run())
     inter = run.intermediates(w.T)
     assert inter["status"] == 0
@@ -99,7 +99,7 @@ def test_parity_full_size_sampled(name, orc):
     in HBM); routing compared in full, outputs on sampled tokens that the oracle
     recomputes from host-generated inputs."""
     w = CONFIGS[name]
-    run = G.GpuRun(w, device_weights=True)
+    run = G.DeviceRun(w, device_weights=True)
     out = out_bits(run.run())
     inter = run.intermediates(w.T)
     assert inter["status"] == 0
@@ -120,8 +120,8 @@ def test_fused_schedule_equals_split_bit_for_bit(name):
     """One persistent launch of both GEMMs computes the same tiles as one launch
     per linear: outputs and intermediates are identical."""
     w = CONFIGS.get(name) or SMALL_CASES[name]
-    a = G.GpuRun(w, device_weights=True, schedule="fused")
-    b = G.GpuRun(w, device_weights=True, schedule="split")
+    a = G.DeviceRun(w, device_weights=True, schedule="fused")
+    b = G.DeviceRun(w, device_weights=True, schedule="split")
     oa, ob = out_bits(a.run()), out_bits(b.run())
     ia, ib = a.intermediates(w.T), b.intermediates(w.T)
     assert ia["status"] == 0 and ib["status"] == 0
@@ -141,7 +141,7 @@ def test_parity_with_the_other_tile_width(name, tiles, orc):
     h = workloads.host_inputs(w)
     ref = oracle_run(orc, w, h)
     for schedule in ("fused", "split"):
-        run = G.GpuRun(w, inputs=h, schedule=schedule, tiles=tiles)
+        run = G.DeviceRun(w, inputs=h, schedule=schedule, tiles=tiles)
         out = out_bits(run.run())
         inter = run.intermediates(w.T)
         assert inter["status"] == 0
@@ -154,7 +154,7 @@ def test_tile_widths_agree_bit_for_bit(name):
     order: the outputs and intermediates of the three widths are identical
     (with E4M3 weights the 16-token tiles hold four weight blocks)."""
     w = SMALL_CASES[name]
-    runs = [G.GpuRun(w, device_weights=True, tiles=t) for t in (16, 112, 224)]
+    runs = [G.DeviceRun(w, device_weights=True, tiles=t) for t in (16, 112, 224)]
     outs = [out_bits(r.run()) for r in runs]
     inters = [r.intermediates(w.T) for r in runs]
     for o, i in zip(outs[1:], inters[1:]):

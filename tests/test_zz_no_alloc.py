@@ -31,7 +31,7 @@ def test_noalloc_matches_mm_run_on_two_calls_in_a_row():
     import moe_expert_layer_scan_gb300 as mm
 
     w = Workload("noalloc", T=8, H=7168, I=2048, E=16, k=8, seed=301)
-    run = G.GpuRun(w)
+    run = G.DeviceRun(w)
     inputs = [run.d, {k: torch.from_numpy(np.ascontiguousarray(v)).cuda()
                       for k, v in workloads.host_inputs(w.replace(seed=302)).items()}]
     s = torch.cuda.current_stream().cuda_stream
