@@ -44,10 +44,10 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 # (gemm_source_hash) and for the kernel named (fused "gemm" or "l1_gemm").
 NCU_TRAFFIC = {
     # decode (fused GEMM): E=64 capture (42 experts touched) scaled to the 61 experts one launch touches
-    "decode": {"src": "088ba0c1e54361e5", "kernel": "gemm", "bytes": 1442267733},
+    "decode": {"src": "be902d7cc0cdd9f4", "kernel": "gemm", "bytes": 1441261244},
     # prefill (L1 GEMM of the split schedule, 224-token tiles, one CTA per tile): T=2048/E=32
     # capture (16384 rows) scaled x8 to 131072 rows
-    "prefill": {"src": "088ba0c1e54361e5", "kernel": "l1_gemm", "bytes": 5257148416},
+    "prefill": {"src": "be902d7cc0cdd9f4", "kernel": "l1_gemm", "bytes": 5241108480},
 }
 
 
@@ -434,7 +434,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
-    ap.add_argument("--tiles", type=int, default=-1, choices=[-1, 16, 112, 224],
+    ap.add_argument("--tiles", type=int, default=-1, choices=[-1, 16, 64, 112, 224],
                     help="token-tile width (-1: the library's choice)")
     ap.add_argument("--schedule", default="auto", choices=["auto", "fused", "split"],
                     help="GEMM schedule: one persistent launch for both linears, one per linear, or the "

@@ -119,6 +119,9 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
 /* Token-tile width of the grouped GEMMs ("tuned expert-load buckets").
  *   MM_TILES_16: 16-token tiles pairing two 128-row weight blocks, one MMA
  *     stream per block, no cluster (weight-stream bound calls);
+ *   MM_TILES_64: 64-token tiles, otherwise as MM_TILES_112 but with five
+ *     pipeline stages instead of four (more weight bytes in flight); only for
+ *     calls with E + S <= 300 experts, larger calls run MM_TILES_112;
  *   MM_TILES_112: 112-token tiles, eight epilogue warps, two TMEM
  *     accumulator buffers so that a tile's epilogue overlaps the next tile's
  *     MMAs;
@@ -133,7 +136,10 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
  *     MM_TILES224_MIN_ROWS_PER_EXPERT rows per expert, and above
  *     MM_TILES224_MIN_ROWS_PER_EXPERT_FUSED when the call runs fused (there an
  *     expert's 113-128 rows take one 224-token tile instead of two 112-token
- *     tiles), MM_TILES_112 between:
+ *     tiles), MM_TILES_64 up to MM_TILES64_MAX_ROWS_PER_EXPERT rows per expert
+ *     when the call has no shared expert (a shared expert receives every
+ *     token, far above the average, and would take many 64-token tiles),
+ *     MM_TILES_112 between:
  *     the crossovers measured on GB300 at H = 7168, I = 2048, 256 experts,
  *     top-8 and at H = 4096, I = 1536, 128 experts, top-8
  *     (moe_expert_layer_scan_gb300/tune_tiles.py).
@@ -141,14 +147,16 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
  * Other values: MM_ERR_INVALID_ARG. */
 #define MM_TILES_AUTO (-1)
 #define MM_TILES_16 16
+#define MM_TILES_64 64
 #define MM_TILES_112 112
 #define MM_TILES_224 224
 #define MM_TILES16_MAX_ROWS_PER_EXPERT 12
+#define MM_TILES64_MAX_ROWS_PER_EXPERT 48
 #define MM_TILES224_MIN_ROWS_PER_EXPERT 192
 #define MM_TILES224_MIN_ROWS_PER_EXPERT_FUSED 112
 MM_API mm_status_t mm_set_tile_policy(mm_handle_t h, int policy);
 
-/* The token-tile width (16, 112 or 224) a call of T tokens runs with under the
+/* The token-tile width (16, 64, 112 or 224) a call of T tokens runs with under the
  * handle's current policy. Host only. */
 MM_API mm_status_t mm_token_tile_width(mm_handle_t h, int T, int* width);
 

@@ -39,7 +39,7 @@ struct mm_handle {
   int32_t* expert_stats;
   // weight format: MM_WEIGHTS_MXFP4 / MM_WEIGHTS_MXFP8
   int w_fmt;
-  // token-tile width: MM_TILES_AUTO / _16 / _112 / _224
+  // token-tile width: MM_TILES_AUTO / _16 / _64 / _112 / _224
   int tiles;
   // optional per-launch events (route, gather, L1, L2, combine, end) and the
   // stage name of each recorded interval
@@ -127,7 +127,9 @@ bool use_fused(const mm_handle* h, int T) {
 // stages (at most kDeepMaxExperts experts), 4 = 16-token tiles with four weight
 // blocks (E4M3 weights, at most kQuadMaxExperts experts, I a multiple of 256:
 // measured 97% -> 100% of the copy bandwidth at decode; with E2M1 weights it
-// was 2% slower than variant 2), 1 = 112-token tiles, 3 = 224-token tiles.
+// was 2% slower than variant 2), 5 = 64-token tiles with five stages (at most
+// kDeepMaxExperts experts; 112-token tiles otherwise), 1 = 112-token tiles,
+// 3 = 224-token tiles.
 int variant_for(const mm_handle* h, int T) {
   const long long rows = (long long)T * (h->k + h->S), ep = h->E + h->S;
   int width = h->tiles;
@@ -135,15 +137,19 @@ int variant_for(const mm_handle* h, int T) {
     width = rows <= MM_TILES16_MAX_ROWS_PER_EXPERT * ep    ? MM_TILES_16
             : rows >= MM_TILES224_MIN_ROWS_PER_EXPERT * ep ? MM_TILES_224
             : rows > MM_TILES224_MIN_ROWS_PER_EXPERT_FUSED * ep && use_fused(h, T) ? MM_TILES_224
+            : rows <= MM_TILES64_MAX_ROWS_PER_EXPERT * ep && h->S == 0              ? MM_TILES_64
                                                                                    : MM_TILES_112;
   if (width == MM_TILES_112) return 1;
   if (width == MM_TILES_224) return 3;
+  if (width == MM_TILES_64) return h->E + h->S <= kDeepMaxExperts ? 5 : 1;
   if (h->w_fmt == MM_WEIGHTS_MXFP8 && h->E + h->S <= kQuadMaxExperts && h->I % 256 == 0 && !quad_disabled())
     return 4;
   return (h->E + h->S <= kDeepMaxExperts && !deep_disabled()) ? 2 : 0;
 }
 
-int tile_width(int variant) { return variant == 1 ? kBnLarge : variant == 3 ? kBnWide : kBnSmall; }
+int tile_width(int variant) {
+  return variant == 1 ? kBnLarge : variant == 3 ? kBnWide : variant == 5 ? kBnMid : kBnSmall;
+}
 
 }  // namespace
 
@@ -214,7 +220,8 @@ mm_status_t mm_set_schedule(mm_handle_t h, int schedule) {
 }
 
 mm_status_t mm_set_tile_policy(mm_handle_t h, int policy) {
-  if (!h || (policy != MM_TILES_AUTO && policy != MM_TILES_16 && policy != MM_TILES_112 && policy != MM_TILES_224))
+  if (!h || (policy != MM_TILES_AUTO && policy != MM_TILES_16 && policy != MM_TILES_64 && policy != MM_TILES_112 &&
+             policy != MM_TILES_224))
     return MM_ERR_INVALID_ARG;
   h->tiles = policy;
   return MM_OK;

@@ -17,7 +17,7 @@
 // element, the same 128-byte SMEM rows) and the expert's token rows are
 // the N operand (E4M3), N = the tile's rows rounded up to 16. One CTA per SM
 // walks a flat list of (expert, weight blocks, token tile) tiles; an expert's
-// rows are split into equal token tiles of at most BN (16, 112 or 224) rows.
+// rows are split into equal token tiles of at most BN (16, 64, 112 or 224) rows.
 //
 // Warp roles: warp 0 = TMA producer; one MMA-issuing warp per weight block of
 // a tile (NA = 2: warps 1 and 2; NA = 4 adds warps 4 + EPI and 5 + EPI), one
@@ -50,8 +50,8 @@
 namespace mm {
 
 // Epilogue warps: one per TMEM lane quadrant for the 16-column decode tiles,
-// two for the 112-token tiles (their L1 epilogue is as long as the main
-// loop), three for the 224-token tiles, whose epilogue runs between tiles
+// two for the 64- and 112-token tiles (their L1 epilogue is as long as the
+// main loop), three for the 224-token tiles, whose epilogue runs between tiles
 // (measured against two: prefill L2 GEMM 1.69 -> 1.61 ms; four were slower,
 // at 96 registers a thread).
 // One MMA-issuing warp per weight block of a tile (NA of them): warp 0 is the
@@ -85,9 +85,10 @@ struct GemmCfg {
   static constexpr int B_OFF = A_OFF + STAGES * NA * A_BYTES;
   static constexpr int SF_OFF = B_OFF + STAGES * B_BYTES;
   static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE_BYTES;
-  // The deep 16-token configuration (six stages) keeps room for them by
-  // supporting at most kDeepMaxExperts experts and two scale groups in flight.
-  static constexpr bool DEEP = BN == 16 && STAGES > 5;
+  // The deep configurations (16-token tiles with six stages, 64-token tiles
+  // with five) keep room for them by supporting at most kDeepMaxExperts
+  // experts and two scale groups in flight.
+  static constexpr bool DEEP = (BN == kBnSmall && STAGES > 5) || (BN == kBnMid && STAGES > 4);
   // copies of the two tile tables and the row offsets ([experts + 1] each)
   static constexpr int TAB_OFF = BAR_OFF + 256;
   static constexpr int TAB_INTS = (NA > 2 ? kQuadMaxExperts : DEEP ? kDeepMaxExperts : kMaxExperts) + 1;
@@ -871,12 +872,14 @@ static int launch(const GemmMaps* maps, const GemmArgs* g1, const GemmArgs* g2, 
 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
 // five, measured as fast as six).
-constexpr int kStagesSmall = 5, kStagesSmallDeep = 6, kStagesLarge = 4, kStagesWide = 3, kStagesQuad = 3;
+constexpr int kStagesSmall = 5, kStagesSmallDeep = 6, kStagesLarge = 4, kStagesWide = 3, kStagesQuad = 3,
+              kStagesMid = 5;
 // CTAs per launch of each instantiation: [mode][variant] (variant 2: 16-token
 // tiles with six stages, for at most kDeepMaxExperts experts; variant 3:
 // 224-token tiles; variant 4: 16-token tiles with four weight blocks, for at
-// most kQuadMaxExperts experts)
-static int g_ctas[3][5];
+// most kQuadMaxExperts experts; variant 5: 64-token tiles, for at most
+// kDeepMaxExperts experts)
+static int g_ctas[3][6];
 
 }  // namespace mm
 
@@ -898,6 +901,9 @@ extern "C" int mm_gemm_prepare(void) {
   if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesQuad, 1, 4>(&g_ctas[kModeL1][4]))) return e;
   if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesQuad, 1, 4>(&g_ctas[kModeL2][4]))) return e;
   if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesQuad, 1, 4>(&g_ctas[kModeFused][4]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnMid, kStagesMid, 1>(&g_ctas[kModeL1][5]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnMid, kStagesMid, 1>(&g_ctas[kModeL2][5]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnMid, kStagesMid, 1>(&g_ctas[kModeFused][5]))) return e;
   return 0;
 }
 
@@ -909,6 +915,7 @@ extern "C" int mm_gemm_epilogue_warps(int variant) {
   return variant == 1   ? mm::Warps<mm::kBnLarge, 2>::EPI
          : variant == 3 ? mm::Warps<mm::kBnWide, 2>::EPI
          : variant == 4 ? mm::Warps<mm::kBnSmall, 4>::EPI
+         : variant == 5 ? mm::Warps<mm::kBnMid, 2>::EPI
                         : mm::Warps<mm::kBnSmall, 2>::EPI;
 }
 
@@ -916,6 +923,7 @@ extern "C" int mm_gemm_token_scale_box_rows(int variant) {
   return variant == 1   ? mm::GemmCfg<mm::kBnLarge, mm::kStagesLarge, mm::kClusterLarge>::RAW_B_ROWS
          : variant == 3 ? mm::GemmCfg<mm::kBnWide, mm::kStagesWide, mm::kClusterLarge>::RAW_B_ROWS
          : variant == 4 ? mm::GemmCfg<mm::kBnSmall, mm::kStagesQuad, 1, 4>::RAW_B_ROWS
+         : variant == 5 ? mm::GemmCfg<mm::kBnMid, mm::kStagesMid, 1>::RAW_B_ROWS
                         : mm::GemmCfg<mm::kBnSmall, mm::kStagesSmall, 1>::RAW_B_ROWS;
 }
 
@@ -931,12 +939,14 @@ extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, con
            : variant == 2 ? launch<kModeL1, kBnSmall, kStagesSmallDeep, 1>(maps, a, a, n, st)
            : variant == 3 ? launch<kModeL1, kBnWide, kStagesWide, kClusterLarge>(maps, a, a, n, st)
            : variant == 4 ? launch<kModeL1, kBnSmall, kStagesQuad, 1, 4>(maps, a, a, n, st)
+           : variant == 5 ? launch<kModeL1, kBnMid, kStagesMid, 1>(maps, a, a, n, st)
                           : launch<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
   }
   return variant == 0   ? launch<kModeL2, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
          : variant == 2 ? launch<kModeL2, kBnSmall, kStagesSmallDeep, 1>(maps, a, a, n, st)
          : variant == 3 ? launch<kModeL2, kBnWide, kStagesWide, kClusterLarge>(maps, a, a, n, st)
          : variant == 4 ? launch<kModeL2, kBnSmall, kStagesQuad, 1, 4>(maps, a, a, n, st)
+         : variant == 5 ? launch<kModeL2, kBnMid, kStagesMid, 1>(maps, a, a, n, st)
                         : launch<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
 }
 
@@ -949,5 +959,6 @@ extern "C" int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const
          : variant == 2 ? launch<kModeFused, kBnSmall, kStagesSmallDeep, 1>(maps, g1, g2, n, st)
          : variant == 3 ? launch<kModeFused, kBnWide, kStagesWide, kClusterLarge>(maps, g1, g2, n, st)
          : variant == 4 ? launch<kModeFused, kBnSmall, kStagesQuad, 1, 4>(maps, g1, g2, n, st)
+         : variant == 5 ? launch<kModeFused, kBnMid, kStagesMid, 1>(maps, g1, g2, n, st)
                         : launch<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(maps, g1, g2, n, st);
 }

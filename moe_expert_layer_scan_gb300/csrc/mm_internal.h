@@ -30,6 +30,11 @@ constexpr int kBnLarge = 112;
 // same work); their two 224-column accumulators fill TMEM, so there is one
 // accumulator buffer. For the compute-bound calls with many rows per expert.
 constexpr int kBnWide = 224;
+// 64-token tiles: the MMA shape and epilogue of the 112-token tiles with a
+// smaller token box, which leaves room for a fifth pipeline stage (more weight
+// bytes in flight) when the call has at most kDeepMaxExperts experts. For the
+// weight-bandwidth bound calls with a few dozen rows per expert.
+constexpr int kBnMid = 64;
 // CTAs per cluster of the 112- and 224-token tiles. With 2, the CTAs of a
 // cluster take adjacent weight tiles of the same (expert, token tile) and each
 // multicasts its share of the token tile to both, halving the token tile's L2
@@ -37,8 +42,9 @@ constexpr int kBnWide = 224;
 // that lock-step measured 0.7-1% slower than single CTAs (mid, skewed,
 // prefill), so the kernels run without clusters.
 constexpr int kClusterLarge = 1;
-// 16-token tiles run six pipeline stages (instead of five) when the call has
-// at most this many experts (E + S): the smaller tile tables make room.
+// 16-token tiles run six pipeline stages (instead of five), and 64-token tiles
+// exist at all (five stages), when the call has at most this many experts
+// (E + S): the smaller tile tables and fewer scale groups make room.
 constexpr int kDeepMaxExperts = 300;
 // 16-token tiles with four 128-row weight blocks per tile (two gate/up pairs in
 // L1, four W2 blocks in L2) and four MMA-issuing warps: twice the MMA issue
@@ -173,7 +179,8 @@ int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream
 int mm_launch_combine(const mm::CombineArgs* a, void* stream);
 // variant: 0 = small tiles, 1 = large tiles, 2 = small tiles with six stages
 // (E + S <= kDeepMaxExperts), 3 = 224-token tiles, 4 = small tiles with four
-// weight blocks (E + S <= kQuadMaxExperts, I % 256 == 0). maps: the launch's tensor maps (a
+// weight blocks (E + S <= kQuadMaxExperts, I % 256 == 0), 5 = 64-token tiles
+// (E + S <= kDeepMaxExperts). maps: the launch's tensor maps (a
 // single-linear launch reads w1/a1/wsf1/asf1 for L1 and w2/a2/wsf2/asf2 for L2).
 int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a, int num_ctas, void* stream);
 // One persistent launch of both GEMMs: every L1 tile, then every L2 tile; an L2

@@ -1,15 +1,17 @@
 """Measures the token-tile crossovers of the grouped GEMMs on this GPU.
 
     python -m moe_expert_layer_scan_gb300.tune_tiles [--workload prefill] [--tokens 64,128,256,384,512]
-                                                     [--widths 16,112,224]
+                                                     [--widths 16,64,112,224]
 
 For each token count, runs the whole forward with each token-tile width
 (schedule chosen by the library) on seeded synthetic inputs of the workload's
 shape (weights generated in device memory), L2 flushed between steps, and
 prints the median step time of each and the mean routed rows per expert. The
-library's automatic policy switches from 16- to 112-token tiles above
-MM_TILES16_MAX_ROWS_PER_EXPERT rows per expert and from 112- to 224-token
-tiles at MM_TILES224_MIN_ROWS_PER_EXPERT, the crossovers this measures.
+library's automatic policy switches from 16-token tiles above
+MM_TILES16_MAX_ROWS_PER_EXPERT rows per expert (to 64-token tiles up to
+MM_TILES64_MAX_ROWS_PER_EXPERT when the call has no shared expert, then
+112-token tiles) and to 224-token tiles at MM_TILES224_MIN_ROWS_PER_EXPERT,
+the crossovers this measures.
 """
 from __future__ import annotations
 

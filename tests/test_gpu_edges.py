@@ -77,10 +77,10 @@ def test_duplicate_experts_small_variant(orc):
     G.assert_out_close(bits(run.run()), ref_out(orc, w, h)["out"])
 
 
-@pytest.mark.parametrize("tiles", [-1, 224])
+@pytest.mark.parametrize("tiles", [-1, 64, 224])
 def test_hot_expert_many_tiles(orc, tiles):
     """One expert receives every token: several full token tiles plus a ragged
-    tail (112-token tiles by the automatic policy, or 224-token tiles)."""
+    tail (112-token tiles by the automatic policy, or 64- or 224-token tiles)."""
     w = Workload("hot", T=300, H=256, I=256, E=4, k=1, seed=206)
     h = workloads.host_inputs(w)
     h["topk_idx"] = np.zeros_like(h["topk_idx"])
@@ -167,25 +167,37 @@ def test_weight_format_validation_and_switch(orc):
 
 
 def test_tile_policy_validation():
-    """The three widths and the automatic policy are accepted, anything else rejected."""
+    """The four widths and the automatic policy are accepted, anything else rejected;
+    64-token tiles exist for at most 300 experts, larger calls run 112-token tiles."""
     import moe_expert_layer_scan_gb300 as mm
     moe = mm.MegaMoE(8, 512, 256, 2, 0)
-    for t in (mm.MM_TILES_16, mm.MM_TILES_112, mm.MM_TILES_224, mm.MM_TILES_AUTO):
+    for t in (mm.MM_TILES_16, mm.MM_TILES_64, mm.MM_TILES_112, mm.MM_TILES_224, mm.MM_TILES_AUTO):
         mm.mm_set_tile_policy(moe.h, t)
     for bad in (0, 32, 128, 200, 256):
         with pytest.raises(mm.MMError):
             mm.mm_set_tile_policy(moe.h, bad)
+    mm.mm_set_tile_policy(moe.h, mm.MM_TILES_64)
+    assert mm.mm_token_tile_width(moe.h, 64) == 64
+    for e, s, width in ((299, 1, 64), (300, 1, 112), (512, 0, 112)):
+        big = mm.MegaMoE(e, 512, 256, 2, s, tiles=mm.MM_TILES_64)
+        assert mm.mm_token_tile_width(big.h, 64) == width, (e, s)
 
 
 def test_token_tile_width_policy():
     """AUTO: 16-token tiles up to 12 routed rows per expert on average, 224 from
-    192 (or above 112 when the call runs fused), 112 between; a fixed policy
-    is reported as set."""
+    192 (or above 112 when the call runs fused), 64 up to 48 without a shared
+    expert, 112 between; a fixed policy is reported as set."""
     import moe_expert_layer_scan_gb300 as mm
     moe = mm.MegaMoE(256, 7168, 2048, 8, 0)
     assert mm.mm_token_tile_width(moe.h, 8) == 16          # decode: 0.25 rows per expert
     assert mm.mm_token_tile_width(moe.h, 384) == 16        # 12 rows per expert
-    assert mm.mm_token_tile_width(moe.h, 385) == 112
+    assert mm.mm_token_tile_width(moe.h, 385) == 64
+    assert mm.mm_token_tile_width(moe.h, 1536) == 64       # 48 rows per expert
+    assert mm.mm_token_tile_width(moe.h, 1537) == 112
+    with_shared = mm.MegaMoE(256, 7168, 2048, 8, 1)
+    assert mm.mm_token_tile_width(with_shared.h, 1024) == 112  # 36 rows per expert, one shared expert
+    many = mm.MegaMoE(512, 7168, 2048, 8, 0)
+    assert mm.mm_token_tile_width(many.h, 2048) == 112     # 32 rows per expert, above 300 experts
     assert mm.mm_token_tile_width(moe.h, 3584) == 112      # 112 rows per expert
     assert mm.mm_token_tile_width(moe.h, 3585) == 224      # fused, above 112
     assert mm.mm_token_tile_width(moe.h, 4096) == 224      # 128: still fused

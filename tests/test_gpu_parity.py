@@ -16,8 +16,9 @@ from workloads import CONFIGS, Workload
 pytestmark = pytest.mark.gpu
 
 # Several tiles and ragged tails at sizes the oracle finishes in seconds,
-# covering the three token-tile widths (16-token tiles up to 12 routed rows
-# per expert on average, 224-token tiles from 192, 112-token tiles between).
+# covering the four token-tile widths (16-token tiles up to 12 routed rows
+# per expert on average, 64-token tiles up to 48 without a shared expert,
+# 224-token tiles from 192, 112-token tiles between).
 SMALL_CASES = {
     "tiny": CONFIGS["tiny"],
     "decode_e16": Workload("decode_e16", T=8, H=7168, I=2048, E=16, k=8, seed=101),
@@ -133,7 +134,10 @@ def test_fused_schedule_equals_split_bit_for_bit(name):
 @pytest.mark.parametrize("name,tiles", [("decode_e16", 112), ("small_tiles", 112), ("mid_t32", 16),
                                         ("skewed_t48", 16), ("fp8w_small", 112), ("decode_e16", 224),
                                         ("prefill_t256", 224), ("ragged", 224), ("fp8w_large", 224),
-                                        ("wide_t480", 112), ("wide_t480", 16)])
+                                        ("wide_t480", 112), ("wide_t480", 16), ("mid_t32", 64),
+                                        ("prefill_t256", 64), ("wide_shared", 64), ("ragged", 64),
+                                        ("skewed_t48", 64), ("odd_h_large", 64), ("fp8w_large", 64),
+                                        ("mid_t32", 112), ("clamp_active", 112)])
 def test_parity_with_the_other_tile_width(name, tiles, orc):
     """Each token-tile width is correct on the token counts the automatic policy
     gives to the other one."""
@@ -151,10 +155,10 @@ def test_parity_with_the_other_tile_width(name, tiles, orc):
 @pytest.mark.parametrize("name", ["wide_shared", "prefill_t256", "fp8w_wide", "fp8w_small"])
 def test_tile_widths_agree_bit_for_bit(name):
     """Every token-tile width runs each output element's K loop in the same
-    order: the outputs and intermediates of the three widths are identical
+    order: the outputs and intermediates of the four widths are identical
     (with E4M3 weights the 16-token tiles hold four weight blocks)."""
     w = SMALL_CASES[name]
-    runs = [G.DeviceRun(w, device_weights=True, tiles=t) for t in (16, 112, 224)]
+    runs = [G.DeviceRun(w, device_weights=True, tiles=t) for t in (16, 64, 112, 224)]
     outs = [out_bits(r.run()) for r in runs]
     inters = [r.intermediates(w.T) for r in runs]
     for o, i in zip(outs[1:], inters[1:]):
