@@ -38,6 +38,18 @@ def test_binding_mirrors_the_c_names():
         assert hasattr(mm, name), f"binding lacks {name}"
 
 
+def test_binding_constants_match_the_header():
+    """Every policy, format and device-status value the header defines has the
+    same name and value in the binding."""
+    hdr = open(os.path.join(ROOT, "include", "megamoe.h")).read()
+    defs = {n: int(v.strip("()").rstrip("u"), 0)
+            for n, v in re.findall(r"#define\s+(MM_\w+)\s+(\(?-?(?:0x[0-9a-fA-F]+|\d+)u?\)?)", hdr)}
+    wanted = [n for n in defs if re.match(r"MM_(TILES|SCHEDULE|WEIGHTS|DEV)_", n)]
+    assert {"MM_TILES_AUTO", "MM_TILES_16", "MM_TILES_64", "MM_TILES_112", "MM_TILES_224"} <= set(wanted)
+    for n in wanted:
+        assert getattr(mm, n) == defs[n], n
+
+
 def test_status_strings(lib):
     assert mm.mm_status_string(0) == "ok"
     assert mm.mm_status_string(3) == "workspace too small"
