@@ -94,13 +94,25 @@ def _gen_weights(w):
     return gen
 
 
-@pytest.mark.parametrize("name", ["decode", "mid", "skewed", "prefill", "decode_fp8w", "prefill_fp8w"])
+# Full-size layer shapes at token counts where the automatic policy takes the
+# 64-token tiles (32 routed rows per expert on average), with that width.
+FULL_EXTRA = {
+    "mid_t512": (CONFIGS["mid"].replace(T=512, name="mid_t512"), 64),
+    "prefill_t1024": (CONFIGS["prefill"].replace(T=1024, name="prefill_t1024"), 64),
+}
+
+
+@pytest.mark.parametrize("name", ["decode", "mid", "skewed", "prefill", "decode_fp8w", "prefill_fp8w",
+                                  "mid_t512", "prefill_t1024"])
 def test_parity_full_size_sampled(name, orc):
     """Full workload in the benchmark's launch configuration (weights generated
     in HBM); routing compared in full, outputs on sampled tokens that the oracle
     recomputes from host-generated inputs."""
-    w = CONFIGS[name]
+    import moe_expert_layer_scan_gb300 as mm
+    w, width = FULL_EXTRA[name] if name in FULL_EXTRA else (CONFIGS[name], None)
     run = G.DeviceRun(w, device_weights=True)
+    if width is not None:
+        assert mm.mm_token_tile_width(run.moe.h, w.T) == width
     out = out_bits(run.run())
     inter = run.intermediates(w.T)
     assert inter["status"] == 0
