@@ -136,8 +136,9 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
  *     MM_TILES224_MIN_ROWS_PER_EXPERT rows per expert, and above
  *     MM_TILES224_MIN_ROWS_PER_EXPERT_FUSED when the call runs fused (there an
  *     expert's 113-128 rows take one 224-token tile instead of two 112-token
- *     tiles), MM_TILES_64 from there up to MM_TILES64_MAX_ROWS_PER_EXPERT
- *     rows per expert when the call has no shared expert (a shared expert
+ *     tiles), MM_TILES_64 above MM_TILES16_MAX_ROWS_PER_EXPERT and up to
+ *     MM_TILES64_MAX_ROWS_PER_EXPERT rows per expert when the call has no
+ *     shared expert (a shared expert
  *     receives every token, far above the average, and would take many
  *     64-token tiles) and E <= 300, MM_TILES_112 otherwise:
  *     the crossovers measured on GB300 at H = 7168, I = 2048, 256 experts,
