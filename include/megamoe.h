@@ -76,11 +76,14 @@ typedef enum {
  * 5 stage free (scale-factor writer), 6 (L2 tiles of the fused schedule) token
  * rows stored by the L1 epilogues; bit 15 for mm_debug_timeout_probe. */
 
-/* Human-readable name of a status code (static string). */
+/* Human-readable name of a status code (static string). The pages have no
+ * counterpart: their Python entry points raise exceptions instead. */
 MM_API const char* mm_status_string(mm_status_t s);
 
-/* Creates a handle for one layer shape (the pages' get_block_m_for_mega_moe /
- * fp8_fp4_mega_moe setup; "MegaMoE research report" sec. 6, I1).
+/* Creates a handle for one layer shape ("MegaMoE research report" sec. 6.4,
+ * the per-shape set-up calls get_block_m_for_mega_moe and
+ * get_symm_buffer_size_for_mega_moe that precede fp8_fp4_mega_moe;
+ * "MEGAMOE_SM90_DESIGN" sec. 16.1 API Design).
  *   E           routed experts, 1 <= E and E + S <= 1024
  *   H           hidden size; multiple of 128, 128 <= H <= 16384
  *   I           intermediate size; multiple of 128, 128 <= I <= 16384
@@ -116,9 +119,12 @@ MM_API mm_status_t mm_set_options(mm_handle_t h, float swiglu_clamp, int fast_ma
 #define MM_FUSED_MAX_ROWS_PER_EXPERT 128
 MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
 
-/* Token-tile width of the grouped GEMMs ("tuned expert-load buckets").
+/* Token-tile width of the grouped GEMMs: the tuned expert-load buckets of
+ * "MEGAMOE_SM90_DESIGN" sec. 13.1 (BLOCK_M chosen from three buckets by the
+ * load) and "MegaMoE research report" sec. 5.5 (kernel configuration routed by
+ * token count).
  *   MM_TILES_16: 16-token tiles pairing two 128-row weight blocks, one MMA
- *     stream per block, no cluster (weight-stream bound calls);
+ *     stream per block (weight-stream bound calls);
  *   MM_TILES_64: 64-token tiles, otherwise as MM_TILES_112 but with five
  *     pipeline stages instead of four (more weight bytes in flight); only for
  *     calls with E + S <= 300 experts, larger calls run MM_TILES_112;
@@ -142,8 +148,7 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
  *     receives every token, far above the average, and would take many
  *     64-token tiles) and E <= 300, MM_TILES_112 otherwise:
  *     the crossovers measured on GB300 at H = 7168, I = 2048, 256 experts,
- *     top-8 and at H = 4096, I = 1536, 128 experts, top-8
- *     (moe_expert_layer_scan_gb300/tune_tiles.py).
+ *     top-8 and at H = 4096, I = 1536, 128 experts, top-8.
  * Every width computes the same tiles' sums; the results are identical.
  * Other values: MM_ERR_INVALID_ARG. */
 #define MM_TILES_AUTO (-1)
@@ -158,10 +163,14 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
 MM_API mm_status_t mm_set_tile_policy(mm_handle_t h, int policy);
 
 /* The token-tile width (16, 64, 112 or 224) a call of T tokens runs with under the
- * handle's current policy. Host only. */
+ * handle's current policy (the counterpart of get_block_m_for_mega_moe,
+ * "MegaMoE research report" sec. 6.4, which returns the block the kernel
+ * aligns an expert's tokens to). Host only. */
 MM_API mm_status_t mm_token_tile_width(mm_handle_t h, int T, int* width);
 
-/* Weight element format (both linears). MM_WEIGHTS_MXFP4 (the default): E2M1
+/* Weight element format (both linears; the weight recipes (1,1,32) MXFP4 and
+ * FP8 of the "SM90 FP8 x MXFP4 MegaMoE" pull request #411 page, and
+ * "MEGAMOE_SM90_DESIGN" sec. 15.2 Weight SF Layout). MM_WEIGHTS_MXFP4 (the default): E2M1
  * codes packed two per byte, the even K index in the low nibble (OCP MXFP4).
  * MM_WEIGHTS_MXFP8: E4M3 codes, one byte per element (OCP MXFP8; the FP8 x FP8
  * variant of the pages' SM90 recipe, with the UE8M0-per-32 block scales the
@@ -172,9 +181,11 @@ MM_API mm_status_t mm_token_tile_width(mm_handle_t h, int T, int* width);
 #define MM_WEIGHTS_MXFP8 1
 MM_API mm_status_t mm_set_weight_format(mm_handle_t h, int format);
 
-/* Expert-parallel-ready routing outputs ("MegaMoE research report", the
- * dispatch step of the expert-parallel layer and its per-rank receive
- * statistics; here every expert is local and nothing is sent).
+/* Expert-parallel-ready routing outputs ("MegaMoE research report" sec. 4.1,
+ * the dispatch warps' expert counts and source metadata; "MEGAMOE_SM90_DESIGN"
+ * sec. 16.1, the cumulative_local_expert_recv_stats argument, and sec. 21
+ * Phase 2 step 2.3, the per-rank receive counts; here every expert is local
+ * and nothing is sent).
  *
  * mm_set_ep_ranks: the routed experts are owned by num_ranks destination
  * ranks in contiguous blocks of E / num_ranks (rank g owns experts
@@ -195,12 +206,20 @@ MM_API mm_status_t mm_set_weight_format(mm_handle_t h, int format);
 MM_API mm_status_t mm_set_ep_ranks(mm_handle_t h, int num_ranks);
 MM_API mm_status_t mm_set_expert_stats(mm_handle_t h, int32_t* cumulative_counts);
 
-/* Bytes of device workspace mm_run needs for T tokens (T >= 0). The
- * workspace holds the routing tables, the gathered FP8 L1 operand, the FP8 L2
- * operand, the BF16 per-slot L2 output and a status word. */
+/* Bytes of device workspace mm_run needs for T tokens (T >= 0): the local
+ * form of the symmetric buffer whose layout get_symm_buffer_size_for_mega_moe
+ * computes ("MegaMoE research report" sec. 6.4; "MEGAMOE_SM90_DESIGN" sec. 16.1).
+ * The workspace holds the routing tables, the gathered FP8 L1 operand, the FP8 L2
+ * operand, the BF16 per-slot L2 output and a status word. Host only; MM_OK, or
+ * MM_ERR_INVALID_ARG for a null handle or pointer or T < 0. */
 MM_API mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes);
 
-/* Runs the path for T tokens, asynchronously on `stream`.
+/* Runs the path for T tokens, asynchronously on `stream`: the local form of
+ * fp8_fp4_mega_moe ("MegaMoE research report" sec. 6.4 and sec. 4.1) and of the
+ * fp8_mega_moe argument list of "MEGAMOE_SM90_DESIGN" sec. 16.1 (activations,
+ * the L1 and L2 weight tuples, the workspace, top-k); the workspace is
+ * re-initialised by the call itself, as the design's sec. 21 Phase 2 step 2.2
+ * and Phase 6 step 6.6 require of two calls in a row.
  *   x_fp8    device, [T][H] E4M3                                  (16-byte aligned)
  *   x_sf     device, [T][H/32] UE8M0                               (4-byte aligned)
  *   topk_idx device, [T][topk] int32, each in [0, E) or -1 (slot disabled);
@@ -225,14 +244,24 @@ MM_API mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x
                    void* out_bf16, void* ws, size_t ws_bytes, mm_stream_t stream);
 
 /* Synchronises `stream` and returns in *device_status the MM_DEV_* bits the
- * last mm_run on this workspace recorded (0 = none). */
+ * last mm_run on this workspace recorded (0 = none). The pages' kernels poll
+ * arrival counters until the other side completes (the "SM90 FP8 x MXFP4
+ * MegaMoE" pull request #411 page's review of the dispatch completion
+ * protocol: a waiter polls and eventually times out; "MEGAMOE_SM90_DESIGN"
+ * sec. 21, the no-hang criteria of Phase 2 step 2.6 and Phase 3 step 3.8);
+ * here every wait is bounded and an expiry is reported through this word
+ * instead of a hang. Returns MM_ERR_INVALID_ARG for null arguments and
+ * MM_ERR_CUDA if the copy or the synchronisation fails. */
 MM_API mm_status_t mm_get_status(mm_handle_t h, const void* ws, mm_stream_t stream, uint32_t* device_status);
 
-/* Number of kernel launches one mm_run for T tokens enqueues. */
+/* Number of kernel launches one mm_run for T tokens enqueues (host only). The
+ * pages have no counterpart; it states the split into kernels that
+ * "MegaMoE research report" sec. 4.1 (one fused kernel) and sec. 4.3 (pr-352's
+ * split L1/L2 kernels) compare. */
 MM_API mm_status_t mm_launches_per_run(mm_handle_t h, int T, int* launches);
 
-/* Debug/test views into a workspace after mm_run for T tokens (device
- * pointers; contents valid once the stream has reached them):
+/* Device pointers into a workspace after mm_run for T tokens (contents valid
+ * once the stream has reached them):
  *   counts [E+S] int32, offsets [E+S+1] int32, perm [T(k+S)] int32 (pool row -> slot
  *   t*(k+S)+j), pos [T(k+S)] int32 (slot -> pool row or -1), row_w [T(k+S)] float,
  *   pool_x [rows][H] u8, pool_sf [rows][H/32] u8, l2a [rows][I] u8 (E4M3),
@@ -254,15 +283,24 @@ typedef struct {
   int32_t* rank_offsets; /* [ep_ranks + 1], see mm_set_ep_ranks */
 } mm_debug_views_t;
 
+/* Test views (mm_debug_views_t above) into a workspace used by mm_run for T
+ * tokens: the local form of the verification views of "MEGAMOE_SM90_DEV" (the
+ * 2026-06-18 00:46 entry, l1_accum_debug for single-tile accumulator checks)
+ * and of the dispatch products that "MEGAMOE_SM90_DESIGN" sec. 21 Phase 2
+ * checks against the routing reference. Host only (pointer arithmetic on ws);
+ * MM_ERR_INVALID_ARG for null arguments or T < 0. */
 MM_API mm_status_t mm_debug_views(mm_handle_t h, void* ws, int T, mm_debug_views_t* views);
 
-/* Test hook for the bounded-wait machinery: launches one CTA that waits on an
+/* Test hook for the bounded-wait machinery behind mm_get_status (the pages'
+ * no-hang criteria, "MEGAMOE_SM90_DESIGN" sec. 21 Phase 3 steps 3.2 and 3.8):
+ * launches one CTA that waits on an
  * mbarrier nothing ever arrives on, gives up after timeout_ns nanoseconds,
  * sets MM_DEV_TIMEOUT in the workspace status word and returns. The GPU stays
  * usable. ws must hold at least 256 bytes. */
 MM_API mm_status_t mm_debug_timeout_probe(void* ws, uint64_t timeout_ns, mm_stream_t stream);
 
-/* Test hook for the SiLU division: the L1 epilogue divides the gate by
+/* Test hook for the SiLU division of "MEGAMOE_SM90_DESIGN" sec. 10.1 (silu =
+ * gate / (1 + exp(-gate)), fast_math off): the L1 epilogue divides the gate by
  * 1 + exp(-gate) with a branch-free Newton-Raphson reciprocal and Markstein's
  * residual correction instead of the IEEE division routine. This compares it
  * with __frcp_rn / __fdiv_rn on the GPU. counts: device memory, 5 x uint64,
@@ -277,7 +315,9 @@ MM_API mm_status_t mm_debug_timeout_probe(void* ws, uint64_t timeout_ns, mm_stre
  * pairs <= 2^40. Asynchronous on `stream`. */
 MM_API mm_status_t mm_debug_div_check(uint64_t pairs, uint64_t seed, unsigned long long* counts, mm_stream_t stream);
 
-/* Per-launch timing for measurement: with profiling on, mm_run records a CUDA
+/* Per-launch timing for measurement, the local form of the pages' per-phase
+ * profiling switch ("MEGAMOE_SM90_DESIGN" sec. 18, DG_SM90_MOE_PHASE_PROFILE,
+ * and sec. 19.4): with profiling on, mm_run records a CUDA
  * event on its stream before each launch and after the last one. mm_profile_last
  * waits for the last recorded event and writes up to n durations in
  * milliseconds into ms, one per launch of the last profiled mm_run (route,
@@ -316,7 +356,10 @@ MM_API mm_status_t mm_run_noalloc(mm_handle_t h, int T, const void* x_fp8, const
                                   const float* topk_w, const void* w1, const void* w1_sf, const void* w2,
                                   const void* w2_sf, void* out_bf16, mm_stream_t stream);
 
-/* Destroys a handle (NULL is ignored). */
+/* Destroys a handle made by mm_create (the same set-up passages:
+ * "MegaMoE research report" sec. 6.4; "MEGAMOE_SM90_DESIGN" sec. 16.1).
+ * NULL is ignored. Frees only the handle's host memory and its profiling
+ * events; the caller's buffers and workspaces are untouched. */
 MM_API void mm_destroy(mm_handle_t h);
 
 #ifdef __cplusplus

@@ -98,24 +98,6 @@ bool encode_sf(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, u
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// MM_DEEP=0 keeps 16-token tiles at five stages (measurement only).
-bool deep_disabled() {
-  static const bool off = [] {
-    const char* e = getenv("MM_DEEP");
-    return e && e[0] == '0';
-  }();
-  return off;
-}
-
-// MM_QUAD=0 keeps 16-token tiles at two weight blocks (measurement only).
-bool quad_disabled() {
-  static const bool off = [] {
-    const char* e = getenv("MM_QUAD");
-    return e && e[0] == '0';
-  }();
-  return off;
-}
-
 // Whether a call of T tokens runs both GEMMs in one launch.
 bool use_fused(const mm_handle* h, int T) {
   if (h->schedule != MM_SCHEDULE_AUTO) return h->schedule == MM_SCHEDULE_FUSED;
@@ -142,9 +124,9 @@ int variant_for(const mm_handle* h, int T) {
   if (width == MM_TILES_112) return 1;
   if (width == MM_TILES_224) return 3;
   if (width == MM_TILES_64) return h->E + h->S <= kDeepMaxExperts ? 5 : 1;
-  if (h->w_fmt == MM_WEIGHTS_MXFP8 && h->E + h->S <= kQuadMaxExperts && h->I % 256 == 0 && !quad_disabled())
+  if (h->w_fmt == MM_WEIGHTS_MXFP8 && h->E + h->S <= kQuadMaxExperts && h->I % 256 == 0)
     return 4;
-  return (h->E + h->S <= kDeepMaxExperts && !deep_disabled()) ? 2 : 0;
+  return (h->E + h->S <= kDeepMaxExperts) ? 2 : 0;
 }
 
 int tile_width(int variant) {
@@ -291,7 +273,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   // otherwise the scale warp loads them itself (two-block tiles only).
   const bool sf_tma = h->H % 512 == 0 && h->I % 512 == 0 && aligned(w1_sf, 16) && aligned(w2_sf, 16);
   int variant = variant_for(h, T);
-  if (variant == 4 && !sf_tma) variant = (h->E + h->S <= kDeepMaxExperts && !deep_disabled()) ? 2 : 0;
+  if (variant == 4 && !sf_tma) variant = (h->E + h->S <= kDeepMaxExperts) ? 2 : 0;
   const int bn1 = tile_width(variant);
   const int bn2 = bn1;
 
@@ -315,11 +297,10 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ra.status = reinterpret_cast<uint32_t*>(base + L.status);
   ra.T = T; ra.E = h->E; ra.k = h->k; ra.S = h->S;
   ra.bn_l1 = bn1; ra.bn_l2 = bn2;
-  const int cs = mm_gemm_cluster(variant);
   const int na = mm_gemm_blocks(variant);                 // 128-row weight blocks per tile
   const int f1 = h->I / (64 * na), f2 = (h->H + 128 * na - 1) / (128 * na);  // weight tiles per expert
-  ra.fb_l1 = (f1 + cs - 1) / cs;                         // tile-table entries: groups of cs weight tiles
-  ra.fb_l2 = (f2 + cs - 1) / cs;
+  ra.fb_l1 = f1;
+  ra.fb_l2 = f2;
   int ev_i = 0;
   // an event before each launch (named for it) and one after the last
   auto mark = [&](const char* next) {
@@ -362,10 +343,10 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   memset(&maps, 0, sizeof(maps));
   maps.w1 = h->tm_w1;
   maps.w2 = h->tm_w2;
-  // token boxes: each CTA of a cluster loads (and multicasts) 1/cs of the token tile
-  if (!encode_2d(&maps.a1, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, (uint32_t)(bn1 / cs)))
+  // token boxes: the whole token tile
+  if (!encode_2d(&maps.a1, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, (uint32_t)bn1))
     return MM_ERR_CUDA;
-  if (!encode_2d(&maps.a2, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)(bn2 / cs)))
+  if (!encode_2d(&maps.a2, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)bn2))
     return MM_ERR_CUDA;
   if (sf_tma) {
     if (h->w1sf_key != w1_sf) {

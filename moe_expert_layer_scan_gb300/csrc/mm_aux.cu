@@ -16,16 +16,6 @@
 
 namespace mm {
 
-// MM_ROUTE_SMALL=0 routes small calls with the general one-CTA kernel
-// (measurement only).
-inline bool route_small_disabled() {
-  static const bool off = [] {
-    const char* e = getenv("MM_ROUTE_SMALL");
-    return e && e[0] == '0';
-  }();
-  return off;
-}
-
 __device__ __forceinline__ int slot_expert(const RouteArgs& a, long s, bool* bad) {
   const int Kp = a.k + a.S;
   const long t = s / Kp;
@@ -469,21 +459,21 @@ extern "C" int mm_launch_route(const mm::RouteArgs* a, void* stream) {
     attr_set = true;
   }
   cudaStream_t st = (cudaStream_t)stream;
-  if (R <= mm::kRouteSmallMax && !mm::route_small_disabled()) {
+  if (R <= mm::kRouteSmallMax) {
     // the first kernel of a forward: ordinary stream order behind the previous work
-    return (int)mm::launch_kernel(mm::route_small_kernel, dim3(1), dim3(1024), 0, st, false, 1, *a);
+    return (int)mm::launch_kernel(mm::route_small_kernel, dim3(1), dim3(1024), 0, st, false, *a);
   }
   if (R <= mm::kRouteSingleMax) {
     // the first kernel of a forward: ordinary stream order behind the previous work
     return (int)mm::launch_kernel(mm::route_kernel, dim3(1), dim3(1024), sizeof(int) * (32 * (size_t)Ep + 72), st,
-                                  false, 1, *a);
+                                  false, *a);
   }
   const int G = (int)((R + mm::kRouteChunk - 1) / mm::kRouteChunk);
   cudaError_t e = mm::launch_kernel(mm::route_count_kernel, dim3(G), dim3(1024), sizeof(int) * (size_t)Ep, st, false,
-                                    1, *a);
-  if (e == cudaSuccess) e = mm::launch_kernel(mm::route_scan_kernel, dim3(1), dim3(1024), 0, st, true, 1, *a, G);
+                                    *a);
+  if (e == cudaSuccess) e = mm::launch_kernel(mm::route_scan_kernel, dim3(1), dim3(1024), 0, st, true, *a, G);
   if (e == cudaSuccess)
-    e = mm::launch_kernel(mm::route_place_kernel, dim3(G), dim3(1024), sizeof(int) * 32 * (size_t)Ep, st, true, 1, *a);
+    e = mm::launch_kernel(mm::route_place_kernel, dim3(G), dim3(1024), sizeof(int) * 32 * (size_t)Ep, st, true, *a);
   return (int)e;
 }
 
@@ -491,7 +481,7 @@ extern "C" int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, v
   if (rows_upper_bound <= 0) return 0;
   int blocks = (rows_upper_bound + 7) / 8;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  return (int)mm::launch_kernel(mm::gather_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, true, 1, *a);
+  return (int)mm::launch_kernel(mm::gather_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, true, *a);
 }
 
 extern "C" int mm_launch_combine(const mm::CombineArgs* a, void* stream) {
@@ -499,7 +489,7 @@ extern "C" int mm_launch_combine(const mm::CombineArgs* a, void* stream) {
   const long threads = (long)a->T * (a->H / 8);
   long blocks = (threads + 127) / 128;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  return (int)mm::launch_kernel(mm::combine_kernel, dim3((unsigned)blocks), dim3(128), 0, (cudaStream_t)stream, true, 1,
+  return (int)mm::launch_kernel(mm::combine_kernel, dim3((unsigned)blocks), dim3(128), 0, (cudaStream_t)stream, true,
                                 *a);
 }
 

@@ -66,7 +66,7 @@ struct Warps {
 
 enum : int { kModeL2 = 0, kModeL1 = 1, kModeFused = 2 };
 
-template <int BN, int STAGES, int CS, int NA_ = 2>
+template <int BN, int STAGES, int NA_ = 2>
 struct GemmCfg {
   static constexpr int BM = 128;                         // weight rows per MMA
   static constexpr int BK = 128;                         // K per stage
@@ -78,7 +78,6 @@ struct GemmCfg {
   static constexpr int A_BYTES = BM * BK;                // 16 KB in SMEM (4-bit codes padded to bytes)
   static constexpr int A_TX = BM * BK / 2;               // transaction bytes of one weight box (packed 4-bit size)
   static constexpr int B_BYTES = BN * BK;
-  static constexpr int B_PART_ROWS = BN / CS;            // token rows each CTA of a cluster loads (multicast)
   static constexpr int SFB_ROWS = BN <= 128 ? 128 : 256;
   static constexpr int SF_STAGE_BYTES = NA * 512 + SFB_ROWS * 4;
   static constexpr int A_OFF = 0;
@@ -122,7 +121,7 @@ struct GemmCfg {
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(BN <= RAW_B_ROWS, "every token row of a tile has its scale row in the raw group");
   static_assert(B_BYTES % 1024 == 0, "B tiles must keep 1024-byte alignment");
-  static_assert(BN % (8 * CS) == 0, "each multicast share must be whole 8-row swizzle atoms");
+  static_assert(BN % 8 == 0, "token tiles are whole 8-row swizzle atoms");
 };
 
 struct Tile {
@@ -130,15 +129,14 @@ struct Tile {
   bool active;  // this CTA has a weight tile (fb < fb_total)
 };
 
-// Tile index -> expert, token tile and this CTA's weight tile: the table
-// counts weight-tile groups of cs tiles (one per CTA of a cluster). The tile
-// table and the row offsets are shared-memory copies. An expert's rows are
+// Tile index -> expert, token tile and weight tile. The tile table and the
+// row offsets are shared-memory copies. An expert's rows are
 // split into the fewest token tiles of at most bn rows, all of one size
 // rounded up to 16 (the last takes the rest): 256 rows with bn = 224 give two
 // tiles of 128, not 224 + 32 (a tile costs its weight stream and a per-K-step
 // instruction floor whatever its row count).
 static __device__ __noinline__ Tile decode_tile(int tile, const int* tstart, const int* offs, int Ep, int fb_total,
-                                           int bn, int rank, int cs) {
+                                           int bn) {
   int lo = 0, hi = Ep - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -150,9 +148,8 @@ static __device__ __noinline__ Tile decode_tile(int tile, const int* tstart, con
   const int local = tile - tstart[lo];
   const int cnt = offs[lo + 1] - offs[lo];
   const int ntt = (cnt + bn - 1) / bn;
-  const int grp = local / ntt;
-  const int tt = local - grp * ntt;
-  t.fb = grp * cs + rank;
+  t.fb = local / ntt;
+  const int tt = local - t.fb * ntt;
   t.active = t.fb < fb_total;
   const int per = ((cnt + ntt - 1) / ntt + 15) & ~15;  // <= bn, and (ntt - 1) * per < cnt
   t.row0 = offs[lo] + tt * per;
@@ -233,11 +230,11 @@ __device__ __forceinline__ float inv_scale(uint32_t code) {
   return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(1u << (n + 149));
 }
 
-template <int MODE, int BN, int STAGES, int CS, int NA>
+template <int MODE, int BN, int STAGES, int NA>
 __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g1,
                 const __grid_constant__ GemmArgs g2) {
-  using C = GemmCfg<BN, STAGES, CS, NA>;
+  using C = GemmCfg<BN, STAGES, NA>;
   using W = Warps<BN, NA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -256,7 +253,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);     // TMA expect_tx arrival
       mbar_init(&sfready[s], 1);  // the scale warp's tcgen05.commit
-      mbar_init(&empty[s], C::NI * CS);  // one tcgen05.commit per issuing thread of every CTA of the cluster
+      mbar_init(&empty[s], C::NI);  // one tcgen05.commit per issuing thread
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], C::NI);  // tcgen05.commit after the last K step, per issuing thread
@@ -286,7 +283,6 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (CS > 1) cluster_sync();  // barriers initialised cluster-wide before any multicast
   tc_fence_after();
   // the prologue above overlaps the previous kernel; its outputs are read below
   pdl_trigger();
@@ -308,19 +304,17 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
   const int n1 = MODE == kModeL2 ? 0 : s_t1[g1.Ep];
   const int num_tiles = MODE == kModeL1 ? n1 : n1 + s_t2[g2.Ep];
   auto is_l1 = [&](int tile) { return MODE == kModeL1 || (MODE == kModeFused && tile < n1); };
-  const int rank = CS > 1 ? (int)cluster_ctarank() : 0;
   // flat tile index -> tile of its phase
   auto tile_of = [&](int tile, bool l1) {
-    return decode_tile(l1 ? tile : tile - n1, l1 ? s_t1 : s_t2, s_off, g1.Ep, l1 ? g1.fb_total : g2.fb_total, BN,
-                       rank, CS);
+    return decode_tile(l1 ? tile : tile - n1, l1 ? s_t1 : s_t2, s_off, g1.Ep, l1 ? g1.fb_total : g2.fb_total, BN);
   };
-  // This CTA's (cluster's) tile sequence: tiles g, g + G, ... (concurrent
+  // This CTA's tile sequence: tiles g, g + G, ... (concurrent
   // CTAs work on adjacent tiles, so their weight streams stay close in HBM).
   // Fused: the L1 tiles that way; the r = n1 mod G CTAs that hold one L1 tile
   // more are still busy with it when the others reach the L2 tiles, so the
   // first A = (G - r) * round(K1 / K2) L2 tiles go round-robin to the other
   // G - r CTAs only (about one L1 tile's worth each), the rest to all G.
-  const int G = gridDim.x / CS, g = blockIdx.x / CS;
+  const int G = gridDim.x, g = blockIdx.x;
   int r_l1 = 0, n_early = 0;
   if (MODE == kModeFused) {
     r_l1 = n1 % G;
@@ -349,7 +343,6 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
     if (t < n1) return t + G < n1 ? t + G : l2_first();
     return l2_next(t - n1);
   };
-  constexpr uint16_t kAllCtas = (uint16_t)((1u << CS) - 1u);
   // wait sites reported in the status word on expiry: L1 tiles s, L2 tiles 8 + s
   constexpr uint32_t kSiteReady = 8u + 6u;  // an L2 tile waiting for its L1 rows (fused)
   int* l2rdy = reinterpret_cast<int*>(smem + C::L2RDY_OFF);
@@ -443,29 +436,17 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         uint8_t* sA = smem + C::A_OFF + s * C::NA * C::A_BYTES;
         uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
         if (lane == 0) {
-          // the whole token tile lands here: this CTA's share and the others' multicasts
           mbar_arrive_expect_tx(&full[s], (uint32_t)nact * a_tx + C::B_BYTES);
 #pragma unroll
           for (int u = 0; u < C::NA; ++u)
             if ((amask >> u) & 1u) tma_load_2d(sA + u * C::A_BYTES, tw, &full[s], kb * C::BK, block_wrow(g, t, u, C::NA));
-          if constexpr (CS == 1) {
-            tma_load_2d(sB, ta, &full[s], kb * C::BK, t.row0);
-          } else {
-            tma_load_2d_multicast(sB + rank * C::B_PART_ROWS * C::BK, ta, &full[s], kb * C::BK,
-                                  t.row0 + rank * C::B_PART_ROWS, kAllCtas);
-          }
+          tma_load_2d(sB, ta, &full[s], kb * C::BK, t.row0);
         }
       }
       cur_ready = next_ready;
     }
     const GemmArgs& gl = MODE == kModeL1 ? g1 : g2;  // status word and limit (shared by both)
     constexpr uint32_t kSiteTail = (MODE == kModeL1 ? 0u : 8u) + 4u;
-    if (ok && CS > 1) {
-      // Producer tail: wait until every CTA has released the last stages, so
-      // that no remote tcgen05.commit arrival targets this CTA after it exits.
-      for (uint32_t j = (it > (uint32_t)STAGES ? it - STAGES : 0u); j < it; ++j)
-        if (!mbar_wait(&empty[j % STAGES], (j / STAGES) & 1u, abort_flag, gl.status, gl.timeout_ns, kSiteTail)) break;
-    }
     if (!ok) {
       // Let the copies already issued land before the CTA can exit (the
       // stage's barrier may never complete if another role gave up, so the
@@ -692,9 +673,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
               tc_mma_mxf8f6f4(d, da + 2u * k, db + 2u * k, id, sfa, sfb, (kb > 0 || k > 0) ? 1u : 0u);
             }
           }
-          // the stage is free once every CTA the token tile was multicast to is done with it
-          if constexpr (CS == 1) tc_commit(&empty[s]);
-          else tc_commit_multicast(&empty[s], kAllCtas);
+          tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
         if (!ok) break;
         tc_commit(&tfull[buf]);
@@ -824,50 +803,30 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  // no CTA leaves while another may still multicast into it or arrive on its barriers
-  if constexpr (CS > 1) cluster_sync();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
-template <int MODE, int BN, int STAGES, int CS, int NA = 2>
+template <int MODE, int BN, int STAGES, int NA = 2>
 static int set_smem_attr(int* max_ctas) {
-  using C = GemmCfg<BN, STAGES, CS, NA>;
-  auto k = gemm_kernel<MODE, BN, STAGES, CS, NA>;
+  using C = GemmCfg<BN, STAGES, NA>;
+  auto k = gemm_kernel<MODE, BN, STAGES, NA>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return (int)e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   *max_ctas = sms;
-  if (CS > 1) {
-    // persistent grid: only as many clusters as can be resident at once
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3((unsigned)(sms / CS * CS));
-    cfg.blockDim = dim3(Warps<BN, NA>::THREADS);
-    cfg.dynamicSmemBytes = C::SMEM_BYTES;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, k, &cfg);
-    if (e != cudaSuccess || clusters < 1) return e != cudaSuccess ? (int)e : (int)cudaErrorInvalidConfiguration;
-    *max_ctas = clusters * CS;
-  }
   return 0;
 }
 
-template <int MODE, int BN, int STAGES, int CS, int NA = 2>
+template <int MODE, int BN, int STAGES, int NA = 2>
 static int launch(const GemmMaps* maps, const GemmArgs* g1, const GemmArgs* g2, int num_ctas, cudaStream_t st) {
-  using C = GemmCfg<BN, STAGES, CS, NA>;
-  return (int)launch_kernel(gemm_kernel<MODE, BN, STAGES, CS, NA>, dim3((unsigned)num_ctas),
-                            dim3(Warps<BN, NA>::THREADS), C::SMEM_BYTES, st, true, CS, *maps, *g1, *g2);
+  using C = GemmCfg<BN, STAGES, NA>;
+  return (int)launch_kernel(gemm_kernel<MODE, BN, STAGES, NA>, dim3((unsigned)num_ctas),
+                            dim3(Warps<BN, NA>::THREADS), C::SMEM_BYTES, st, true, *maps, *g1, *g2);
 }
 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
@@ -886,30 +845,28 @@ static int g_ctas[3][6];
 extern "C" int mm_gemm_prepare(void) {
   using namespace mm;
   int e = 0;
-  if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesSmall, 1>(&g_ctas[kModeL1][0]))) return e;
-  if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesSmall, 1>(&g_ctas[kModeL2][0]))) return e;
-  if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesSmall, 1>(&g_ctas[kModeFused][0]))) return e;
-  if ((e = set_smem_attr<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(&g_ctas[kModeL1][1]))) return e;
-  if ((e = set_smem_attr<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(&g_ctas[kModeL2][1]))) return e;
-  if ((e = set_smem_attr<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(&g_ctas[kModeFused][1]))) return e;
-  if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesSmallDeep, 1>(&g_ctas[kModeL1][2]))) return e;
-  if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesSmallDeep, 1>(&g_ctas[kModeL2][2]))) return e;
-  if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesSmallDeep, 1>(&g_ctas[kModeFused][2]))) return e;
-  if ((e = set_smem_attr<kModeL1, kBnWide, kStagesWide, kClusterLarge>(&g_ctas[kModeL1][3]))) return e;
-  if ((e = set_smem_attr<kModeL2, kBnWide, kStagesWide, kClusterLarge>(&g_ctas[kModeL2][3]))) return e;
-  if ((e = set_smem_attr<kModeFused, kBnWide, kStagesWide, kClusterLarge>(&g_ctas[kModeFused][3]))) return e;
-  if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesQuad, 1, 4>(&g_ctas[kModeL1][4]))) return e;
-  if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesQuad, 1, 4>(&g_ctas[kModeL2][4]))) return e;
-  if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesQuad, 1, 4>(&g_ctas[kModeFused][4]))) return e;
-  if ((e = set_smem_attr<kModeL1, kBnMid, kStagesMid, 1>(&g_ctas[kModeL1][5]))) return e;
-  if ((e = set_smem_attr<kModeL2, kBnMid, kStagesMid, 1>(&g_ctas[kModeL2][5]))) return e;
-  if ((e = set_smem_attr<kModeFused, kBnMid, kStagesMid, 1>(&g_ctas[kModeFused][5]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesSmall>(&g_ctas[kModeL1][0]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesSmall>(&g_ctas[kModeL2][0]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesSmall>(&g_ctas[kModeFused][0]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnLarge, kStagesLarge>(&g_ctas[kModeL1][1]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnLarge, kStagesLarge>(&g_ctas[kModeL2][1]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnLarge, kStagesLarge>(&g_ctas[kModeFused][1]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesSmallDeep>(&g_ctas[kModeL1][2]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesSmallDeep>(&g_ctas[kModeL2][2]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesSmallDeep>(&g_ctas[kModeFused][2]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnWide, kStagesWide>(&g_ctas[kModeL1][3]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnWide, kStagesWide>(&g_ctas[kModeL2][3]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnWide, kStagesWide>(&g_ctas[kModeFused][3]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesQuad, 4>(&g_ctas[kModeL1][4]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesQuad, 4>(&g_ctas[kModeL2][4]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesQuad, 4>(&g_ctas[kModeFused][4]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnMid, kStagesMid>(&g_ctas[kModeL1][5]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnMid, kStagesMid>(&g_ctas[kModeL2][5]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnMid, kStagesMid>(&g_ctas[kModeFused][5]))) return e;
   return 0;
 }
 
 extern "C" int mm_gemm_blocks(int variant) { return variant == 4 ? 4 : 2; }
-
-extern "C" int mm_gemm_cluster(int variant) { return variant == 1 || variant == 3 ? mm::kClusterLarge : 1; }
 
 extern "C" int mm_gemm_epilogue_warps(int variant) {
   return variant == 1   ? mm::Warps<mm::kBnLarge, 2>::EPI
@@ -920,11 +877,11 @@ extern "C" int mm_gemm_epilogue_warps(int variant) {
 }
 
 extern "C" int mm_gemm_token_scale_box_rows(int variant) {
-  return variant == 1   ? mm::GemmCfg<mm::kBnLarge, mm::kStagesLarge, mm::kClusterLarge>::RAW_B_ROWS
-         : variant == 3 ? mm::GemmCfg<mm::kBnWide, mm::kStagesWide, mm::kClusterLarge>::RAW_B_ROWS
-         : variant == 4 ? mm::GemmCfg<mm::kBnSmall, mm::kStagesQuad, 1, 4>::RAW_B_ROWS
-         : variant == 5 ? mm::GemmCfg<mm::kBnMid, mm::kStagesMid, 1>::RAW_B_ROWS
-                        : mm::GemmCfg<mm::kBnSmall, mm::kStagesSmall, 1>::RAW_B_ROWS;
+  return variant == 1   ? mm::GemmCfg<mm::kBnLarge, mm::kStagesLarge>::RAW_B_ROWS
+         : variant == 3 ? mm::GemmCfg<mm::kBnWide, mm::kStagesWide>::RAW_B_ROWS
+         : variant == 4 ? mm::GemmCfg<mm::kBnSmall, mm::kStagesQuad, 4>::RAW_B_ROWS
+         : variant == 5 ? mm::GemmCfg<mm::kBnMid, mm::kStagesMid>::RAW_B_ROWS
+                        : mm::GemmCfg<mm::kBnSmall, mm::kStagesSmall>::RAW_B_ROWS;
 }
 
 extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a, int num_ctas,
@@ -935,19 +892,19 @@ extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, con
   const int mode = l1 ? kModeL1 : kModeL2;
   const int n = g_ctas[mode][variant];
   if (l1) {
-    return variant == 0   ? launch<kModeL1, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
-           : variant == 2 ? launch<kModeL1, kBnSmall, kStagesSmallDeep, 1>(maps, a, a, n, st)
-           : variant == 3 ? launch<kModeL1, kBnWide, kStagesWide, kClusterLarge>(maps, a, a, n, st)
-           : variant == 4 ? launch<kModeL1, kBnSmall, kStagesQuad, 1, 4>(maps, a, a, n, st)
-           : variant == 5 ? launch<kModeL1, kBnMid, kStagesMid, 1>(maps, a, a, n, st)
-                          : launch<kModeL1, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
+    return variant == 0   ? launch<kModeL1, kBnSmall, kStagesSmall>(maps, a, a, n, st)
+           : variant == 2 ? launch<kModeL1, kBnSmall, kStagesSmallDeep>(maps, a, a, n, st)
+           : variant == 3 ? launch<kModeL1, kBnWide, kStagesWide>(maps, a, a, n, st)
+           : variant == 4 ? launch<kModeL1, kBnSmall, kStagesQuad, 4>(maps, a, a, n, st)
+           : variant == 5 ? launch<kModeL1, kBnMid, kStagesMid>(maps, a, a, n, st)
+                          : launch<kModeL1, kBnLarge, kStagesLarge>(maps, a, a, n, st);
   }
-  return variant == 0   ? launch<kModeL2, kBnSmall, kStagesSmall, 1>(maps, a, a, n, st)
-         : variant == 2 ? launch<kModeL2, kBnSmall, kStagesSmallDeep, 1>(maps, a, a, n, st)
-         : variant == 3 ? launch<kModeL2, kBnWide, kStagesWide, kClusterLarge>(maps, a, a, n, st)
-         : variant == 4 ? launch<kModeL2, kBnSmall, kStagesQuad, 1, 4>(maps, a, a, n, st)
-         : variant == 5 ? launch<kModeL2, kBnMid, kStagesMid, 1>(maps, a, a, n, st)
-                        : launch<kModeL2, kBnLarge, kStagesLarge, kClusterLarge>(maps, a, a, n, st);
+  return variant == 0   ? launch<kModeL2, kBnSmall, kStagesSmall>(maps, a, a, n, st)
+         : variant == 2 ? launch<kModeL2, kBnSmall, kStagesSmallDeep>(maps, a, a, n, st)
+         : variant == 3 ? launch<kModeL2, kBnWide, kStagesWide>(maps, a, a, n, st)
+         : variant == 4 ? launch<kModeL2, kBnSmall, kStagesQuad, 4>(maps, a, a, n, st)
+         : variant == 5 ? launch<kModeL2, kBnMid, kStagesMid>(maps, a, a, n, st)
+                        : launch<kModeL2, kBnLarge, kStagesLarge>(maps, a, a, n, st);
 }
 
 extern "C" int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const mm::GemmArgs* g1,
@@ -955,10 +912,10 @@ extern "C" int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const
   using namespace mm;
   cudaStream_t st = (cudaStream_t)stream;
   const int n = g_ctas[kModeFused][variant];
-  return variant == 0   ? launch<kModeFused, kBnSmall, kStagesSmall, 1>(maps, g1, g2, n, st)
-         : variant == 2 ? launch<kModeFused, kBnSmall, kStagesSmallDeep, 1>(maps, g1, g2, n, st)
-         : variant == 3 ? launch<kModeFused, kBnWide, kStagesWide, kClusterLarge>(maps, g1, g2, n, st)
-         : variant == 4 ? launch<kModeFused, kBnSmall, kStagesQuad, 1, 4>(maps, g1, g2, n, st)
-         : variant == 5 ? launch<kModeFused, kBnMid, kStagesMid, 1>(maps, g1, g2, n, st)
-                        : launch<kModeFused, kBnLarge, kStagesLarge, kClusterLarge>(maps, g1, g2, n, st);
+  return variant == 0   ? launch<kModeFused, kBnSmall, kStagesSmall>(maps, g1, g2, n, st)
+         : variant == 2 ? launch<kModeFused, kBnSmall, kStagesSmallDeep>(maps, g1, g2, n, st)
+         : variant == 3 ? launch<kModeFused, kBnWide, kStagesWide>(maps, g1, g2, n, st)
+         : variant == 4 ? launch<kModeFused, kBnSmall, kStagesQuad, 4>(maps, g1, g2, n, st)
+         : variant == 5 ? launch<kModeFused, kBnMid, kStagesMid>(maps, g1, g2, n, st)
+                        : launch<kModeFused, kBnLarge, kStagesLarge>(maps, g1, g2, n, st);
 }

@@ -35,13 +35,6 @@ constexpr int kBnWide = 224;
 // bytes in flight) when the call has at most kDeepMaxExperts experts. For the
 // weight-bandwidth bound calls with a few dozen rows per expert.
 constexpr int kBnMid = 64;
-// CTAs per cluster of the 112- and 224-token tiles. With 2, the CTAs of a
-// cluster take adjacent weight tiles of the same (expert, token tile) and each
-// multicasts its share of the token tile to both, halving the token tile's L2
-// reads; a stage is then released only when both CTAs are done with it, and
-// that lock-step measured 0.7-1% slower than single CTAs (mid, skewed,
-// prefill), so the kernels run without clusters.
-constexpr int kClusterLarge = 1;
 // 16-token tiles run six pipeline stages (instead of five), and 64-token tiles
 // exist at all (five stages), when the call has at most this many experts
 // (E + S): the smaller tile tables and fewer scale groups make room.
@@ -188,7 +181,6 @@ int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, const mm::Gemm
 int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const mm::GemmArgs* g1, const mm::GemmArgs* g2,
                          void* stream);
 int mm_gemm_prepare(void);  // sets the dynamic shared-memory limits and the persistent grid sizes
-int mm_gemm_cluster(int variant);  // CTAs per cluster of the variant
 int mm_gemm_blocks(int variant);   // 128-row weight blocks per tile (2 or 4)
 int mm_gemm_epilogue_warps(int variant);  // epilogue warps per CTA (arrivals per L1 tile in the fused schedule)
 int mm_gemm_token_scale_box_rows(int variant);  // token rows per TMA box of the token scale rows

@@ -80,3 +80,49 @@ def test_binding_return_types():
     assert L.mm_profile_name.restype is ctypes.c_char_p
     assert L.mm_destroy.restype is None
     assert L.mm_run.restype is ctypes.c_int
+
+
+PAGE_NAMES = ("MegaMoE research report", "MEGAMOE_SM90_DESIGN", "MEGAMOE_SM90_DEV", "pull request #411")
+
+
+def declaration_comments():
+    """(symbol, the comment block that documents it) for every MM_API
+    declaration: the nearest comment above it, with only #defines, blank lines
+    and the other declarations of the same group in between."""
+    lines = open(os.path.join(ROOT, "include", "megamoe.h")).read().split("\n")
+    out = []
+    for i, line in enumerate(lines):
+        m = re.match(r"MM_API\s+[\w\s\*]+?\b(mm_\w+)\s*\(", line)
+        if not m:
+            continue
+        j = i - 1
+        while j >= 0:
+            t = lines[j].strip()
+            if t.endswith("*/"):
+                break
+            prev_decl = t.startswith("MM_API") or (t.endswith(");") and not t.startswith("}"))
+            cont = lines[j].startswith(" ") and not t.startswith("*") and not t.startswith("/*")
+            if t == "" or t.startswith("#define") or prev_decl or cont:
+                j -= 1
+                continue
+            j = -1
+        if j < 0:
+            out.append((m.group(1), None))
+            continue
+        k = j
+        while k >= 0 and "/*" not in lines[k]:
+            k -= 1
+        out.append((m.group(1), "\n".join(lines[k:j + 1])))
+    return out
+
+
+def test_every_boundary_call_cites_its_passage():
+    """Each declaration is documented by a comment that names the page (and
+    section) defining the operation, or says that the pages have none."""
+    decls = declaration_comments()
+    assert {n for n, _ in decls} == set(declared_symbols())
+    for name, comment in decls:
+        assert comment is not None, f"{name}: no comment directly above the declaration"
+        flat = " ".join(w for w in comment.split() if w not in ("/*", "*", "*/"))
+        assert any(p in flat for p in PAGE_NAMES) or "no counterpart" in flat, \
+            f"{name}: its comment names no page of the method"
