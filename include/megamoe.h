@@ -89,8 +89,11 @@ MM_API const char* mm_status_string(mm_status_t s);
  *   I           intermediate size; multiple of 128, 128 <= I <= 16384
  *   topk        routed slots per token, 1 <= topk <= 16
  *   num_shared  shared experts S, 0 <= S <= 4, topk + S <= 16
- * The handle owns only host memory. Returns MM_ERR_UNSUPPORTED for shapes
- * outside these limits and MM_ERR_CUDA if the device is not sm_103 (GB300). */
+ * The handle owns only host memory. It serves the device current at creation;
+ * creating it also looks up the device address of the library's fixed scratch
+ * array (see mm_run_noalloc). Returns MM_ERR_UNSUPPORTED for shapes outside
+ * these limits and MM_ERR_CUDA if the device is not sm_103 (GB300) or a CUDA
+ * query fails. */
 MM_API mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_shared);
 
 /* SwiGLU options (the SM90 design's activation_clamp / fast_math arguments,
@@ -342,9 +345,12 @@ MM_API const char* mm_profile_name(mm_handle_t h, int i);
  *   - Calls whose workspace (mm_workspace_bytes(h, T)) exceeds 32 MiB are
  *     rejected with MM_ERR_WORKSPACE_TOO_SMALL before anything is enqueued
  *     (up to T = 143 tokens at H = 7168, I = 2048, E = 256, top-8).
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture on the device.
+ *   - mm_create looks up the array's device address (cudaGetSymbolAddress,
+ *     on the device current at creation; that first use of the library's
+ *     device code on the device is also when the driver backs the array) and
+ *     keeps it in the handle, so this call does no set-up of its own. A handle
+ *     serves only the device it was created on (MM_ERR_CUDA otherwise) and
+ *     must be recreated after a cudaDeviceReset on that device.
  *   - Nothing is allocated or freed: no cudaMalloc, cudaFree or allocating
  *     library routine is called.
  *   - All calls in the process share the one array, which keeps the last

@@ -8,12 +8,21 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
-#include <mutex>
 #include <new>
 
 #include "mm_internal.h"
 
 using namespace mm;
+
+// Scratch for mm_run_noalloc: a fixed-size device array owned by this library,
+// for callers that cannot allocate device memory where they run the layer.
+// Host code must not use the symbol as an address: mm_create looks up its
+// device address (cudaGetSymbolAddress, on the device current at creation)
+// and keeps it in the handle.
+namespace {
+constexpr size_t kStaticWorkspaceBytes = size_t(32) << 20;
+static __device__ __align__(256) uint8_t mm_static_ws[kStaticWorkspaceBytes];
+}  // namespace
 
 struct mm_handle {
   int E, H, I, k, S;
@@ -22,6 +31,7 @@ struct mm_handle {
   int device;
   int num_sms;
   unsigned long long timeout_ns;
+  void* static_ws;  // device address of mm_static_ws on this handle's device
   // cached weight tensor maps (keyed by base pointer)
   const void* w1_key;
   const void* w2_key;
@@ -167,10 +177,13 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
   if (major != 10 || minor != 3) return MM_ERR_CUDA;  // built for sm_103a only
   if (!encode_fn()) return MM_ERR_CUDA;
   if (mm_gemm_prepare() != 0) return MM_ERR_CUDA;
+  void* static_ws = nullptr;
+  if (cudaGetSymbolAddress(&static_ws, mm_static_ws) != cudaSuccess || !static_ws) return MM_ERR_CUDA;
   mm_handle* h = new (std::nothrow) mm_handle();
   if (!h) return MM_ERR_INVALID_ARG;
   h->E = E; h->H = H; h->I = I; h->k = topk; h->S = num_shared;
   h->clamp = 0.0f; h->fast_math = 0; h->device = dev; h->num_sms = sms;
+  h->static_ws = static_ws;
   h->timeout_ns = 4000000000ull;
   if (const char* t = getenv("MM_DEVICE_TIMEOUT_MS")) {
     long ms = atol(t);
@@ -495,17 +508,6 @@ mm_status_t mm_debug_timeout_probe(void* ws, uint64_t timeout_ns, mm_stream_t st
 
 }  // extern "C"
 
-// Scratch for mm_run_noalloc: fixed-size device memory owned by this library
-// (callers of that entry point cannot allocate). Host code must not use the
-// symbol as an address; the device address is looked up once per device.
-namespace {
-constexpr size_t kStaticWorkspaceBytes = size_t(32) << 20;
-constexpr int kMaxDevices = 64;
-static __device__ __align__(256) uint8_t mm_static_ws[kStaticWorkspaceBytes];
-void* g_static_ws[kMaxDevices];
-std::mutex g_static_ws_mu;
-}  // namespace
-
 extern "C" {
 
 mm_status_t mm_run_noalloc(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, const int32_t* topk_idx,
@@ -513,20 +515,10 @@ mm_status_t mm_run_noalloc(mm_handle_t h, int T, const void* x_fp8, const void* 
                            void* out_bf16, mm_stream_t stream) {
   if (!h || T < 0) return MM_ERR_INVALID_ARG;
   if (make_layout(h->E, h->S, h->H, h->I, h->k, T).total > kStaticWorkspaceBytes) return MM_ERR_WORKSPACE_TOO_SMALL;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device || dev < 0 || dev >= kMaxDevices) return MM_ERR_CUDA;
-  void* ws = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_static_ws_mu);
-    if (!g_static_ws[dev]) {
-      void* p = nullptr;
-      if (cudaGetSymbolAddress(&p, mm_static_ws) != cudaSuccess || !p) return MM_ERR_CUDA;
-      g_static_ws[dev] = p;
-    }
-    ws = g_static_ws[dev];
-  }
-  return mm_run(h, T, x_fp8, x_sf, topk_idx, topk_w, w1, w1_sf, w2, w2_sf, out_bf16, ws, kStaticWorkspaceBytes,
-                stream);
+  // the array's address on the handle's device, looked up by mm_create (mm_run
+  // checks that this device is current)
+  return mm_run(h, T, x_fp8, x_sf, topk_idx, topk_w, w1, w1_sf, w2, w2_sf, out_bf16, h->static_ws,
+                kStaticWorkspaceBytes, stream);
 }
 
 void mm_destroy(mm_handle_t h) {

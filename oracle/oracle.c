@@ -400,7 +400,12 @@ void orc_l2_rows(int R, int H, int I, int w_fmt, const int32_t* expert_of_row, c
       const uint8_t* sr = w2_sf + (e * H + h) * (I / 32);
       float acc = 0.0f;
       for (long i = 0; i < I; ++i) {
+#if MUT(14)
+        float a = orc_e4m3_to_float(q[r * I + i]); /* mistake: activation scale dropped in the L2-only path */
+        (void)qsf;
+#else
         float a = orc_e4m3_to_float(q[r * I + i]) * orc_ue8m0_to_float(qsf[r * (I / 32) + i / 32]);
+#endif
         acc += a * (orc_weight(wr, i, w_fmt) * orc_ue8m0_to_float(sr[orc_sf_index(i)]));
       }
       acc2[r * H + h] = acc;

@@ -60,9 +60,11 @@ int orc_forward(const orc_dims* d, const uint8_t* x, const uint8_t* x_sf, const 
                 const uint8_t* w2_sf, uint16_t* out, float* acc1, uint8_t* q, uint8_t* qsf, uint16_t* z,
                 int nthreads);
 
-/* L2 alone from given E4M3 activations (used to pin the L2 contraction):
+/* L2 alone from given E4M3 activations ("MegaMoE on SM100/SM90" research
+ * report sec. 4.1, Linear2 phase; "MEGAMOE_SM90_DESIGN" sec. 11.1):
  * acc2[r][h] = sum_i deq(q[r][i]) * deq(W2[e_r][h][i]), float, ascending i;
- * w_fmt as in orc_dims. */
+ * w_fmt as in orc_dims. The L2 step of orc_forward computes the same sums, so
+ * the BF16 of acc2 equals orc_forward's per-slot rows z. */
 void orc_l2_rows(int R, int H, int I, int w_fmt, const int32_t* expert_of_row, const uint8_t* q,
                  const uint8_t* qsf, const uint8_t* w2, const uint8_t* w2_sf, float* acc2);
 

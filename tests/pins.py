@@ -327,6 +327,31 @@ def pin_l2(o, w, d, res):
     return fails
 
 
+def pin_l2_rows(o, w, d, res):
+    """The L2-only oracle call on the path's own E4M3 activations: within
+    Higham's FP32 summation bound of a float64 matmul of the independently
+    dequantised operands, and its BF16 equal to the path's per-slot rows."""
+    tok, ex, _ = _rows(w, d, res)
+    n = len(tok)
+    if n == 0:
+        return []
+    q, qsf = np.ascontiguousarray(res["q"][:n]), np.ascontiguousarray(res["q_sf"][:n])
+    acc2 = o.l2_rows(ex.astype(np.int32), q, qsf, d["w2"], d["w2_sf"], w.H, w.I, w.w_fmt).astype(np.float64)
+    qv = deq_x(q, qsf)
+    fails = []
+    for r in range(n):
+        W2 = deq_w(d["w2"][ex[r]], d["w2_sf"][ex[r]], w.w_fmt)  # [H, I]
+        ref = W2 @ qv[r]
+        bound = gamma(w.I) * (np.abs(W2) @ np.abs(qv[r])) + 1e-30
+        if (np.abs(acc2[r] - ref) > bound).any():
+            fails.append(f"{w.name}: L2-only accumulator outside the FP32 summation bound at row {r}")
+            break
+    z16 = torch.from_numpy(acc2.astype(np.float32)).to(torch.bfloat16).view(torch.uint16).numpy()
+    if not np.array_equal(z16, res["z"][:n]):
+        fails.append(f"{w.name}: BF16 of the L2-only accumulators differs from the path's per-slot rows")
+    return fails
+
+
 def pin_combine(o, w, d, res):
     ex = slot_experts(d["topk_idx"], w.E, w.S).reshape(w.T, w.Kp)
     pos = res["pos"].reshape(w.T, w.Kp)
@@ -418,6 +443,7 @@ def all_pins(o):
         out[f"l1[{w.name}]"] = pin_l1(o, w, d, res)
         out[f"swiglu_requant[{w.name}]"] = pin_swiglu_requant(o, w, d, res)
         out[f"l2[{w.name}]"] = pin_l2(o, w, d, res)
+        out[f"l2_rows[{w.name}]"] = pin_l2_rows(o, w, d, res)
         out[f"combine[{w.name}]"] = pin_combine(o, w, d, res)
         out[f"f64_model[{w.name}]"] = pin_f64_model(o, w, d, res)
     return out

@@ -10,7 +10,7 @@ MUTANTS = {
     1: "E2M1 nibble order", 2: "gate/up swapped", 3: "requant scale rounded down", 4: "top-k weight dropped",
     5: "W2 read transposed", 6: "activation scale dropped", 7: "combine drops a slot", 8: "SiLU sign",
     9: "unstable routing order", 10: "per-128 scale granularity", 11: "BF16 truncation", 12: "E4M3 truncation",
-    13: "FP8 weights read as E2M1",
+    13: "FP8 weights read as E2M1", 14: "L2-only rows drop the activation scale",
 }
 
 

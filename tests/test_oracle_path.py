@@ -27,6 +27,10 @@ def test_l2_within_bound(orc, case):
     assert pins.pin_l2(orc, *case) == []
 
 
+def test_l2_only_rows_within_bound_and_equal_to_the_path(orc, case):
+    assert pins.pin_l2_rows(orc, *case) == []
+
+
 def test_combine_is_bf16_of_slot_sum(orc, case):
     assert pins.pin_combine(orc, *case) == []
 
