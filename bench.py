@@ -1,10 +1,13 @@
 #!/usr/bin/env python
 """Benchmark of the GB300 MoE expert path (route -> L1 -> SwiGLU/requant -> L2 -> combine).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|tiny|mid|skewed|prefill]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload prefill|decode|tiny|mid|skewed|...]
                     [--impl ours|reference]
 
-Prints one JSON line. A step is one mm_run over the workload's batch with all
+Prints one JSON line. The default workload is prefill (T = 16384 tokens, the
+largest one-GPU configuration, tensor bound); with it, the decode workload
+(T = 8, weight-stream bound) is timed in the same process after it and
+reported under "decode". A step is one mm_run over the workload's batch with all
 inputs resident in HBM (weights generated in device memory); L2 is flushed
 between steps (a 256 MB write, outside the timed events). `value` is tokens per
 second over all ranks. `e2e` repeats the measurement through the public Python
@@ -85,50 +88,83 @@ def algorithmic(w, counts):
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling (every 20 ms) of SM clock, power and throttle reasons
+    over the whole run; `summary(windows)` keeps the samples taken inside the
+    timed windows (host wall-clock intervals)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 20):
         self.idx = gpu_index
+        self.interval_ms = interval_ms
         self.proc = None
         self.path = None
+        self.rows = []
 
     def start(self):
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.interval_ms)],
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)  # the sampler's first rows precede the first timed window
         except (OSError, FileNotFoundError):
             self.proc = None
 
     def stop(self):
         if self.proc is None:
-            return None
-        time.sleep(0.25)
+            return
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
-                    rows.append(parts)
+                if len(parts) >= 10:
+                    self.rows.append(parts)
         os.unlink(self.path)
-        if not rows:
+
+    @staticmethod
+    def _epoch(ts: str):
+        try:
+            import datetime
+            return datetime.datetime.strptime(ts, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+
+    def summary(self, windows):
+        """Median SM clock, max clock and the throttle reasons seen in the
+        samples inside the timed windows [(t0, t1), ...]; with no sample inside
+        a window (a window shorter than the sampling interval) the sample
+        nearest to each window stands in, and `in_window` says how many were
+        inside."""
+        if not self.rows:
+            return None
+        num = lambda v: float(v) if v.replace(".", "").isdigit() else None
+        samples = [(self._epoch(r[0]), num(r[2]), num(r[3]), r) for r in self.rows]
+        samples = [x for x in samples if x[0] is not None]
+        inside = [x for x in samples if any(a <= x[0] <= b for a, b in windows)]
+        picked = list(inside)
+        if not inside:
+            for a, b in windows:
+                mid = (a + b) / 2
+                near = min(samples, key=lambda x: abs(x[0] - mid), default=None)
+                if near is not None and near not in picked:
+                    picked.append(near)
+        if not picked:
+            return None
+        sm = [x[1] for x in picked if x[1] is not None]
+        mx = [x[2] for x in picked if x[2] is not None]
+        reasons = sorted({self.REASONS[i] for x in picked for i in range(4) if x[3][6 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(picked), "in_window": len(inside),
+                "interval_ms": self.interval_ms, "timed_windows_s": round(sum(b - a for a, b in windows), 4)}
 
 
 def max_over_ranks(dist, total_ms, e2e_ms, device):
@@ -217,16 +253,15 @@ def workload_config(w):
 
 
 # ----------------------------------------------------------------------------- our arm
-def run_ours(args, world, rank, local):
+def measure(args, w, dist, steps, warmup, with_e2e, windows):
+    """Times one workload: K whole forwards device-timed (nothing recorded
+    between their kernels), K more with an event between kernels (per-kernel
+    durations), then optionally the end-to-end pass. Appends the host
+    wall-clock interval of every timed pass to `windows` (for the clock
+    record). Returns the timings and the algorithmic work of one step."""
     import torch
     import moe_expert_layer_scan_gb300 as mm
 
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    w = workloads.CONFIGS[args.workload]
     d = workloads.device_inputs(w)
     moe = mm.MegaMoE(w.E, w.H, w.I, w.k, w.S, swiglu_clamp=w.clamp, schedule=args.schedule, weight_format=w.w_fmt,
                      tiles=args.tiles)
@@ -235,62 +270,97 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     ins = (d["x"], d["x_sf"], d["topk_idx"], d["topk_w"], d["w1"], d["w1_sf"], d["w2"], d["w2_sf"])
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.zero_()
         moe.run(*ins, out=out)
     torch.cuda.synchronize()
     if moe.status() != 0:
         raise RuntimeError(f"device status {moe.status()} after warm-up")
-    counts = torch.empty(w.Ep, dtype=torch.int32)
     v = moe.views(w.T)
-    counts.copy_(moe.ws[v.counts - moe.ws.data_ptr():v.counts - moe.ws.data_ptr() + 4 * w.Ep].view(torch.int32).cpu())
-    alg = algorithmic(w, counts.numpy())
+    off = v.counts - moe.ws.data_ptr()
+    counts = moe.ws[off:off + 4 * w.Ep].view(torch.int32).cpu().numpy()
+    alg = algorithmic(w, counts)
 
-    # ---- device-resident timing: K whole forwards, nothing recorded between their kernels
+    # device-resident timing: K whole forwards, nothing recorded between their kernels
     # (so each kernel's prologue overlaps its predecessor's tail as in production) ...
-    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    clocks = Clocks(torch.cuda.current_device()) if rank == 0 else None
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    if clocks:
-        clocks.start()
-    for i in range(args.steps):
+    t_host = time.time()
+    for i in range(steps):
         flush.zero_()
         e0[i].record()
         moe.run(*ins, out=out)
         e1[i].record()
     torch.cuda.synchronize()
+    windows.append((t_host, time.time()))
     # ... then K more with an event between every two kernels, for the per-kernel durations
     mm.mm_profile_enable(moe.h, True)
     per_kernel = []
-    for i in range(args.steps):
+    t_host = time.time()
+    for i in range(steps):
         flush.zero_()
         moe.run(*ins, out=out)
         per_kernel.append(mm.mm_profile_stages(moe.h))
     torch.cuda.synchronize()
+    windows.append((t_host, time.time()))
     mm.mm_profile_enable(moe.h, False)
-    clk = clocks.stop() if clocks else None
     if dist:
         dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in zip(e0, e1)]
-    total_ms = sum(step_ms)
+    total_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1))
     if moe.status() != 0:
         raise RuntimeError(f"device status {moe.status()} after the timed steps")
 
-    # ---- end-to-end through the public API with host buffers
     e2e_ms, h2d, d2h = None, 0, 0
-    if not args.no_e2e:
-        e2e_ms, h2d, d2h = measure_e2e(args, w, d, moe, out, flush, dist)
+    if with_e2e:
+        e2e_ms, h2d, d2h = measure_e2e(args, w, d, moe, out, dist, steps, windows)
+    res = dict(total_ms=total_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, per_kernel=per_kernel, alg=alg,
+               tile_width=mm.mm_token_tile_width(moe.h, w.T), launches=moe.launches(w.T))
+    del moe, d, out, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = workloads.CONFIGS[args.workload]
+    clocks = Clocks(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    windows, dec_windows = [], []
+    main = measure(args, w, dist, args.steps, args.warmup, not args.no_e2e, windows)
+    dec = None
+    if world == 1 and w.name == "prefill" and not args.no_decode_record:
+        # the decode-shape line timed in the same process (both targets of the method in one run)
+        dw = workloads.CONFIGS["decode"]
+        dec = measure(args, dw, None, DECODE_RECORD_STEPS, args.warmup, False, dec_windows)
+        dec["w"] = dw
+    if clocks:
+        clocks.stop()
+    total_ms, e2e_ms = main["total_ms"], main["e2e_ms"]
     if dist:
         total_ms, e2e_ms = max_over_ranks(dist, total_ms, e2e_ms, device="cuda")
     if rank != 0:
         return
-    report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk)
+    main["total_ms"], main["e2e_ms"] = total_ms, e2e_ms
+    clk = clocks.summary(windows) if clocks else None
+    dclk = clocks.summary(dec_windows) if clocks and dec else None
+    report(args, w, world, main, clk, dec=dec, dec_clk=dclk)
 
 
-def measure_e2e(args, w, d, moe, out, flush, dist):
+# steps of the decode-shape record (its forwards take ~0.26 ms: 200 of them fill a few clock samples)
+DECODE_RECORD_STEPS = 200
+
+
+def measure_e2e(args, w, d, moe, out, dist, steps, windows):
     """Throughput through the public call with the inputs in pinned host memory:
     every step copies its inputs host->device, runs the forward and copies the
     output device->host. As a serving loop would, the copies run on two copy
@@ -344,29 +414,30 @@ def measure_e2e(args, w, d, moe, out, flush, dist):
     if dist:
         dist.barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host = time.time()
     t0.record(s_in)
-    for i in range(args.steps):
+    for i in range(steps):
         step(i)
     s_out.wait_stream(comp)
     t1.record(s_out)
     torch.cuda.synchronize()
+    windows.append((t_host, time.time()))
     if dist:
         dist.barrier()
     e2e_ms = t0.elapsed_time(t1)
-    last = (args.steps - 1) & 1
+    last = (steps - 1) & 1
     assert torch.equal(hout[last], douts[last].cpu()), "end-to-end output differs from the device output"
     return e2e_ms, h2d, d2h
 
 
-def report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk):
-    import moe_expert_layer_scan_gb300 as mm
-    ms = total_ms / args.steps
-    tokens = w.T * world
-    value = tokens / (ms / 1e3)
-    kern = {n: statistics.mean(p[n] for p in per_kernel) for n in per_kernel[0]}
+def roofline_of(w, alg, kern, ms_step):
+    """Roofline records of one step: the dominant kernel's (the fused grouped
+    GEMM, or with one launch per linear the L1 GEMM, which holds two thirds of
+    the weights and FLOPs) from its mean event duration, and the whole
+    forward's (all launches) from the step time. Bound by whichever of bytes
+    over HBM bandwidth and FLOPs over the FP8 tensor peak takes longer for the
+    dominant kernel."""
     peaks, peak_src = load_peaks()
-    # the dominant kernel: the fused grouped GEMM (both linears in one launch)
-    # or, with one launch per linear, the L1 GEMM (two thirds of the weights and FLOPs)
     fused = "gemm" in kern
     k_name = "gemm" if fused else "l1_gemm"
     k_ms = kern.get(k_name)
@@ -374,33 +445,61 @@ def report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk
     k_flops = alg["flops"] if fused else alg["l1_flops"]
     hbm = float(peaks["hbm_gbs"])
     fp8_peak = float(peaks["bf16_tflops"]) * FP8_OVER_BF16
-    balance = fp8_peak * 1e12 / (hbm * 1e9)
-    if k_flops / k_bytes < balance:
-        achieved = k_bytes / (k_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"}
-    else:
-        achieved = k_flops / (k_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp8_peak,
-                "peak_source": f"{peak_src} bf16_tflops (burst) x {FP8_OVER_BF16} nominal FP8/BF16 ratio"}
+    tensor_bound = k_flops / k_bytes >= fp8_peak * 1e12 / (hbm * 1e9)
+    hbm_src = f"{peak_src} hbm_gbs (STREAM-style copy)"
+    tc_src = f"{peak_src} bf16_tflops (burst) x {FP8_OVER_BF16} nominal FP8/BF16 ratio"
+
+    def rec(bytes_, flops, ms):
+        if tensor_bound:
+            a = flops / (ms / 1e3) / 1e12
+            return {"bound": "tensor", "achieved": a, "peak": fp8_peak, "unit": "TFLOP/s", "frac": a / fp8_peak,
+                    "peak_source": tc_src}
+        a = bytes_ / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": a, "peak": hbm, "unit": "GB/s", "frac": a / hbm, "peak_source": hbm_src}
+
+    roof = rec(k_bytes, k_flops, k_ms)
     tr = NCU_TRAFFIC.get(w.name)
     roof["traffic"] = tr["bytes"] if tr and tr.get("src") == gemm_source_hash() and tr.get("kernel") == k_name \
         else None
     roof["kernel"] = ("gemm_kernel<fused> (mm_gemm.cu): L1 then L2 tiles in one launch" if fused
                       else "gemm_kernel<L1> (mm_gemm.cu)")
+    roof["scope"] = "dominant kernel, mean CUDA-event duration over the per-kernel pass"
     roof["algorithmic_bytes_per_launch"] = k_bytes
     roof["algorithmic_flops_per_launch"] = k_flops
     roof["kernel_ms"] = k_ms
+    step = rec(alg["l1_bytes"] + alg["l2_bytes"], alg["flops"], ms_step)
+    step["scope"] = ("whole forward (route, gather, both grouped GEMMs, combine) over ms_per_step: "
+                     "the fraction of the roofline the fused MoE path reaches")
+    step["algorithmic_bytes"] = alg["l1_bytes"] + alg["l2_bytes"]
+    step["algorithmic_flops"] = alg["flops"]
+    return roof, step, ("fused" if fused else "split")
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+
+def clock_record(clk, ms):
+    if not clk:
+        return clk
+    clk = dict(clk)
+    if clk.get("sm_mhz"):
+        clk["ms_per_step_x_sm_mhz"] = ms * clk["sm_mhz"]
+    return clk
+
+
+def report(args, w, world, main, clk, dec=None, dec_clk=None):
+    steps = args.steps
+    ms = main["total_ms"] / steps
+    tokens = w.T * world
+    value = tokens / (ms / 1e3)
+    alg = main["alg"]
+    kern = {n: statistics.mean(p[n] for p in main["per_kernel"]) for n in main["per_kernel"][0]}
+    roof, roof_step, sched = roofline_of(w, alg, kern, ms)
+    e2e_ms = main["e2e_ms"]
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": dtype_of(w), "data": "synthetic",
-            "config": dict(workload_config(w), parallelism=f"{world} independent replicas" if world > 1 else "1 GPU",
-                           gemm_schedule=("fused" if "gemm" in kern else "split")
-                           + (" (auto)" if args.schedule == "auto" else ""),
-                           token_tiles=f"{mm.mm_token_tile_width(moe.h, w.T)}"
-                           + (" (auto)" if args.tiles == -1 else "")),
+            "config": workload_config(w),
+            "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU",
+            "gemm_schedule": sched + (" (auto)" if args.schedule == "auto" else ""),
+            "token_tiles": f"{main['tile_width']}" + (" (auto)" if args.tiles == -1 else ""),
             "tflops": alg["flops"] * world / (ms / 1e3) / 1e12,
             "hbm_gbs_whole_step": (alg["l1_bytes"] + alg["l2_bytes"]) / (ms / 1e3) / 1e9,
             "kernels_ms": kern,
@@ -408,14 +507,29 @@ def report(args, w, world, total_ms, e2e_ms, h2d, d2h, per_kernel, alg, moe, clk
                                "kernels (which serialises them); ms_per_step is the pass without those events",
             "rows": alg["rows"], "experts_touched": alg["touched"],
             "roofline": roof,
+            "roofline_step": roof_step,
             "e2e": None if e2e_ms is None else
-            {"value": tokens / (e2e_ms / args.steps / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / args.steps,
+            {"value": tokens / (e2e_ms / steps / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": main["h2d"],
+             "d2h_bytes_per_step": main["d2h"], "ms_per_step": e2e_ms / steps,
              "method": "pinned host inputs and output; per step input copy, forward, output copy, the copies on "
                        "two streams overlapping the neighbouring steps' forwards; wall time over the steps; no L2 "
                        "flush (every step streams more than L2)"},
-            "gpu_launches": moe.launches(w.T) * args.steps,
-            "clocks": clk}
+            "gpu_launches": main["launches"] * steps,
+            "clocks": clock_record(clk, ms)}
+    if dec is not None:
+        dw = dec["w"]
+        dsteps = DECODE_RECORD_STEPS
+        dms = dec["total_ms"] / dsteps
+        dkern = {n: statistics.mean(p[n] for p in dec["per_kernel"]) for n in dec["per_kernel"][0]}
+        droof, dstep, dsched = roofline_of(dw, dec["alg"], dkern, dms)
+        line["decode"] = {"config": workload_config(dw), "steps": dsteps, "warmup": args.warmup, "ms_per_step": dms,
+                          "tokens_per_s": dw.T / (dms / 1e3), "gemm_schedule": dsched,
+                          "token_tiles": f"{dec['tile_width']}", "kernels_ms": dkern,
+                          "rows": dec["alg"]["rows"], "experts_touched": dec["alg"]["touched"],
+                          "roofline": droof, "roofline_step": dstep, "gpu_launches": dec["launches"] * dsteps,
+                          "clocks": clock_record(dec_clk, dms),
+                          "note": "the decode workload timed in the same process after the main line, same method "
+                                  "(device-timed forwards, L2 flushed between steps; per-kernel pass after)"}
     if world == 1 and not args.no_cpu_baseline:
         n_tok = sample_tokens_for(w)
         times, nt, ne, cores = time_oracle(w, n_tok, reps=1)
@@ -430,10 +544,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode", choices=list(workloads.CONFIGS))
+    ap.add_argument("--workload", default="prefill", choices=list(workloads.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
+    ap.add_argument("--no-decode-record", action="store_true",
+                    help="with the prefill workload, skip the decode-shape record timed after it")
     ap.add_argument("--tiles", type=int, default=-1, choices=[-1, 16, 64, 112, 224],
                     help="token-tile width (-1: the library's choice)")
     ap.add_argument("--schedule", default="auto", choices=["auto", "fused", "split"],
