@@ -114,25 +114,32 @@ class Oracle:
                 nthreads: int | None = None, weight_in_combine: bool = False):
         """Run the path. dims: T,H,I,E,k,S,clamp. Returns dict(out=uint16 [T,H], ...)."""
         T, H, I, E, k, S = (int(dims[n]) for n in ("T", "H", "I", "E", "k", "S"))
-        w_fmt = int(dims.get("w_fmt", 0))  # 0: E2M1 weights (MXFP4), 1: E4M3 weights (MXFP8)
+        # 0: E2M1 weights (MXFP4), 1: E4M3 weights (MXFP8), both UE8M0 per 32;
+        # 2: the float-scale FP8 recipe (float32 scales per 128 x 128 weight block and per (row, 128))
+        w_fmt = int(dims.get("w_fmt", 0))
         d = _Dims(T, H, I, E, k, S, float(dims.get("clamp", 0.0)), int(weight_in_combine), w_fmt)
         wb = 1 if w_fmt else 2  # weight elements per byte is 2 for E2M1
         R = T * (k + S)
         c = np.ascontiguousarray
-        x, x_sf = c(x, np.uint8), c(x_sf, np.uint8)
+        sfd = np.float32 if w_fmt == 2 else np.uint8
+        x, x_sf = c(x, np.uint8), c(x_sf, sfd)
         topk_idx, topk_w = c(topk_idx, np.int32), c(topk_w, np.float32)
-        w1, w1_sf, w2, w2_sf = c(w1, np.uint8), c(w1_sf, np.uint8), c(w2, np.uint8), c(w2_sf, np.uint8)
-        assert x.shape == (T, H) and x_sf.shape == (T, H // 32)
+        w1, w1_sf, w2, w2_sf = c(w1, np.uint8), c(w1_sf, sfd), c(w2, np.uint8), c(w2_sf, sfd)
         assert topk_idx.shape == (T, k) and topk_w.shape == (T, k)
-        assert w1.size == (E + S) * 2 * I * H // wb and w1_sf.size == (E + S) * 2 * I * H // 32
-        assert w2.size == (E + S) * H * I // wb and w2_sf.size == (E + S) * H * I // 32
+        assert w1.size == (E + S) * 2 * I * H // wb and w2.size == (E + S) * H * I // wb
+        if w_fmt == 2:
+            assert x.shape == (T, H) and x_sf.shape == (T, H // 128)
+            assert w1_sf.size == (E + S) * 2 * I * H // (128 * 128) and w2_sf.size == (E + S) * H * I // (128 * 128)
+        else:
+            assert x.shape == (T, H) and x_sf.shape == (T, H // 32)
+            assert w1_sf.size == (E + S) * 2 * I * H // 32 and w2_sf.size == (E + S) * H * I // 32
         out = np.zeros((T, H), np.uint16)
         res = dict(out=out)
         acc1 = q = qsf = None
         if intermediates:
             acc1 = np.zeros((R, 2 * I), np.float32)
             q = np.zeros((R, I), np.uint8)
-            qsf = np.zeros((R, I // 32), np.uint8)
+            qsf = np.zeros((R, I // 128), np.float32) if w_fmt == 2 else np.zeros((R, I // 32), np.uint8)
             res.update(acc1=acc1, q=q, q_sf=qsf)
         z = np.zeros((R, H), np.uint16)
         res["z"] = z
@@ -149,9 +156,10 @@ class Oracle:
         expert_of_row = np.ascontiguousarray(expert_of_row, np.int32)
         R = expert_of_row.size
         acc2 = np.zeros((R, H), np.float32)
+        sfd = np.float32 if w_fmt == 2 else np.uint8
         self.lib.orc_l2_rows(R, H, I, int(w_fmt), _p(expert_of_row), _p(np.ascontiguousarray(q, np.uint8)),
-                             _p(np.ascontiguousarray(q_sf, np.uint8)), _p(np.ascontiguousarray(w2, np.uint8)),
-                             _p(np.ascontiguousarray(w2_sf, np.uint8)), _p(acc2))
+                             _p(np.ascontiguousarray(q_sf, sfd)), _p(np.ascontiguousarray(w2, np.uint8)),
+                             _p(np.ascontiguousarray(w2_sf, sfd)), _p(acc2))
         return acc2
 
 

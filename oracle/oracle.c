@@ -30,6 +30,17 @@
  *  - shared experts sit at expert indices E..E+S-1, slot k+s of every token,
  *    with weight 1; a topk_idx of -1 disables its slot.
  *
+ * The float-scale FP8 recipe (w_fmt 2; "MEGAMOE_SM90_DESIGN" sec. 5.3 scale
+ * application, sec. 10.1 steps 4-5 exact float L2-activation scale, sec. 15.2
+ * weight scale layout (E, N/128, K/128)): every weight and activation element
+ * is E4M3 with a float32 scale per 128 along K (weights: per 128 x 128 block).
+ * Readings: each 128-long K block's partial sum is taken in FP32 over the
+ * unscaled E4M3 products, multiplied by (activation scale x weight scale) and
+ * added to the FP32 accumulator in ascending block order; the L2-activation
+ * scale is one float32 per (row, 128 along I), amax / 448 by one IEEE
+ * division (1 when amax is 0), and the E4M3 code is the nearest-even
+ * saturating encoding of y / scale.
+ *
  * Build with -ffp-contract=off. Defining ORC_MUTANT to a non-zero value plants
  * one deliberate mistake (used only to show that the pin tests catch it).
  */
@@ -326,6 +337,91 @@ static void orc_one_row(const orc_job* J, long r, float* xh, float* a1, float* y
   }
 }
 
+/* Float scale of a 128-long block: the float32 stored at element i of a
+ * float32 array passed as bytes. */
+static float orc_f32_at(const uint8_t* base, long i) {
+  float v;
+  memcpy(&v, base + 4 * i, 4);
+  return v;
+}
+
+/* One pool row under the float-scale FP8 recipe (w_fmt 2): L1 per 128-K
+ * block with float scales, SwiGLU x weight, float per-128 requantise, L2 per
+ * 128-K block, BF16. */
+static void orc_one_row_f128(const orc_job* J, long r, float* xh, float* a1, float* y, float* qh) {
+  const orc_dims* d = J->d;
+  const int H = d->H, I = d->I, k = d->k, Kp = d->k + d->S;
+  const long HB = H / 128, IB = I / 128;
+  long s = J->perm[r], t = s / Kp;
+  int j = (int)(s % Kp);
+  int e = (j < k) ? J->topk_idx[t * k + j] : d->E + (j - k);
+  float wgt = (j < k) ? J->topk_w[t * k + j] : 1.0f;
+
+  /* unscaled E4M3 activation row; its scales stay per block */
+  for (long kk = 0; kk < H; ++kk) xh[kk] = orc_e4m3_to_float(J->x[t * H + kk]);
+  /* L1: acc1[n] = sum_b (sx[t][b] * sw1[e][n/128][b]) * sum_{k in b} x[k] * W1[e][n][k] */
+  for (long n = 0; n < 2L * I; ++n) {
+    const uint8_t* wr = J->w1 + ((long)e * 2 * I + n) * H;
+    float acc = 0.0f;
+    for (long b = 0; b < HB; ++b) {
+      float part = 0.0f;
+      for (long kk = 128 * b; kk < 128 * b + 128; ++kk) part += xh[kk] * orc_e4m3_to_float(wr[kk]);
+#if MUT(15)
+      float sc = orc_f32_at(J->x_sf, t * HB + b); /* mistake: weight block scale dropped */
+#else
+      float sc = orc_f32_at(J->x_sf, t * HB + b) * orc_f32_at(J->w1_sf, ((long)e * (2 * I / 128) + n / 128) * HB + b);
+#endif
+      acc += part * sc;
+    }
+    a1[n] = acc;
+  }
+  if (J->acc1) memcpy(J->acc1 + r * 2L * I, a1, sizeof(float) * 2 * (size_t)I);
+
+  /* SwiGLU: y = silu(clamp(g)) * clamp(u) * w */
+  for (long n = 0; n < I; ++n) {
+    float g = a1[n], u = a1[I + n];
+    if (d->clamp > 0.0f) {
+      g = fminf(fmaxf(g, -d->clamp), d->clamp);
+      u = fminf(fmaxf(u, -d->clamp), d->clamp);
+    }
+    float silu = g / (1.0f + expf(-g));
+    float v = silu * u;
+    if (!d->weight_in_combine) v = v * wgt;
+    y[n] = v;
+  }
+  /* requantise per 128 along I: float scale amax / 448, E4M3 of y / scale */
+  float qs[128]; /* the row's L2-activation scales (I / 128 <= 128) */
+  for (long b = 0; b < IB; ++b) {
+    float amax = 0.0f;
+    for (long n = 128 * b; n < 128 * b + 128; ++n) amax = fmaxf(amax, fabsf(y[n]));
+    float sc = amax / 448.0f;
+    if (!(sc > 0.0f)) sc = 1.0f;
+#if MUT(16)
+    sc = amax / 256.0f; /* mistake: scale from the wrong format maximum */
+    if (!(sc > 0.0f)) sc = 1.0f;
+#endif
+    for (long n = 128 * b; n < 128 * b + 128; ++n) {
+      uint8_t qq = orc_float_to_e4m3(y[n] / sc);
+      if (J->q) J->q[r * I + n] = qq;
+      qh[n] = orc_e4m3_to_float(qq);
+    }
+    if (J->qsf) memcpy(J->qsf + 4 * (r * IB + b), &sc, 4);
+    qs[b] = sc;
+  }
+  /* L2: z[h] = bf16(sum_b (sq[b] * sw2[e][h/128][b]) * sum_{i in b} q[i] * W2[e][h][i]) */
+  for (long h = 0; h < H; ++h) {
+    const uint8_t* wr = J->w2 + ((long)e * H + h) * I;
+    float acc = 0.0f;
+    for (long b = 0; b < IB; ++b) {
+      float part = 0.0f;
+      for (long i = 128 * b; i < 128 * b + 128; ++i) part += qh[i] * orc_e4m3_to_float(wr[i]);
+      float sc = qs[b] * orc_f32_at(J->w2_sf, ((long)e * HB + h / 128) * IB + b);
+      acc += part * sc;
+    }
+    J->z[r * H + h] = orc_float_to_bf16(acc);
+  }
+}
+
 static void* orc_worker(void* arg) {
   const orc_job* J = (const orc_job*)arg;
   const orc_dims* d = J->d;
@@ -333,7 +429,10 @@ static void* orc_worker(void* arg) {
   float* a1 = (float*)malloc(sizeof(float) * 2 * (size_t)d->I);
   float* y = (float*)malloc(sizeof(float) * (size_t)d->I);
   float* qh = (float*)malloc(sizeof(float) * (size_t)d->I);
-  for (long r = J->th; r < J->nrows; r += J->nth) orc_one_row(J, r, xh, a1, y, qh);
+  for (long r = J->th; r < J->nrows; r += J->nth) {
+    if (d->w_fmt == 2) orc_one_row_f128(J, r, xh, a1, y, qh);
+    else orc_one_row(J, r, xh, a1, y, qh);
+  }
   free(xh); free(a1); free(y); free(qh);
   return NULL;
 }
@@ -343,7 +442,8 @@ int orc_forward(const orc_dims* d, const uint8_t* x, const uint8_t* x_sf, const 
                 const uint8_t* w2_sf, uint16_t* out, float* acc1, uint8_t* q, uint8_t* qsf, uint16_t* z,
                 int nthreads) {
   if (!d || d->T < 0 || d->H % 32 || d->I % 32 || d->E < 1 || d->k < 1 || d->S < 0) return -1;
-  if (d->w_fmt != 0 && d->w_fmt != 1) return -1;
+  if (d->w_fmt != 0 && d->w_fmt != 1 && d->w_fmt != 2) return -1;
+  if (d->w_fmt == 2 && (d->H % 128 || d->I % 128 || d->I > 16384)) return -1;
   const int T = d->T, H = d->H, k = d->k, Kp = d->k + d->S, Ep = d->E + d->S;
   long R = (long)T * Kp;
   int32_t* counts = (int32_t*)malloc(sizeof(int32_t) * ((size_t)Ep + 1));
@@ -393,6 +493,24 @@ int orc_forward(const orc_dims* d, const uint8_t* x, const uint8_t* x_sf, const 
 
 void orc_l2_rows(int R, int H, int I, int w_fmt, const int32_t* expert_of_row, const uint8_t* q,
                  const uint8_t* qsf, const uint8_t* w2, const uint8_t* w2_sf, float* acc2) {
+  if (w_fmt == 2) {
+    const long HB = H / 128, IB = I / 128;
+    for (long r = 0; r < R; ++r) {
+      long e = expert_of_row[r];
+      for (long h = 0; h < H; ++h) {
+        const uint8_t* wr = w2 + (e * H + h) * I;
+        float acc = 0.0f;
+        for (long b = 0; b < IB; ++b) {
+          float part = 0.0f;
+          for (long i = 128 * b; i < 128 * b + 128; ++i)
+            part += orc_e4m3_to_float(q[r * I + i]) * orc_e4m3_to_float(wr[i]);
+          acc += part * (orc_f32_at(qsf, r * IB + b) * orc_f32_at(w2_sf, (e * HB + h / 128) * IB + b));
+        }
+        acc2[r * H + h] = acc;
+      }
+    }
+    return;
+  }
   for (long r = 0; r < R; ++r) {
     long e = expert_of_row[r];
     for (long h = 0; h < H; ++h) {

@@ -58,12 +58,21 @@ def unpack_e2m1(packed) -> np.ndarray:
 
 def deq_w(codes, sf, fmt: int = 0) -> np.ndarray:
     """Weights from their codes: E2M1 packed two per byte (fmt 0, OCP MXFP4) or
-    E4M3 one per byte (fmt 1, OCP MXFP8), times the UE8M0 scale of each 32."""
+    E4M3 one per byte (fmt 1, OCP MXFP8), times the UE8M0 scale of each 32; or
+    (fmt 2, the float-scale recipe) E4M3 times the float32 scale of each
+    128 x 128 block (sf [..., rows/128, K/128])."""
+    if fmt == 2:
+        return deq_e4m3(codes) * np.repeat(np.repeat(np.asarray(sf, np.float64), 128, axis=-2), 128, axis=-1)
     vals = deq_e4m3(codes) if fmt else e2m1_table()[unpack_e2m1(codes)]
     return vals * np.repeat(deq_ue8m0(sf), 32, axis=-1)
 
 
 def deq_x(x, sf) -> np.ndarray:
+    """Activations: E4M3 times the UE8M0 scale of each 32, or (float32 scales,
+    the float-scale recipe) times the float scale of each 128."""
+    sf = np.asarray(sf)
+    if sf.dtype == np.float32:
+        return deq_e4m3(x) * np.repeat(sf.astype(np.float64), 128, axis=-1)
     return deq_e4m3(x) * np.repeat(deq_ue8m0(sf), 32, axis=-1)
 
 
@@ -213,7 +222,16 @@ PIN_WORKLOADS = [
     workloads.Workload("pin_shared", T=12, H=256, I=128, E=5, k=3, S=1, clamp=0.75, zipf=1.2, seed=21),
     # FP8 (MXFP8) weights
     workloads.Workload("pin_fp8w", T=10, H=256, I=128, E=4, k=2, S=1, seed=22, w_fmt=1),
+    # the float-scale FP8 recipe (float32 scales per 128 x 128 weight block and per (row, 128))
+    workloads.Workload("pin_fp8f128", T=10, H=384, I=256, E=4, k=2, S=1, clamp=2.0, seed=23, w_fmt=2),
 ]
+
+
+def summation_terms(w, K: int) -> int:
+    """Roundings on one accumulator's path: K for an ascending FP32 sum; for
+    the float-scale recipe 128 per block sum, one each for the scale product,
+    the scaled partial and its addition, and one per block in the outer sum."""
+    return 128 + 3 + K // 128 if w.w_fmt == 2 else K
 
 
 def run_case(o, w, topk_idx=None, topk_w=None):
@@ -241,7 +259,7 @@ def pin_l1(o, w, d, res):
     for r in range(len(tok)):
         W1 = deq_w(d["w1"][ex[r]], d["w1_sf"][ex[r]], w.w_fmt)  # [2I, H]
         ref = W1 @ x[tok[r]]
-        bound = gamma(w.H) * (np.abs(W1) @ np.abs(x[tok[r]])) + 1e-30
+        bound = gamma(summation_terms(w, w.H)) * (np.abs(W1) @ np.abs(x[tok[r]])) + 1e-30
         err = np.abs(res["acc1"][r].astype(np.float64) - ref)
         if (err > bound).any():
             fails.append(f"{w.name}: L1 accumulator outside the FP32 summation bound at row {r}")
@@ -287,6 +305,8 @@ def pin_swiglu_requant(o, w, d, res):
         g, u = np.clip(g, -w.clamp, w.clamp), np.clip(u, -w.clamp, w.clamp)
     y = _silu64(g) * u * wt[:, None]
     q, qsf = res["q"][: len(wt)], res["q_sf"][: len(wt)]
+    if w.w_fmt == 2:
+        return _pin_requant_float(w, y, q, qsf)
     s = np.repeat(deq_ue8m0(qsf), 32, axis=1)
     fails = []
     amax = np.abs(y).reshape(len(wt), I // 32, 32).max(axis=2)
@@ -310,6 +330,31 @@ def pin_swiglu_requant(o, w, d, res):
     return fails
 
 
+def _pin_requant_float(w, y, q, qsf):
+    """Float-scale recipe: the scale of each (row, 128) is amax / 448 (within
+    float32 rounding of the float64 amax), and each E4M3 code is torch's cast
+    of y / scale, at most one E4M3 step off where float32 vs float64 decides."""
+    n, I = y.shape
+    fails = []
+    amax = np.abs(y).reshape(n, I // 128, 128).max(axis=2)
+    sc = qsf.astype(np.float64)
+    want = np.where(amax > 0, amax / 448.0, 1.0)
+    if (np.abs(sc - want) > 2.0 ** -20 * want).any():
+        fails.append(f"{w.name}: float L2-activation scale is not amax/448")
+    s = np.repeat(sc, 128, axis=1)
+    ref_q = torch.from_numpy(np.clip(y / s, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got_v, ref_v = deq_e4m3(q), deq_e4m3(ref_q)
+    diff = got_v != ref_v
+    if diff.mean() > 2e-3:
+        fails.append(f"{w.name}: {diff.mean():.2%} of E4M3 L2 activations differ from torch's cast")
+    ulp = np.maximum(np.abs(y / s) * 2.0 ** -3, 2.0 ** -9)
+    if (np.abs(got_v - ref_v) > ulp * 1.0001).any():
+        fails.append(f"{w.name}: an E4M3 L2 activation is more than one step off")
+    if (np.abs(y / s) > 448 * (1 + 1e-5)).any():
+        fails.append(f"{w.name}: an L2 activation saturates")
+    return fails
+
+
 def pin_l2(o, w, d, res):
     tok, ex, _ = _rows(w, d, res)
     n = len(tok)
@@ -320,7 +365,7 @@ def pin_l2(o, w, d, res):
         W2 = deq_w(d["w2"][ex[r]], d["w2_sf"][ex[r]], w.w_fmt)  # [H, I]
         ref = W2 @ qv[r]
         tot = np.abs(W2) @ np.abs(qv[r])
-        bound = gamma(w.I) * tot * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(ref) + 1e-30
+        bound = gamma(summation_terms(w, w.I)) * tot * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(ref) + 1e-30
         if (np.abs(z[r] - ref) > bound).any():
             fails.append(f"{w.name}: L2 BF16 row {r} outside FP32-sum + BF16-rounding bound")
             break
@@ -342,7 +387,7 @@ def pin_l2_rows(o, w, d, res):
     for r in range(n):
         W2 = deq_w(d["w2"][ex[r]], d["w2_sf"][ex[r]], w.w_fmt)  # [H, I]
         ref = W2 @ qv[r]
-        bound = gamma(w.I) * (np.abs(W2) @ np.abs(qv[r])) + 1e-30
+        bound = gamma(summation_terms(w, w.I)) * (np.abs(W2) @ np.abs(qv[r])) + 1e-30
         if (np.abs(acc2[r] - ref) > bound).any():
             fails.append(f"{w.name}: L2-only accumulator outside the FP32 summation bound at row {r}")
             break

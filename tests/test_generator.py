@@ -56,3 +56,33 @@ def test_fp8_weights_quantise_the_same_values():
     err = np.abs(v8 - v4).max()
     assert err <= 0.5 * np.abs(v4).max()   # same draws (FP4 is the coarse one)
     assert np.corrcoef(v4.ravel(), v8.ravel())[0, 1] > 0.98
+
+
+def test_float_recipe_inputs_follow_their_definition():
+    """Float-scale recipe inputs, rebuilt from single normal draws: each
+    activation group of 128 has the scale float32(amax) / 448 and torch's E4M3
+    cast of v / scale; each 128 x 128 weight block has a scale in
+    [std * 5/448, 2 * std * 5/448) and the E4M3 cast of w / scale."""
+    import torch
+    lib = workloads._lib_host()
+    w = workloads.Workload("gf", T=3, H=256, I=128, E=2, k=1, seed=11, w_fmt=2)
+    x, xs = workloads.x_host(w)
+    assert x.shape == (3, 256) and xs.shape == (3, 2) and xs.dtype == np.float32
+    key = lib.syn_key(w.seed, 1)
+    raw = np.array([lib.syn_normal_at(key, i) for i in range(3 * 256)], np.float32)
+    v = torch.from_numpy(raw).to(torch.bfloat16).to(torch.float32).numpy().reshape(3, 2, 128)
+    sc = np.abs(v).max(axis=2) / np.float32(448.0)
+    assert np.array_equal(xs, sc.astype(np.float32))
+    codes = torch.from_numpy(np.clip(v / sc[..., None], -448, 448)).to(torch.float8_e4m3fn)
+    assert np.array_equal(x.reshape(3, 2, 128), codes.view(torch.uint8).numpy())
+    c, s = workloads.w_host(w, workloads.TAG_W1)
+    assert c.shape == (2, 256, 256) and s.shape == (2, 2, 2) and s.dtype == np.float32
+    lo = np.float32(w.std1) * np.float32(5.0 / 448.0)
+    assert (s >= lo * (1 - 1e-6)).all() and (s < 2 * lo).all()
+    assert len(np.unique(s)) == s.size                       # an independent draw per block
+    wkey = lib.syn_key(w.seed, workloads.TAG_W1)
+    for e, n, kk in ((0, 0, 0), (1, 200, 130), (1, 255, 255), (0, 129, 7)):
+        idx = (e * 256 + n) * 256 + kk
+        val = np.float32(lib.syn_normal_at(wkey, idx)) * np.float32(w.std1)
+        q = torch.tensor([np.clip(val / s[e, n // 128, kk // 128], -448, 448)]).to(torch.float8_e4m3fn)
+        assert c[e, n, kk] == q.view(torch.uint8).item()

@@ -11,6 +11,7 @@ MUTANTS = {
     5: "W2 read transposed", 6: "activation scale dropped", 7: "combine drops a slot", 8: "SiLU sign",
     9: "unstable routing order", 10: "per-128 scale granularity", 11: "BF16 truncation", 12: "E4M3 truncation",
     13: "FP8 weights read as E2M1", 14: "L2-only rows drop the activation scale",
+    15: "float recipe: weight block scale dropped", 16: "float recipe: L2-activation scale from the wrong maximum",
 }
 
 

@@ -52,7 +52,10 @@ class Workload:
     clamp: float = 0.0
     zipf: float = 0.0
     seed: int = 0
-    w_fmt: int = 0  # weights: 0 = E2M1 (MXFP4, two per byte), 1 = E4M3 (MXFP8, one per byte)
+    # weights: 0 = E2M1 (MXFP4, two per byte), 1 = E4M3 (MXFP8, one per byte), both with UE8M0 per 32;
+    # 2 = the float-scale FP8 recipe (E4M3 weights with a float32 scale per 128 x 128 block,
+    # activations with a float32 scale per (token, 128))
+    w_fmt: int = 0
 
     @property
     def Ep(self) -> int:
@@ -90,9 +93,19 @@ class Workload:
         """Bytes per weight element: 1/2 (E2M1) or 1 (E4M3)."""
         return 1.0 if self.w_fmt else 0.5
 
+    @property
+    def w_sf_bytes(self) -> float:
+        """Weight scale bytes per element: one UE8M0 byte per 32, or one float32 per 128 x 128."""
+        return 4.0 / (128 * 128) if self.w_fmt == 2 else 1.0 / 32.0
+
+    @property
+    def a_sf_bytes(self) -> float:
+        """Activation scale bytes per element: one UE8M0 byte per 32, or one float32 per 128."""
+        return 4.0 / 128 if self.w_fmt == 2 else 1.0 / 32.0
+
     def expert_bytes(self) -> float:
-        """Weight bytes one expert streams: W1 + W2 codes and scales (1/32 B per element)."""
-        return 3.0 * self.H * self.I * (self.w_elem_bytes + 1.0 / 32.0)
+        """Weight bytes one expert streams: W1 + W2 codes and scales."""
+        return 3.0 * self.H * self.I * (self.w_elem_bytes + self.w_sf_bytes)
 
 
 CONFIGS = {
@@ -104,6 +117,9 @@ CONFIGS = {
     # FP8 (MXFP8) weight variants of the decode and prefill shapes
     "decode_fp8w": Workload("decode_fp8w", T=8, H=7168, I=2048, E=256, k=8, seed=5, w_fmt=1),
     "prefill_fp8w": Workload("prefill_fp8w", T=16384, H=7168, I=2048, E=256, k=8, seed=6, w_fmt=1),
+    # the float-scale FP8 recipe (1, 128, 128) at the decode and prefill shapes
+    "decode_fp8f128": Workload("decode_fp8f128", T=8, H=7168, I=2048, E=256, k=8, seed=7, w_fmt=2),
+    "prefill_fp8f128": Workload("prefill_fp8f128", T=16384, H=7168, I=2048, E=256, k=8, seed=8, w_fmt=2),
 }
 
 
@@ -139,6 +155,10 @@ def _lib_host():
         lib.syn_gen_w.restype = None
         lib.syn_gen_w8.argtypes = [u64, i32, i32, i32, i32, i32, f32, p, p, i32]
         lib.syn_gen_w8.restype = None
+        lib.syn_gen_x128.argtypes = [u64, i32, i32, i32, p, p]
+        lib.syn_gen_x128.restype = None
+        lib.syn_gen_w8f.argtypes = [u64, i32, i32, i32, i32, i32, f32, p, p, i32]
+        lib.syn_gen_w8f.restype = None
         lib.syn_gen_routing.argtypes = [u64, i32, i32, i32, ctypes.c_double, p, p]
         lib.syn_gen_routing.restype = i32
         lib.syn_u64_at.argtypes = [u64, u64]
@@ -164,6 +184,10 @@ def _lib_dev():
         lib.syn_dev_gen_w.restype = i32
         lib.syn_dev_gen_w8.argtypes = [u64, i32, i32, i32, i32, i32, f32, p, p, p]
         lib.syn_dev_gen_w8.restype = i32
+        lib.syn_dev_gen_x128.argtypes = [u64, i32, i32, p, p, p]
+        lib.syn_dev_gen_x128.restype = i32
+        lib.syn_dev_gen_w8f.argtypes = [u64, i32, i32, i32, i32, i32, f32, p, p, p]
+        lib.syn_dev_gen_w8f.restype = i32
         _dev = lib
     return _dev
 
@@ -189,14 +213,22 @@ def routing(w: Workload, T: int | None = None):
     return idx, wt
 
 
+def x_sf_shape(w: Workload, n: int):
+    """Shape and dtype of the activation scales of n rows."""
+    return ((n, w.H // 128), np.float32) if w.w_fmt == 2 else ((n, w.H // 32), np.uint8)
+
+
 def x_host(w: Workload, t0: int = 0, t1: int | None = None):
-    """Activation rows [t0, t1): (x_fp8 uint8 [n,H], x_sf uint8 [n,H/32])."""
+    """Activation rows [t0, t1): (x_fp8 uint8 [n,H], x_sf uint8 [n,H/32], or float32
+    [n,H/128] for the float-scale recipe)."""
     t1 = w.T if t1 is None else t1
     n = max(0, t1 - t0)
     x = np.zeros((n, w.H), np.uint8)
-    sf = np.zeros((n, w.H // 32), np.uint8)
+    shape, dt = x_sf_shape(w, n)
+    sf = np.zeros(shape, dt)
     if n:
-        _lib_host().syn_gen_x(w.seed, w.H, t0, t1, _ptr(x), _ptr(sf))
+        gen = _lib_host().syn_gen_x128 if w.w_fmt == 2 else _lib_host().syn_gen_x
+        gen(w.seed, w.H, t0, t1, _ptr(x), _ptr(sf))
     return x, sf
 
 
@@ -210,17 +242,27 @@ def code_bytes(w: Workload, K: int) -> int:
     return K if w.w_fmt else K // 2
 
 
+def w_sf_shape(w: Workload, which: int, n: int):
+    """Shape and dtype of the weight scales of n experts."""
+    rows, K = weight_shape(w, which)
+    if w.w_fmt == 2:
+        return (n, rows // 128, K // 128), np.float32
+    return (n, rows, K // 32), np.uint8
+
+
 def w_host(w: Workload, which: int, e0: int = 0, e1: int | None = None, nthreads: int | None = None):
     """Weights of experts [e0, e1): (codes uint8 [n,rows,K/2] (E2M1) or [n,rows,K] (E4M3),
-    scales uint8 [n,rows,K/32])."""
+    scales uint8 [n,rows,K/32], or float32 [n,rows/128,K/128] for the float-scale recipe)."""
     e1 = w.Ep if e1 is None else e1
     rows, K = weight_shape(w, which)
     n = max(0, e1 - e0)
     codes = np.zeros((n, rows, code_bytes(w, K)), np.uint8)
-    sf = np.zeros((n, rows, K // 32), np.uint8)
+    shape, dt = w_sf_shape(w, which, n)
+    sf = np.zeros(shape, dt)
     std = w.std1 if which == TAG_W1 else w.std2
     if n:
-        gen = _lib_host().syn_gen_w8 if w.w_fmt else _lib_host().syn_gen_w
+        lib = _lib_host()
+        gen = lib.syn_gen_w8f if w.w_fmt == 2 else lib.syn_gen_w8 if w.w_fmt else lib.syn_gen_w
         gen(w.seed, which, rows, K, e0, e1, std, _ptr(codes), _ptr(sf), nthreads or _nthreads())
     return codes, sf
 
@@ -239,7 +281,8 @@ def x_device(w: Workload, x, x_sf, stream=None):
     """Fill torch CUDA uint8 tensors x [T,H] and x_sf [T,H/32] on the device."""
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
-    rc = _lib_dev().syn_dev_gen_x(w.seed, x.shape[0], w.H, x.data_ptr(), x_sf.data_ptr(), s.cuda_stream)
+    gen = _lib_dev().syn_dev_gen_x128 if w.w_fmt == 2 else _lib_dev().syn_dev_gen_x
+    rc = gen(w.seed, x.shape[0], w.H, x.data_ptr(), x_sf.data_ptr(), s.cuda_stream)
     if rc != 0:
         raise RuntimeError(f"device x generator failed ({rc})")
 
@@ -251,7 +294,8 @@ def w_device(w: Workload, which: int, codes, sf, e0: int = 0, e1: int | None = N
     rows, K = weight_shape(w, which)
     std = w.std1 if which == TAG_W1 else w.std2
     s = stream if stream is not None else torch.cuda.current_stream()
-    gen = _lib_dev().syn_dev_gen_w8 if w.w_fmt else _lib_dev().syn_dev_gen_w
+    lib = _lib_dev()
+    gen = lib.syn_dev_gen_w8f if w.w_fmt == 2 else lib.syn_dev_gen_w8 if w.w_fmt else lib.syn_dev_gen_w
     rc = gen(w.seed, which, rows, K, e0, e1, std, codes.data_ptr(), sf.data_ptr(), s.cuda_stream)
     if rc != 0:
         raise RuntimeError(f"device weight generator failed ({rc})")
@@ -263,14 +307,16 @@ def device_inputs(w: Workload, device="cuda"):
     idx, wt = routing(w)
     out = dict(topk_idx=torch.from_numpy(idx).to(device), topk_w=torch.from_numpy(wt).to(device))
     x = torch.empty((w.T, w.H), dtype=torch.uint8, device=device)
-    xsf = torch.empty((w.T, w.H // 32), dtype=torch.uint8, device=device)
+    shape, dt = x_sf_shape(w, w.T)
+    xsf = torch.empty(shape, dtype=torch.float32 if dt == np.float32 else torch.uint8, device=device)
     if w.T:
         x_device(w, x, xsf)
     out.update(x=x, x_sf=xsf)
     for which, name in ((TAG_W1, "w1"), (TAG_W2, "w2")):
         rows, K = weight_shape(w, which)
         c = torch.empty((w.Ep, rows, code_bytes(w, K)), dtype=torch.uint8, device=device)
-        s = torch.empty((w.Ep, rows, K // 32), dtype=torch.uint8, device=device)
+        shape, dt = w_sf_shape(w, which, w.Ep)
+        s = torch.empty(shape, dtype=torch.float32 if dt == np.float32 else torch.uint8, device=device)
         w_device(w, which, c, s)
         out[name] = c
         out[name + "_sf"] = s

@@ -17,6 +17,16 @@ void syn_gen_x(uint64_t seed, int H, int t0, int t1, uint8_t* x, uint8_t* x_sf) 
                   x + (size_t)(t - t0) * H + (size_t)g * 32, x_sf + (size_t)(t - t0) * G + g);
 }
 
+/* x rows [t0, t1) for the float-scale recipe: E4M3 bytes + float32 scale per 128. */
+void syn_gen_x128(uint64_t seed, int H, int t0, int t1, uint8_t* x, float* x_sf) {
+  uint64_t key = syn_stream_key(seed, SYN_TAG_X);
+  int G = H / 128;
+  for (int t = t0; t < t1; ++t)
+    for (int g = 0; g < G; ++g)
+      syn_group_x128(key, (uint64_t)t * (uint64_t)H + (uint64_t)g * 128u,
+                     x + (size_t)(t - t0) * H + (size_t)g * 128, x_sf + (size_t)(t - t0) * G + g);
+}
+
 typedef struct {
   uint64_t key;
   int rows, K, e0, e1, th, nth, fp8;
@@ -60,6 +70,51 @@ static void syn_gen_w_any(uint64_t seed, int which, int rows_per_expert, int K, 
   }
   for (int i = 1; i < nthreads; ++i) pthread_create(&tid[i], NULL, syn_w_worker, &jobs[i]);
   syn_w_worker(&jobs[0]);
+  for (int i = 1; i < nthreads; ++i) pthread_join(tid[i], NULL);
+}
+
+typedef struct {
+  uint64_t key, skey;
+  int rows, K, e0, e1, th, nth;
+  float std_;
+  uint8_t* w;
+  float* w_sf;
+} syn_w8f_job;
+
+static void* syn_w8f_worker(void* arg) {
+  syn_w8f_job* j = (syn_w8f_job*)arg;
+  const int RB = j->rows / 128, KB = j->K / 128;
+  long total = (long)(j->e1 - j->e0) * j->rows;
+  for (long r = j->th; r < total; r += j->nth) {
+    long e = j->e0 + r / j->rows, n = r % j->rows;
+    uint64_t base = ((uint64_t)e * (uint64_t)j->rows + (uint64_t)n) * (uint64_t)j->K;
+    for (int kb = 0; kb < KB; ++kb) {
+      uint64_t bi = ((uint64_t)e * (uint64_t)RB + (uint64_t)(n / 128)) * (uint64_t)KB + (uint64_t)kb;
+      float sc = syn_block_scale(j->skey, bi, j->std_);
+      if (n % 128 == 0) j->w_sf[((size_t)(r / j->rows) * RB + (size_t)(n / 128)) * KB + kb] = sc;
+      for (int k = 128 * kb; k < 128 * kb + 128; ++k)
+        j->w[(size_t)r * j->K + k] = syn_elem_w8f(j->key, base + (uint64_t)k, j->std_, sc);
+    }
+  }
+  return NULL;
+}
+
+/* Weights for the float-scale recipe, experts [e0, e1): E4M3 [n][rows][K] and
+ * float32 block scales [n][rows/128][K/128]. */
+void syn_gen_w8f(uint64_t seed, int which, int rows_per_expert, int K, int e0, int e1,
+                 float std_, uint8_t* w, float* w_sf, int nthreads) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  syn_w8f_job jobs[256];
+  pthread_t tid[256];
+  for (int i = 0; i < nthreads; ++i) {
+    jobs[i].key = syn_stream_key(seed, (uint64_t)which);
+    jobs[i].skey = syn_stream_key(seed, (uint64_t)(SYN_TAG_BLOCK_SF + (which - SYN_TAG_W1)));
+    jobs[i].rows = rows_per_expert; jobs[i].K = K; jobs[i].e0 = e0; jobs[i].e1 = e1;
+    jobs[i].th = i; jobs[i].nth = nthreads; jobs[i].std_ = std_; jobs[i].w = w; jobs[i].w_sf = w_sf;
+  }
+  for (int i = 1; i < nthreads; ++i) pthread_create(&tid[i], NULL, syn_w8f_worker, &jobs[i]);
+  syn_w8f_worker(&jobs[0]);
   for (int i = 1; i < nthreads; ++i) pthread_join(tid[i], NULL);
 }
 

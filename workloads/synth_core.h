@@ -26,6 +26,14 @@
  *   for E4M3, 6 for E2M1), elements rounded to nearest-even in the element
  *   format after division by s.
  *
+ *   Float-scale FP8 recipe (weights and activations E4M3, float32 scales per
+ *   128 along K): an activation group of 128 takes the scale amax / 448 (one
+ *   IEEE division) and its elements the nearest-even E4M3 of v / scale; a
+ *   128 x 128 weight block takes a seeded scale std * 5/448 * u, u in [1, 2)
+ *   on a 2^-23 grid (within a factor of two of the amax scale of a normal
+ *   block, and never a power of two by construction except for u = 1), and
+ *   its elements the E4M3 of w / scale (saturating beyond 448).
+ *
  * None of this is a step of the expert computation itself; it only builds the
  * FP8 / MXFP4 byte tensors that both the CUDA path and the oracle consume.
  */
@@ -49,7 +57,8 @@ enum {
   SYN_TAG_ROUTE = 4,    /* uniform top-k draws (partial Fisher-Yates) */
   SYN_TAG_ZIPF_PERM = 5,/* permutation of experts for Zipf ranks    */
   SYN_TAG_ZIPF_DRAW = 6,/* weighted draws for Zipf routing          */
-  SYN_TAG_LOGITS = 7    /* router logits for the top-k weights      */
+  SYN_TAG_LOGITS = 7,   /* router logits for the top-k weights      */
+  SYN_TAG_BLOCK_SF = 8  /* + (which - SYN_TAG_W1): float weight block scales */
 };
 
 SYN_FN uint32_t syn_f2u(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
@@ -213,6 +222,37 @@ SYN_FN void syn_group_w8(uint64_t key, uint64_t idx0, float std_, uint8_t* q32, 
   float inv = syn_pow2(127 - (int)code);
   for (int j = 0; j < 32; ++j) q32[j] = syn_e4m3_encode(v[j] * inv);
   *sf = code;
+}
+
+/* One 128-element group of activations for the float-scale recipe:
+ * bf16(N(0,1)) -> E4M3 with a float32 scale amax / 448 (1 when amax is 0).
+ * Element j is stream element idx0 + j (the values of syn_group_x). */
+SYN_FN void syn_group_x128(uint64_t key, uint64_t idx0, uint8_t* q, float* sf) {
+  float v[128];
+  float amax = 0.0f;
+  for (int j = 0; j < 128; ++j) {
+    v[j] = syn_round_bf16(syn_normal(key, idx0 + (uint64_t)j));
+    float a = v[j] < 0.0f ? -v[j] : v[j];
+    if (a > amax) amax = a;
+  }
+  float s = amax / 448.0f;
+  if (!(s > 0.0f)) s = 1.0f;
+  for (int j = 0; j < 128; ++j) q[j] = syn_e4m3_encode(v[j] / s);
+  *sf = s;
+}
+
+/* Float32 scale of 128 x 128 weight block `idx` of stream `key`:
+ * (std * 5/448) * u with u = 1 + m * 2^-23, m the top 23 bits of the draw. */
+SYN_FN float syn_block_scale(uint64_t key, uint64_t idx, float std_) {
+  uint64_t d = syn_u64(key, idx);
+  float u = 1.0f + (float)(uint32_t)(d >> 41) * (1.0f / 8388608.0f);
+  return (std_ * 0x1.6db6dcp-7f) * u;
+}
+
+/* One weight element of the float-scale recipe: E4M3 of (N(0,1) * std) / scale,
+ * stream element idx (the values of syn_group_w / syn_group_w8). */
+SYN_FN uint8_t syn_elem_w8f(uint64_t key, uint64_t idx, float std_, float scale) {
+  return syn_e4m3_encode((syn_normal(key, idx) * std_) / scale);
 }
 
 #endif /* SYNTH_CORE_H */

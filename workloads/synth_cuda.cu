@@ -63,6 +63,45 @@ __global__ void syn_w8_kernel(uint64_t key, int rows, int K, int e0, long long g
   }
 }
 
+__global__ void syn_x128_kernel(uint64_t key, int H, long long groups, uint8_t* x, float* x_sf) {
+  const int G = H / 128;
+  for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < groups;
+       g += (long long)gridDim.x * blockDim.x) {
+    long long t = g / G, gg = g % G;
+    uint8_t q[128];
+    float sf;
+    syn_group_x128(key, (uint64_t)t * (uint64_t)H + (uint64_t)gg * 128u, q, &sf);
+    uint4* dst = reinterpret_cast<uint4*>(x + (size_t)t * H + (size_t)gg * 128);
+    for (int c = 0; c < 8; ++c) {
+      uint4 a;
+      memcpy(&a, q + 16 * c, 16);
+      dst[c] = a;
+    }
+    x_sf[(size_t)t * G + gg] = sf;
+  }
+}
+
+/* One thread per 16 consecutive elements of a row within one 128-wide K block. */
+__global__ void syn_w8f_kernel(uint64_t key, uint64_t skey, int rows, int K, int e0, long long chunks, float std_,
+                               uint8_t* w, float* w_sf) {
+  const int C = K / 16, RB = rows / 128, KB = K / 128;
+  for (long long c = blockIdx.x * (long long)blockDim.x + threadIdx.x; c < chunks;
+       c += (long long)gridDim.x * blockDim.x) {
+    long long r = c / C, cc = c % C;            /* r: row within the requested experts */
+    long long e = e0 + r / rows, n = r % rows;
+    int kb = (int)(cc / 8);
+    uint64_t bi = ((uint64_t)e * (uint64_t)RB + (uint64_t)(n / 128)) * (uint64_t)KB + (uint64_t)kb;
+    float sc = syn_block_scale(skey, bi, std_);
+    uint64_t base = ((uint64_t)e * (uint64_t)rows + (uint64_t)n) * (uint64_t)K + (uint64_t)cc * 16u;
+    uint8_t q[16];
+    for (int j = 0; j < 16; ++j) q[j] = syn_elem_w8f(key, base + (uint64_t)j, std_, sc);
+    uint4 a;
+    memcpy(&a, q, 16);
+    *reinterpret_cast<uint4*>(w + (size_t)r * K + (size_t)cc * 16) = a;
+    if (n % 128 == 0 && cc % 8 == 0) w_sf[((size_t)(r / rows) * RB + (size_t)(n / 128)) * KB + kb] = sc;
+  }
+}
+
 static int syn_grid(long long groups) {
   long long b = (groups + 255) / 256;
   if (b > 152 * 64) b = 152 * 64;
@@ -96,5 +135,25 @@ extern "C" int syn_dev_gen_w8(uint64_t seed, int which, int rows_per_expert, int
   long long groups = (long long)(e1 - e0) * rows_per_expert * (K / 32);
   syn_w8_kernel<<<syn_grid(groups), 256, 0, (cudaStream_t)stream>>>(
       syn_stream_key(seed, (uint64_t)which), rows_per_expert, K, e0, groups, std_, (uint8_t*)w, (uint8_t*)w_sf);
+  return (int)cudaGetLastError();
+}
+
+extern "C" int syn_dev_gen_x128(uint64_t seed, int T, int H, void* x, void* x_sf, void* stream) {
+  if (T <= 0) return 0;
+  if (H % 128) return -1;
+  long long groups = (long long)T * (H / 128);
+  syn_x128_kernel<<<syn_grid(groups), 256, 0, (cudaStream_t)stream>>>(
+      syn_stream_key(seed, SYN_TAG_X), H, groups, (uint8_t*)x, (float*)x_sf);
+  return (int)cudaGetLastError();
+}
+
+extern "C" int syn_dev_gen_w8f(uint64_t seed, int which, int rows_per_expert, int K, int e0, int e1,
+                               float std_, void* w, void* w_sf, void* stream) {
+  if (e1 <= e0) return 0;
+  if (K % 128 || rows_per_expert % 128) return -1;
+  long long chunks = (long long)(e1 - e0) * rows_per_expert * (K / 16);
+  syn_w8f_kernel<<<syn_grid(chunks), 256, 0, (cudaStream_t)stream>>>(
+      syn_stream_key(seed, (uint64_t)which), syn_stream_key(seed, (uint64_t)(SYN_TAG_BLOCK_SF + (which - SYN_TAG_W1))),
+      rows_per_expert, K, e0, chunks, std_, (uint8_t*)w, (float*)w_sf);
   return (int)cudaGetLastError();
 }
