@@ -77,11 +77,11 @@ def algorithmic(w, counts):
     counts = np.asarray(counts)
     R = int(counts.sum())
     touched = int((counts > 0).sum())
-    sf = 1.0 / 32.0
-    w1 = touched * 2 * w.I * w.H * (w.w_elem_bytes + sf)
-    w2 = touched * w.H * w.I * (w.w_elem_bytes + sf)
-    l1_act = R * w.H * (1 + sf) + R * w.I * (1 + sf)          # pool rows in, FP8 L2 operand out
-    l2_act = R * w.I * (1 + sf) + R * w.H * 2                  # FP8 L2 operand in, BF16 slot rows out
+    wsf, asf = w.w_sf_bytes, w.a_sf_bytes                       # scale bytes per element
+    w1 = touched * 2 * w.I * w.H * (w.w_elem_bytes + wsf)
+    w2 = touched * w.H * w.I * (w.w_elem_bytes + wsf)
+    l1_act = R * w.H * (1 + asf) + R * w.I * (1 + asf)        # pool rows in, FP8 L2 operand out
+    l2_act = R * w.I * (1 + asf) + R * w.H * 2                  # FP8 L2 operand in, BF16 slot rows out
     return dict(rows=R, touched=touched, flops=6.0 * w.H * w.I * R, l1_flops=4.0 * w.H * w.I * R,
                 l2_flops=2.0 * w.H * w.I * R, l1_bytes=w1 + l1_act, l2_bytes=w2 + l2_act,
                 weight_bytes=w1 + w2)
@@ -242,13 +242,14 @@ def run_reference(args, world, rank):
 
 
 def dtype_of(w):
-    return ("fp8xfp8" if w.w_fmt else "fp8xfp4") + " (fp32 accumulate)"
+    return {0: "fp8xfp4", 1: "fp8xfp8", 2: "fp8xfp8 float-scaled"}[w.w_fmt] + " (fp32 accumulate)"
 
 
 def workload_config(w):
     return {"workload": w.name, "T": w.T, "H": w.H, "I": w.I, "E": w.E, "topk": w.k, "shared": w.S,
             "swiglu_clamp": w.clamp, "routing": f"zipf({w.zipf})" if w.zipf else "uniform", "seed": w.seed,
-            "weights": "MXFP8 (E4M3 + UE8M0/32)" if w.w_fmt else "MXFP4 (E2M1 + UE8M0/32)",
+            "weights": {0: "MXFP4 (E2M1 + UE8M0/32)", 1: "MXFP8 (E4M3 + UE8M0/32)",
+                        2: "FP8 E4M3 + float32 scale per 128x128 block (activations float32 per 128)"}[w.w_fmt],
             "l2": "flushed between steps (256 MB write outside the timed events)"}
 
 

@@ -178,10 +178,22 @@ MM_API mm_status_t mm_token_tile_width(mm_handle_t h, int T, int* width);
  * MM_WEIGHTS_MXFP8: E4M3 codes, one byte per element (OCP MXFP8; the FP8 x FP8
  * variant of the pages' SM90 recipe, with the UE8M0-per-32 block scales the
  * block-scaled tensor-core MMA reads instead of float scales per 128). Either
- * way one UE8M0 scale per 32 elements along K. Other values:
- * MM_ERR_INVALID_ARG. */
+ * way one UE8M0 scale per 32 elements along K. MM_WEIGHTS_FP8_F128: below.
+ * Other values: MM_ERR_INVALID_ARG. */
 #define MM_WEIGHTS_MXFP4 0
 #define MM_WEIGHTS_MXFP8 1
+/* MM_WEIGHTS_FP8_F128: the float-scale FP8 recipe (1, 128, 128) of the SM90
+ * design ("MEGAMOE_SM90_DESIGN" sec. 5.3 and 15.2). Weights E4M3, one byte per
+ * element, with one float32 scale per 128 x 128 block; activations x with one
+ * float32 scale per (token, 128 along H); the L2 activations the path makes
+ * get one float32 scale per (row, 128 along I), amax / 448. Buffers of mm_run:
+ *   x_sf  float32 [T][H/128]                 (4-byte aligned)
+ *   w1    [E+S][2I][H] E4M3,  w1_sf float32 [E+S][2I/128][H/128]
+ *   w2    [E+S][H][I] E4M3,   w2_sf float32 [E+S][H/128][I/128]
+ * Each 128-long K block is an unscaled FP8 partial sum (kind::f8f6f4) that the
+ * epilogue warps multiply by the two scales and accumulate in FP32. Token
+ * tiles are 16 or 64 wide (a 112 or 224 policy runs 64). */
+#define MM_WEIGHTS_FP8_F128 2
 MM_API mm_status_t mm_set_weight_format(mm_handle_t h, int format);
 
 /* Expert-parallel-ready routing outputs ("MegaMoE research report" sec. 4.1,
@@ -225,15 +237,18 @@ MM_API mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes);
  * and Phase 6 step 6.6 require of two calls in a row.
  *   x_fp8    device, [T][H] E4M3                                  (16-byte aligned)
  *   x_sf     device, [T][H/32] UE8M0                               (4-byte aligned)
+ *            (MM_WEIGHTS_FP8_F128: [T][H/128] float32)
  *   topk_idx device, [T][topk] int32, each in [0, E) or -1 (slot disabled);
  *            other values disable the slot and set MM_DEV_BAD_ROUTING
  *   topk_w   device, [T][topk] float32 (need not sum to 1)
  *   w1       device, [E+S][2I][H/2] E2M1 packed; rows [0,I) gate, [I,2I) up   (32-byte aligned)
- *            (MM_WEIGHTS_MXFP8: [E+S][2I][H] E4M3)
+ *            (MM_WEIGHTS_MXFP8, MM_WEIGHTS_FP8_F128: [E+S][2I][H] E4M3)
  *   w1_sf    device, [E+S][2I][H/32] UE8M0                                     (4-byte aligned)
+ *            (MM_WEIGHTS_FP8_F128: [E+S][2I/128][H/128] float32)
  *   w2       device, [E+S][H][I/2] E2M1 packed                                  (32-byte aligned)
- *            (MM_WEIGHTS_MXFP8: [E+S][H][I] E4M3)
+ *            (MM_WEIGHTS_MXFP8, MM_WEIGHTS_FP8_F128: [E+S][H][I] E4M3)
  *   w2_sf    device, [E+S][H][I/32] UE8M0                                      (4-byte aligned)
+ *            (MM_WEIGHTS_FP8_F128: [E+S][H/128][I/128] float32)
  *   out_bf16 device, [T][H] bfloat16, fully overwritten               (16-byte aligned)
  *   ws       device workspace of ws_bytes >= mm_workspace_bytes(T) (256-byte aligned),
  *            fully re-initialised by every call, so it can be reused; two calls that
@@ -268,7 +283,8 @@ MM_API mm_status_t mm_launches_per_run(mm_handle_t h, int T, int* launches);
  *   counts [E+S] int32, offsets [E+S+1] int32, perm [T(k+S)] int32 (pool row -> slot
  *   t*(k+S)+j), pos [T(k+S)] int32 (slot -> pool row or -1), row_w [T(k+S)] float,
  *   pool_x [rows][H] u8, pool_sf [rows][H/32] u8, l2a [rows][I] u8 (E4M3),
- *   l2a_sf [rows][I/32] u8 (UE8M0), z [rows][H] bf16, status (uint32). Rows are in
+ *   l2a_sf [rows][I/32] u8 (UE8M0; MM_WEIGHTS_FP8_F128: [rows][I/128] float32, the
+ *   same bytes), z [rows][H] bf16, status (uint32). Rows are in
  *   pool order (expert-sorted); only the first offsets[E+S] rows are defined. */
 typedef struct {
   int32_t* counts;

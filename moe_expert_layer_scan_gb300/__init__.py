@@ -134,11 +134,13 @@ def mm_set_tile_policy(h: int, policy: int = MM_TILES_AUTO) -> None:
     _check(lib().mm_set_tile_policy(h, int(policy)), "mm_set_tile_policy")
 
 
-MM_WEIGHTS_MXFP4, MM_WEIGHTS_MXFP8 = 0, 1
+MM_WEIGHTS_MXFP4, MM_WEIGHTS_MXFP8, MM_WEIGHTS_FP8_F128 = 0, 1, 2
 
 
 def mm_set_weight_format(h: int, fmt: int) -> None:
-    """MM_WEIGHTS_MXFP4 (E2M1, two per byte) or MM_WEIGHTS_MXFP8 (E4M3, one per byte)."""
+    """MM_WEIGHTS_MXFP4 (E2M1, two per byte), MM_WEIGHTS_MXFP8 (E4M3, one per byte), both with UE8M0 per
+    32, or MM_WEIGHTS_FP8_F128 (E4M3 with float32 scales per 128 x 128 block; activations with float32
+    scales per (token, 128))."""
     _check(lib().mm_set_weight_format(h, int(fmt)), "mm_set_weight_format")
 
 

@@ -125,6 +125,10 @@ bool use_fused(const mm_handle* h, int T) {
 int variant_for(const mm_handle* h, int T) {
   const long long rows = (long long)T * (h->k + h->S), ep = h->E + h->S;
   int width = h->tiles;
+  // float-scale weights: 16- or 64-token tiles (the epilogue keeps the
+  // promoted sums in registers, which wider tiles would not fit)
+  if (h->w_fmt == MM_WEIGHTS_FP8_F128)
+    return width == MM_TILES_16 || (width == MM_TILES_AUTO && rows <= MM_TILES16_MAX_ROWS_PER_EXPERT * ep) ? 6 : 7;
   if (width == MM_TILES_AUTO)
     width = rows <= MM_TILES16_MAX_ROWS_PER_EXPERT * ep    ? MM_TILES_16
             : rows >= MM_TILES224_MIN_ROWS_PER_EXPERT * ep ? MM_TILES_224
@@ -140,7 +144,7 @@ int variant_for(const mm_handle* h, int T) {
 }
 
 int tile_width(int variant) {
-  return variant == 1 ? kBnLarge : variant == 3 ? kBnWide : variant == 5 ? kBnMid : kBnSmall;
+  return variant == 1 ? kBnLarge : variant == 3 ? kBnWide : variant == 5 || variant == 7 ? kBnMid : kBnSmall;
 }
 
 }  // namespace
@@ -223,7 +227,8 @@ mm_status_t mm_set_tile_policy(mm_handle_t h, int policy) {
 }
 
 mm_status_t mm_set_weight_format(mm_handle_t h, int format) {
-  if (!h || (format != MM_WEIGHTS_MXFP4 && format != MM_WEIGHTS_MXFP8)) return MM_ERR_INVALID_ARG;
+  if (!h || (format != MM_WEIGHTS_MXFP4 && format != MM_WEIGHTS_MXFP8 && format != MM_WEIGHTS_FP8_F128))
+    return MM_ERR_INVALID_ARG;
   if (format != h->w_fmt) h->w1_key = h->w2_key = nullptr;  // cached weight maps describe the old layout
   h->w_fmt = format;
   return MM_OK;
@@ -284,7 +289,8 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   // Scale rows by TMA when every scale row is a whole number of 16-byte groups
   // (K a multiple of 512) and the weight scale tensors are 16-byte aligned;
   // otherwise the scale warp loads them itself (two-block tiles only).
-  const bool sf_tma = h->H % 512 == 0 && h->I % 512 == 0 && aligned(w1_sf, 16) && aligned(w2_sf, 16);
+  const bool sf_tma = h->w_fmt != MM_WEIGHTS_FP8_F128 && h->H % 512 == 0 && h->I % 512 == 0 && aligned(w1_sf, 16) &&
+                      aligned(w2_sf, 16);
   int variant = variant_for(h, T);
   if (variant == 4 && !sf_tma) variant = (h->E + h->S <= kDeepMaxExperts) ? 2 : 0;
   const int bn1 = tile_width(variant);
@@ -304,6 +310,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ra.chunk_base = reinterpret_cast<int32_t*>(base + L.chunk_base);
   ra.chunk_bad = reinterpret_cast<int32_t*>(base + L.chunk_bad);
   ra.ready = reinterpret_cast<int32_t*>(base + L.ready);
+  ra.sched = reinterpret_cast<int32_t*>(base + L.sched);
   ra.rank_offsets = reinterpret_cast<int32_t*>(base + L.rank_offsets);
   ra.stats = h->expert_stats;
   ra.ep_ranks = h->ep_ranks;
@@ -395,6 +402,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g1.sf_tma = sf_tma ? 1 : 0;
   g1.ready = reinterpret_cast<int32_t*>(base + L.ready);
   g1.ready_target = f1 * mm_gemm_epilogue_warps(variant);
+  g1.tile_ctr = ra.sched + 0;
 
   GemmArgs g2 = g1;
   g2.w_sf = static_cast<const uint8_t*>(w2_sf);
@@ -406,6 +414,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g2.out_z = reinterpret_cast<uint16_t*>(base + L.z);
   g2.K = h->I; g2.rows_w = h->H; g2.fb_total = f2;
   g2.w_sf_vec = aligned(w2_sf, 16) && (h->I / 32) % 16 == 0;
+  g2.tile_ctr = ra.sched + 1;  // the L2 launch of the split schedule (the fused launch uses g1's)
   g2.act_sf_vec = (h->I / 32) % 16 == 0;
   if (use_fused(h, T)) {
     mark("gemm");

@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(1024, 1) route_small_kernel(RouteArgs a) {
   if (tid == 0) bad_any = 0;
   if (tid < Ep) cnt[tid] = 0;
   for (int i = tid; i <= R; i += blockDim.x) a.ready[i] = 0;
+  if (tid < kSchedCounters) a.sched[tid] = 0;
   __syncthreads();
   bool bad = false;
   int e = -1;
@@ -210,6 +211,7 @@ __global__ void __launch_bounds__(1024, 1) route_kernel(RouteArgs a) {
   const int tid = threadIdx.x;
   if (tid == 0) bad_any = 0;
   for (long i = tid; i <= R; i += blockDim.x) a.ready[i] = 0;
+  if (tid < kSchedCounters) a.sched[tid] = 0;
   const bool bad = warp_histograms(a, 0, R, hist);
   if (bad) bad_any = 1;
   int tot = 0;
@@ -242,6 +244,7 @@ __global__ void __launch_bounds__(1024) route_count_kernel(RouteArgs a) {
   for (int i = threadIdx.x; i < Ep; i += blockDim.x) hist[i] = 0;
   for (long i = c0 + threadIdx.x; i < c1; i += blockDim.x) a.ready[i] = 0;
   if (blockIdx.x == 0 && threadIdx.x == 0) a.ready[R] = 0;
+  if (blockIdx.x == 0 && threadIdx.x < kSchedCounters) a.sched[threadIdx.x] = 0;
   __syncthreads();
   bool bad = false;
   for (long s = c0 + threadIdx.x; s < c1; s += blockDim.x) {

@@ -66,7 +66,15 @@ struct Warps {
 
 enum : int { kModeL2 = 0, kModeL1 = 1, kModeFused = 2 };
 
-template <int BN, int STAGES, int NA_ = 2>
+// PROMO: the float-scale FP8 recipe (E4M3 weights with a float32 scale per
+// 128 x 128 block, activations with a float32 scale per (row, 128)). The
+// block-scaled MMA reads only power-of-two scales, so each 128-long K block
+// is an unscaled kind::f8f6f4 partial sum in TMEM (double-buffered); the
+// epilogue warps multiply it by (activation scale x weight scale) and add it
+// to their FP32 registers ("MEGAMOE_SM90_DESIGN" sec. 5.3, scale factors
+// applied in software after the MMA), then store the sum into the tile's
+// accumulator columns for the usual epilogue.
+template <int BN, int STAGES, int NA_ = 2, bool PROMO = false>
 struct GemmCfg {
   static constexpr int BM = 128;                         // weight rows per MMA
   static constexpr int BK = 128;                         // K per stage
@@ -79,28 +87,47 @@ struct GemmCfg {
   static constexpr int A_TX = BM * BK / 2;               // transaction bytes of one weight box (packed 4-bit size)
   static constexpr int B_BYTES = BN * BK;
   static constexpr int SFB_ROWS = BN <= 128 ? 128 : 256;
-  static constexpr int SF_STAGE_BYTES = NA * 512 + SFB_ROWS * 4;
+  static constexpr int SF_STAGE_BYTES = PROMO ? 0 : NA * 512 + SFB_ROWS * 4;
   static constexpr int A_OFF = 0;
   static constexpr int B_OFF = A_OFF + STAGES * NA * A_BYTES;
   static constexpr int SF_OFF = B_OFF + STAGES * B_BYTES;
   static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE_BYTES;
+  static constexpr int RAW_G_MAX = 3;  // scale-row groups in flight (RAW_G below) at most
   // The deep configurations (16-token tiles with six stages, 64-token tiles
   // with five) keep room for them by supporting at most kDeepMaxExperts
   // experts and two scale groups in flight.
   static constexpr bool DEEP = (BN == kBnSmall && STAGES > 5) || (BN == kBnMid && STAGES > 4);
+  // tiles handed from the producer to the other warps: a ring of RING tile
+  // indices with a full/empty mbarrier pair per slot; every role except the
+  // producer consumes each tile once (the scale warp, the MMA issuers and the
+  // epilogue warps)
+  static constexpr int RING = 4;
+  static constexpr int CONSUMERS = 1 + NI + Warps<BN, NA_>::EPI;
+  // barriers (full, empty, sfready per stage; two accumulator pairs; the raw
+  // scale groups' pair; the ring's pair per slot), the TMEM address, the abort
+  // flag and the tile ring, rounded up to 16 bytes
+  // (PROMO: eight more, the L1 epilogue's exchange of per-quadrant amax values)
+  static constexpr int XBARS = PROMO ? 8 : 0;
+  static constexpr int BAR_BYTES =
+      ((3 * STAGES + 4 + 2 * RAW_G_MAX + 2 * RING + XBARS) * 8 + 8 + 4 * RING + 15) / 16 * 16;
   // copies of the two tile tables and the row offsets ([experts + 1] each)
-  static constexpr int TAB_OFF = BAR_OFF + 256;
+  static constexpr int TAB_OFF = BAR_OFF + BAR_BYTES;
   static constexpr int TAB_INTS = (NA > 2 ? kQuadMaxExperts : DEEP ? kDeepMaxExperts : kMaxExperts) + 1;
   // L2 tiles whose L1 rows the producer has seen stored (fused schedule)
   static constexpr int L2RDY_OFF = TAB_OFF + 3 * TAB_INTS * 4;
   // TMA-loaded scale rows: RAW_G groups of four K steps; per group 16 bytes of
   // each of 128 rows for each weight block and of RAW_B_ROWS token rows
-  static constexpr int RAW_G = DEEP || NA > 2 ? 2 : 3;
+  static constexpr int RAW_G = PROMO ? 1 : DEEP || NA > 2 ? 2 : 3;  // (PROMO: unused, kept well-formed)
+  static_assert(RAW_G <= RAW_G_MAX, "barrier region sized for RAW_G_MAX groups");
   static constexpr int RAW_ROWS_BYTES = 128 * 16;
   static constexpr int RAW_B_ROWS = BN <= 32 ? 32 : (BN <= 128 ? 128 : 256);
   static constexpr int RAW_B_BYTES = RAW_B_ROWS * 16;
   static constexpr int RAW_GROUP_BYTES = NA * RAW_ROWS_BYTES + RAW_B_BYTES;
-  static constexpr int RAW_OFF = (L2RDY_OFF + 16 + 127) / 128 * 128;
+  // PROMO: per-quadrant column maxima exchanged by the L1 epilogue warps,
+  // [2 buffers][2 warp halves][4 quadrants][32 columns] floats
+  static constexpr int XA_OFF = L2RDY_OFF + 16;
+  static constexpr int XA_BYTES = PROMO ? 2 * 2 * 4 * 32 * 4 : 0;
+  static constexpr int RAW_OFF = (XA_OFF + XA_BYTES + 127) / 128 * 128;
   static constexpr int SMEM_BYTES = RAW_OFF + RAW_G * RAW_GROUP_BYTES + 1024;  // + alignment slack
   // TMEM columns: the accumulator buffers, then one scale-factor slot per
   // stage (every scale-factor address stays a multiple of 4 columns)
@@ -111,9 +138,13 @@ struct GemmCfg {
   // Two accumulator buffers (the epilogue of one tile overlaps the main loop
   // of the next) where TMEM holds them; the 224-token tiles fill TMEM with one
   // and the epilogue drains it between tiles.
-  static constexpr int ACC_BUFS = 2 * ACC_COLS + STAGES * SF_STAGE_COLS <= 512 ? 2 : 1;
+  // PROMO: one accumulator region (each epilogue warp writes and then reads
+  // only its own columns) and two partial-sum buffers after it, no scale slots.
+  static constexpr int ACC_BUFS = PROMO ? 1 : 2 * ACC_COLS + STAGES * SF_STAGE_COLS <= 512 ? 2 : 1;
   static constexpr int SF_BASE = ACC_BUFS * ACC_COLS;
-  static constexpr int TMEM_USED = SF_BASE + STAGES * SF_STAGE_COLS;
+  static constexpr int PART_BASE = ACC_COLS;
+  static constexpr int TMEM_USED = PROMO ? 3 * ACC_COLS : SF_BASE + STAGES * SF_STAGE_COLS;
+  static_assert(!PROMO || (NA == 2 && (BN == 16 || BN == 64)), "promotion: 16- and 64-token two-block tiles");
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
   static_assert(TMEM_USED <= 512, "TMEM budget");
@@ -230,11 +261,11 @@ __device__ __forceinline__ float inv_scale(uint32_t code) {
   return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(1u << (n + 149));
 }
 
-template <int MODE, int BN, int STAGES, int NA>
+template <int MODE, int BN, int STAGES, int NA, bool PROMO>
 __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
     gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmArgs g1,
                 const __grid_constant__ GemmArgs g2) {
-  using C = GemmCfg<BN, STAGES, NA>;
+  using C = GemmCfg<BN, STAGES, NA, PROMO>;
   using W = Warps<BN, NA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -245,8 +276,15 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
   uint64_t* sfready = tempty + 2;      // [STAGES] a stage's scales are in TMEM (tcgen05.commit of the copies)
   uint64_t* rfull = sfready + STAGES;  // [RAW_G] TMA scale rows landed
   uint64_t* rempty = rfull + C::RAW_G;  // [RAW_G] scale warp done with a group
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rempty + C::RAW_G);
+  uint64_t* tr_full = rempty + C::RAW_G;  // [RING] a tile index is in the ring slot
+  uint64_t* tr_empty = tr_full + C::RING;  // [RING] every consumer has read the slot
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tr_empty + C::RING);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* tring = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [RING] tile indices
+  // PROMO: amax exchange barriers [buffer * 2 + half]: written by the four
+  // quadrant warps of a half, and read by them
+  uint64_t* xwrit = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF + C::BAR_BYTES - 8 * C::XBARS);
+  uint64_t* xread = xwrit + C::XBARS / 2;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -263,6 +301,11 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       mbar_init(&rfull[b], 1);   // producer's expect_tx arrival
       mbar_init(&rempty[b], 1);  // scale warp, lane 0
     }
+    for (int b = 0; b < C::RING; ++b) {
+      mbar_init(&tr_full[b], 1);              // the producer's arrival after writing the index
+      mbar_init(&tr_empty[b], C::CONSUMERS);  // one arrival per consuming warp
+    }
+    for (int b = 0; b < C::XBARS; ++b) mbar_init(&xwrit[b], 4);  // (xread follows xwrit) four quadrant warps
     *abort_flag = 0;
     *reinterpret_cast<int*>(smem + C::L2RDY_OFF) = 0;
     fence_mbar_init();
@@ -308,40 +351,29 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
   auto tile_of = [&](int tile, bool l1) {
     return decode_tile(l1 ? tile : tile - n1, l1 ? s_t1 : s_t2, s_off, g1.Ep, l1 ? g1.fb_total : g2.fb_total, BN);
   };
-  // This CTA's tile sequence: tiles g, g + G, ... (concurrent
-  // CTAs work on adjacent tiles, so their weight streams stay close in HBM).
-  // Fused: the L1 tiles that way; the r = n1 mod G CTAs that hold one L1 tile
-  // more are still busy with it when the others reach the L2 tiles, so the
-  // first A = (G - r) * round(K1 / K2) L2 tiles go round-robin to the other
-  // G - r CTAs only (about one L1 tile's worth each), the rest to all G.
-  const int G = gridDim.x, g = blockIdx.x;
-  int r_l1 = 0, n_early = 0;
-  if (MODE == kModeFused) {
-    r_l1 = n1 % G;
-    const int s1 = g1.K / 128, s2 = g2.K / 128;
-    const long long a = (long long)(G - r_l1) * ((s1 + s2 / 2) / s2);
-    n_early = r_l1 == 0 ? 0 : (int)(a < num_tiles - n1 ? a : num_tiles - n1);
-  }
-  // first L2 tile (index past the L1 tiles) of this CTA, and the one after j
-  auto l2_first = [&]() {
-    const int j = g >= r_l1 && g - r_l1 < n_early ? g - r_l1 : n_early + g;
-    return n1 + j < num_tiles ? n1 + j : num_tiles;
-  };
-  auto l2_next = [&](int j) {
-    int jn;
-    if (j < n_early) {
-      jn = j + (G - r_l1);
-      if (jn >= n_early) jn = n_early + g;
-    } else {
-      jn = j + G;
-    }
-    return n1 + jn < num_tiles ? n1 + jn : num_tiles;
-  };
-  const int tile0 = MODE != kModeFused || g < n1 ? g : l2_first();
-  auto next_tile = [&](int t) {
-    if (MODE != kModeFused) return t + G;
-    if (t < n1) return t + G < n1 ? t + G : l2_first();
-    return l2_next(t - n1);
+  // wait site of the tile ring (status bit 8 + 15)
+  constexpr uint32_t kSiteRing = 15u;
+  // Dynamic tile schedule: the producer claims tiles from the launch's
+  // counter (zeroed by the routing kernel), in increasing index order across
+  // all CTAs, and hands each to the other roles through the tile ring. Tiles
+  // claimed at about the same time are adjacent (concurrent CTAs share weight
+  // blocks through L2), CTAs that finish early take more, and in the fused
+  // schedule every L1 tile is claimed, by a running CTA, before any L2 tile:
+  // an L2 tile only waits for L1 tiles that running CTAs hold and finish
+  // without waiting on anything, so the waits end whether or not the whole
+  // grid is resident at once.
+  // Consumer side: the next tile of this CTA, num_tiles or more when there are
+  // no more, -1 when the wait gave up. whole_warp: all 32 lanes call it (else
+  // one thread).
+  auto take_tile = [&](uint32_t& n, bool whole_warp) -> int {
+    const int slot = (int)(n % C::RING);
+    const uint32_t ph = (n / C::RING) & 1u;
+    if (!mbar_wait(&tr_full[slot], ph, abort_flag, g1.status, g1.timeout_ns, kSiteRing, 0)) return -1;
+    const int t = tring[slot];
+    if (whole_warp) __syncwarp();
+    if (!whole_warp || lane == 0) mbar_arrive(&tr_empty[slot]);
+    ++n;
+    return t;
   };
   // wait sites reported in the status word on expiry: L1 tiles s, L2 tiles 8 + s
   constexpr uint32_t kSiteReady = 8u + 6u;  // an L2 tile waiting for its L1 rows (fused)
@@ -380,12 +412,35 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
     // the current tile) so that the wait is usually over before the tile
     // starts; every observation is handed on to the scale-factor warp
     // (l2rdy counts this CTA's L2 tiles observed ready, in tile order).
-    uint32_t it = 0, gi = 0;  // stages and scale groups issued
+    uint32_t it = 0, gi = 0, pub = 0;  // stages, scale groups and ring slots issued
     bool ok = true;
     bool cur_ready = false;  // the current tile's counter was seen complete by a peek
     // transaction bytes of one 128x128 weight box: packed E2M1 or E4M3
     const uint32_t a_tx = g1.w_fp8 ? (uint32_t)(C::BM * C::BK) : (uint32_t)C::A_TX;
-    for (int tile = tile0; tile < num_tiles && ok; tile = next_tile(tile)) {
+    // claim: lane 0's atomic on the launch's tile counter (its result is read
+    // later, so the round trip overlaps the next stage's wait); publish: the
+    // index into the next ring slot once every consumer has read its old one
+    int claimed = 0;
+    auto claim = [&]() {
+      if (lane == 0) claimed = atomicAdd(g1.tile_ctr, 1);
+    };
+    auto publish = [&]() -> int {
+      const int t = __shfl_sync(0xffffffffu, claimed, 0);
+      const int slot = (int)(pub % C::RING);
+      const uint32_t ph = (pub / C::RING) & 1u;
+      if (!mbar_wait(&tr_empty[slot], ph ^ 1u, abort_flag, g1.status, g1.timeout_ns, kSiteRing)) return -1;
+      if (lane == 0) {
+        tring[slot] = t;
+        mbar_arrive(&tr_full[slot]);
+      }
+      __syncwarp();
+      ++pub;
+      return t;
+    };
+    claim();
+    int tile = publish();
+    ok = tile >= 0;
+    while (ok && tile < num_tiles) {
       const bool l1 = is_l1(tile);
       const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
@@ -404,9 +459,9 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         break;
       }
       bool next_ready = false;
-      const int ntile = next_tile(tile);
+      int ntile = -1;  // the next tile, claimed during this one's first stage and published at its second
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
-        if (sf_tma && (kb & 3) == 0) {
+        if (!PROMO && sf_tma && (kb & 3) == 0) {
           // this group's scale rows (16 bytes = four K steps per row) into a raw slot
           const int gslot = (int)(gi % C::RAW_G);
           const uint32_t gph = (gi / C::RAW_G) & 1u;
@@ -425,10 +480,15 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           }
           ++gi;
         }
-        if (MODE == kModeFused && kb == (kblocks > 1 ? 1 : 0) && ntile < num_tiles && !is_l1(ntile)) {
-          const Tile tn = tile_of(ntile, false);
-          next_ready = counter_ready_relay(g1.ready + tn.row0, g1.ready_target, false, l2rdy, abort_flag, g1.status,
-                                           g1.timeout_ns, kSiteReady) == 1;
+        if (kb == 1) {
+          ntile = publish();
+          if (ntile < 0) { ok = false; break; }
+          // fused: peek at the next L2 tile's counter (usually complete by the time it starts)
+          if (MODE == kModeFused && ntile < num_tiles && !is_l1(ntile)) {
+            const Tile tn = tile_of(ntile, false);
+            next_ready = counter_ready_relay(g1.ready + tn.row0, g1.ready_target, false, l2rdy, abort_flag,
+                                             g1.status, g1.timeout_ns, kSiteReady) == 1;
+          }
         }
         const int s = (int)(it % STAGES);
         const uint32_t ph = (it / STAGES) & 1u;
@@ -442,8 +502,15 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
             if ((amask >> u) & 1u) tma_load_2d(sA + u * C::A_BYTES, tw, &full[s], kb * C::BK, block_wrow(g, t, u, C::NA));
           tma_load_2d(sB, ta, &full[s], kb * C::BK, t.row0);
         }
+        if (kb == 0) claim();
+      }
+      if (!ok) break;
+      if (kblocks == 1) {
+        ntile = publish();
+        if (ntile < 0) { ok = false; break; }
       }
       cur_ready = next_ready;
+      tile = ntile;
     }
     const GemmArgs& gl = MODE == kModeL1 ? g1 : g2;  // status word and limit (shared by both)
     constexpr uint32_t kSiteTail = (MODE == kModeL1 ? 0u : 8u) + 4u;
@@ -458,16 +525,18 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
                   gl.timeout_ns < 10000000ull ? gl.timeout_ns : 10000000ull, kSiteTail);
       }
     }
-  } else if (warp == 3 && sf_tma) {
+  } else if (warp == 3 && !PROMO && sf_tma) {
     // ------------------------------------------------------------ scale-factor transposer
     // The producer TMA-loads each group's scale rows (16 bytes = four K steps
     // per row) into a raw slot; per K step this warp writes the layout
     // tcgen05.cp.32x128b.warpx4 reads: 16 bytes per lane l holding the step's
     // four scale bytes of rows l, l+32, l+64, l+96 of each 128-row group.
     constexpr int NB = C::SFB_ROWS / 32;
-    uint32_t it = 0, gi = 0;
+    uint32_t it = 0, gi = 0, tn = 0;
     bool ok = true;
-    for (int tile = tile0; tile < num_tiles && ok; tile = next_tile(tile)) {
+    for (;;) {
+      const int tile = take_tile(tn, true);
+      if (tile < 0 || tile >= num_tiles) break;
       const bool l1 = is_l1(tile);
       const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
@@ -515,8 +584,9 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           ++it;
         }
       }
+      if (!ok) break;
     }
-  } else if (warp == 3 && C::NA == 2) {
+  } else if (warp == 3 && !PROMO && C::NA == 2) {
     // ------------------------------------------------------------ scale-factor producer
     // (tiles of two weight blocks only: the host runs four-block tiles only
     // with TMA-loaded scale rows)
@@ -561,10 +631,10 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       if (MODE != kModeFused || is_l1(tile)) return true;
       return wait_shared_counter(l2rdy, ++l2seen, abort_flag, g1.status, g1.timeout_ns, kSiteReady);
     };
-    uint32_t it = 0;
-    bool ok = true;
-    int tile = tile0, kg = 0;
-    if (tile < num_tiles) {
+    uint32_t it = 0, tn = 0;
+    int tile = take_tile(tn, true), kg = 0;
+    bool ok = tile >= 0;
+    if (ok && tile < num_tiles) {
       ok = ready_wait(tile);
       if (ok) load_group(tile, kg, ca, cb);
     }
@@ -578,8 +648,9 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       const uint32_t cur_mask = block_mask(g, tc);
       int ntile = tile, nkg = kg + 4;
       if (nkg >= kblocks) {
-        ntile = next_tile(tile);
+        ntile = take_tile(tn, true);  // published by the producer during this tile's first stages
         nkg = 0;
+        if (ntile < 0) break;
       }
       const bool has_next = ntile < num_tiles;
       // a next group whose L1 rows are not all stored yet is loaded after this
@@ -627,6 +698,15 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       tile = ntile;
       kg = nkg;
     }
+  } else if (warp == 3) {
+    // (float-scale tiles have no UE8M0 scales to stage; four-block tiles
+    // always take their scale rows by TMA. This warp still consumes the ring
+    // so that every slot is released.)
+    uint32_t tn = 0;
+    for (;;) {
+      const int tile = take_tile(tn, true);
+      if (tile < 0 || tile >= num_tiles) break;
+    }
   } else if (warp == 1 || warp == 2 || warp >= 4 + W::EPI) {
     // ------------------------------------------------------------ MMA issuers
     // One thread per weight block (warps 1, 2, then 4 + EPI ...): one warp
@@ -637,14 +717,44 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       const int u = warp <= 2 ? warp - 1 : warp - (4 + W::EPI) + 2;
       // A (weights): E2M1 (format 5) or E4M3 (format 0); B (tokens): E4M3
       const uint32_t a_fmt = g1.w_fp8 ? 0u : 5u;
-      uint32_t it = 0, tcount = 0;
+      uint32_t it = 0, tcount = 0, tn = 0, pk = 0;  // pk: K blocks issued (PROMO partial buffers)
       bool ok = true;
-      for (int tile = tile0; tile < num_tiles && ok; tile = next_tile(tile), ++tcount) {
+      for (;; ++tcount) {
+        const int tile = take_tile(tn, false);
+        if (tile < 0 || tile >= num_tiles) break;
         const bool l1 = is_l1(tile);
         const Phase g = phase_of(l1, g1, g2);
         const uint32_t site0 = l1 ? 0u : 8u;
         const Tile t = tile_of(tile, l1);
         const int kblocks = g.K / C::BK;
+        if constexpr (PROMO) {
+          // one unscaled partial sum per K block into partial buffer pk & 1
+          const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
+          const bool active = block_active(g, t, u, C::NA);
+          const uint32_t id = idesc_f8f6f4_e4m3(n_mma);
+          for (int kb = 0; kb < kblocks; ++kb, ++it, ++pk) {
+            const int s = (int)(it % STAGES);
+            const uint32_t ph = (it / STAGES) & 1u;
+            const int pb = (int)(pk & 1u);
+            if (!mbar_wait(&full[s], ph, abort_flag, g1.status, g1.timeout_ns, site0 + 2)) { ok = false; break; }
+            if (!mbar_wait(&tempty[pb], ((pk >> 1) & 1u) ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (active) {
+              const uint32_t d = tmem + (uint32_t)(C::PART_BASE + pb * C::ACC_COLS + u * BN);
+              const uint64_t da = sdesc_kmajor_sw128(smem_u32(smem + C::A_OFF + (s * C::NA + u) * C::A_BYTES));
+              const uint64_t db = sdesc_kmajor_sw128(smem_u32(smem + C::B_OFF + s * C::B_BYTES));
+#pragma unroll
+              for (int k = 0; k < 4; ++k) tc_mma_f8f6f4(d, da + 2u * k, db + 2u * k, id, k > 0 ? 1u : 0u);
+            }
+            tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
+            tc_commit(&tfull[pb]);  // the partial sum is complete
+          }
+          if (!ok) break;
+          continue;
+        }
         const int buf = C::ACC_BUFS == 2 ? (int)(tcount & 1u) : 0;
         const uint32_t bph = (C::ACC_BUFS == 2 ? tcount >> 1 : tcount) & 1u;
         if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 1)) break;
@@ -686,17 +796,96 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
     // a quadrant take alternate 16-column chunks of the token tile.
     const int q = warp & 3;
     const int half = (warp - 4) >> 2;  // 0 when there is one warp per quadrant
-    uint32_t tcount = 0;
-    for (int tile = tile0; tile < num_tiles; tile = next_tile(tile), ++tcount) {
+    uint32_t tcount = 0, tn = 0, pk = 0, xc = 0;  // pk, xc: PROMO partial sums and amax exchanges
+    for (;; ++tcount) {
+      const int tile = take_tile(tn, true);
+      if (tile < 0 || tile >= num_tiles) break;
       const bool l1 = is_l1(tile);
       const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
       const Tile t = tile_of(tile, l1);
       const int buf = C::ACC_BUFS == 2 ? (int)(tcount & 1u) : 0;
       const uint32_t bph = (C::ACC_BUFS == 2 ? tcount >> 1 : tcount) & 1u;
-      if (!mbar_wait(&tfull[buf], bph, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 256)) break;
+      const uint32_t lanes = (uint32_t)(32 * q) << 16;
+      if constexpr (PROMO) {
+        // The warp's 16-column chunks are the ones the epilogue below reads:
+        // L1 in chunks of 32 (64-token tiles) or 16, L2 in chunks of 16, the
+        // warps of a quadrant alternating. Per K block: wait for the partial
+        // sum, load it, hand the buffer back, scale and accumulate.
+        constexpr int CH = BN / 16 / (W::EPI / 4);
+        constexpr int NCL1 = BN > 16 ? 32 : 16;
+        auto chunk_col = [&](int i) {
+          return l1 ? NCL1 * half + (i / (NCL1 / 16)) * NCL1 * (W::EPI / 4) + 16 * (i % (NCL1 / 16))
+                    : 16 * half + i * 16 * (W::EPI / 4);
+        };
+        const int KB = g.K / C::BK;
+        const float* wsf = reinterpret_cast<const float*>(g.w_sf);
+        const float* asf = reinterpret_cast<const float*>(g.act_sf);
+        // fused L2 tiles: their activation scales were stored during this
+        // launch (the producer saw the tile's counter complete before loading it)
+        const bool fresh = MODE == kModeFused && !l1;
+        if (fresh) {
+          if (lane == 0) (void)ld_acquire_gpu(g1.ready + t.row0);
+          __syncwarp();
+        }
+        float acc[C::NA][CH][16];
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++pk) {
+          const int pb = (int)(pk & 1u);
+          if (!mbar_wait(&tfull[pb], (pk >> 1) & 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 64)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t r[C::NA][CH][16];
+#pragma unroll
+          for (int u = 0; u < C::NA; ++u)
+#pragma unroll
+            for (int i = 0; i < CH; ++i)
+              if (chunk_col(i) < t.nrows && block_active(g, t, u, C::NA))
+                tmem_ld_x16(tmem + lanes + (uint32_t)(C::PART_BASE + pb * C::ACC_COLS + u * BN + chunk_col(i)),
+                            r[u][i]);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[pb]);
+          float sw[C::NA];
+#pragma unroll
+          for (int u = 0; u < C::NA; ++u)
+            sw[u] = block_active(g, t, u, C::NA) ? __ldg(wsf + (size_t)(block_wrow(g, t, u, C::NA) / 128) * KB + kb)
+                                                 : 0.0f;
+#pragma unroll
+          for (int i = 0; i < CH; ++i) {
+            if (chunk_col(i) >= t.nrows) continue;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = chunk_col(i) + j;
+              const float* ap = asf + (size_t)(t.row0 + col) * KB + kb;
+              const float sa = col < t.nrows ? (fresh ? __ldcg(ap) : __ldg(ap)) : 0.0f;
+#pragma unroll
+              for (int u = 0; u < C::NA; ++u) {
+                // (columns past the tile's rows, and absent blocks, stay 0)
+                const float part = col < t.nrows && sw[u] != 0.0f
+                                       ? __fmul_rn(__uint_as_float(r[u][i][j]), __fmul_rn(sa, sw[u]))
+                                       : 0.0f;
+                acc[u][i][j] = kb == 0 ? part : __fadd_rn(acc[u][i][j], part);
+              }
+            }
+          }
+        }
+        if (!ok) break;
+        // the sums into the accumulator columns the epilogue below reads
+#pragma unroll
+        for (int u = 0; u < C::NA; ++u)
+#pragma unroll
+          for (int i = 0; i < CH; ++i)
+            if (chunk_col(i) < t.nrows) tmem_st_x16(tmem + lanes + (uint32_t)(u * BN + chunk_col(i)), acc[u][i]);
+        tmem_st_wait();
+      } else {
+        if (!mbar_wait(&tfull[buf], bph, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 256)) break;
+      }
       tc_fence_after();
-      const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * C::ACC_COLS);
+      const uint32_t tbase = tmem + lanes + (uint32_t)(buf * C::ACC_COLS);
       if (MODE != kModeL2 && l1) {
         // The per-column amax over the warp's 32 features (one UE8M0 group) is
         // a transpose-reduction: after the exchange steps lane c (32 columns)
@@ -756,15 +945,45 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           }
           if (NC == 16) v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
           const int mycol = lane >> (5 - LOG2NC);
+          const bool col_lead = (lane & ((1 << (5 - LOG2NC)) - 1)) == 0;
+          if constexpr (PROMO) {
+            // float scale per (row, 128 features): the maximum over the four
+            // quadrant warps of this half (exchanged through shared memory,
+            // double-buffered, with bounded barrier waits), amax / 448 by IEEE
+            // division (1 when amax is 0), elements E4M3 of y / scale
+            const int xb = (int)(xc & 1u), xi = xb * 2 + half;
+            float* xa = reinterpret_cast<float*>(smem + C::XA_OFF) + xi * 128;
+            if (xc >= 2 &&
+                !mbar_wait(&xread[xi], ((xc - 2) >> 1) & 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 3)) break;
+            if (col_lead) xa[q * 32 + mycol] = v[0];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xwrit[xi]);
+            if (!mbar_wait(&xwrit[xi], (xc >> 1) & 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 3)) break;
+            const float am = fmaxf(fmaxf(xa[mycol], xa[32 + mycol]), fmaxf(xa[64 + mycol], xa[96 + mycol]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xread[xi]);
+            ++xc;
+            float sc = __fdiv_rn(am, 448.0f);
+            if (!(sc > 0.0f)) sc = 1.0f;
+            if (q == 0 && col_lead && mycol < ncol)
+              reinterpret_cast<float*>(g1.out_sf)[(size_t)(t.row0 + c0 + mycol) * (g1.I / 128) + fblk] = sc;
+#pragma unroll
+            for (int j = 0; j < NC; ++j) {
+              const float sj = __shfl_sync(0xffffffffu, sc, j << (5 - LOG2NC));
+              const uint8_t qb = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(y[j], sj), __NV_SATFINITE, __NV_E4M3);
+              if (j < ncol) g1.out_q[(size_t)(t.row0 + c0 + j) * g1.I + feat] = qb;
+            }
+          } else {
           const uint32_t code = requant_code(v[0]);  // column c0 + mycol
           const float inv = inv_scale(code);
-          if ((lane & ((1 << (5 - LOG2NC)) - 1)) == 0 && mycol < ncol)
+          if (col_lead && mycol < ncol)
             g1.out_sf[(size_t)(t.row0 + c0 + mycol) * (g1.I / 32) + fblk * 4 + q] = (uint8_t)code;
 #pragma unroll
           for (int j = 0; j < NC; ++j) {
             const float ij = __shfl_sync(0xffffffffu, inv, j << (5 - LOG2NC));
             const uint8_t qb = (uint8_t)__nv_cvt_float_to_fp8(__fmul_rn(y[j], ij), __NV_SATFINITE, __NV_E4M3);
             if (j < ncol) g1.out_q[(size_t)(t.row0 + c0 + j) * g1.I + feat] = qb;
+          }
           }
         }
         }
@@ -797,7 +1016,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (!PROMO && lane == 0) mbar_arrive(&tempty[buf]);
     }
   }
 
@@ -809,10 +1028,10 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
   }
 }
 
-template <int MODE, int BN, int STAGES, int NA = 2>
+template <int MODE, int BN, int STAGES, int NA = 2, bool PROMO = false>
 static int set_smem_attr(int* max_ctas) {
-  using C = GemmCfg<BN, STAGES, NA>;
-  auto k = gemm_kernel<MODE, BN, STAGES, NA>;
+  using C = GemmCfg<BN, STAGES, NA, PROMO>;
+  auto k = gemm_kernel<MODE, BN, STAGES, NA, PROMO>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return (int)e;
   int dev = 0, sms = 0;
@@ -822,23 +1041,24 @@ static int set_smem_attr(int* max_ctas) {
   return 0;
 }
 
-template <int MODE, int BN, int STAGES, int NA = 2>
+template <int MODE, int BN, int STAGES, int NA = 2, bool PROMO = false>
 static int launch(const GemmMaps* maps, const GemmArgs* g1, const GemmArgs* g2, int num_ctas, cudaStream_t st) {
-  using C = GemmCfg<BN, STAGES, NA>;
-  return (int)launch_kernel(gemm_kernel<MODE, BN, STAGES, NA>, dim3((unsigned)num_ctas),
+  using C = GemmCfg<BN, STAGES, NA, PROMO>;
+  return (int)launch_kernel(gemm_kernel<MODE, BN, STAGES, NA, PROMO>, dim3((unsigned)num_ctas),
                             dim3(Warps<BN, NA>::THREADS), C::SMEM_BYTES, st, true, *maps, *g1, *g2);
 }
 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
 // five, measured as fast as six).
 constexpr int kStagesSmall = 5, kStagesSmallDeep = 6, kStagesLarge = 4, kStagesWide = 3, kStagesQuad = 3,
-              kStagesMid = 5;
+              kStagesMid = 5, kStagesPromoSmall = 5, kStagesPromoMid = 4;
 // CTAs per launch of each instantiation: [mode][variant] (variant 2: 16-token
 // tiles with six stages, for at most kDeepMaxExperts experts; variant 3:
 // 224-token tiles; variant 4: 16-token tiles with four weight blocks, for at
 // most kQuadMaxExperts experts; variant 5: 64-token tiles, for at most
-// kDeepMaxExperts experts)
-static int g_ctas[3][6];
+// kDeepMaxExperts experts; variants 6 and 7: 16- and 64-token tiles of the
+// float-scale recipe)
+static int g_ctas[3][8];
 
 }  // namespace mm
 
@@ -863,6 +1083,12 @@ extern "C" int mm_gemm_prepare(void) {
   if ((e = set_smem_attr<kModeL1, kBnMid, kStagesMid>(&g_ctas[kModeL1][5]))) return e;
   if ((e = set_smem_attr<kModeL2, kBnMid, kStagesMid>(&g_ctas[kModeL2][5]))) return e;
   if ((e = set_smem_attr<kModeFused, kBnMid, kStagesMid>(&g_ctas[kModeFused][5]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnSmall, kStagesPromoSmall, 2, true>(&g_ctas[kModeL1][6]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnSmall, kStagesPromoSmall, 2, true>(&g_ctas[kModeL2][6]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnSmall, kStagesPromoSmall, 2, true>(&g_ctas[kModeFused][6]))) return e;
+  if ((e = set_smem_attr<kModeL1, kBnMid, kStagesPromoMid, 2, true>(&g_ctas[kModeL1][7]))) return e;
+  if ((e = set_smem_attr<kModeL2, kBnMid, kStagesPromoMid, 2, true>(&g_ctas[kModeL2][7]))) return e;
+  if ((e = set_smem_attr<kModeFused, kBnMid, kStagesPromoMid, 2, true>(&g_ctas[kModeFused][7]))) return e;
   return 0;
 }
 
@@ -872,7 +1098,7 @@ extern "C" int mm_gemm_epilogue_warps(int variant) {
   return variant == 1   ? mm::Warps<mm::kBnLarge, 2>::EPI
          : variant == 3 ? mm::Warps<mm::kBnWide, 2>::EPI
          : variant == 4 ? mm::Warps<mm::kBnSmall, 4>::EPI
-         : variant == 5 ? mm::Warps<mm::kBnMid, 2>::EPI
+         : variant == 5 || variant == 7 ? mm::Warps<mm::kBnMid, 2>::EPI
                         : mm::Warps<mm::kBnSmall, 2>::EPI;
 }
 
@@ -893,6 +1119,8 @@ extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, con
   const int n = g_ctas[mode][variant];
   if (l1) {
     return variant == 0   ? launch<kModeL1, kBnSmall, kStagesSmall>(maps, a, a, n, st)
+           : variant == 6 ? launch<kModeL1, kBnSmall, kStagesPromoSmall, 2, true>(maps, a, a, n, st)
+           : variant == 7 ? launch<kModeL1, kBnMid, kStagesPromoMid, 2, true>(maps, a, a, n, st)
            : variant == 2 ? launch<kModeL1, kBnSmall, kStagesSmallDeep>(maps, a, a, n, st)
            : variant == 3 ? launch<kModeL1, kBnWide, kStagesWide>(maps, a, a, n, st)
            : variant == 4 ? launch<kModeL1, kBnSmall, kStagesQuad, 4>(maps, a, a, n, st)
@@ -900,6 +1128,8 @@ extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, con
                           : launch<kModeL1, kBnLarge, kStagesLarge>(maps, a, a, n, st);
   }
   return variant == 0   ? launch<kModeL2, kBnSmall, kStagesSmall>(maps, a, a, n, st)
+         : variant == 6 ? launch<kModeL2, kBnSmall, kStagesPromoSmall, 2, true>(maps, a, a, n, st)
+         : variant == 7 ? launch<kModeL2, kBnMid, kStagesPromoMid, 2, true>(maps, a, a, n, st)
          : variant == 2 ? launch<kModeL2, kBnSmall, kStagesSmallDeep>(maps, a, a, n, st)
          : variant == 3 ? launch<kModeL2, kBnWide, kStagesWide>(maps, a, a, n, st)
          : variant == 4 ? launch<kModeL2, kBnSmall, kStagesQuad, 4>(maps, a, a, n, st)
@@ -913,6 +1143,8 @@ extern "C" int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const
   cudaStream_t st = (cudaStream_t)stream;
   const int n = g_ctas[kModeFused][variant];
   return variant == 0   ? launch<kModeFused, kBnSmall, kStagesSmall>(maps, g1, g2, n, st)
+         : variant == 6 ? launch<kModeFused, kBnSmall, kStagesPromoSmall, 2, true>(maps, g1, g2, n, st)
+         : variant == 7 ? launch<kModeFused, kBnMid, kStagesPromoMid, 2, true>(maps, g1, g2, n, st)
          : variant == 2 ? launch<kModeFused, kBnSmall, kStagesSmallDeep>(maps, g1, g2, n, st)
          : variant == 3 ? launch<kModeFused, kBnWide, kStagesWide>(maps, g1, g2, n, st)
          : variant == 4 ? launch<kModeFused, kBnSmall, kStagesQuad, 4>(maps, g1, g2, n, st)

@@ -17,6 +17,9 @@ constexpr int kRowMargin = 256;    // pool rows beyond the last valid row that t
 constexpr int kRouteChunk = 8192;  // slots per CTA when routing runs on several CTAs
 constexpr int kRouteSingleMax = 16384;  // up to this many slots, one CTA routes everything
 constexpr int kRouteSmallMax = 512;     // up to this many slots, the lean one-CTA routing kernel
+// Tile counters of the persistent GEMM launches (0: the L1 or fused launch,
+// 1: the L2 launch of the split schedule), zeroed by the routing kernel.
+constexpr int kSchedCounters = 4;
 
 // Token-tile widths (the largest MMA N) of the GEMM variants. "small" serves
 // decode-like calls (few rows per expert), "large" and "wide" everything else;
@@ -50,7 +53,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Byte offsets of every workspace region for one (shape, T).
 struct Layout {
-  size_t status, counts, offsets, tiles_l1, tiles_l2, rank_offsets, perm, pos, row_w, chunk_cnt, chunk_base,
+  size_t status, sched, counts, offsets, tiles_l1, tiles_l2, rank_offsets, perm, pos, row_w, chunk_cnt, chunk_base,
       chunk_bad, ready;
   size_t pool_x, pool_sf, l2a, l2a_sf, z, total;
   int rows_cap;
@@ -64,6 +67,7 @@ inline Layout make_layout(int E, int S, int H, int I, int k, int T) {
   size_t o = 0;
   auto take = [&](size_t bytes, size_t align) { o = align_up(o, align); size_t at = o; o += bytes; return at; };
   L.status = take(256, 256);
+  L.sched = take(sizeof(int32_t) * kSchedCounters, 256);
   L.counts = take(sizeof(int32_t) * Ep, 256);
   L.offsets = take(sizeof(int32_t) * (Ep + 1), 256);
   L.tiles_l1 = take(sizeof(int32_t) * (Ep + 1), 256);
@@ -101,6 +105,7 @@ struct RouteArgs {
   int32_t* chunk_base;  // [G][E+S] first pool row of each chunk's slots per expert
   int32_t* chunk_bad;   // [G] out-of-range ids seen in the chunk
   int32_t* ready;       // [R + 1] arrival counters of the fused GEMM, zeroed here
+  int32_t* sched;       // [kSchedCounters] tile counters of the GEMM launches, zeroed here
   int T, E, k, S;
   int bn_l1, bn_l2;  // token-tile widths of the two GEMMs
   int fb_l1, fb_l2;  // weight tiles per expert: I/128 (gate/up pairs) and ceil(H/256)
@@ -145,6 +150,7 @@ struct GemmArgs {
   int32_t* ready;
   int ready_target;
   int w_fp8;  // weights are E4M3 (one byte per element) instead of packed E2M1
+  int32_t* tile_ctr;  // this launch's tile counter (zero at launch): CTAs claim tiles in index order
   int sf_tma;  // scale rows are loaded by TMA (every K a multiple of 512, 16-byte aligned scale tensors)
 };
 

@@ -48,6 +48,22 @@ def assert_l2a_close(q_gpu, sf_gpu, q_ref, sf_ref, what="L2 activations"):
     assert sdiff <= 2e-3, f"{what}: {sdiff:.3%} of UE8M0 scales differ"
 
 
+def assert_l2a_close_float(q_gpu, sf_gpu, q_ref, sf_ref, what="L2 activations (float scales)"):
+    """Float-scale recipe: the per-(row, 128) scales agree to float rounding
+    (amax / 448 from sums in a different order) and the E4M3 activations up to
+    one E4M3 step where FP32 rounding order decides, on a small fraction."""
+    sg = np.ascontiguousarray(sf_gpu).view(np.float32).astype(np.float64)
+    sr = np.asarray(sf_ref, np.float32).astype(np.float64)
+    assert sg.shape == sr.shape
+    assert (np.abs(sg - sr) <= 1e-3 * sr).all(), f"{what}: scales differ by more than 1e-3 relative"
+    vg = e4m3_to_f64(q_gpu) * np.repeat(sg, 128, axis=1)
+    vr = e4m3_to_f64(q_ref) * np.repeat(sr, 128, axis=1)
+    frac = (vg != vr).mean() if vg.size else 0.0
+    assert frac <= 5e-3, f"{what}: {frac:.3%} of elements differ"
+    step = np.maximum(np.abs(vr) * 2.0 ** -3, np.repeat(sr, 128, axis=1) * 2.0 ** -9) * (1 + 1e-3)
+    assert (np.abs(vg - vr) <= step + 1e-3 * np.abs(vr)).all(), f"{what}: an element differs by more than one step"
+
+
 class DeviceRun:
     """Owns a handle, device inputs and a workspace for one workload."""
 
@@ -76,8 +92,8 @@ class DeviceRun:
         torch.cuda.synchronize()
         return out
 
-    def status(self) -> int:
-        return self.moe.status()
+    def status(self, stream=None) -> int:
+        return self.moe.status(stream)
 
     def intermediates(self, T: int):
         """Host copies of the routing tables and the pool-order intermediates."""
