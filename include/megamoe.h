@@ -74,7 +74,8 @@ typedef enum {
  * bit 8 + s for the L1 GEMM and 16 + s for the L2 GEMM, s = 0 stage free,
  * 1 accumulator free, 2 stage loaded, 3 accumulator ready, 4 copy drain,
  * 5 stage free (scale-factor writer), 6 (L2 tiles of the fused schedule) token
- * rows stored by the L1 epilogues; bit 15 for mm_debug_timeout_probe. */
+ * rows stored by the L1 epilogues; bit 15 for mm_debug_timeout_probe; bit 23
+ * for the hand-off of tile indices from the loading warp to the others. */
 
 /* Human-readable name of a status code (static string). The pages have no
  * counterpart: their Python entry points raise exceptions instead. */

@@ -368,6 +368,14 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
     return MM_ERR_CUDA;
   if (!encode_2d(&maps.a2, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)bn2))
     return MM_ERR_CUDA;
+  if (variant == 3) {
+    // narrower token boxes for the tiles that hold at most 112 or 32 rows
+    if (!encode_2d(&maps.a1n, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, (uint32_t)(bn1 / 2)) ||
+        !encode_2d(&maps.a2n, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)(bn2 / 2)) ||
+        !encode_2d(&maps.a1s, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, 32u) ||
+        !encode_2d(&maps.a2s, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, 32u))
+      return MM_ERR_CUDA;
+  }
   if (sf_tma) {
     if (h->w1sf_key != w1_sf) {
       if (!encode_sf(&h->tm_w1sf, w1_sf, (uint64_t)h->H / 32, (uint64_t)Ep * 2 * h->I)) return MM_ERR_CUDA;

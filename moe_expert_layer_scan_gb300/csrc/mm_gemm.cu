@@ -143,6 +143,13 @@ struct GemmCfg {
   static constexpr int ACC_BUFS = PROMO ? 1 : 2 * ACC_COLS + STAGES * SF_STAGE_COLS <= 512 ? 2 : 1;
   static constexpr int SF_BASE = ACC_BUFS * ACC_COLS;
   static constexpr int PART_BASE = ACC_COLS;
+  // HALF: with one accumulator buffer (224-token tiles), a tile of at most
+  // HALF_N rows needs only half of it (its two blocks at HALF_N columns
+  // apart), so such narrow tiles alternate between the two halves and the
+  // epilogue of one overlaps the main loop of the next; a wider tile takes
+  // both halves.
+  static constexpr bool HALF = !PROMO && ACC_BUFS == 1;
+  static constexpr int HALF_N = BN / 2;
   static constexpr int TMEM_USED = PROMO ? 3 * ACC_COLS : SF_BASE + STAGES * SF_STAGE_COLS;
   static_assert(!PROMO || (NA == 2 && (BN == 16 || BN == 64)), "promotion: 16- and 64-token two-block tiles");
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
@@ -449,7 +456,11 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       const int nact = __popc(amask);
       const int kblocks = g.K / C::BK;
       const CUtensorMap* tw = l1 ? &maps.w1 : &maps.w2;
-      const CUtensorMap* ta = l1 ? &maps.a1 : &maps.a2;
+      // the token box: the smallest of the launch's boxes that holds the tile
+      const int brows = !C::HALF ? BN : t.nrows <= 32 ? 32 : t.nrows <= C::HALF_N ? C::HALF_N : BN;
+      const CUtensorMap* ta = !C::HALF || brows == BN ? (l1 ? &maps.a1 : &maps.a2)
+                              : brows == 32 ? (l1 ? &maps.a1s : &maps.a2s)
+                                            : (l1 ? &maps.a1n : &maps.a2n);
       const CUtensorMap* twsf = l1 ? &maps.wsf1 : &maps.wsf2;
       const CUtensorMap* tasf = l1 ? &maps.asf1 : &maps.asf2;
       if (MODE == kModeFused && !l1 && !cur_ready &&
@@ -496,7 +507,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         uint8_t* sA = smem + C::A_OFF + s * C::NA * C::A_BYTES;
         uint8_t* sB = smem + C::B_OFF + s * C::B_BYTES;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], (uint32_t)nact * a_tx + C::B_BYTES);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)nact * a_tx + (uint32_t)(brows * C::BK));
 #pragma unroll
           for (int u = 0; u < C::NA; ++u)
             if ((amask >> u) & 1u) tma_load_2d(sA + u * C::A_BYTES, tw, &full[s], kb * C::BK, block_wrow(g, t, u, C::NA));
@@ -718,6 +729,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       // A (weights): E2M1 (format 5) or E4M3 (format 0); B (tokens): E4M3
       const uint32_t a_fmt = g1.w_fp8 ? 0u : 5u;
       uint32_t it = 0, tcount = 0, tn = 0, pk = 0;  // pk: K blocks issued (PROMO partial buffers)
+      uint32_t hc0 = 0, hc1 = 0, nt = 0;  // HALF: uses of each half, the next narrow tile's half
       bool ok = true;
       for (;; ++tcount) {
         const int tile = take_tile(tn, false);
@@ -755,11 +767,27 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           if (!ok) break;
           continue;
         }
-        const int buf = C::ACC_BUFS == 2 ? (int)(tcount & 1u) : 0;
-        const uint32_t bph = (C::ACC_BUFS == 2 ? tcount >> 1 : tcount) & 1u;
-        if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 1)) break;
+        int buf = C::ACC_BUFS == 2 ? (int)(tcount & 1u) : 0;
+        uint32_t d;
+        const bool narrow = C::HALF && t.nrows <= C::HALF_N;
+        if (C::HALF && narrow) {
+          buf = (int)nt;
+          nt ^= 1u;
+          if (!mbar_wait(&tempty[buf], ((buf ? hc1 : hc0) & 1u) ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 1))
+            break;
+          d = tmem + (uint32_t)(buf * (C::ACC_COLS / 2) + u * C::HALF_N);
+        } else if (C::HALF) {
+          nt = 0;
+          if (!mbar_wait(&tempty[0], (hc0 & 1u) ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 1) ||
+              !mbar_wait(&tempty[1], (hc1 & 1u) ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 1))
+            break;
+          d = tmem + (uint32_t)(u * BN);
+        } else {
+          const uint32_t bph = (C::ACC_BUFS == 2 ? tcount >> 1 : tcount) & 1u;
+          if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 1)) break;
+          d = tmem + (uint32_t)(buf * C::ACC_COLS + u * BN);
+        }
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * C::ACC_COLS + u * BN);
         const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
         const bool active = block_active(g, t, u, C::NA);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
@@ -786,7 +814,16 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
         if (!ok) break;
-        tc_commit(&tfull[buf]);
+        if (C::HALF && !narrow) {
+          // a wide tile fills both halves: both complete with it
+          tc_commit(&tfull[0]);
+          tc_commit(&tfull[1]);
+          ++hc0;
+          ++hc1;
+        } else {
+          tc_commit(&tfull[buf]);
+          if (C::HALF) (buf ? hc1 : hc0) += 1u;
+        }
       }
     }
     __syncwarp();
@@ -797,6 +834,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
     const int q = warp & 3;
     const int half = (warp - 4) >> 2;  // 0 when there is one warp per quadrant
     uint32_t tcount = 0, tn = 0, pk = 0, xc = 0;  // pk, xc: PROMO partial sums and amax exchanges
+    uint32_t hc0 = 0, hc1 = 0, nt = 0;             // HALF: as the MMA warps count them
     for (;; ++tcount) {
       const int tile = take_tile(tn, true);
       if (tile < 0 || tile >= num_tiles) break;
@@ -804,9 +842,21 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
       const Tile t = tile_of(tile, l1);
-      const int buf = C::ACC_BUFS == 2 ? (int)(tcount & 1u) : 0;
+      int buf = C::ACC_BUFS == 2 ? (int)(tcount & 1u) : 0;
       const uint32_t bph = (C::ACC_BUFS == 2 ? tcount >> 1 : tcount) & 1u;
       const uint32_t lanes = (uint32_t)(32 * q) << 16;
+      // HALF: a narrow tile's accumulators sit in half `buf` (blocks HALF_N
+      // columns apart), a wide tile's in both (blocks BN apart)
+      const bool narrow = C::HALF && t.nrows <= C::HALF_N;
+      uint32_t acc_base = (uint32_t)(buf * C::ACC_COLS), bstride = BN;
+      if (C::HALF && narrow) {
+        buf = (int)nt;
+        nt ^= 1u;
+        acc_base = (uint32_t)(buf * (C::ACC_COLS / 2));
+        bstride = C::HALF_N;
+      } else if (C::HALF) {
+        nt = 0;
+      }
       if constexpr (PROMO) {
         // The warp's 16-column chunks are the ones the epilogue below reads:
         // L1 in chunks of 32 (64-token tiles) or 16, L2 in chunks of 16, the
@@ -881,11 +931,16 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           for (int i = 0; i < CH; ++i)
             if (chunk_col(i) < t.nrows) tmem_st_x16(tmem + lanes + (uint32_t)(u * BN + chunk_col(i)), acc[u][i]);
         tmem_st_wait();
+      } else if (C::HALF && !narrow) {
+        if (!mbar_wait(&tfull[0], hc0 & 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 256) ||
+            !mbar_wait(&tfull[1], hc1 & 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 256))
+          break;
       } else {
-        if (!mbar_wait(&tfull[buf], bph, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 256)) break;
+        const uint32_t ph = C::HALF ? ((buf ? hc1 : hc0) & 1u) : bph;
+        if (!mbar_wait(&tfull[buf], ph, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 256)) break;
       }
       tc_fence_after();
-      const uint32_t tbase = tmem + lanes + (uint32_t)(buf * C::ACC_COLS);
+      const uint32_t tbase = tmem + lanes + acc_base;
       if (MODE != kModeL2 && l1) {
         // The per-column amax over the warp's 32 features (one UE8M0 group) is
         // a transpose-reduction: after the exchange steps lane c (32 columns)
@@ -898,7 +953,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         constexpr int LOG2NC = NC == 32 ? 5 : 4;
         // feature block j of the tile: gate accumulator 2j, up accumulator 2j + 1
         for (int jb = 0; jb < C::NA / 2; ++jb) {
-        const uint32_t tg = tbase + (uint32_t)(2 * jb * BN), tu = tg + (uint32_t)BN;
+        const uint32_t tg = tbase + 2u * (uint32_t)jb * bstride, tu = tg + bstride;
         const int fblk = t.fb * (C::NA / 2) + jb;  // 128-feature block of the intermediate
         const int feat = fblk * 128 + 32 * q + lane;
         for (int c0 = NC * half; t.active && c0 < t.nrows; c0 += NC * (W::EPI / 4)) {
@@ -996,7 +1051,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         if (!block_active(g2p, t, 2 * jb, C::NA)) break;
         const bool two = block_active(g2p, t, 2 * jb + 1, C::NA);
         const int feat = (t.fb * C::NA + 2 * jb) * 128 + 32 * q + lane;
-        const uint32_t tg = tbase + (uint32_t)(2 * jb * BN), th = tg + (uint32_t)BN;
+        const uint32_t tg = tbase + 2u * (uint32_t)jb * bstride, th = tg + bstride;
         for (int c0 = 16 * half; c0 < t.nrows; c0 += 16 * (W::EPI / 4)) {
           uint32_t gv[16], hv[16];
           tmem_ld_x16(tg + (uint32_t)c0, gv);
@@ -1016,7 +1071,17 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (!PROMO && lane == 0) mbar_arrive(&tempty[buf]);
+      if (C::HALF && !narrow) {
+        if (lane == 0) {
+          mbar_arrive(&tempty[0]);
+          mbar_arrive(&tempty[1]);
+        }
+        ++hc0;
+        ++hc1;
+      } else {
+        if (!PROMO && lane == 0) mbar_arrive(&tempty[buf]);
+        if (C::HALF) (buf ? hc1 : hc0) += 1u;
+      }
     }
   }
 

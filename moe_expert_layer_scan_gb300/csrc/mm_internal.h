@@ -159,6 +159,8 @@ struct GemmArgs {
 struct GemmMaps {
   CUtensorMap w1, a1, w2, a2;
   CUtensorMap wsf1, asf1, wsf2, asf2;
+  // 224-token tiles: token boxes of 112 and 32 rows for the narrower tiles
+  CUtensorMap a1n, a2n, a1s, a2s;
 };
 
 struct CombineArgs {

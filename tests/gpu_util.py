@@ -49,19 +49,21 @@ def assert_l2a_close(q_gpu, sf_gpu, q_ref, sf_ref, what="L2 activations"):
 
 
 def assert_l2a_close_float(q_gpu, sf_gpu, q_ref, sf_ref, what="L2 activations (float scales)"):
-    """Float-scale recipe: the per-(row, 128) scales agree to float rounding
-    (amax / 448 from sums in a different order) and the E4M3 activations up to
-    one E4M3 step where FP32 rounding order decides, on a small fraction."""
+    """Float-scale recipe: each per-(row, 128) scale is amax / 448 of the row's
+    SwiGLU outputs, so a last-bit difference in the largest of them (FP32
+    rounding order, exp) moves the scale by an ulp: scales agree to 1e-6
+    relative. The E4M3 codes are the same bytes up to one E4M3 step where the
+    rounding order decides, on a small fraction of elements."""
     sg = np.ascontiguousarray(sf_gpu).view(np.float32).astype(np.float64)
     sr = np.asarray(sf_ref, np.float32).astype(np.float64)
     assert sg.shape == sr.shape
-    assert (np.abs(sg - sr) <= 1e-3 * sr).all(), f"{what}: scales differ by more than 1e-3 relative"
+    assert (np.abs(sg - sr) <= 1e-6 * sr).all(), f"{what}: scales differ by more than 1e-6 relative"
+    frac = (np.asarray(q_gpu) != np.asarray(q_ref)).mean() if sr.size else 0.0
+    assert frac <= 2e-3, f"{what}: {frac:.3%} of E4M3 codes differ"
     vg = e4m3_to_f64(q_gpu) * np.repeat(sg, 128, axis=1)
     vr = e4m3_to_f64(q_ref) * np.repeat(sr, 128, axis=1)
-    frac = (vg != vr).mean() if vg.size else 0.0
-    assert frac <= 5e-3, f"{what}: {frac:.3%} of elements differ"
-    step = np.maximum(np.abs(vr) * 2.0 ** -3, np.repeat(sr, 128, axis=1) * 2.0 ** -9) * (1 + 1e-3)
-    assert (np.abs(vg - vr) <= step + 1e-3 * np.abs(vr)).all(), f"{what}: an element differs by more than one step"
+    step = np.maximum(np.abs(vr) * 2.0 ** -3, np.repeat(sr, 128, axis=1) * 2.0 ** -9)
+    assert (np.abs(vg - vr) <= step * (1 + 1e-5)).all(), f"{what}: an element differs by more than one E4M3 step"
 
 
 class DeviceRun:

@@ -149,7 +149,7 @@ def test_schedule_choice_and_validation():
 
 def test_weight_format_validation_and_switch(orc):
     """Switching the weight format re-describes the cached weight layout: the
-    same handle runs an MXFP4 and then an MXFP8 problem correctly."""
+    same handle runs an MXFP4, an MXFP8 and a float-scale FP8 problem correctly."""
     import torch
     import moe_expert_layer_scan_gb300 as mm
     w4 = Workload("fmt4", T=6, H=256, I=128, E=4, k=2, seed=305)
@@ -162,8 +162,15 @@ def test_weight_format_validation_and_switch(orc):
     d8 = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in h8.items()}
     out8 = bits(run.run(**d8))
     G.assert_out_close(out8, ref_out(orc, w8, h8)["out"])
+    # and to the float-scale format (float32 scale tensors of other shapes)
+    wf = w4.replace(name="fmtf", w_fmt=2)
+    hf = workloads.host_inputs(wf)
+    mm.mm_set_weight_format(run.moe.h, mm.MM_WEIGHTS_FP8_F128)
+    df = {k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in hf.items()}
+    outf = bits(run.run(**df))
+    G.assert_out_close(outf, ref_out(orc, wf, hf)["out"])
     with pytest.raises(mm.MMError):
-        mm.mm_set_weight_format(run.moe.h, 2)
+        mm.mm_set_weight_format(run.moe.h, 3)
 
 
 def test_tile_policy_validation():

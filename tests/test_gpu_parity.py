@@ -39,6 +39,13 @@ SMALL_CASES = {
     "wide_t480": Workload("wide_t480", T=480, H=512, I=256, E=4, k=2, seed=112),
     "wide_shared": Workload("wide_shared", T=600, H=384, I=384, E=3, k=2, S=1, clamp=2.0, seed=113),
     "fp8w_wide": Workload("fp8w_wide", T=300, H=512, I=256, E=2, k=2, seed=114, w_fmt=1),
+    # the float-scale FP8 recipe: 16-token tiles; 64-token tiles with a shared
+    # expert, clamp and three feature blocks; a ragged case with an odd number
+    # of W2 blocks; several 64-token tiles per expert
+    "f128_small": Workload("f128_small", T=8, H=1024, I=512, E=8, k=4, seed=120, w_fmt=2),
+    "f128_mid": Workload("f128_mid", T=64, H=768, I=384, E=4, k=2, S=1, clamp=3.0, seed=121, w_fmt=2),
+    "f128_ragged": Workload("f128_ragged", T=37, H=384, I=384, E=5, k=3, S=1, seed=122, w_fmt=2),
+    "f128_multi": Workload("f128_multi", T=300, H=512, I=256, E=2, k=2, seed=123, w_fmt=2),
 }
 
 
@@ -75,7 +82,10 @@ def test_parity_small(name, schedule, orc):
     assert inter["status"] == 0
     n = int(ref["offsets"][-1])
     check_routing(inter, ref, n)
-    G.assert_l2a_close(inter["l2a"], inter["l2a_sf"], ref["q"][:n], ref["q_sf"][:n])
+    if w.w_fmt == 2:
+        G.assert_l2a_close_float(inter["l2a"], inter["l2a_sf"], ref["q"][:n], ref["q_sf"][:n])
+    else:
+        G.assert_l2a_close(inter["l2a"], inter["l2a_sf"], ref["q"][:n], ref["q_sf"][:n])
     G.assert_out_close(inter["z"], ref["z"][:n], "L2 per-slot rows")
     G.assert_out_close(out, ref["out"])
 
@@ -103,7 +113,7 @@ FULL_EXTRA = {
 
 
 @pytest.mark.parametrize("name", ["decode", "mid", "skewed", "prefill", "decode_fp8w", "prefill_fp8w",
-                                  "mid_t512", "prefill_t1024"])
+                                  "decode_fp8f128", "prefill_fp8f128", "mid_t512", "prefill_t1024"])
 def test_parity_full_size_sampled(name, orc):
     """Full workload in the benchmark's launch configuration (weights generated
     in HBM); routing compared in full, outputs on sampled tokens that the oracle
@@ -128,7 +138,8 @@ def test_parity_full_size_sampled(name, orc):
     G.assert_out_close(out[tokens], ref["out"], f"{name} sampled tokens")
 
 
-@pytest.mark.parametrize("name", ["decode", "prefill_t256", "skewed_t48", "wide_shared", "fp8w_small"])
+@pytest.mark.parametrize("name", ["decode", "prefill_t256", "skewed_t48", "wide_shared", "fp8w_small", "f128_small",
+                                  "f128_mid"])
 def test_fused_schedule_equals_split_bit_for_bit(name):
     """One persistent launch of both GEMMs computes the same tiles as one launch
     per linear: outputs and intermediates are identical."""
@@ -164,11 +175,12 @@ def test_parity_with_the_other_tile_width(name, tiles, orc):
         G.assert_out_close(out, ref["out"])
 
 
-@pytest.mark.parametrize("name", ["wide_shared", "prefill_t256", "fp8w_wide", "fp8w_small"])
+@pytest.mark.parametrize("name", ["wide_shared", "prefill_t256", "fp8w_wide", "fp8w_small", "f128_mid", "f128_multi"])
 def test_tile_widths_agree_bit_for_bit(name):
     """Every token-tile width runs each output element's K loop in the same
     order: the outputs and intermediates of the four widths are identical
-    (with E4M3 weights the 16-token tiles hold four weight blocks)."""
+    (with E4M3 weights the 16-token tiles hold four weight blocks; float-scale
+    weights run 16- and 64-token tiles, a wider policy runs 64)."""
     w = SMALL_CASES[name]
     runs = [G.DeviceRun(w, device_weights=True, tiles=t) for t in (16, 64, 112, 224)]
     outs = [out_bits(r.run()) for r in runs]
