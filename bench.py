@@ -439,8 +439,10 @@ def roofline_of(w, alg, kern, ms_step):
     over HBM bandwidth and FLOPs over the FP8 tensor peak takes longer for the
     dominant kernel."""
     peaks, peak_src = load_peaks()
-    fused = "gemm" in kern
-    k_name = "gemm" if fused else "l1_gemm"
+    # "gemm": both linears in one launch; "gemms": both linears as the two
+    # concurrent per-expert-width launch pairs (timed together)
+    fused = "gemm" in kern or "gemms" in kern
+    k_name = ("gemm" if "gemm" in kern else "gemms") if fused else "l1_gemm"
     k_ms = kern.get(k_name)
     k_bytes = alg["l1_bytes"] + alg["l2_bytes"] if fused else alg["l1_bytes"]
     k_flops = alg["flops"] if fused else alg["l1_flops"]
@@ -462,8 +464,9 @@ def roofline_of(w, alg, kern, ms_step):
     tr = NCU_TRAFFIC.get(w.name)
     roof["traffic"] = tr["bytes"] if tr and tr.get("src") == gemm_source_hash() and tr.get("kernel") == k_name \
         else None
-    roof["kernel"] = ("gemm_kernel<fused> (mm_gemm.cu): L1 then L2 tiles in one launch" if fused
-                      else "gemm_kernel<L1> (mm_gemm.cu)")
+    roof["kernel"] = ("gemm_kernel<fused> (mm_gemm.cu): L1 then L2 tiles in one launch" if k_name == "gemm"
+                      else "gemm_kernel<L1>, <L2> (mm_gemm.cu): both linears, light and heavy experts on "
+                           "concurrent launches" if k_name == "gemms" else "gemm_kernel<L1> (mm_gemm.cu)")
     roof["scope"] = "dominant kernel, mean CUDA-event duration over the per-kernel pass"
     roof["algorithmic_bytes_per_launch"] = k_bytes
     roof["algorithmic_flops_per_launch"] = k_flops
@@ -473,7 +476,7 @@ def roofline_of(w, alg, kern, ms_step):
                      "the fraction of the roofline the fused MoE path reaches")
     step["algorithmic_bytes"] = alg["l1_bytes"] + alg["l2_bytes"]
     step["algorithmic_flops"] = alg["flops"]
-    return roof, step, ("fused" if fused else "split")
+    return roof, step, ("fused" if k_name == "gemm" else "split, per-expert widths" if k_name == "gemms" else "split")
 
 
 def clock_record(clk, ms):
@@ -500,7 +503,8 @@ def report(args, w, world, main, clk, dec=None, dec_clk=None):
             "config": workload_config(w),
             "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU",
             "gemm_schedule": sched + (" (auto)" if args.schedule == "auto" else ""),
-            "token_tiles": f"{main['tile_width']}" + (" (auto)" if args.tiles == -1 else ""),
+            "token_tiles": ("per expert (112 / 224)" if args.tiles == 0 else f"{main['tile_width']}")
+                           + (" (auto)" if args.tiles == -1 else ""),
             "tflops": alg["flops"] * world / (ms / 1e3) / 1e12,
             "hbm_gbs_whole_step": (alg["l1_bytes"] + alg["l2_bytes"]) / (ms / 1e3) / 1e9,
             "kernels_ms": kern,
@@ -551,8 +555,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     ap.add_argument("--no-decode-record", action="store_true",
                     help="with the prefill workload, skip the decode-shape record timed after it")
-    ap.add_argument("--tiles", type=int, default=-1, choices=[-1, 16, 64, 112, 224],
-                    help="token-tile width (-1: the library's choice)")
+    ap.add_argument("--tiles", type=int, default=-1, choices=[-1, 0, 16, 64, 112, 224],
+                    help="token-tile width (-1: the library's choice; 0: per expert, by its routed rows)")
     ap.add_argument("--schedule", default="auto", choices=["auto", "fused", "split"],
                     help="GEMM schedule: one persistent launch for both linears, one per linear, or the "
                          "library's choice from the rows per expert (default)")

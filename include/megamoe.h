@@ -156,6 +156,18 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
  * Every width computes the same tiles' sums; the results are identical.
  * Other values: MM_ERR_INVALID_ARG. */
 #define MM_TILES_AUTO (-1)
+/* MM_TILES_PER_EXPERT: the token-tile width by each expert's routed rows
+ * ("MEGAMOE_SM90_DESIGN" sec. 12.1 and 13.1, BLOCK_M by expert load; the
+ * concurrent launches on disjoint SM partitions of "MegaMoE research report"
+ * sec. 12, PR357, without green contexts), for calls that run the split
+ * schedule (others run as MM_TILES_AUTO): the experts
+ * with more than 112 rows on 224-token tiles and the others on 112-token
+ * tiles, as two persistent launches per linear that share the SMs (the heavy
+ * experts' launches on a stream of the handle, forked from and joined back
+ * into the caller's stream; the split of the SMs follows each class's tile
+ * count). For load distributions with a few very hot experts and many light
+ * ones. Results are identical to the other widths. */
+#define MM_TILES_PER_EXPERT 0
 #define MM_TILES_16 16
 #define MM_TILES_64 64
 #define MM_TILES_112 112

@@ -51,6 +51,10 @@ struct mm_handle {
   int w_fmt;
   // token-tile width: MM_TILES_AUTO / _16 / _64 / _112 / _224
   int tiles;
+  // per-expert tile widths: the heavy class's launches run on this stream,
+  // forked from and joined back into the caller's stream by the two events
+  cudaStream_t side;
+  cudaEvent_t fork, join;
   // optional per-launch events (route, gather, L1, L2, combine, end) and the
   // stage name of each recorded interval
   bool profile;
@@ -135,12 +139,20 @@ int variant_for(const mm_handle* h, int T) {
             : rows > MM_TILES224_MIN_ROWS_PER_EXPERT_FUSED * ep && use_fused(h, T) ? MM_TILES_224
             : rows <= MM_TILES64_MAX_ROWS_PER_EXPERT * ep && h->S == 0              ? MM_TILES_64
                                                                                    : MM_TILES_112;
-  if (width == MM_TILES_112) return 1;
+  if (width == MM_TILES_112 || width == MM_TILES_PER_EXPERT) return 1;  // (per expert: the light class)
   if (width == MM_TILES_224) return 3;
   if (width == MM_TILES_64) return h->E + h->S <= kDeepMaxExperts ? 5 : 1;
   if (h->w_fmt == MM_WEIGHTS_MXFP8 && h->E + h->S <= kQuadMaxExperts && h->I % 256 == 0)
     return 4;
   return (h->E + h->S <= kDeepMaxExperts) ? 2 : 0;
+}
+
+// Whether a call runs per-expert tile widths: two concurrent launches per
+// linear, the experts with more than 112 routed rows on 224-token tiles and
+// the others on 112-token tiles (split schedule, MXFP4/MXFP8 weights).
+bool use_dual(const mm_handle* h, int T) {
+  if (h->w_fmt == MM_WEIGHTS_FP8_F128 || use_fused(h, T) || T == 0) return false;
+  return h->tiles == MM_TILES_PER_EXPERT;
 }
 
 int tile_width(int variant) {
@@ -201,6 +213,16 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
   h->tiles = MM_TILES_AUTO;
   h->profile = false;
   h->n_recorded = 0;
+  if (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess) {
+    delete h;
+    return MM_ERR_CUDA;
+  }
+  if (cudaEventCreateWithFlags(&h->fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaStreamDestroy(h->side);
+    delete h;
+    return MM_ERR_CUDA;
+  }
   *out = h;
   return MM_OK;
 }
@@ -220,7 +242,7 @@ mm_status_t mm_set_schedule(mm_handle_t h, int schedule) {
 
 mm_status_t mm_set_tile_policy(mm_handle_t h, int policy) {
   if (!h || (policy != MM_TILES_AUTO && policy != MM_TILES_16 && policy != MM_TILES_64 && policy != MM_TILES_112 &&
-             policy != MM_TILES_224))
+             policy != MM_TILES_224 && policy != MM_TILES_PER_EXPERT))
     return MM_ERR_INVALID_ARG;
   h->tiles = policy;
   return MM_OK;
@@ -263,7 +285,7 @@ mm_status_t mm_token_tile_width(mm_handle_t h, int T, int* width) {
 mm_status_t mm_launches_per_run(mm_handle_t h, int T, int* launches) {
   if (!h || !launches || T < 0) return MM_ERR_INVALID_ARG;
   const int route = mm_route_launches(T * (h->k + h->S));
-  *launches = T == 0 ? route : route + (use_fused(h, T) ? 3 : 4);
+  *launches = T == 0 ? route : route + (use_fused(h, T) ? 3 : use_dual(h, T) ? 6 : 4);
   return MM_OK;
 }
 
@@ -295,6 +317,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   if (variant == 4 && !sf_tma) variant = (h->E + h->S <= kDeepMaxExperts) ? 2 : 0;
   const int bn1 = tile_width(variant);
   const int bn2 = bn1;
+  const bool fused = use_fused(h, T), dual = use_dual(h, T);
 
   RouteArgs ra;
   ra.topk_idx = topk_idx;
@@ -303,6 +326,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ra.offsets = reinterpret_cast<int32_t*>(base + L.offsets);
   ra.tiles_l1 = reinterpret_cast<int32_t*>(base + L.tiles_l1);
   ra.tiles_l2 = reinterpret_cast<int32_t*>(base + L.tiles_l2);
+  ra.eorder = reinterpret_cast<int32_t*>(base + L.eorder);
   ra.perm = reinterpret_cast<int32_t*>(base + L.perm);
   ra.pos = reinterpret_cast<int32_t*>(base + L.pos);
   ra.row_w = reinterpret_cast<float*>(base + L.row_w);
@@ -317,6 +341,8 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ra.status = reinterpret_cast<uint32_t*>(base + L.status);
   ra.T = T; ra.E = h->E; ra.k = h->k; ra.S = h->S;
   ra.bn_l1 = bn1; ra.bn_l2 = bn2;
+  ra.bn_heavy = dual ? kBnWide : bn1;
+  ra.dual_sms = dual ? h->num_sms : 0;
   const int na = mm_gemm_blocks(variant);                 // 128-row weight blocks per tile
   const int f1 = h->I / (64 * na), f2 = (h->H + 128 * na - 1) / (128 * na);  // weight tiles per expert
   ra.fb_l1 = f1;
@@ -391,6 +417,20 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
     if (!encode_sf(&maps.asf1, base + L.pool_sf, (uint64_t)h->H / 32, (uint64_t)L.rows_cap, tb)) return MM_ERR_CUDA;
     if (!encode_sf(&maps.asf2, base + L.l2a_sf, (uint64_t)h->I / 32, (uint64_t)L.rows_cap, tb)) return MM_ERR_CUDA;
   }
+  GemmMaps maps_w;  // per-expert widths: the heavy class's 224-token tiles (token and token-scale boxes)
+  if (dual) {
+    maps_w = maps;
+    const uint32_t tbw = (uint32_t)mm_gemm_token_scale_box_rows(3);
+    if (!encode_2d(&maps_w.a1, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, (uint32_t)kBnWide) ||
+        !encode_2d(&maps_w.a2, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)kBnWide) ||
+        !encode_2d(&maps_w.a1n, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, (uint32_t)(kBnWide / 2)) ||
+        !encode_2d(&maps_w.a2n, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, (uint32_t)(kBnWide / 2)) ||
+        !encode_2d(&maps_w.a1s, base + L.pool_x, false, (uint64_t)h->H, (uint64_t)L.rows_cap, 32u) ||
+        !encode_2d(&maps_w.a2s, base + L.l2a, false, (uint64_t)h->I, (uint64_t)L.rows_cap, 32u) ||
+        (sf_tma && (!encode_sf(&maps_w.asf1, base + L.pool_sf, (uint64_t)h->H / 32, (uint64_t)L.rows_cap, tbw) ||
+                    !encode_sf(&maps_w.asf2, base + L.l2a_sf, (uint64_t)h->I / 32, (uint64_t)L.rows_cap, tbw))))
+      return MM_ERR_CUDA;
+  }
 
   GemmArgs g1;
   memset(&g1, 0, sizeof(g1));
@@ -398,6 +438,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g1.act_sf = base + L.pool_sf;
   g1.offsets = ra.offsets;
   g1.tile_start = ra.tiles_l1;
+  g1.eorder = ra.eorder;
   g1.row_w = ra.row_w;
   g1.out_q = base + L.l2a;
   g1.out_sf = base + L.l2a_sf;
@@ -411,6 +452,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g1.ready = reinterpret_cast<int32_t*>(base + L.ready);
   g1.ready_target = f1 * mm_gemm_epilogue_warps(variant);
   g1.tile_ctr = ra.sched + 0;
+  g1.sched = ra.sched;
 
   GemmArgs g2 = g1;
   g2.w_sf = static_cast<const uint8_t*>(w2_sf);
@@ -424,7 +466,28 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g2.w_sf_vec = aligned(w2_sf, 16) && (h->I / 32) % 16 == 0;
   g2.tile_ctr = ra.sched + 1;  // the L2 launch of the split schedule (the fused launch uses g1's)
   g2.act_sf_vec = (h->I / 32) % 16 == 0;
-  if (use_fused(h, T)) {
+  if (dual) {
+    // the light class on the caller's stream (112-token tiles), the heavy
+    // class on the side stream (224-token tiles), on disjoint SMs: each
+    // launch's CTAs beyond its class's share leave at once
+    mark("gemms");
+    GemmArgs l1n = g1, l2n = g2, l1w = g1, l2w = g2;
+    l1n.tile_class = l2n.tile_class = 1;
+    l1w.tile_class = l2w.tile_class = 2;
+    l1w.tile_ctr = ra.sched + 2;
+    l2w.tile_ctr = ra.sched + 3;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaEventRecord(h->fork, st) != cudaSuccess || cudaStreamWaitEvent(h->side, h->fork, 0) != cudaSuccess)
+      return MM_ERR_CUDA;
+    // (ordinary stream order throughout: a launch allowed to start early would
+    // hold SMs in its wait that the other class's launch is meant to get)
+    if (mm_launch_gemm_class(1, variant, &maps, &l1n, stream) != 0) return MM_ERR_CUDA;
+    if (mm_launch_gemm_class(1, 3, &maps_w, &l1w, h->side) != 0) return MM_ERR_CUDA;
+    if (mm_launch_gemm_class(0, variant, &maps, &l2n, stream) != 0) return MM_ERR_CUDA;
+    if (mm_launch_gemm_class(0, 3, &maps_w, &l2w, h->side) != 0) return MM_ERR_CUDA;
+    if (cudaEventRecord(h->join, h->side) != cudaSuccess || cudaStreamWaitEvent(st, h->join, 0) != cudaSuccess)
+      return MM_ERR_CUDA;
+  } else if (fused) {
     mark("gemm");
     if (mm_launch_gemm_fused(variant, &maps, &g1, &g2, stream) != 0)
       return MM_ERR_CUDA;
@@ -441,7 +504,8 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   ca.out = static_cast<uint16_t*>(out_bf16);
   ca.T = T; ca.H = h->H; ca.Kp = Kp;
   mark("combine");
-  if (mm_launch_combine(&ca, stream) != 0) return MM_ERR_CUDA;
+  // (after the join of two streams: ordinary stream order)
+  if (mm_launch_combine(&ca, stream, !dual) != 0) return MM_ERR_CUDA;
   mark(nullptr);
   h->n_recorded = ev_i;
   return MM_OK;
@@ -540,6 +604,9 @@ mm_status_t mm_run_noalloc(mm_handle_t h, int T, const void* x_fp8, const void* 
 
 void mm_destroy(mm_handle_t h) {
   if (!h) return;
+  cudaEventDestroy(h->fork);
+  cudaEventDestroy(h->join);
+  cudaStreamDestroy(h->side);
   if (h->profile)
     for (int i = 0; i < 6; ++i) cudaEventDestroy(h->ev[i]);
   delete h;

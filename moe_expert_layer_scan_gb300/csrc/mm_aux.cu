@@ -122,11 +122,26 @@ __device__ int offsets_and_tiles(const RouteArgs& a, int tot, int* scratch) {
     a.offsets[tid] = excl;
   }
   if (tid == 0) a.offsets[Ep] = total_rows;
-  int t1 = 0, t2 = 0;
-  if (tid < Ep) {
-    t1 = (tot + a.bn_l1 - 1) / a.bn_l1 * a.fb_l1;
-    t2 = (tot + a.bn_l2 - 1) / a.bn_l2 * a.fb_l2;
+  // Tile order. With per-expert tile widths (dual_sms > 0): the experts with
+  // more than one token tile ("heavy", compute bound) first, then the rest
+  // (weight-stream bound), each group in expert order, so that each class's
+  // launch takes one range of tiles. Otherwise the expert order (nheavy = 0).
+  __shared__ int pt1[kMaxExperts], pt2[kMaxExperts];
+  int nheavy = 0, p = tid;
+  bool heavy = false;
+  if (a.dual_sms > 0) {
+    heavy = tid < Ep && tot > a.bn_l1;
+    const int hrank = block_exclusive_scan(heavy ? 1 : 0, scratch, &nheavy);
+    p = heavy ? hrank : nheavy + (tid - hrank);
   }
+  if (tid < Ep) {
+    const int bn1 = heavy ? a.bn_heavy : a.bn_l1, bn2 = heavy ? a.bn_heavy : a.bn_l2;
+    pt1[p] = (tot + bn1 - 1) / bn1 * a.fb_l1;
+    pt2[p] = (tot + bn2 - 1) / bn2 * a.fb_l2;
+    a.eorder[p] = tid;
+  }
+  __syncthreads();
+  const int t1 = tid < Ep ? pt1[tid] : 0, t2 = tid < Ep ? pt2[tid] : 0;
   int n1, n2;
   const int e1 = block_exclusive_scan(t1, scratch, &n1);
   const int e2 = block_exclusive_scan(t2, scratch, &n2);
@@ -138,6 +153,22 @@ __device__ int offsets_and_tiles(const RouteArgs& a, int tot, int* scratch) {
     a.tiles_l1[Ep] = n1;
     a.tiles_l2[Ep] = n2;
   }
+  // the heavy experts' tiles: the prefix at position nheavy (all tiles when
+  // every expert is heavy)
+  if (tid == (nheavy < Ep ? nheavy : 0)) {
+    const int h1 = nheavy < Ep ? e1 : n1;
+    a.tiles_l1[Ep + 1] = h1;
+    a.tiles_l2[Ep + 1] = nheavy < Ep ? e2 : n2;
+    if (a.dual_sms > 0) {
+      // the heavy class's share of the SMs, by the classes' weighted L1 tiles
+      const long long cw = (long long)h1 * kCostHeavyTile, cl = (long long)(n1 - h1) * kCostLightTile;
+      int g = cw + cl > 0 ? (int)((2 * cw * a.dual_sms + (cw + cl)) / (2 * (cw + cl))) : 0;
+      if (cw > 0 && g < 1) g = 1;
+      if (cl > 0 && g > a.dual_sms - 1) g = a.dual_sms - 1;
+      a.sched[kSchedHeavyCtas] = g;
+    }
+  }
+  if (tid == 0) a.sched[kSchedHeavyExperts] = nheavy;
   // Expert-parallel-ready outputs. With the routed experts split over ranks in
   // contiguous blocks, the expert-major order is also rank-major, so each
   // destination rank's rows are one range of the sorted order. The shared
@@ -487,12 +518,12 @@ extern "C" int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, v
   return (int)mm::launch_kernel(mm::gather_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, true, *a);
 }
 
-extern "C" int mm_launch_combine(const mm::CombineArgs* a, void* stream) {
+extern "C" int mm_launch_combine(const mm::CombineArgs* a, void* stream, bool pdl) {
   if (a->T <= 0) return 0;
   const long threads = (long)a->T * (a->H / 8);
   long blocks = (threads + 127) / 128;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  return (int)mm::launch_kernel(mm::combine_kernel, dim3((unsigned)blocks), dim3(128), 0, (cudaStream_t)stream, true,
+  return (int)mm::launch_kernel(mm::combine_kernel, dim3((unsigned)blocks), dim3(128), 0, (cudaStream_t)stream, pdl,
                                 *a);
 }
 

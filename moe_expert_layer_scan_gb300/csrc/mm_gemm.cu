@@ -110,11 +110,6 @@ struct GemmCfg {
   static constexpr int XBARS = PROMO ? 8 : 0;
   static constexpr int BAR_BYTES =
       ((3 * STAGES + 4 + 2 * RAW_G_MAX + 2 * RING + XBARS) * 8 + 8 + 4 * RING + 15) / 16 * 16;
-  // copies of the two tile tables and the row offsets ([experts + 1] each)
-  static constexpr int TAB_OFF = BAR_OFF + BAR_BYTES;
-  static constexpr int TAB_INTS = (NA > 2 ? kQuadMaxExperts : DEEP ? kDeepMaxExperts : kMaxExperts) + 1;
-  // L2 tiles whose L1 rows the producer has seen stored (fused schedule)
-  static constexpr int L2RDY_OFF = TAB_OFF + 3 * TAB_INTS * 4;
   // TMA-loaded scale rows: RAW_G groups of four K steps; per group 16 bytes of
   // each of 128 rows for each weight block and of RAW_B_ROWS token rows
   static constexpr int RAW_G = PROMO ? 1 : DEEP || NA > 2 ? 2 : 3;  // (PROMO: unused, kept well-formed)
@@ -125,8 +120,18 @@ struct GemmCfg {
   static constexpr int RAW_GROUP_BYTES = NA * RAW_ROWS_BYTES + RAW_B_BYTES;
   // PROMO: per-quadrant column maxima exchanged by the L1 epilogue warps,
   // [2 buffers][2 warp halves][4 quadrants][32 columns] floats
-  static constexpr int XA_OFF = L2RDY_OFF + 16;
   static constexpr int XA_BYTES = PROMO ? 2 * 2 * 4 * 32 * 4 : 0;
+  // copies of the two tile tables and the row offsets ([experts + 1] each),
+  // and, where shared memory has room, of the tile-order expert list
+  static constexpr int TAB_OFF = BAR_OFF + BAR_BYTES;
+  static constexpr int TAB_INTS = (NA > 2 ? kQuadMaxExperts : DEEP ? kDeepMaxExperts : kMaxExperts) + 1;
+  static constexpr int smem_with(int tables) {
+    return ((TAB_OFF + tables * TAB_INTS * 4 + 16 + XA_BYTES + 127) / 128 * 128) + RAW_G * RAW_GROUP_BYTES + 1024;
+  }
+  static constexpr bool EO_SMEM = smem_with(4) <= 232448;
+  // L2 tiles whose L1 rows the producer has seen stored (fused schedule)
+  static constexpr int L2RDY_OFF = TAB_OFF + (EO_SMEM ? 4 : 3) * TAB_INTS * 4;
+  static constexpr int XA_OFF = L2RDY_OFF + 16;
   static constexpr int RAW_OFF = (XA_OFF + XA_BYTES + 127) / 128 * 128;
   static constexpr int SMEM_BYTES = RAW_OFF + RAW_G * RAW_GROUP_BYTES + 1024;  // + alignment slack
   // TMEM columns: the accumulator buffers, then one scale-factor slot per
@@ -167,14 +172,15 @@ struct Tile {
   bool active;  // this CTA has a weight tile (fb < fb_total)
 };
 
-// Tile index -> expert, token tile and weight tile. The tile table and the
-// row offsets are shared-memory copies. An expert's rows are
+// Tile index -> expert, token tile and weight tile. The tile table (in tile
+// order: position j holds expert eorder[j]) and the row offsets are
+// shared-memory copies. An expert's rows are
 // split into the fewest token tiles of at most bn rows, all of one size
 // rounded up to 16 (the last takes the rest): 256 rows with bn = 224 give two
 // tiles of 128, not 224 + 32 (a tile costs its weight stream and a per-K-step
 // instruction floor whatever its row count).
-static __device__ __noinline__ Tile decode_tile(int tile, const int* tstart, const int* offs, int Ep, int fb_total,
-                                           int bn) {
+static __device__ __noinline__ Tile decode_tile(int tile, const int* tstart, const int32_t* eorder, const int* offs,
+                                           int Ep, int fb_total, int bn) {
   int lo = 0, hi = Ep - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -182,15 +188,15 @@ static __device__ __noinline__ Tile decode_tile(int tile, const int* tstart, con
     else hi = mid - 1;
   }
   Tile t;
-  t.e = lo;
+  t.e = eorder ? eorder[lo] : lo;  // (null: the tile order is the expert order)
   const int local = tile - tstart[lo];
-  const int cnt = offs[lo + 1] - offs[lo];
+  const int cnt = offs[t.e + 1] - offs[t.e];
   const int ntt = (cnt + bn - 1) / bn;
   t.fb = local / ntt;
   const int tt = local - t.fb * ntt;
   t.active = t.fb < fb_total;
   const int per = ((cnt + ntt - 1) / ntt + 15) & ~15;  // <= bn, and (ntt - 1) * per < cnt
-  t.row0 = offs[lo] + tt * per;
+  t.row0 = offs[t.e] + tt * per;
   t.nrows = min(per, cnt - tt * per);
   return t;
 }
@@ -340,15 +346,20 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
   int* s_t1 = reinterpret_cast<int*>(smem + C::TAB_OFF);  // L1 tile table
   int* s_t2 = s_t1 + C::TAB_INTS;                         // L2 tile table
   int* s_off = s_t2 + C::TAB_INTS;                        // row offsets per expert
+  int* s_eo = s_off + C::TAB_INTS;                        // tile-order expert list (EO_SMEM)
   {
     const GemmArgs& ga = MODE == kModeL2 ? g2 : g1;
     for (int i = threadIdx.x; i <= ga.Ep; i += blockDim.x) {
       if (MODE != kModeL2) s_t1[i] = g1.tile_start[i];
       if (MODE != kModeL1) s_t2[i] = g2.tile_start[i];
       s_off[i] = ga.offsets[i];
+      if (C::EO_SMEM && i < ga.Ep) s_eo[i] = ga.eorder[i];
     }
   }
   __syncthreads();
+  // the tile order is the expert order when every expert is heavy or none is
+  const int nheavy = g1.sched[kSchedHeavyExperts];
+  const int32_t* eord = nheavy == 0 || nheavy == g1.Ep ? nullptr : C::EO_SMEM ? s_eo : g1.eorder;
   const uint32_t tmem = *tmem_slot;
   // tiles [0, n1) are L1 tiles, [n1, num_tiles) L2 tiles
   const int n1 = MODE == kModeL2 ? 0 : s_t1[g1.Ep];
@@ -356,8 +367,27 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
   auto is_l1 = [&](int tile) { return MODE == kModeL1 || (MODE == kModeFused && tile < n1); };
   // flat tile index -> tile of its phase
   auto tile_of = [&](int tile, bool l1) {
-    return decode_tile(l1 ? tile : tile - n1, l1 ? s_t1 : s_t2, s_off, g1.Ep, l1 ? g1.fb_total : g2.fb_total, BN);
+    return decode_tile(l1 ? tile : tile - n1, l1 ? s_t1 : s_t2, eord, s_off, g1.Ep,
+                       l1 ? g1.fb_total : g2.fb_total, BN);
   };
+  // Per-expert tile widths (split schedule): this launch serves one class of
+  // experts, the heavy ones (tiles [0, h) of the phase, on the first
+  // sched[kSchedHeavyCtas] CTAs) or the others (tiles [h, end), on the CTAs
+  // below grid - sched[kSchedHeavyCtas]); the other CTAs leave at once, so the
+  // two classes' launches share the SMs.
+  int t_lo = 0, t_hi = num_tiles;
+  bool cta_serves = true;
+  if (g1.tile_class != 0) {
+    const int h = g1.tile_start[g1.Ep + 1];  // (single-linear launch: g1 is its own phase)
+    const int heavy_ctas = g1.sched[kSchedHeavyCtas];
+    if (g1.tile_class == 2) {
+      t_hi = h;
+      cta_serves = (int)blockIdx.x < heavy_ctas;
+    } else {
+      t_lo = h;
+      cta_serves = (int)blockIdx.x < (int)gridDim.x - heavy_ctas;
+    }
+  }
   // wait site of the tile ring (status bit 8 + 15)
   constexpr uint32_t kSiteRing = 15u;
   // Dynamic tile schedule: the producer claims tiles from the launch's
@@ -371,7 +401,9 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
   // grid is resident at once.
   // Consumer side: the next tile of this CTA, num_tiles or more when there are
   // no more, -1 when the wait gave up. whole_warp: all 32 lanes call it (else
-  // one thread).
+  // one thread). Each consumer takes its next tile early, during the current
+  // one (the producer publishes it during the current tile's second stage),
+  // so that the hand-off stays off the path between two tiles.
   auto take_tile = [&](uint32_t& n, bool whole_warp) -> int {
     const int slot = (int)(n % C::RING);
     const uint32_t ph = (n / C::RING) & 1u;
@@ -424,15 +456,21 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
     bool cur_ready = false;  // the current tile's counter was seen complete by a peek
     // transaction bytes of one 128x128 weight box: packed E2M1 or E4M3
     const uint32_t a_tx = g1.w_fp8 ? (uint32_t)(C::BM * C::BK) : (uint32_t)C::A_TX;
-    // claim: lane 0's atomic on the launch's tile counter (its result is read
-    // later, so the round trip overlaps the next stage's wait); publish: the
-    // index into the next ring slot once every consumer has read its old one
-    int claimed = 0;
-    auto claim = [&]() {
-      if (lane == 0) claimed = atomicAdd(g1.tile_ctr, 1);
+    // claim: lane 0's atomic on the launch's tile counter; two claims are in
+    // flight (the next tile's and the one after), each read a whole tile after
+    // it was issued, so the atomic's round trip never stalls the loads.
+    // publish: the index into the next ring slot once every consumer has read
+    // its old one. (A claimed tile is always processed by this running CTA
+    // after its current one, and claims rise monotonically, so an L2 tile is
+    // never claimed ahead of an L1 tile a running CTA still has to claim.)
+    int claim_a = 0, claim_b = 0;
+    bool next_in_a = true;  // which of the two holds the next tile's claim
+    auto claim = [&](int& c) {
+      if (lane == 0) c = cta_serves ? t_lo + atomicAdd(g1.tile_ctr, 1) : t_hi;
     };
-    auto publish = [&]() -> int {
-      const int t = __shfl_sync(0xffffffffu, claimed, 0);
+    auto publish = [&](int c) -> int {
+      int t = __shfl_sync(0xffffffffu, c, 0);
+      if (t >= t_hi) t = num_tiles;  // no more tiles of this launch
       const int slot = (int)(pub % C::RING);
       const uint32_t ph = (pub / C::RING) & 1u;
       if (!mbar_wait(&tr_empty[slot], ph ^ 1u, abort_flag, g1.status, g1.timeout_ns, kSiteRing)) return -1;
@@ -444,9 +482,16 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       ++pub;
       return t;
     };
-    claim();
-    int tile = publish();
+    claim(claim_a);
+    int tile = publish(claim_a);
+    claim(claim_a);  // the second tile, in flight during the first
     ok = tile >= 0;
+    // the next tile's index: published during the current tile's second stage
+    auto publish_next = [&]() -> int {
+      const int t = next_in_a ? publish(claim_a) : publish(claim_b);
+      next_in_a = !next_in_a;
+      return t;
+    };
     while (ok && tile < num_tiles) {
       const bool l1 = is_l1(tile);
       const Phase g = phase_of(l1, g1, g2);
@@ -492,7 +537,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           ++gi;
         }
         if (kb == 1) {
-          ntile = publish();
+          ntile = publish_next();
           if (ntile < 0) { ok = false; break; }
           // fused: peek at the next L2 tile's counter (usually complete by the time it starts)
           if (MODE == kModeFused && ntile < num_tiles && !is_l1(ntile)) {
@@ -513,11 +558,14 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
             if ((amask >> u) & 1u) tma_load_2d(sA + u * C::A_BYTES, tw, &full[s], kb * C::BK, block_wrow(g, t, u, C::NA));
           tma_load_2d(sB, ta, &full[s], kb * C::BK, t.row0);
         }
-        if (kb == 0) claim();
+        if (kb == 0) {  // the tile after next
+          if (next_in_a) claim(claim_b);
+          else claim(claim_a);
+        }
       }
       if (!ok) break;
       if (kblocks == 1) {
-        ntile = publish();
+        ntile = publish_next();
         if (ntile < 0) { ok = false; break; }
       }
       cur_ready = next_ready;
@@ -545,9 +593,9 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
     constexpr int NB = C::SFB_ROWS / 32;
     uint32_t it = 0, gi = 0, tn = 0;
     bool ok = true;
-    for (;;) {
-      const int tile = take_tile(tn, true);
-      if (tile < 0 || tile >= num_tiles) break;
+    int tile = take_tile(tn, true);
+    while (tile >= 0 && tile < num_tiles) {
+      int next = -2;  // the next tile, taken after this tile's first scale group
       const bool l1 = is_l1(tile);
       const Phase g = phase_of(l1, g1, g2);
       const uint32_t site0 = l1 ? 0u : 8u;
@@ -594,8 +642,10 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           if (lane == 0) copy_scales(s, amask, sF);
           ++it;
         }
+        if (ok && kg == 0) next = take_tile(tn, true);
       }
       if (!ok) break;
+      tile = next == -2 ? take_tile(tn, true) : next;
     }
   } else if (warp == 3 && !PROMO && C::NA == 2) {
     // ------------------------------------------------------------ scale-factor producer
@@ -731,9 +781,10 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       uint32_t it = 0, tcount = 0, tn = 0, pk = 0;  // pk: K blocks issued (PROMO partial buffers)
       uint32_t hc0 = 0, hc1 = 0, nt = 0;  // HALF: uses of each half, the next narrow tile's half
       bool ok = true;
+      int tile = take_tile(tn, false);
       for (;; ++tcount) {
-        const int tile = take_tile(tn, false);
         if (tile < 0 || tile >= num_tiles) break;
+        int next = -2;  // the next tile, taken after this tile's first K step
         const bool l1 = is_l1(tile);
         const Phase g = phase_of(l1, g1, g2);
         const uint32_t site0 = l1 ? 0u : 8u;
@@ -763,8 +814,10 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
             }
             tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
             tc_commit(&tfull[pb]);  // the partial sum is complete
+            if (kb == 0) next = take_tile(tn, false);
           }
           if (!ok) break;
+          tile = next == -2 ? take_tile(tn, false) : next;
           continue;
         }
         int buf = C::ACC_BUFS == 2 ? (int)(tcount & 1u) : 0;
@@ -812,6 +865,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
             }
           }
           tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+          if (kb == 0) next = take_tile(tn, false);
         }
         if (!ok) break;
         if (C::HALF && !narrow) {
@@ -824,6 +878,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           tc_commit(&tfull[buf]);
           if (C::HALF) (buf ? hc1 : hc0) += 1u;
         }
+        tile = next == -2 ? take_tile(tn, false) : next;
       }
     }
     __syncwarp();
@@ -835,8 +890,8 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
     const int half = (warp - 4) >> 2;  // 0 when there is one warp per quadrant
     uint32_t tcount = 0, tn = 0, pk = 0, xc = 0;  // pk, xc: PROMO partial sums and amax exchanges
     uint32_t hc0 = 0, hc1 = 0, nt = 0;             // HALF: as the MMA warps count them
+    int tile = take_tile(tn, true);
     for (;; ++tcount) {
-      const int tile = take_tile(tn, true);
       if (tile < 0 || tile >= num_tiles) break;
       const bool l1 = is_l1(tile);
       const Phase g = phase_of(l1, g1, g2);
@@ -871,52 +926,90 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         const int KB = g.K / C::BK;
         const float* wsf = reinterpret_cast<const float*>(g.w_sf);
         const float* asf = reinterpret_cast<const float*>(g.act_sf);
-        // fused L2 tiles: their activation scales were stored during this
-        // launch (the producer saw the tile's counter complete before loading it)
+        // fused L2 tiles: their activation scales are stored during this launch
+        // by the L1 epilogues of the token tile, so wait (acquire, bounded) for
+        // the tile's arrival counter before reading any of them; this warp may
+        // take the tile from the ring before the producer has seen it complete
         const bool fresh = MODE == kModeFused && !l1;
         if (fresh) {
-          if (lane == 0) (void)ld_acquire_gpu(g1.ready + t.row0);
-          __syncwarp();
+          int rdy = 1;
+          if (lane == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_gpu(g1.ready + t.row0) < g1.ready_target) {
+              __nanosleep(64);
+              if (*abort_flag) { rdy = 0; break; }
+              if (globaltimer_ns() - t0 > g1.timeout_ns) {
+                *abort_flag = 1;
+                atomicOr(g1.status, MM_DEV_TIMEOUT | (1u << (8u + kSiteReady)));
+                rdy = 0;
+                break;
+              }
+            }
+          }
+          rdy = __shfl_sync(0xffffffffu, rdy, 0);
+          __syncwarp();  // orders lane 0's acquire before the other lanes' loads
+          if (!rdy) break;
         }
         float acc[C::NA][CH][16];
-        bool ok = true;
-        for (int kb = 0; kb < KB; ++kb, ++pk) {
-          const int pb = (int)(pk & 1u);
-          if (!mbar_wait(&tfull[pb], (pk >> 1) & 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 64)) {
-            ok = false;
-            break;
+        // scales of K block kb: lane l < 16 holds the activation scale of column
+        // chunk_col(i) + l (shuffled to the other lanes), sw[u] the weight
+        // block's; the next block's are loaded before waiting for this one
+        auto load_sa = [&](int kb, float (&sa)[CH]) {
+#pragma unroll
+          for (int i = 0; i < CH; ++i) {
+            const int col = chunk_col(i) + (lane & 15);
+            const float* ap = asf + (size_t)(t.row0 + col) * KB + kb;
+            sa[i] = col < t.nrows ? (fresh ? __ldcg(ap) : __ldg(ap)) : 0.0f;
           }
-          tc_fence_after();
-          uint32_t r[C::NA][CH][16];
-#pragma unroll
-          for (int u = 0; u < C::NA; ++u)
-#pragma unroll
-            for (int i = 0; i < CH; ++i)
-              if (chunk_col(i) < t.nrows && block_active(g, t, u, C::NA))
-                tmem_ld_x16(tmem + lanes + (uint32_t)(C::PART_BASE + pb * C::ACC_COLS + u * BN + chunk_col(i)),
-                            r[u][i]);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[pb]);
-          float sw[C::NA];
+        };
+        auto load_sw = [&](int kb, float (&sw)[C::NA]) {
 #pragma unroll
           for (int u = 0; u < C::NA; ++u)
             sw[u] = block_active(g, t, u, C::NA) ? __ldg(wsf + (size_t)(block_wrow(g, t, u, C::NA) / 128) * KB + kb)
                                                  : 0.0f;
+        };
+        float sa_n[CH], sw_n[C::NA];
+        load_sa(0, sa_n);
+        load_sw(0, sw_n);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++pk) {
+          float sa[CH], sw[C::NA];
 #pragma unroll
-          for (int i = 0; i < CH; ++i) {
-            if (chunk_col(i) >= t.nrows) continue;
+          for (int i = 0; i < CH; ++i) sa[i] = sa_n[i];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int col = chunk_col(i) + j;
-              const float* ap = asf + (size_t)(t.row0 + col) * KB + kb;
-              const float sa = col < t.nrows ? (fresh ? __ldcg(ap) : __ldg(ap)) : 0.0f;
+          for (int u = 0; u < C::NA; ++u) sw[u] = sw_n[u];
+          if (kb + 1 < KB) {
+            load_sa(kb + 1, sa_n);
+            load_sw(kb + 1, sw_n);
+          }
+          const int pb = (int)(pk & 1u);
+          if (!mbar_wait(&tfull[pb], (pk >> 1) & 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
-              for (int u = 0; u < C::NA; ++u) {
+          for (int u = 0; u < C::NA; ++u) {
+            uint32_t r[CH][16];
+            const bool act = block_active(g, t, u, C::NA);
+#pragma unroll
+            for (int i = 0; i < CH; ++i)
+              if (act && chunk_col(i) < t.nrows)
+                tmem_ld_x16(tmem + lanes + (uint32_t)(C::PART_BASE + pb * C::ACC_COLS + u * BN + chunk_col(i)), r[i]);
+            tmem_ld_wait();
+            if (u + 1 == C::NA) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&tempty[pb]);  // this partial buffer may be overwritten
+            }
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
                 // (columns past the tile's rows, and absent blocks, stay 0)
-                const float part = col < t.nrows && sw[u] != 0.0f
-                                       ? __fmul_rn(__uint_as_float(r[u][i][j]), __fmul_rn(sa, sw[u]))
+                const float sj = __shfl_sync(0xffffffffu, sa[i], j);
+                const float part = act && chunk_col(i) + j < t.nrows
+                                       ? __fmul_rn(__uint_as_float(r[i][j]), __fmul_rn(sj, sw[u]))
                                        : 0.0f;
                 acc[u][i][j] = kb == 0 ? part : __fadd_rn(acc[u][i][j], part);
               }
@@ -939,6 +1032,8 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         const uint32_t ph = C::HALF ? ((buf ? hc1 : hc0) & 1u) : bph;
         if (!mbar_wait(&tfull[buf], ph, abort_flag, g1.status, g1.timeout_ns, site0 + 3, 256)) break;
       }
+      // the next tile (published long before this one's accumulator completed)
+      const int next = take_tile(tn, true);
       tc_fence_after();
       const uint32_t tbase = tmem + lanes + acc_base;
       if (MODE != kModeL2 && l1) {
@@ -1082,6 +1177,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         if (!PROMO && lane == 0) mbar_arrive(&tempty[buf]);
         if (C::HALF) (buf ? hc1 : hc0) += 1u;
       }
+      tile = next;
     }
   }
 
@@ -1107,10 +1203,11 @@ static int set_smem_attr(int* max_ctas) {
 }
 
 template <int MODE, int BN, int STAGES, int NA = 2, bool PROMO = false>
-static int launch(const GemmMaps* maps, const GemmArgs* g1, const GemmArgs* g2, int num_ctas, cudaStream_t st) {
+static int launch(const GemmMaps* maps, const GemmArgs* g1, const GemmArgs* g2, int num_ctas, cudaStream_t st,
+                  bool pdl = true) {
   using C = GemmCfg<BN, STAGES, NA, PROMO>;
   return (int)launch_kernel(gemm_kernel<MODE, BN, STAGES, NA, PROMO>, dim3((unsigned)num_ctas),
-                            dim3(Warps<BN, NA>::THREADS), C::SMEM_BYTES, st, true, *maps, *g1, *g2);
+                            dim3(Warps<BN, NA>::THREADS), C::SMEM_BYTES, st, pdl, *maps, *g1, *g2);
 }
 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
@@ -1200,6 +1297,20 @@ extern "C" int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, con
          : variant == 4 ? launch<kModeL2, kBnSmall, kStagesQuad, 4>(maps, a, a, n, st)
          : variant == 5 ? launch<kModeL2, kBnMid, kStagesMid>(maps, a, a, n, st)
                         : launch<kModeL2, kBnLarge, kStagesLarge>(maps, a, a, n, st);
+}
+
+extern "C" int mm_launch_gemm_class(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a,
+                                    void* stream) {
+  using namespace mm;
+  cudaStream_t st = (cudaStream_t)stream;
+  // the heavy class runs 224-token tiles, the light class 112-token tiles
+  if (variant == 3)
+    return l1 ? launch<kModeL1, kBnWide, kStagesWide>(maps, a, a, g_ctas[kModeL1][3], st, false)
+              : launch<kModeL2, kBnWide, kStagesWide>(maps, a, a, g_ctas[kModeL2][3], st, false);
+  if (variant == 1)
+    return l1 ? launch<kModeL1, kBnLarge, kStagesLarge>(maps, a, a, g_ctas[kModeL1][1], st, false)
+              : launch<kModeL2, kBnLarge, kStagesLarge>(maps, a, a, g_ctas[kModeL2][1], st, false);
+  return (int)cudaErrorInvalidValue;
 }
 
 extern "C" int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const mm::GemmArgs* g1,

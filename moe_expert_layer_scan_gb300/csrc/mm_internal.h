@@ -17,9 +17,20 @@ constexpr int kRowMargin = 256;    // pool rows beyond the last valid row that t
 constexpr int kRouteChunk = 8192;  // slots per CTA when routing runs on several CTAs
 constexpr int kRouteSingleMax = 16384;  // up to this many slots, one CTA routes everything
 constexpr int kRouteSmallMax = 512;     // up to this many slots, the lean one-CTA routing kernel
-// Tile counters of the persistent GEMM launches (0: the L1 or fused launch,
-// 1: the L2 launch of the split schedule), zeroed by the routing kernel.
-constexpr int kSchedCounters = 4;
+// Scheduling words of a forward, zeroed by the routing kernel: the tile
+// counters of the persistent GEMM launches (0: the L1 or fused launch, 1: the
+// L2 launch of the split schedule) and the number of heavy experts (those
+// with more than one token tile; the tile order puts them first).
+constexpr int kSchedCounters = 8;
+constexpr int kSchedHeavyExperts = 4;
+// Per-expert tile widths (two concurrent launches, one per expert class): the
+// heavy experts' tiles run 224 tokens wide on kSchedHeavyCtas of the SMs, the
+// others 112 wide on the rest; counters 0/1 are the light class's L1/L2
+// launches, 2/3 the heavy class's. The routing kernel splits the SMs in
+// proportion to each class's tiles weighted by their measured relative cost
+// (a heavy 224-token tile computes up to twice the rows of a light tile).
+constexpr int kSchedHeavyCtas = 5;
+constexpr int kCostHeavyTile = 3, kCostLightTile = 2;
 
 // Token-tile widths (the largest MMA N) of the GEMM variants. "small" serves
 // decode-like calls (few rows per expert), "large" and "wide" everything else;
@@ -53,8 +64,8 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Byte offsets of every workspace region for one (shape, T).
 struct Layout {
-  size_t status, sched, counts, offsets, tiles_l1, tiles_l2, rank_offsets, perm, pos, row_w, chunk_cnt, chunk_base,
-      chunk_bad, ready;
+  size_t status, sched, counts, offsets, tiles_l1, tiles_l2, eorder, rank_offsets, perm, pos, row_w, chunk_cnt,
+      chunk_base, chunk_bad, ready;
   size_t pool_x, pool_sf, l2a, l2a_sf, z, total;
   int rows_cap;
 };
@@ -70,8 +81,9 @@ inline Layout make_layout(int E, int S, int H, int I, int k, int T) {
   L.sched = take(sizeof(int32_t) * kSchedCounters, 256);
   L.counts = take(sizeof(int32_t) * Ep, 256);
   L.offsets = take(sizeof(int32_t) * (Ep + 1), 256);
-  L.tiles_l1 = take(sizeof(int32_t) * (Ep + 1), 256);
-  L.tiles_l2 = take(sizeof(int32_t) * (Ep + 1), 256);
+  L.tiles_l1 = take(sizeof(int32_t) * (Ep + 2), 256);
+  L.tiles_l2 = take(sizeof(int32_t) * (Ep + 2), 256);
+  L.eorder = take(sizeof(int32_t) * Ep, 256);
   L.rank_offsets = take(sizeof(int32_t) * (E + 1), 256);
   L.perm = take(sizeof(int32_t) * (R + 1), 256);
   L.pos = take(sizeof(int32_t) * (R + 1), 256);
@@ -95,8 +107,13 @@ struct RouteArgs {
   const float* topk_w;
   int32_t* counts;
   int32_t* offsets;
+  // Tile tables in tile order: the experts with more than one token tile
+  // ("heavy") first, then the others, each in expert order; eorder[j] is the
+  // expert at position j, tiles_*[j] the first tile of position j,
+  // tiles_*[Ep] the tile count and tiles_*[Ep + 1] the heavy experts' tiles.
   int32_t* tiles_l1;
   int32_t* tiles_l2;
+  int32_t* eorder;
   int32_t* perm;
   int32_t* pos;
   float* row_w;
@@ -107,7 +124,9 @@ struct RouteArgs {
   int32_t* ready;       // [R + 1] arrival counters of the fused GEMM, zeroed here
   int32_t* sched;       // [kSchedCounters] tile counters of the GEMM launches, zeroed here
   int T, E, k, S;
-  int bn_l1, bn_l2;  // token-tile widths of the two GEMMs
+  int bn_l1, bn_l2;  // token-tile widths of the two GEMMs (per-expert widths: of the light experts)
+  int bn_heavy;      // token-tile width of the heavy experts (bn_l1 unless the widths are per expert)
+  int dual_sms;      // per-expert widths: the SMs to split between the two classes (0: one class)
   int fb_l1, fb_l2;  // weight tiles per expert: I/128 (gate/up pairs) and ceil(H/256)
   // expert-parallel-ready outputs: the routed experts split over ep_ranks
   // destination ranks in contiguous blocks; rank_offsets[g] = first sorted row
@@ -132,7 +151,8 @@ struct GemmArgs {
   const uint8_t* w_sf;        // [Ep * rows_w][K/32] UE8M0
   const uint8_t* act_sf;      // [rows_cap][K/32]     UE8M0
   const int32_t* offsets;     // [Ep + 1]
-  const int32_t* tile_start;  // [Ep + 1]
+  const int32_t* tile_start;  // [Ep + 2] in tile order (see RouteArgs)
+  const int32_t* eorder;      // [Ep] expert at each tile-order position
   const float* row_w;         // L1: top-k weight per pool row
   uint8_t* out_q;             // L1: [rows_cap][I] E4M3
   uint8_t* out_sf;            // L1: [rows_cap][I/32] UE8M0
@@ -151,6 +171,11 @@ struct GemmArgs {
   int ready_target;
   int w_fp8;  // weights are E4M3 (one byte per element) instead of packed E2M1
   int32_t* tile_ctr;  // this launch's tile counter (zero at launch): CTAs claim tiles in index order
+  // 0: every tile of the phase; 1: the light experts' tiles only, on the CTAs
+  // below (grid - sched[kSchedHeavyCtas]); 2: the heavy experts' tiles only,
+  // on the CTAs below sched[kSchedHeavyCtas] (per-expert tile widths)
+  int tile_class;
+  const int32_t* sched;  // the forward's scheduling words (kSched*)
   int sf_tma;  // scale rows are loaded by TMA (every K a multiple of 512, 16-byte aligned scale tensors)
 };
 
@@ -177,13 +202,17 @@ extern "C" {
 int mm_launch_route(const mm::RouteArgs* a, void* stream);
 int mm_route_launches(int slots);  // kernels mm_launch_route enqueues for this many slots
 int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream);
-int mm_launch_combine(const mm::CombineArgs* a, void* stream);
+int mm_launch_combine(const mm::CombineArgs* a, void* stream, bool pdl);
 // variant: 0 = small tiles, 1 = large tiles, 2 = small tiles with six stages
 // (E + S <= kDeepMaxExperts), 3 = 224-token tiles, 4 = small tiles with four
 // weight blocks (E + S <= kQuadMaxExperts, I % 256 == 0), 5 = 64-token tiles
 // (E + S <= kDeepMaxExperts). maps: the launch's tensor maps (a
 // single-linear launch reads w1/a1/wsf1/asf1 for L1 and w2/a2/wsf2/asf2 for L2).
 int mm_launch_gemm(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a, int num_ctas, void* stream);
+// A single-linear launch of the 112- or 224-token tiles (variant 1 or 3) in
+// ordinary stream order (no programmatic serialisation): the per-expert-width
+// launches, which must not hold SMs early.
+int mm_launch_gemm_class(int l1, int variant, const mm::GemmMaps* maps, const mm::GemmArgs* a, void* stream);
 // One persistent launch of both GEMMs: every L1 tile, then every L2 tile; an L2
 // tile starts once the L1 epilogues of its token tile have arrived on `ready`.
 int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const mm::GemmArgs* g1, const mm::GemmArgs* g2,

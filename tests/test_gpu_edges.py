@@ -174,13 +174,15 @@ def test_weight_format_validation_and_switch(orc):
 
 
 def test_tile_policy_validation():
-    """The four widths and the automatic policy are accepted, anything else rejected;
-    64-token tiles exist for at most 300 experts, larger calls run 112-token tiles."""
+    """The four widths, the per-expert widths and the automatic policy are
+    accepted, anything else rejected; 64-token tiles exist for at most 300
+    experts, larger calls run 112-token tiles."""
     import moe_expert_layer_scan_gb300 as mm
     moe = mm.MegaMoE(8, 512, 256, 2, 0)
-    for t in (mm.MM_TILES_16, mm.MM_TILES_64, mm.MM_TILES_112, mm.MM_TILES_224, mm.MM_TILES_AUTO):
+    for t in (mm.MM_TILES_16, mm.MM_TILES_64, mm.MM_TILES_112, mm.MM_TILES_224, mm.MM_TILES_PER_EXPERT,
+              mm.MM_TILES_AUTO):
         mm.mm_set_tile_policy(moe.h, t)
-    for bad in (0, 32, 128, 200, 256):
+    for bad in (1, 32, 128, 200, 256):
         with pytest.raises(mm.MMError):
             mm.mm_set_tile_policy(moe.h, bad)
     mm.mm_set_tile_policy(moe.h, mm.MM_TILES_64)

@@ -46,6 +46,9 @@ SMALL_CASES = {
     "f128_mid": Workload("f128_mid", T=64, H=768, I=384, E=4, k=2, S=1, clamp=3.0, seed=121, w_fmt=2),
     "f128_ragged": Workload("f128_ragged", T=37, H=384, I=384, E=5, k=3, S=1, seed=122, w_fmt=2),
     "f128_multi": Workload("f128_multi", T=300, H=512, I=256, E=2, k=2, seed=123, w_fmt=2),
+    # Zipf-skewed load with a shared expert: experts above and below 112 rows
+    # (both classes of the per-expert tile widths)
+    "dual_mix": Workload("dual_mix", T=256, H=512, I=256, E=16, k=4, S=1, zipf=1.2, seed=124),
 }
 
 
@@ -190,3 +193,29 @@ def test_tile_widths_agree_bit_for_bit(name):
         assert np.array_equal(o, outs[0])
         for k in ("l2a", "l2a_sf", "z"):
             assert np.array_equal(i[k], inters[0][k]), k
+
+
+@pytest.mark.parametrize("name", ["dual_mix", "skewed_t48", "wide_shared", "fp8w_large"])
+def test_per_expert_tile_widths(name, orc):
+    """Per-expert tile widths (split schedule): the heavy experts' 224-token
+    tiles on one launch and the others' 112-token tiles on a concurrent one
+    compute the same sums as one launch of 112-token tiles, bit for bit, and
+    match the oracle (cases with both classes, with only light and with only
+    heavy experts)."""
+    import moe_expert_layer_scan_gb300 as mm
+    w = SMALL_CASES[name]
+    h = workloads.host_inputs(w)
+    ref = oracle_run(orc, w, h)
+    a = G.DeviceRun(w, inputs=h, schedule="split", tiles=mm.MM_TILES_PER_EXPERT)
+    b = G.DeviceRun(w, inputs=h, schedule="split", tiles=112)
+    assert a.moe.launches(w.T) == b.moe.launches(w.T) + 2
+    oa, ob = out_bits(a.run()), out_bits(b.run())
+    ia, ib = a.intermediates(w.T), b.intermediates(w.T)
+    assert ia["status"] == 0 and ib["status"] == 0
+    if name == "dual_mix":
+        c = np.sort(ia["counts"])
+        assert c[-1] > 112 and c[0] <= 112   # both classes present
+    assert np.array_equal(oa, ob)
+    for k in ("l2a", "l2a_sf", "z"):
+        assert np.array_equal(ia[k], ib[k]), k
+    G.assert_out_close(oa, ref["out"])
