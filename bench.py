@@ -503,7 +503,8 @@ def report(args, w, world, main, clk, dec=None, dec_clk=None):
             "config": workload_config(w),
             "parallelism": f"{world} independent replicas" if world > 1 else "1 GPU",
             "gemm_schedule": sched + (" (auto)" if args.schedule == "auto" else ""),
-            "token_tiles": ("per expert (112 / 224)" if args.tiles == 0 else f"{main['tile_width']}")
+            "token_tiles": ("per expert (112 / 224)" if args.tiles == 0
+                            else "224 on CTA pairs" if args.tiles == -2 else f"{main['tile_width']}")
                            + (" (auto)" if args.tiles == -1 else ""),
             "tflops": alg["flops"] * world / (ms / 1e3) / 1e12,
             "hbm_gbs_whole_step": (alg["l1_bytes"] + alg["l2_bytes"]) / (ms / 1e3) / 1e9,
@@ -555,8 +556,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     ap.add_argument("--no-decode-record", action="store_true",
                     help="with the prefill workload, skip the decode-shape record timed after it")
-    ap.add_argument("--tiles", type=int, default=-1, choices=[-1, 0, 16, 64, 112, 224],
-                    help="token-tile width (-1: the library's choice; 0: per expert, by its routed rows)")
+    ap.add_argument("--tiles", type=int, default=-1, choices=[-2, -1, 0, 16, 64, 112, 224],
+                    help="token-tile width (-1: the library's choice; 0: per expert, by its routed rows; "
+                         "-2: 224-token tiles on CTA pairs)")
     ap.add_argument("--schedule", default="auto", choices=["auto", "fused", "split"],
                     help="GEMM schedule: one persistent launch for both linears, one per linear, or the "
                          "library's choice from the rows per expert (default)")

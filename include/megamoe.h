@@ -168,6 +168,19 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
  * count). For load distributions with a few very hot experts and many light
  * ones. Results are identical to the other widths. */
 #define MM_TILES_PER_EXPERT 0
+/* MM_TILES_224_PAIRS: the 224-token tiles of the split schedule on CTA pairs
+ * ("MEGAMOE_SM90_DESIGN" sec. 4.1: pr-304's 2-CTA cluster, the leader CTA
+ * issuing the UMMA and the scale-factor copies into TMEM, double-buffered
+ * TMEM accumulators): clusters of two CTAs compute M = 256 block-scaled MMAs
+ * (tcgen05 cta_group::2), each CTA holding 128 weight rows, half of the token
+ * tile and its own 224-column accumulator, twice, so that each tile's
+ * epilogue runs under the next tile's MMAs. Needs the scale rows by TMA (H
+ * and I multiples of 512, 16-byte aligned scale tensors) and a split call;
+ * other calls run as MM_TILES_224. Results are identical to the other
+ * widths. Measured slower than MM_TILES_224 at prefill: one thread issues
+ * every MMA of a pair, and its per-K-step waits and commits cannot overlap
+ * another issuer's MMAs. */
+#define MM_TILES_224_PAIRS (-2)
 #define MM_TILES_16 16
 #define MM_TILES_64 64
 #define MM_TILES_112 112

@@ -121,6 +121,7 @@ def mm_set_schedule(h: int, schedule="auto") -> None:
 
 MM_TILES_AUTO, MM_TILES_16, MM_TILES_64, MM_TILES_112, MM_TILES_224 = -1, 16, 64, 112, 224
 MM_TILES_PER_EXPERT = 0
+MM_TILES_224_PAIRS = -2
 
 
 def mm_token_tile_width(h: int, T: int) -> int:
@@ -131,8 +132,8 @@ def mm_token_tile_width(h: int, T: int) -> int:
 
 
 def mm_set_tile_policy(h: int, policy: int = MM_TILES_AUTO) -> None:
-    """Token-tile width: MM_TILES_AUTO, MM_TILES_16, MM_TILES_64, MM_TILES_112, MM_TILES_224 or
-    MM_TILES_PER_EXPERT."""
+    """Token-tile width: MM_TILES_AUTO, MM_TILES_16, MM_TILES_64, MM_TILES_112, MM_TILES_224,
+    MM_TILES_PER_EXPERT or MM_TILES_224_PAIRS."""
     _check(lib().mm_set_tile_policy(h, int(policy)), "mm_set_tile_policy")
 
 

@@ -1,5 +1,5 @@
-"""Builds libmegamoe.so (sm_103a) in-tree with nvcc: the three translation
-units compile in parallel, then link into one shared library."""
+"""Builds libmegamoe.so (sm_103a) in-tree with nvcc: the translation units
+compile in parallel, then link into one shared library."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -10,7 +10,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmegamoe.so")
-SOURCES = ["mm_api.cu", "mm_aux.cu", "mm_gemm.cu"]
+SOURCES = ["mm_api.cu", "mm_aux.cu", "mm_gemm.cu", "mm_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-diag-suppress", "1160"]

@@ -41,6 +41,11 @@ struct mm_handle {
   CUtensorMap tm_w2;
   CUtensorMap tm_w1sf;  // scale rows, 16-byte x 128-row boxes
   CUtensorMap tm_w2sf;
+  // CTA-pair L1 launches: W1 and its scale rows in 64-row boxes (keyed by w1 / w1_sf)
+  const void* w1h_key;
+  const void* w1sfh_key;
+  CUtensorMap tm_w1h;
+  CUtensorMap tm_w1sfh;
   // GEMM schedule: MM_SCHEDULE_AUTO / _SPLIT / _FUSED
   int schedule;
   // expert-parallel-ready routing: destination ranks and the caller's
@@ -140,7 +145,7 @@ int variant_for(const mm_handle* h, int T) {
             : rows <= MM_TILES64_MAX_ROWS_PER_EXPERT * ep && h->S == 0              ? MM_TILES_64
                                                                                    : MM_TILES_112;
   if (width == MM_TILES_112 || width == MM_TILES_PER_EXPERT) return 1;  // (per expert: the light class)
-  if (width == MM_TILES_224) return 3;
+  if (width == MM_TILES_224 || width == MM_TILES_224_PAIRS) return 3;
   if (width == MM_TILES_64) return h->E + h->S <= kDeepMaxExperts ? 5 : 1;
   if (h->w_fmt == MM_WEIGHTS_MXFP8 && h->E + h->S <= kQuadMaxExperts && h->I % 256 == 0)
     return 4;
@@ -206,6 +211,7 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
     if (ms > 0) h->timeout_ns = (unsigned long long)ms * 1000000ull;
   }
   h->w1_key = h->w2_key = h->w1sf_key = h->w2sf_key = nullptr;
+  h->w1h_key = h->w1sfh_key = nullptr;
   h->schedule = MM_SCHEDULE_AUTO;
   h->ep_ranks = 1;
   h->expert_stats = nullptr;
@@ -242,7 +248,7 @@ mm_status_t mm_set_schedule(mm_handle_t h, int schedule) {
 
 mm_status_t mm_set_tile_policy(mm_handle_t h, int policy) {
   if (!h || (policy != MM_TILES_AUTO && policy != MM_TILES_16 && policy != MM_TILES_64 && policy != MM_TILES_112 &&
-             policy != MM_TILES_224 && policy != MM_TILES_PER_EXPERT))
+             policy != MM_TILES_224 && policy != MM_TILES_PER_EXPERT && policy != MM_TILES_224_PAIRS))
     return MM_ERR_INVALID_ARG;
   h->tiles = policy;
   return MM_OK;
@@ -251,7 +257,7 @@ mm_status_t mm_set_tile_policy(mm_handle_t h, int policy) {
 mm_status_t mm_set_weight_format(mm_handle_t h, int format) {
   if (!h || (format != MM_WEIGHTS_MXFP4 && format != MM_WEIGHTS_MXFP8 && format != MM_WEIGHTS_FP8_F128))
     return MM_ERR_INVALID_ARG;
-  if (format != h->w_fmt) h->w1_key = h->w2_key = nullptr;  // cached weight maps describe the old layout
+  if (format != h->w_fmt) h->w1_key = h->w2_key = h->w1h_key = nullptr;  // cached weight maps describe the old layout
   h->w_fmt = format;
   return MM_OK;
 }
@@ -318,6 +324,8 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   const int bn1 = tile_width(variant);
   const int bn2 = bn1;
   const bool fused = use_fused(h, T), dual = use_dual(h, T);
+  // CTA pairs: the split schedule's 224-token tiles when asked for (scale rows by TMA)
+  const bool pair = h->tiles == MM_TILES_224_PAIRS && !fused && sf_tma && mm_pair_ctas() >= 2;
 
   RouteArgs ra;
   ra.topk_idx = topk_idx;
@@ -413,6 +421,18 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
     }
     maps.wsf1 = h->tm_w1sf;
     maps.wsf2 = h->tm_w2sf;
+    if (pair) {
+      if (h->w1h_key != w1) {
+        if (!encode_2d(&h->tm_w1h, w1, fp4, (uint64_t)h->H, (uint64_t)Ep * 2 * h->I, 64)) return MM_ERR_CUDA;
+        h->w1h_key = w1;
+      }
+      if (h->w1sfh_key != w1_sf) {
+        if (!encode_sf(&h->tm_w1sfh, w1_sf, (uint64_t)h->H / 32, (uint64_t)Ep * 2 * h->I, 64)) return MM_ERR_CUDA;
+        h->w1sfh_key = w1_sf;
+      }
+      maps.w1h = h->tm_w1h;
+      maps.wsf1h = h->tm_w1sfh;
+    }
     const uint32_t tb = (uint32_t)mm_gemm_token_scale_box_rows(variant);
     if (!encode_sf(&maps.asf1, base + L.pool_sf, (uint64_t)h->H / 32, (uint64_t)L.rows_cap, tb)) return MM_ERR_CUDA;
     if (!encode_sf(&maps.asf2, base + L.l2a_sf, (uint64_t)h->I / 32, (uint64_t)L.rows_cap, tb)) return MM_ERR_CUDA;
@@ -493,9 +513,13 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
       return MM_ERR_CUDA;
   } else {
     mark("l1_gemm");
-    if (mm_launch_gemm(1, variant, &maps, &g1, h->num_sms, stream) != 0) return MM_ERR_CUDA;
+    if ((pair ? mm_launch_gemm_pair(1, &maps, &g1, stream)
+              : mm_launch_gemm(1, variant, &maps, &g1, h->num_sms, stream)) != 0)
+      return MM_ERR_CUDA;
     mark("l2_gemm");
-    if (mm_launch_gemm(0, variant, &maps, &g2, h->num_sms, stream) != 0) return MM_ERR_CUDA;
+    if ((pair ? mm_launch_gemm_pair(0, &maps, &g2, stream)
+              : mm_launch_gemm(0, variant, &maps, &g2, h->num_sms, stream)) != 0)
+      return MM_ERR_CUDA;
   }
 
   CombineArgs ca;

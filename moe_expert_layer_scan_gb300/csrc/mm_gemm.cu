@@ -44,6 +44,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include "mm_common.cuh"
 #include "mm_internal.h"
 #include "mm_ptx.cuh"
 
@@ -167,40 +168,6 @@ struct GemmCfg {
   static_assert(BN % 8 == 0, "token tiles are whole 8-row swizzle atoms");
 };
 
-struct Tile {
-  int e, fb, row0, nrows;
-  bool active;  // this CTA has a weight tile (fb < fb_total)
-};
-
-// Tile index -> expert, token tile and weight tile. The tile table (in tile
-// order: position j holds expert eorder[j]) and the row offsets are
-// shared-memory copies. An expert's rows are
-// split into the fewest token tiles of at most bn rows, all of one size
-// rounded up to 16 (the last takes the rest): 256 rows with bn = 224 give two
-// tiles of 128, not 224 + 32 (a tile costs its weight stream and a per-K-step
-// instruction floor whatever its row count).
-static __device__ __noinline__ Tile decode_tile(int tile, const int* tstart, const int32_t* eorder, const int* offs,
-                                           int Ep, int fb_total, int bn) {
-  int lo = 0, hi = Ep - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tstart[mid] <= tile) lo = mid;
-    else hi = mid - 1;
-  }
-  Tile t;
-  t.e = eorder ? eorder[lo] : lo;  // (null: the tile order is the expert order)
-  const int local = tile - tstart[lo];
-  const int cnt = offs[t.e + 1] - offs[t.e];
-  const int ntt = (cnt + bn - 1) / bn;
-  t.fb = local / ntt;
-  const int tt = local - t.fb * ntt;
-  t.active = t.fb < fb_total;
-  const int per = ((cnt + ntt - 1) / ntt + 15) & ~15;  // <= bn, and (ntt - 1) * per < cnt
-  t.row0 = offs[t.e] + tt * per;
-  t.nrows = min(per, cnt - tt * per);
-  return t;
-}
-
 // The per-phase arguments a role needs for one tile, selected field by field
 // from the L1 or L2 argument block (each a constant-bank read).
 struct Phase {
@@ -246,32 +213,6 @@ __device__ __forceinline__ uint4 load_sf4(const uint8_t* p, bool vec16, int avai
   if (avail > 2) r.z = ld(q + 2);
   if (avail > 3) r.w = ld(q + 3);
   return r;
-}
-
-__device__ __forceinline__ uint32_t word(const uint4& v, int c) {
-  return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
-}
-
-__device__ __forceinline__ void st_shared_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_u32(p)), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
-// UE8M0 code of the smallest power of two >= amax / 448 (IEEE quotient),
-// 127 for amax == 0, clamped to [1, 254].
-__device__ __forceinline__ uint32_t requant_code(float amax) {
-  if (!(amax > 0.0f)) return 127u;
-  const uint32_t b = __float_as_uint(__fdiv_rn(amax, 448.0f));
-  const int e = (int)(b >> 23);
-  int code = (e == 0) ? 1 : (((b & 0x7FFFFFu) == 0u) ? e : e + 1);
-  code = code < 1 ? 1 : (code > 254 ? 254 : code);
-  return (uint32_t)code;
-}
-
-// 2^(127 - code) exactly (a normal or subnormal float for code in [1, 254]).
-__device__ __forceinline__ float inv_scale(uint32_t code) {
-  const int n = 127 - (int)code;
-  return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(1u << (n + 149));
 }
 
 template <int MODE, int BN, int STAGES, int NA, bool PROMO>
@@ -1251,6 +1192,7 @@ extern "C" int mm_gemm_prepare(void) {
   if ((e = set_smem_attr<kModeL1, kBnMid, kStagesPromoMid, 2, true>(&g_ctas[kModeL1][7]))) return e;
   if ((e = set_smem_attr<kModeL2, kBnMid, kStagesPromoMid, 2, true>(&g_ctas[kModeL2][7]))) return e;
   if ((e = set_smem_attr<kModeFused, kBnMid, kStagesPromoMid, 2, true>(&g_ctas[kModeFused][7]))) return e;
+  if ((e = mm_pair_prepare())) return e;
   return 0;
 }
 

@@ -185,7 +185,12 @@ struct GemmMaps {
   CUtensorMap w1, a1, w2, a2;
   CUtensorMap wsf1, asf1, wsf2, asf2;
   // 224-token tiles: token boxes of 112 and 32 rows for the narrower tiles
+  // (the CTA-pair launches load each CTA's half of a token tile with the
+  // 112-row boxes)
   CUtensorMap a1n, a2n, a1s, a2s;
+  // CTA-pair L1 launches: W1 rows and W1 scale rows in boxes of 64 rows (each
+  // CTA's A block is 64 gate rows and the matching 64 up rows)
+  CUtensorMap w1h, wsf1h;
 };
 
 struct CombineArgs {
@@ -217,6 +222,14 @@ int mm_launch_gemm_class(int l1, int variant, const mm::GemmMaps* maps, const mm
 // tile starts once the L1 epilogues of its token tile have arrived on `ready`.
 int mm_launch_gemm_fused(int variant, const mm::GemmMaps* maps, const mm::GemmArgs* g1, const mm::GemmArgs* g2,
                          void* stream);
+// 224-token tiles of the split schedule on CTA pairs (clusters of two CTAs,
+// M = 256 MMAs): each tile covers 256 weight rows (L1: 128 features' gate and
+// up rows; L2: two 128-row W2 blocks) and every CTA double-buffers its
+// 224-column accumulator, so the epilogue of one tile runs under the MMAs of
+// the next. Needs the scale rows by TMA (sf_tma) and an even grid.
+int mm_launch_gemm_pair(int l1, const mm::GemmMaps* maps, const mm::GemmArgs* a, void* stream);
+int mm_pair_prepare(void);  // shared-memory limits and the launch size (CTAs of the clusters resident at once)
+int mm_pair_ctas(void);     // CTAs per CTA-pair launch (0: unavailable)
 int mm_gemm_prepare(void);  // sets the dynamic shared-memory limits and the persistent grid sizes
 int mm_gemm_blocks(int variant);   // 128-row weight blocks per tile (2 or 4)
 int mm_gemm_epilogue_warps(int variant);  // epilogue warps per CTA (arrivals per L1 tile in the fused schedule)

@@ -49,6 +49,12 @@ SMALL_CASES = {
     # Zipf-skewed load with a shared expert: experts above and below 112 rows
     # (both classes of the per-expert tile widths)
     "dual_mix": Workload("dual_mix", T=256, H=512, I=256, E=16, k=4, S=1, zipf=1.2, seed=124),
+    # 224-token tiles on CTA pairs (split schedule, H and I multiples of 512):
+    # full and balanced tiles with a shared expert; E4M3 weights; ragged
+    # experts with clamp and several feature blocks per CTA pair
+    "pair_wide": Workload("pair_wide", T=600, H=1024, I=512, E=3, k=2, S=1, seed=125),
+    "pair_fp8w": Workload("pair_fp8w", T=400, H=512, I=512, E=2, k=2, seed=126, w_fmt=1),
+    "pair_ragged": Workload("pair_ragged", T=333, H=1024, I=1024, E=5, k=3, clamp=3.0, zipf=0.8, seed=127),
 }
 
 
@@ -193,6 +199,30 @@ def test_tile_widths_agree_bit_for_bit(name):
         assert np.array_equal(o, outs[0])
         for k in ("l2a", "l2a_sf", "z"):
             assert np.array_equal(i[k], inters[0][k]), k
+
+
+@pytest.mark.parametrize("name", ["pair_wide", "pair_fp8w", "pair_ragged", "prefill_t256"])
+def test_cta_pair_tiles(name, orc):
+    """224-token tiles on CTA pairs (M = 256 MMAs over two SMs, split
+    schedule): the output, the L2 activations and the per-slot rows match the
+    oracle, and equal the one-CTA 224-token tiles bit for bit (every output
+    element's K loop runs in the same order)."""
+    import moe_expert_layer_scan_gb300 as mm
+    w = SMALL_CASES[name]
+    h = workloads.host_inputs(w)
+    ref = oracle_run(orc, w, h)
+    a = G.DeviceRun(w, inputs=h, schedule="split", tiles=mm.MM_TILES_224_PAIRS)
+    b = G.DeviceRun(w, inputs=h, schedule="split", tiles=224)
+    oa, ob = out_bits(a.run()), out_bits(b.run())
+    ia, ib = a.intermediates(w.T), b.intermediates(w.T)
+    assert ia["status"] == 0 and ib["status"] == 0
+    n = int(ref["offsets"][-1])
+    G.assert_l2a_close(ia["l2a"], ia["l2a_sf"], ref["q"][:n], ref["q_sf"][:n])
+    G.assert_out_close(ia["z"], ref["z"][:n], "L2 per-slot rows")
+    G.assert_out_close(oa, ref["out"])
+    assert np.array_equal(oa, ob)
+    for k in ("l2a", "l2a_sf", "z"):
+        assert np.array_equal(ia[k], ib[k]), k
 
 
 @pytest.mark.parametrize("name", ["dual_mix", "skewed_t48", "wide_shared", "fp8w_large"])
