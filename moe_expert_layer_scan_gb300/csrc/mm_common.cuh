@@ -51,6 +51,32 @@ __device__ __forceinline__ void st_shared_v4(void* p, uint32_t a, uint32_t b, ui
                : "memory");
 }
 
+// One byte per (row, feature) from a chunk held feature-per-lane: lane l's
+// w[c] packs the bytes of feature f0 + l for rows c0 + 4c .. c0 + 4c + 3
+// (byte i: row c0 + 4c + i). Each group of four lanes transposes its 4 x 4
+// blocks (two exchange steps, byte permutes) so that lane 4a + r writes
+// features f0 + 4a .. f0 + 4a + 3 of row c0 + 4c + r as one 4-byte store.
+// Rows at or beyond c0 + nvalid are not written. All 32 lanes call it.
+template <int NW>
+__device__ __forceinline__ void store_u8_rows_4x4(uint8_t* q, size_t ld, int row0, int c0, int nvalid, int f0,
+                                                  const uint32_t (&w)[NW]) {
+  const int lane = threadIdx.x & 31;
+  const bool odd = (lane & 1) != 0, hi = (lane & 2) != 0;
+#pragma unroll
+  for (int c = 0; c < NW; ++c) {
+    // step 1 (lanes 2m, 2m + 1): the even lane keeps rows 0 and 2 of the
+    // group, the odd lane rows 1 and 3, each with both lanes' features
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, w[c], 1);
+    const uint32_t x = odd ? __byte_perm(w[c], r1, 0x3715) : __byte_perm(w[c], r1, 0x6240);
+    // step 2 (lanes 4a + b, 4a + b + 2): the lower lane keeps row b, the
+    // upper row b + 2, each with all four features
+    const uint32_t r2 = __shfl_xor_sync(0xffffffffu, x, 2);
+    const uint32_t out = hi ? __byte_perm(x, r2, 0x3276) : __byte_perm(x, r2, 0x5410);
+    const int row = 4 * c + (lane & 3);
+    if (row < nvalid) *reinterpret_cast<uint32_t*>(q + (size_t)(row0 + c0 + row) * ld + f0 + (lane & ~3)) = out;
+  }
+}
+
 // UE8M0 code of the smallest power of two >= amax / 448 (IEEE quotient),
 // 127 for amax == 0, clamped to [1, 254].
 __device__ __forceinline__ uint32_t requant_code(float amax) {

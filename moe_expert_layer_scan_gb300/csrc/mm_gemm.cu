@@ -1069,12 +1069,14 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           const float inv = inv_scale(code);
           if (col_lead && mycol < ncol)
             g1.out_sf[(size_t)(t.row0 + c0 + mycol) * (g1.I / 32) + fblk * 4 + q] = (uint8_t)code;
+          uint32_t qw[NC / 4];
 #pragma unroll
           for (int j = 0; j < NC; ++j) {
             const float ij = __shfl_sync(0xffffffffu, inv, j << (5 - LOG2NC));
-            const uint8_t qb = (uint8_t)__nv_cvt_float_to_fp8(__fmul_rn(y[j], ij), __NV_SATFINITE, __NV_E4M3);
-            if (j < ncol) g1.out_q[(size_t)(t.row0 + c0 + j) * g1.I + feat] = qb;
+            const uint32_t qb = (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(y[j], ij), __NV_SATFINITE, __NV_E4M3) & 0xFFu;
+            qw[j >> 2] = (j & 3) == 0 ? qb : qw[j >> 2] | (qb << (8 * (j & 3)));
           }
+          store_u8_rows_4x4(g1.out_q, (size_t)g1.I, t.row0, c0, ncol, feat - lane, qw);
           }
         }
         }
@@ -1093,6 +1095,8 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           tmem_ld_x16(tg + (uint32_t)c0, gv);
           tmem_ld_x16(th + (uint32_t)c0, hv);
           tmem_ld_wait();
+          // (measured: 8-byte stores after a 4 x 4 lane transpose, or
+          // evict-first stores, were no faster than these 64-byte rows)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int col = c0 + j;

@@ -447,11 +447,11 @@ __global__ void __launch_bounds__(kPairThreads, 1)
         // lane = W2 row = hidden feature; columns = token rows: BF16 per slot row
         const int blk = 2 * t.fb + (int)rank;
         const bool act = a_active(t);
-        const int feat = blk * 128 + 32 * q + lane;
         for (int c0 = 16 * hcol; act && c0 < t.nrows; c0 += kPairEpiStride) {
           uint32_t v[16];
           tmem_ld_x16(tbase + (uint32_t)c0, v);
           tmem_ld_wait();
+          const int feat = blk * 128 + 32 * q + lane;
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             if (c0 + j < t.nrows)
@@ -531,12 +531,14 @@ __global__ void __launch_bounds__(kPairThreads, 1)
           const float inv = inv_scale(code);
           if ((lane & 3) == 0 && mycol < ncol)
             g.out_sf[(size_t)(t.row0 + cb + mycol) * (g.I / 32) + fgroup] = (uint8_t)code;
+          uint32_t qw[2];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float ij = __shfl_sync(0xffffffffu, inv, j << 2);
-            const uint8_t qb = (uint8_t)__nv_cvt_float_to_fp8(__fmul_rn(y[j], ij), __NV_SATFINITE, __NV_E4M3);
-            if (j < ncol) g.out_q[(size_t)(t.row0 + cb + j) * g.I + feat] = qb;
+            const uint32_t qb = (uint32_t)__nv_cvt_float_to_fp8(__fmul_rn(y[j], ij), __NV_SATFINITE, __NV_E4M3) & 0xFFu;
+            qw[j >> 2] = (j & 3) == 0 ? qb : qw[j >> 2] | (qb << (8 * (j & 3)));
           }
+          store_u8_rows_4x4(g.out_q, (size_t)g.I, t.row0, cb, ncol, feat - lane, qw);
         }
         if (failed) break;
       }
