@@ -46,18 +46,19 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 # capture, keyed by workload, valid only while the GEMM sources hash to `src`
 # (gemm_source_hash) and for the kernel named (fused "gemm" or "l1_gemm").
 NCU_TRAFFIC = {
-    # decode (fused GEMM): E=64 capture (42 experts touched) scaled to the 61 experts one launch touches
-    "decode": {"src": "be902d7cc0cdd9f4", "kernel": "gemm", "bytes": 1441261244},
+    # decode (fused GEMM): E=64 capture (42 experts touched, 992,532,224 bytes) scaled to the 61
+    # experts one launch touches
+    "decode": {"src": "7e9a9affe09eb347", "kernel": "gemm", "bytes": 1441534897},
     # prefill (L1 GEMM of the split schedule, 224-token tiles, one CTA per tile): T=2048/E=32
-    # capture (16384 rows) scaled x8 to 131072 rows
-    "prefill": {"src": "be902d7cc0cdd9f4", "kernel": "l1_gemm", "bytes": 5241108480},
+    # capture (16384 rows, 671,339,520 bytes) scaled x8 to 131072 rows
+    "prefill": {"src": "7e9a9affe09eb347", "kernel": "l1_gemm", "bytes": 5370716160},
 }
 
 
 def gemm_source_hash() -> str:
     """sha256 prefix of the GEMM kernel's sources (kernel, constants, PTX helpers)."""
     h = hashlib.sha256()
-    for name in ("mm_gemm.cu", "mm_internal.h", "mm_ptx.cuh"):
+    for name in ("mm_gemm.cu", "mm_common.cuh", "mm_internal.h", "mm_ptx.cuh"):
         with open(os.path.join(ROOT, "moe_expert_layer_scan_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
