@@ -49,9 +49,11 @@ NCU_TRAFFIC = {
     # decode (fused GEMM): E=64 capture (42 experts touched, 992,532,224 bytes) scaled to the 61
     # experts one launch touches
     "decode": {"src": "7e9a9affe09eb347", "kernel": "gemm", "bytes": 1441534897},
-    # prefill (L1 GEMM of the split schedule, 224-token tiles, one CTA per tile): T=2048/E=32
-    # capture (16384 rows, 671,339,520 bytes) scaled x8 to 131072 rows
-    "prefill": {"src": "7e9a9affe09eb347", "kernel": "l1_gemm", "bytes": 5370716160},
+    # prefill (split schedule, per-expert widths: every expert above 112 rows, so both linears
+    # run the 224-token tiles, one CTA per tile; the light-class launches are empty): T=2048/E=32
+    # capture of the two GEMMs (16384 rows; L1 671,339,520 + L2 482,610,944 bytes) scaled x8 to
+    # 131072 rows
+    "prefill": {"src": "7e9a9affe09eb347", "kernel": "gemms", "bytes": 9231603712},
 }
 
 

@@ -142,17 +142,20 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
  *     with many rows per expert);
  *   MM_TILES_AUTO (the default): MM_TILES_16 while the call routes at most
  *     MM_TILES16_MAX_ROWS_PER_EXPERT rows per expert on average
- *     (T*(topk+S) <= 12*(E+S)), MM_TILES_224 from
- *     MM_TILES224_MIN_ROWS_PER_EXPERT rows per expert, and above
- *     MM_TILES224_MIN_ROWS_PER_EXPERT_FUSED when the call runs fused (there an
- *     expert's 113-128 rows take one 224-token tile instead of two 112-token
- *     tiles), MM_TILES_64 above MM_TILES16_MAX_ROWS_PER_EXPERT and up to
- *     MM_TILES64_MAX_ROWS_PER_EXPERT rows per expert when the call has no
- *     shared expert (a shared expert
- *     receives every token, far above the average, and would take many
- *     64-token tiles) and E <= 300, MM_TILES_112 otherwise:
- *     the crossovers measured on GB300 at H = 7168, I = 2048, 256 experts,
- *     top-8 and at H = 4096, I = 1536, 128 experts, top-8.
+ *     (T*(topk+S) <= 12*(E+S)); above MM_TILES224_MIN_ROWS_PER_EXPERT rows
+ *     per expert MM_TILES_224 when the call runs fused and MM_TILES_PER_EXPERT
+ *     when it runs split (with uniform routing every expert is then above 112
+ *     rows and takes 224-token tiles; a skewed load keeps its light experts
+ *     on 112-token tiles); MM_TILES_64 above MM_TILES16_MAX_ROWS_PER_EXPERT
+ *     and up to MM_TILES64_MAX_ROWS_PER_EXPERT rows per expert when the call
+ *     has no shared expert (a shared expert receives every token, far above
+ *     the average, and would take many 64-token tiles) and E <= 300,
+ *     MM_TILES_112 otherwise: the crossovers measured on GB300 at H = 7168,
+ *     I = 2048, 256 experts, top-8 (above 112 rows per expert an expert's
+ *     rows take one 224-token tile instead of two 112-token ones: 128 rows
+ *     per expert 1.73 against 2.17 ms per forward, 150 rows 1.86 against
+ *     2.27, 192 rows 2.13 against 2.43) and at H = 4096, I = 1536, 128
+ *     experts, top-8.
  * Every width computes the same tiles' sums; the results are identical.
  * Other values: MM_ERR_INVALID_ARG. */
 #define MM_TILES_AUTO (-1)
@@ -165,8 +168,10 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
  * tiles, as two persistent launches per linear that share the SMs (the heavy
  * experts' launches on a stream of the handle, forked from and joined back
  * into the caller's stream; the split of the SMs follows each class's tile
- * count). For load distributions with a few very hot experts and many light
- * ones. Results are identical to the other widths. */
+ * count). MM_TILES_AUTO takes it for every split call above 112 rows per
+ * expert (Zipf-skewed routing with a shared expert, T = 4096: 2.11 against
+ * 2.25 ms per forward with one width). mm_token_tile_width reports 224 for
+ * such calls. Results are identical to the other widths. */
 #define MM_TILES_PER_EXPERT 0
 /* MM_TILES_224_PAIRS: the 224-token tiles of the split schedule on CTA pairs
  * ("MEGAMOE_SM90_DESIGN" sec. 4.1: pr-304's 2-CTA cluster, the leader CTA
@@ -187,8 +192,7 @@ MM_API mm_status_t mm_set_schedule(mm_handle_t h, int schedule);
 #define MM_TILES_224 224
 #define MM_TILES16_MAX_ROWS_PER_EXPERT 12
 #define MM_TILES64_MAX_ROWS_PER_EXPERT 48
-#define MM_TILES224_MIN_ROWS_PER_EXPERT 192
-#define MM_TILES224_MIN_ROWS_PER_EXPERT_FUSED 112
+#define MM_TILES224_MIN_ROWS_PER_EXPERT 112
 MM_API mm_status_t mm_set_tile_policy(mm_handle_t h, int policy);
 
 /* The token-tile width (16, 64, 112 or 224) a call of T tokens runs with under the

@@ -138,13 +138,13 @@ int variant_for(const mm_handle* h, int T) {
   // promoted sums in registers, which wider tiles would not fit)
   if (h->w_fmt == MM_WEIGHTS_FP8_F128)
     return width == MM_TILES_16 || (width == MM_TILES_AUTO && rows <= MM_TILES16_MAX_ROWS_PER_EXPERT * ep) ? 6 : 7;
-  if (width == MM_TILES_AUTO)
-    width = rows <= MM_TILES16_MAX_ROWS_PER_EXPERT * ep    ? MM_TILES_16
-            : rows >= MM_TILES224_MIN_ROWS_PER_EXPERT * ep ? MM_TILES_224
-            : rows > MM_TILES224_MIN_ROWS_PER_EXPERT_FUSED * ep && use_fused(h, T) ? MM_TILES_224
-            : rows <= MM_TILES64_MAX_ROWS_PER_EXPERT * ep && h->S == 0              ? MM_TILES_64
-                                                                                   : MM_TILES_112;
-  if (width == MM_TILES_112 || width == MM_TILES_PER_EXPERT) return 1;  // (per expert: the light class)
+  // (per-expert widths where a call does not run them: as AUTO)
+  if (width == MM_TILES_AUTO || width == MM_TILES_PER_EXPERT)
+    width = rows <= MM_TILES16_MAX_ROWS_PER_EXPERT * ep   ? MM_TILES_16
+            : rows > MM_TILES224_MIN_ROWS_PER_EXPERT * ep ? MM_TILES_224
+            : rows <= MM_TILES64_MAX_ROWS_PER_EXPERT * ep && h->S == 0 ? MM_TILES_64
+                                                                       : MM_TILES_112;
+  if (width == MM_TILES_112) return 1;
   if (width == MM_TILES_224 || width == MM_TILES_224_PAIRS) return 3;
   if (width == MM_TILES_64) return h->E + h->S <= kDeepMaxExperts ? 5 : 1;
   if (h->w_fmt == MM_WEIGHTS_MXFP8 && h->E + h->S <= kQuadMaxExperts && h->I % 256 == 0)
@@ -154,10 +154,16 @@ int variant_for(const mm_handle* h, int T) {
 
 // Whether a call runs per-expert tile widths: two concurrent launches per
 // linear, the experts with more than 112 routed rows on 224-token tiles and
-// the others on 112-token tiles (split schedule, MXFP4/MXFP8 weights).
+// the others on 112-token tiles (split schedule, MXFP4/MXFP8 weights). AUTO
+// takes them for split calls above MM_TILES224_MIN_ROWS_PER_EXPERT rows per
+// expert: with uniform routing every expert is then heavy and the call runs
+// the 224-token tiles alone; with a skewed load the light experts' tiles
+// stay 112 wide.
 bool use_dual(const mm_handle* h, int T) {
   if (h->w_fmt == MM_WEIGHTS_FP8_F128 || use_fused(h, T) || T == 0) return false;
-  return h->tiles == MM_TILES_PER_EXPERT;
+  if (h->tiles == MM_TILES_PER_EXPERT) return true;
+  const long long rows = (long long)T * (h->k + h->S), ep = h->E + h->S;
+  return h->tiles == MM_TILES_AUTO && rows > MM_TILES224_MIN_ROWS_PER_EXPERT * ep;
 }
 
 int tile_width(int variant) {
@@ -284,7 +290,7 @@ mm_status_t mm_workspace_bytes(mm_handle_t h, int T, size_t* bytes) {
 
 mm_status_t mm_token_tile_width(mm_handle_t h, int T, int* width) {
   if (!h || !width || T < 0) return MM_ERR_INVALID_ARG;
-  *width = tile_width(variant_for(h, T));
+  *width = use_dual(h, T) ? kBnWide : tile_width(variant_for(h, T));  // (per expert: the heavy experts' width)
   return MM_OK;
 }
 
@@ -319,11 +325,11 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   // otherwise the scale warp loads them itself (two-block tiles only).
   const bool sf_tma = h->w_fmt != MM_WEIGHTS_FP8_F128 && h->H % 512 == 0 && h->I % 512 == 0 && aligned(w1_sf, 16) &&
                       aligned(w2_sf, 16);
-  int variant = variant_for(h, T);
+  const bool fused = use_fused(h, T), dual = use_dual(h, T);
+  int variant = dual ? 1 : variant_for(h, T);  // (per expert: the light class's tiles)
   if (variant == 4 && !sf_tma) variant = (h->E + h->S <= kDeepMaxExperts) ? 2 : 0;
   const int bn1 = tile_width(variant);
   const int bn2 = bn1;
-  const bool fused = use_fused(h, T), dual = use_dual(h, T);
   // CTA pairs: the split schedule's 224-token tiles when asked for (scale rows by TMA)
   const bool pair = h->tiles == MM_TILES_224_PAIRS && !fused && sf_tma && mm_pair_ctas() >= 2;
 

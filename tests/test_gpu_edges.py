@@ -133,11 +133,11 @@ def test_schedule_choice_and_validation():
     moe = mm.MegaMoE(256, 7168, 2048, 8, 0)
     small = mm.mm_launches_per_run(moe.h, 8)          # 64 rows over 256 experts: fused
     at = mm.mm_launches_per_run(moe.h, 4096)          # 128 rows per expert: still fused
-    above = mm.mm_launches_per_run(moe.h, 4097)       # just above: split (same routing launches)
-    assert above == at + 1
+    above = mm.mm_launches_per_run(moe.h, 4097)       # just above: split, per-expert widths
+    assert above == at + 3                            # (two launch pairs instead of one fused launch)
     n_big = mm.mm_launches_per_run(moe.h, 16384)      # 512 rows per expert: split
     mm.mm_set_schedule(moe.h, "fused")
-    assert mm.mm_launches_per_run(moe.h, 16384) == n_big - 1
+    assert mm.mm_launches_per_run(moe.h, 16384) == n_big - 3
     assert mm.mm_launches_per_run(moe.h, 8) == small
     mm.mm_set_schedule(moe.h, "split")
     assert mm.mm_launches_per_run(moe.h, 8) == small + 1
@@ -193,9 +193,10 @@ def test_tile_policy_validation():
 
 
 def test_token_tile_width_policy():
-    """AUTO: 16-token tiles up to 12 routed rows per expert on average, 224 from
-    192 (or above 112 when the call runs fused), 64 up to 48 without a shared
-    expert, 112 between; a fixed policy is reported as set."""
+    """AUTO: 16-token tiles up to 12 routed rows per expert on average, 224
+    above 112 (per-expert widths, reported as 224, when the call runs split),
+    64 up to 48 without a shared expert, 112 between; a fixed policy is
+    reported as set."""
     import moe_expert_layer_scan_gb300 as mm
     moe = mm.MegaMoE(256, 7168, 2048, 8, 0)
     assert mm.mm_token_tile_width(moe.h, 8) == 16          # decode: 0.25 rows per expert
@@ -210,14 +211,14 @@ def test_token_tile_width_policy():
     assert mm.mm_token_tile_width(moe.h, 3584) == 112      # 112 rows per expert
     assert mm.mm_token_tile_width(moe.h, 3585) == 224      # fused, above 112
     assert mm.mm_token_tile_width(moe.h, 4096) == 224      # 128: still fused
-    assert mm.mm_token_tile_width(moe.h, 4097) == 112      # split from here
-    assert mm.mm_token_tile_width(moe.h, 6143) == 112      # just under 192 rows per expert
-    assert mm.mm_token_tile_width(moe.h, 6144) == 224
+    assert mm.mm_token_tile_width(moe.h, 4097) == 224      # split from here: per-expert widths
     assert mm.mm_token_tile_width(moe.h, 16384) == 224     # prefill: 512 rows per expert
     skewed = mm.MegaMoE(256, 7168, 2048, 8, 1)
-    assert mm.mm_token_tile_width(skewed.h, 4096) == 112   # 143 rows per expert
+    assert mm.mm_token_tile_width(skewed.h, 4096) == 224   # 143 rows per expert, split, per expert
+    assert mm.mm_launches_per_run(skewed.h, 4096) == mm.mm_launches_per_run(moe.h, 4097)
     mm.mm_set_schedule(moe.h, "split")
-    assert mm.mm_token_tile_width(moe.h, 4096) == 112      # split below 192 rows per expert
+    assert mm.mm_token_tile_width(moe.h, 4096) == 224      # 128 rows per expert, split: per expert
+    assert mm.mm_token_tile_width(moe.h, 3584) == 112      # 112 rows per expert, split: one width
     mm.mm_set_schedule(moe.h, "auto")
     mm.mm_set_tile_policy(moe.h, mm.MM_TILES_112)
     assert mm.mm_token_tile_width(moe.h, 16384) == 112

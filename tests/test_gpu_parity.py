@@ -18,7 +18,8 @@ pytestmark = pytest.mark.gpu
 # Several tiles and ragged tails at sizes the oracle finishes in seconds,
 # covering the four token-tile widths (16-token tiles up to 12 routed rows
 # per expert on average, 64-token tiles up to 48 without a shared expert,
-# 224-token tiles from 192, 112-token tiles between).
+# 224-token tiles above 112 (per-expert widths when the call runs split),
+# 112-token tiles between).
 SMALL_CASES = {
     "tiny": CONFIGS["tiny"],
     "decode_e16": Workload("decode_e16", T=8, H=7168, I=2048, E=16, k=8, seed=101),
