@@ -70,7 +70,7 @@ enum : int { kModeL2 = 0, kModeL1 = 1, kModeFused = 2 };
 // PROMO: the float-scale FP8 recipe (E4M3 weights with a float32 scale per
 // 128 x 128 block, activations with a float32 scale per (row, 128)). The
 // block-scaled MMA reads only power-of-two scales, so each 128-long K block
-// is an unscaled kind::f8f6f4 partial sum in TMEM (double-buffered); the
+// is an unscaled kind::f8f6f4 partial sum in TMEM (three buffers); the
 // epilogue warps multiply it by (activation scale x weight scale) and add it
 // to their FP32 registers ("MEGAMOE_SM90_DESIGN" sec. 5.3, scale factors
 // applied in software after the MMA), then store the sum into the tile's
@@ -103,6 +103,9 @@ struct GemmCfg {
   // producer consumes each tile once (the scale warp, the MMA issuers and the
   // epilogue warps)
   static constexpr int RING = 4;
+  // accumulator barrier pairs (tfull / tempty): the two accumulator buffers,
+  // or PROMO's three partial-sum buffers
+  static constexpr int NTB = PROMO ? 3 : 2;
   static constexpr int CONSUMERS = 1 + NI + Warps<BN, NA_>::EPI;
   // barriers (full, empty, sfready per stage; two accumulator pairs; the raw
   // scale groups' pair; the ring's pair per slot), the TMEM address, the abort
@@ -110,7 +113,7 @@ struct GemmCfg {
   // (PROMO: eight more, the L1 epilogue's exchange of per-quadrant amax values)
   static constexpr int XBARS = PROMO ? 8 : 0;
   static constexpr int BAR_BYTES =
-      ((3 * STAGES + 4 + 2 * RAW_G_MAX + 2 * RING + XBARS) * 8 + 8 + 4 * RING + 15) / 16 * 16;
+      ((3 * STAGES + 2 * NTB + 2 * RAW_G_MAX + 2 * RING + XBARS) * 8 + 8 + 4 * RING + 15) / 16 * 16;
   // TMA-loaded scale rows: RAW_G groups of four K steps; per group 16 bytes of
   // each of 128 rows for each weight block and of RAW_B_ROWS token rows
   static constexpr int RAW_G = PROMO ? 1 : DEEP || NA > 2 ? 2 : 3;  // (PROMO: unused, kept well-formed)
@@ -120,8 +123,11 @@ struct GemmCfg {
   static constexpr int RAW_B_BYTES = RAW_B_ROWS * 16;
   static constexpr int RAW_GROUP_BYTES = NA * RAW_ROWS_BYTES + RAW_B_BYTES;
   // PROMO: per-quadrant column maxima exchanged by the L1 epilogue warps,
-  // [2 buffers][2 warp halves][4 quadrants][32 columns] floats
-  static constexpr int XA_BYTES = PROMO ? 2 * 2 * 4 * 32 * 4 : 0;
+  // [2 buffers][2 warp halves][4 quadrants][32 columns] floats, then each
+  // epilogue warp's scale products of one K block ([blocks][columns] floats,
+  // at most 2 x 32 for a warp)
+  static constexpr int XA_EXCH_BYTES = 2 * 2 * 4 * 32 * 4;
+  static constexpr int XA_BYTES = PROMO ? XA_EXCH_BYTES + 16 + 8 * 64 * 4 : 0;  // (+16: alignment of the products)
   // copies of the two tile tables and the row offsets ([experts + 1] each),
   // and, where shared memory has room, of the tile-order expert list
   static constexpr int TAB_OFF = BAR_OFF + BAR_BYTES;
@@ -133,6 +139,7 @@ struct GemmCfg {
   // L2 tiles whose L1 rows the producer has seen stored (fused schedule)
   static constexpr int L2RDY_OFF = TAB_OFF + (EO_SMEM ? 4 : 3) * TAB_INTS * 4;
   static constexpr int XA_OFF = L2RDY_OFF + 16;
+  static constexpr int PS_OFF = (XA_OFF + XA_EXCH_BYTES + 15) / 16 * 16;  // PROMO: the scale products (16-byte aligned)
   static constexpr int RAW_OFF = (XA_OFF + XA_BYTES + 127) / 128 * 128;
   static constexpr int SMEM_BYTES = RAW_OFF + RAW_G * RAW_GROUP_BYTES + 1024;  // + alignment slack
   // TMEM columns: the accumulator buffers, then one scale-factor slot per
@@ -145,7 +152,8 @@ struct GemmCfg {
   // of the next) where TMEM holds them; the 224-token tiles fill TMEM with one
   // and the epilogue drains it between tiles.
   // PROMO: one accumulator region (each epilogue warp writes and then reads
-  // only its own columns) and two partial-sum buffers after it, no scale slots.
+  // only its own columns) and three partial-sum buffers after it, no scale
+  // slots (the MMAs run up to two K blocks ahead of the promotion).
   static constexpr int ACC_BUFS = PROMO ? 1 : 2 * ACC_COLS + STAGES * SF_STAGE_COLS <= 512 ? 2 : 1;
   static constexpr int SF_BASE = ACC_BUFS * ACC_COLS;
   static constexpr int PART_BASE = ACC_COLS;
@@ -156,11 +164,13 @@ struct GemmCfg {
   // both halves.
   static constexpr bool HALF = !PROMO && ACC_BUFS == 1;
   static constexpr int HALF_N = BN / 2;
-  static constexpr int TMEM_USED = PROMO ? 3 * ACC_COLS : SF_BASE + STAGES * SF_STAGE_COLS;
+  static constexpr int TMEM_USED = PROMO ? (1 + NTB) * ACC_COLS : SF_BASE + STAGES * SF_STAGE_COLS;
   static_assert(!PROMO || (NA == 2 && (BN == 16 || BN == 64)), "promotion: 16- and 64-token two-block tiles");
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
   static_assert(TMEM_USED <= 512, "TMEM budget");
+  static_assert(!PROMO || Warps<BN, NA_>::EPI * NA * (BN / 16 / (Warps<BN, NA_>::EPI / 4)) * 16 * 4 <= 8 * 64 * 4,
+                "PROMO: the scale products fit their region");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(BN <= RAW_B_ROWS, "every token row of a tile has its scale row in the raw group");
@@ -226,8 +236,8 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* sfready = tempty + 2;      // [STAGES] a stage's scales are in TMEM (tcgen05.commit of the copies)
+  uint64_t* tempty = tfull + C::NTB;
+  uint64_t* sfready = tempty + C::NTB;      // [STAGES] a stage's scales are in TMEM (tcgen05.commit of the copies)
   uint64_t* rfull = sfready + STAGES;  // [RAW_G] TMA scale rows landed
   uint64_t* rempty = rfull + C::RAW_G;  // [RAW_G] scale warp done with a group
   uint64_t* tr_full = rempty + C::RAW_G;  // [RING] a tile index is in the ring slot
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       mbar_init(&sfready[s], 1);  // the scale warp's tcgen05.commit
       mbar_init(&empty[s], C::NI);  // one tcgen05.commit per issuing thread
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < C::NTB; ++b) {
       mbar_init(&tfull[b], C::NI);  // tcgen05.commit after the last K step, per issuing thread
       mbar_init(&tempty[b], W::EPI);  // one arrival per epilogue warp
     }
@@ -732,16 +742,16 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         const Tile t = tile_of(tile, l1);
         const int kblocks = g.K / C::BK;
         if constexpr (PROMO) {
-          // one unscaled partial sum per K block into partial buffer pk & 1
+          // one unscaled partial sum per K block into partial buffer pk % NTB
           const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
           const bool active = block_active(g, t, u, C::NA);
           const uint32_t id = idesc_f8f6f4_e4m3(n_mma);
           for (int kb = 0; kb < kblocks; ++kb, ++it, ++pk) {
             const int s = (int)(it % STAGES);
             const uint32_t ph = (it / STAGES) & 1u;
-            const int pb = (int)(pk & 1u);
+            const int pb = (int)(pk % (uint32_t)C::NTB);
             if (!mbar_wait(&full[s], ph, abort_flag, g1.status, g1.timeout_ns, site0 + 2)) { ok = false; break; }
-            if (!mbar_wait(&tempty[pb], ((pk >> 1) & 1u) ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 1)) {
+            if (!mbar_wait(&tempty[pb], ((pk / (uint32_t)C::NTB) & 1u) ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 1)) {
               ok = false;
               break;
             }
@@ -892,39 +902,65 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
           if (!rdy) break;
         }
         float acc[C::NA][CH][16];
-        // scales of K block kb: lane l < 16 holds the activation scale of column
-        // chunk_col(i) + l (shuffled to the other lanes), sw[u] the weight
-        // block's; the next block's are loaded before waiting for this one
-        auto load_sa = [&](int kb, float (&sa)[CH]) {
 #pragma unroll
-          for (int i = 0; i < CH; ++i) {
-            const int col = chunk_col(i) + (lane & 15);
-            const float* ap = asf + (size_t)(t.row0 + col) * KB + kb;
-            sa[i] = col < t.nrows ? (fresh ? __ldcg(ap) : __ldg(ap)) : 0.0f;
-          }
-        };
-        auto load_sw = [&](int kb, float (&sw)[C::NA]) {
+        for (int u = 0; u < C::NA; ++u)
 #pragma unroll
-          for (int u = 0; u < C::NA; ++u)
-            sw[u] = block_active(g, t, u, C::NA) ? __ldg(wsf + (size_t)(block_wrow(g, t, u, C::NA) / 128) * KB + kb)
-                                                 : 0.0f;
+          for (int i = 0; i < CH; ++i)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[u][i][j] = 0.0f;
+        // Per K block, lane l < 16 * CH owns column chunk_col(l / 16) + l % 16
+        // of the warp's columns: it multiplies that column's activation scale
+        // by each weight block's scale once and stores the products into the
+        // warp's slice of shared memory, from which every lane reads them back
+        // 16 at a time (broadcast loads); each partial sum then takes one FMA.
+        // The scales are loaded AH K blocks ahead (a shift register).
+        constexpr int AH = 4;
+        float* ps = reinterpret_cast<float*>(smem + C::PS_OFF) + (warp - 4) * (C::NA * CH * 16);
+        const int my_i = lane >> 4;
+        const int my_col = my_i < CH ? chunk_col(my_i) + (lane & 15) : 0;
+        const bool my_ok = my_i < CH && my_col < t.nrows;
+        const float* my_ap = asf + (size_t)(t.row0 + my_col) * KB;
+        bool bact[C::NA];
+        const float* wsp[C::NA];
+#pragma unroll
+        for (int u = 0; u < C::NA; ++u) {
+          bact[u] = block_active(g, t, u, C::NA);
+          wsp[u] = wsf + (size_t)(bact[u] ? block_wrow(g, t, u, C::NA) / 128 : 0) * KB;
+        }
+        auto ld_sa = [&](int kb) -> float {
+          return my_ok && kb < KB ? (fresh ? __ldcg(my_ap + kb) : __ldg(my_ap + kb)) : 0.0f;
         };
-        float sa_n[CH], sw_n[C::NA];
-        load_sa(0, sa_n);
-        load_sw(0, sw_n);
+        float sa_q[AH], sw_q[AH][C::NA];
+#pragma unroll
+        for (int a = 0; a < AH; ++a) {
+          sa_q[a] = ld_sa(a);
+#pragma unroll
+          for (int u = 0; u < C::NA; ++u) sw_q[a][u] = bact[u] && a < KB ? __ldg(wsp[u] + a) : 0.0f;
+        }
         bool ok = true;
         for (int kb = 0; kb < KB; ++kb, ++pk) {
-          float sa[CH], sw[C::NA];
+          const float sa = sa_q[0];
+          float sw[C::NA];
 #pragma unroll
-          for (int i = 0; i < CH; ++i) sa[i] = sa_n[i];
+          for (int u = 0; u < C::NA; ++u) sw[u] = sw_q[0][u];
 #pragma unroll
-          for (int u = 0; u < C::NA; ++u) sw[u] = sw_n[u];
-          if (kb + 1 < KB) {
-            load_sa(kb + 1, sa_n);
-            load_sw(kb + 1, sw_n);
+          for (int a = 0; a + 1 < AH; ++a) {
+            sa_q[a] = sa_q[a + 1];
+#pragma unroll
+            for (int u = 0; u < C::NA; ++u) sw_q[a][u] = sw_q[a + 1][u];
           }
-          const int pb = (int)(pk & 1u);
-          if (!mbar_wait(&tfull[pb], (pk >> 1) & 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 3)) {
+          sa_q[AH - 1] = ld_sa(kb + AH);
+#pragma unroll
+          for (int u = 0; u < C::NA; ++u)
+            sw_q[AH - 1][u] = bact[u] && kb + AH < KB ? __ldg(wsp[u] + kb + AH) : 0.0f;
+          __syncwarp();  // the previous K block's reads of the slice are done
+          if (my_i < CH) {
+#pragma unroll
+            for (int u = 0; u < C::NA; ++u) ps[(u * CH + my_i) * 16 + (lane & 15)] = __fmul_rn(sa, sw[u]);
+          }
+          __syncwarp();
+          const int pb = (int)(pk % (uint32_t)C::NTB);
+          if (!mbar_wait(&tfull[pb], (pk / (uint32_t)C::NTB) & 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 3)) {
             ok = false;
             break;
           }
@@ -932,10 +968,9 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
 #pragma unroll
           for (int u = 0; u < C::NA; ++u) {
             uint32_t r[CH][16];
-            const bool act = block_active(g, t, u, C::NA);
 #pragma unroll
             for (int i = 0; i < CH; ++i)
-              if (act && chunk_col(i) < t.nrows)
+              if (bact[u] && chunk_col(i) < t.nrows)
                 tmem_ld_x16(tmem + lanes + (uint32_t)(C::PART_BASE + pb * C::ACC_COLS + u * BN + chunk_col(i)), r[i]);
             tmem_ld_wait();
             if (u + 1 == C::NA) {
@@ -945,19 +980,29 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
             }
 #pragma unroll
             for (int i = 0; i < CH; ++i) {
+              if (!bact[u] || chunk_col(i) >= t.nrows) continue;  // (warp-uniform)
+              const float4* pv = reinterpret_cast<const float4*>(ps + (u * CH + i) * 16);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                // (columns past the tile's rows, and absent blocks, stay 0)
-                const float sj = __shfl_sync(0xffffffffu, sa[i], j);
-                const float part = act && chunk_col(i) + j < t.nrows
-                                       ? __fmul_rn(__uint_as_float(r[i][j]), __fmul_rn(sj, sw[u]))
-                                       : 0.0f;
-                acc[u][i][j] = kb == 0 ? part : __fadd_rn(acc[u][i][j], part);
+              for (int v = 0; v < 4; ++v) {
+                const float4 sc = pv[v];
+                acc[u][i][4 * v + 0] = fmaf(__uint_as_float(r[i][4 * v + 0]), sc.x, acc[u][i][4 * v + 0]);
+                acc[u][i][4 * v + 1] = fmaf(__uint_as_float(r[i][4 * v + 1]), sc.y, acc[u][i][4 * v + 1]);
+                acc[u][i][4 * v + 2] = fmaf(__uint_as_float(r[i][4 * v + 2]), sc.z, acc[u][i][4 * v + 2]);
+                acc[u][i][4 * v + 3] = fmaf(__uint_as_float(r[i][4 * v + 3]), sc.w, acc[u][i][4 * v + 3]);
               }
             }
           }
         }
         if (!ok) break;
+        // columns past the tile's rows (their partial sums are stale TMEM
+        // contents times a zero scale) are cleared before the epilogue sees them
+#pragma unroll
+        for (int u = 0; u < C::NA; ++u)
+#pragma unroll
+          for (int i = 0; i < CH; ++i)
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (chunk_col(i) + j >= t.nrows) acc[u][i][j] = 0.0f;
         // the sums into the accumulator columns the epilogue below reads
 #pragma unroll
         for (int u = 0; u < C::NA; ++u)
