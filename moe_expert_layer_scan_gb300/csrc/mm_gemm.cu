@@ -913,7 +913,8 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         // by each weight block's scale once and stores the products into the
         // warp's slice of shared memory, from which every lane reads them back
         // 16 at a time (broadcast loads); each partial sum then takes one FMA.
-        // The scales are loaded AH K blocks ahead (a shift register).
+        // The scales are loaded AH K blocks ahead: a ring of AH registers,
+        // the K loop unrolled by AH so that each slot is a fixed register.
         constexpr int AH = 4;
         float* ps = reinterpret_cast<float*>(smem + C::PS_OFF) + (warp - 4) * (C::NA * CH * 16);
         const int my_i = lane >> 4;
@@ -930,29 +931,37 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         auto ld_sa = [&](int kb) -> float {
           return my_ok && kb < KB ? (fresh ? __ldcg(my_ap + kb) : __ldg(my_ap + kb)) : 0.0f;
         };
-        float sa_q[AH], sw_q[AH][C::NA];
+        float sa_q[AH];
 #pragma unroll
-        for (int a = 0; a < AH; ++a) {
-          sa_q[a] = ld_sa(a);
+        for (int a = 0; a < AH; ++a) sa_q[a] = ld_sa(a);
+        // weight-block scales 32 K blocks at a time: lane l holds K block
+        // 32 * group + l (the next group's loaded one group ahead)
+        auto ld_sw = [&](int u, int kb) -> float { return bact[u] && kb < KB ? __ldg(wsp[u] + kb) : 0.0f; };
+        float sw_c[C::NA], sw_n[C::NA];
 #pragma unroll
-          for (int u = 0; u < C::NA; ++u) sw_q[a][u] = bact[u] && a < KB ? __ldg(wsp[u] + a) : 0.0f;
+        for (int u = 0; u < C::NA; ++u) {
+          sw_c[u] = ld_sw(u, lane);
+          sw_n[u] = ld_sw(u, 32 + lane);
         }
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb, ++pk) {
-          const float sa = sa_q[0];
+        for (int kb0 = 0; kb0 < KB && ok; kb0 += AH) {
+#pragma unroll
+         for (int a = 0; a < AH; ++a) {
+          const int kb = kb0 + a;
+          if (kb >= KB) break;
+          // slot a of the ring: this K block's scales out, block kb + AH's in
+          const float sa = sa_q[a];
+          sa_q[a] = ld_sa(kb + AH);
+          if (kb > 0 && (kb & 31) == 0) {
+#pragma unroll
+            for (int u = 0; u < C::NA; ++u) {
+              sw_c[u] = sw_n[u];
+              sw_n[u] = ld_sw(u, kb + 32 + lane);
+            }
+          }
           float sw[C::NA];
 #pragma unroll
-          for (int u = 0; u < C::NA; ++u) sw[u] = sw_q[0][u];
-#pragma unroll
-          for (int a = 0; a + 1 < AH; ++a) {
-            sa_q[a] = sa_q[a + 1];
-#pragma unroll
-            for (int u = 0; u < C::NA; ++u) sw_q[a][u] = sw_q[a + 1][u];
-          }
-          sa_q[AH - 1] = ld_sa(kb + AH);
-#pragma unroll
-          for (int u = 0; u < C::NA; ++u)
-            sw_q[AH - 1][u] = bact[u] && kb + AH < KB ? __ldg(wsp[u] + kb + AH) : 0.0f;
+          for (int u = 0; u < C::NA; ++u) sw[u] = __shfl_sync(0xffffffffu, sw_c[u], kb & 31);
           __syncwarp();  // the previous K block's reads of the slice are done
           if (my_i < CH) {
 #pragma unroll
@@ -992,6 +1001,8 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
               }
             }
           }
+          ++pk;
+         }
         }
         if (!ok) break;
         // columns past the tile's rows (their partial sums are stale TMEM
