@@ -381,13 +381,12 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   GatherArgs ga;
   ga.x = static_cast<const uint8_t*>(x_fp8);
   ga.x_sf = static_cast<const uint8_t*>(x_sf);
-  ga.perm = ra.perm;
-  ga.offsets = ra.offsets;
+  ga.pos = ra.pos;
   ga.pool_x = base + L.pool_x;
   ga.pool_sf = base + L.pool_sf;
-  ga.H = h->H; ga.Kp = Kp; ga.Ep = Ep;
+  ga.T = T; ga.H = h->H; ga.Kp = Kp;
   mark("gather");
-  if (mm_launch_gather(&ga, T * Kp, stream) != 0) return MM_ERR_CUDA;
+  if (mm_launch_gather(&ga, stream) != 0) return MM_ERR_CUDA;
 
   // Tensor maps: weights are cached per base pointer, activations live in the workspace.
   const bool fp4 = h->w_fmt == MM_WEIGHTS_MXFP4;

@@ -339,24 +339,56 @@ __global__ void __launch_bounds__(1024, 1) route_place_kernel(RouteArgs a) {
   place_slots(a, c0, c1, hist);
 }
 
-// One warp per pool row: copies the token's FP8 row and its scale row into
-// expert-sorted pool order (the local form of the pages' L1 pool fill).
+// One warp per (token, column chunk of 32 x CW 16-byte pieces): the chunk of
+// the token's FP8 row is read once and written to each of the token's pool
+// rows in expert-sorted order (the local form of the pages' L1 pool fill);
+// the first chunk's warp also copies the scale row. Disabled slots (pool row
+// -1) are skipped. Long calls take 4 KB chunks per warp (CW = 8), short ones
+// 1 KB chunks (CW = 2) so that enough warps run.
+constexpr int kGatherRowsMin = 512;
+template <int CW>
 __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
   pdl_trigger();
   pdl_wait();
-  const int n = a.offsets[a.Ep];
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int vec = a.H / 16, sfw = a.H / 128;
-  for (int r = gw; r < n; r += nw) {
-    const long t = a.perm[r] / a.Kp;
-    const uint4* src = reinterpret_cast<const uint4*>(a.x + t * a.H);
-    uint4* dst = reinterpret_cast<uint4*>(a.pool_x + (size_t)r * a.H);
-    for (int i = lane; i < vec; i += 32) dst[i] = __ldg(src + i);
+  const int nch = (vec + 32 * CW - 1) / (32 * CW);
+  const long items = (long)a.T * nch;
+  for (long item = gw; item < items; item += nw) {
+    const long t = item / nch;
+    const int i0 = (int)(item - t * nch) * 32 * CW + lane;
+    int dst[kMaxSlots];
+#pragma unroll
+    for (int j = 0; j < kMaxSlots; ++j) dst[j] = j < a.Kp ? __ldg(a.pos + t * a.Kp + j) : -1;
+    const uint4* __restrict__ src = reinterpret_cast<const uint4*>(a.x + t * a.H);
+    uint4 v[CW];
+#pragma unroll
+    for (int c = 0; c < CW; ++c)
+      if (i0 + 32 * c < vec) v[c] = __ldg(src + i0 + 32 * c);
+#pragma unroll
+    for (int j = 0; j < kMaxSlots; ++j) {
+      if (dst[j] < 0) continue;
+      uint4* __restrict__ d = reinterpret_cast<uint4*>(a.pool_x + (size_t)dst[j] * a.H);
+#pragma unroll
+      for (int c = 0; c < CW; ++c)
+        if (i0 + 32 * c < vec) d[i0 + 32 * c] = v[c];
+    }
+    if (i0 >= 32) continue;  // the scale row: the token's first chunk
     const uint32_t* ss = reinterpret_cast<const uint32_t*>(a.x_sf + t * (a.H / 32));
-    uint32_t* ds = reinterpret_cast<uint32_t*>(a.pool_sf + (size_t)r * (a.H / 32));
-    for (int i = lane; i < sfw; i += 32) ds[i] = __ldg(ss + i);
+    uint32_t sv[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      if (lane + 32 * c < sfw) sv[c] = __ldg(ss + lane + 32 * c);
+#pragma unroll
+    for (int j = 0; j < kMaxSlots; ++j) {
+      if (dst[j] < 0) continue;
+      uint32_t* ds = reinterpret_cast<uint32_t*>(a.pool_sf + (size_t)dst[j] * (a.H / 32));
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (lane + 32 * c < sfw) ds[lane + 32 * c] = sv[c];
+    }
   }
 }
 
@@ -511,11 +543,18 @@ extern "C" int mm_launch_route(const mm::RouteArgs* a, void* stream) {
   return (int)e;
 }
 
-extern "C" int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream) {
-  if (rows_upper_bound <= 0) return 0;
-  int blocks = (rows_upper_bound + 7) / 8;
+extern "C" int mm_launch_gather(const mm::GatherArgs* a, void* stream) {
+  if (a->T <= 0) return 0;
+  // 4 KB chunks per warp from kGatherRowsMin tokens up, else 1 KB chunks
+  const bool rows = a->T >= mm::kGatherRowsMin;
+  const int per = 32 * (rows ? 8 : 2);
+  const long items = (long)a->T * ((a->H / 16 + per - 1) / per);
+  long blocks = (items + 7) / 8;  // eight warps per block
   if (blocks > 152 * 16) blocks = 152 * 16;
-  return (int)mm::launch_kernel(mm::gather_kernel, dim3(blocks), dim3(256), 0, (cudaStream_t)stream, true, *a);
+  return (int)(rows ? mm::launch_kernel(mm::gather_kernel<8>, dim3((unsigned)blocks), dim3(256), 0,
+                                        (cudaStream_t)stream, true, *a)
+                    : mm::launch_kernel(mm::gather_kernel<2>, dim3((unsigned)blocks), dim3(256), 0,
+                                        (cudaStream_t)stream, true, *a));
 }
 
 extern "C" int mm_launch_combine(const mm::CombineArgs* a, void* stream, bool pdl) {

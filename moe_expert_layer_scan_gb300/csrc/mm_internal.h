@@ -140,11 +140,10 @@ struct RouteArgs {
 struct GatherArgs {
   const uint8_t* x;
   const uint8_t* x_sf;
-  const int32_t* perm;
-  const int32_t* offsets;
+  const int32_t* pos;  // [T * Kp] pool row of each slot, -1 if disabled
   uint8_t* pool_x;
   uint8_t* pool_sf;
-  int H, Kp, Ep;
+  int T, H, Kp;
 };
 
 struct GemmArgs {
@@ -206,7 +205,7 @@ struct CombineArgs {
 extern "C" {
 int mm_launch_route(const mm::RouteArgs* a, void* stream);
 int mm_route_launches(int slots);  // kernels mm_launch_route enqueues for this many slots
-int mm_launch_gather(const mm::GatherArgs* a, int rows_upper_bound, void* stream);
+int mm_launch_gather(const mm::GatherArgs* a, void* stream);
 int mm_launch_combine(const mm::CombineArgs* a, void* stream, bool pdl);
 // variant: 0 = small tiles, 1 = large tiles, 2 = small tiles with six stages
 // (E + S <= kDeepMaxExperts), 3 = 224-token tiles, 4 = small tiles with four
