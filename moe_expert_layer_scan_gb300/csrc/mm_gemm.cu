@@ -70,7 +70,7 @@ enum : int { kModeL2 = 0, kModeL1 = 1, kModeFused = 2 };
 // PROMO: the float-scale FP8 recipe (E4M3 weights with a float32 scale per
 // 128 x 128 block, activations with a float32 scale per (row, 128)). The
 // block-scaled MMA reads only power-of-two scales, so each 128-long K block
-// is an unscaled kind::f8f6f4 partial sum in TMEM (three buffers); the
+// is an unscaled kind::f8f6f4 partial sum in TMEM (one buffer per stage); the
 // epilogue warps multiply it by (activation scale x weight scale) and add it
 // to their FP32 registers ("MEGAMOE_SM90_DESIGN" sec. 5.3, scale factors
 // applied in software after the MMA), then store the sum into the tile's
@@ -104,8 +104,10 @@ struct GemmCfg {
   // epilogue warps)
   static constexpr int RING = 4;
   // accumulator barrier pairs (tfull / tempty): the two accumulator buffers,
-  // or PROMO's three partial-sum buffers
-  static constexpr int NTB = PROMO ? 3 : 2;
+  // or PROMO's partial-sum buffers, one per stage (the K block in stage s
+  // accumulates into buffer s, so the stage's empty barrier also tells the
+  // epilogue that the partial sum is complete)
+  static constexpr int NTB = PROMO ? STAGES : 2;
   static constexpr int CONSUMERS = 1 + NI + Warps<BN, NA_>::EPI;
   // barriers (full, empty, sfready per stage; two accumulator pairs; the raw
   // scale groups' pair; the ring's pair per slot), the TMEM address, the abort
@@ -152,8 +154,8 @@ struct GemmCfg {
   // of the next) where TMEM holds them; the 224-token tiles fill TMEM with one
   // and the epilogue drains it between tiles.
   // PROMO: one accumulator region (each epilogue warp writes and then reads
-  // only its own columns) and three partial-sum buffers after it, no scale
-  // slots (the MMAs run up to two K blocks ahead of the promotion).
+  // only its own columns) and a partial-sum buffer per stage after it, no
+  // scale slots.
   static constexpr int ACC_BUFS = PROMO ? 1 : 2 * ACC_COLS + STAGES * SF_STAGE_COLS <= 512 ? 2 : 1;
   static constexpr int SF_BASE = ACC_BUFS * ACC_COLS;
   static constexpr int PART_BASE = ACC_COLS;
@@ -165,6 +167,7 @@ struct GemmCfg {
   static constexpr bool HALF = !PROMO && ACC_BUFS == 1;
   static constexpr int HALF_N = BN / 2;
   static constexpr int TMEM_USED = PROMO ? (1 + NTB) * ACC_COLS : SF_BASE + STAGES * SF_STAGE_COLS;
+  static_assert(!PROMO || NTB == STAGES, "PROMO: a partial-sum buffer per stage");
   static_assert(!PROMO || (NA == 2 && (BN == 16 || BN == 64)), "promotion: 16- and 64-token two-block tiles");
   static constexpr int TMEM_COLS = TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128
                                    : TMEM_USED <= 256 ? 256 : 512;
@@ -742,7 +745,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         const Tile t = tile_of(tile, l1);
         const int kblocks = g.K / C::BK;
         if constexpr (PROMO) {
-          // one unscaled partial sum per K block into partial buffer pk % NTB
+          // one unscaled partial sum per K block into partial buffer pk % NTB (= its stage)
           const uint32_t n_mma = (uint32_t)((t.nrows + 15) & ~15);
           const bool active = block_active(g, t, u, C::NA);
           const uint32_t id = idesc_f8f6f4_e4m3(n_mma);
@@ -763,8 +766,8 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
 #pragma unroll
               for (int k = 0; k < 4; ++k) tc_mma_f8f6f4(d, da + 2u * k, db + 2u * k, id, k > 0 ? 1u : 0u);
             }
-            tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
-            tc_commit(&tfull[pb]);  // the partial sum is complete
+            // one commit: the stage is free and partial sum pb (= s) is complete
+            tc_commit(&empty[s]);
             if (kb == 0) next = take_tile(tn, false);
           }
           if (!ok) break;
@@ -968,8 +971,10 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
             for (int u = 0; u < C::NA; ++u) ps[(u * CH + my_i) * 16 + (lane & 15)] = __fmul_rn(sa, sw[u]);
           }
           __syncwarp();
+          // the partial sum of this K block is complete when its stage's MMAs are
+          // (K block pk ran in stage pk % STAGES, into buffer pk % NTB: the same)
           const int pb = (int)(pk % (uint32_t)C::NTB);
-          if (!mbar_wait(&tfull[pb], (pk / (uint32_t)C::NTB) & 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 3)) {
+          if (!mbar_wait(&empty[pb], (pk / (uint32_t)C::NTB) & 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 3)) {
             ok = false;
             break;
           }
@@ -1214,7 +1219,7 @@ static int launch(const GemmMaps* maps, const GemmArgs* g1, const GemmArgs* g2, 
 // Pipeline depths: as many stages as the 227 KB of shared memory allows (small:
 // five, measured as fast as six).
 constexpr int kStagesSmall = 5, kStagesSmallDeep = 6, kStagesLarge = 4, kStagesWide = 3, kStagesQuad = 3,
-              kStagesMid = 5, kStagesPromoSmall = 5, kStagesPromoMid = 4;
+              kStagesMid = 5, kStagesPromoSmall = 5, kStagesPromoMid = 3;
 // CTAs per launch of each instantiation: [mode][variant] (variant 2: 16-token
 // tiles with six stages, for at most kDeepMaxExperts experts; variant 3:
 // 224-token tiles; variant 4: 16-token tiles with four weight blocks, for at
