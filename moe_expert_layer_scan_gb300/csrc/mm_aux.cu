@@ -394,7 +394,18 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherArgs a) {
 
 // Each thread owns one 16-byte column chunk (8 BF16 values) of one token: it
 // issues the loads of all the token's slot rows first, then sums them in FP32
-// in slot order and stores the BF16 result.
+// in slot order and stores the BF16 result. MS (8, or kMaxSlots above eight
+// slots per token) sizes the per-thread slot arrays, so that the common
+// top-8 case keeps its registers low and more threads in flight; the slot
+// rows are read once, so their loads skip L1.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+template <int MS>
 __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
   pdl_trigger();
   pdl_wait();
@@ -403,18 +414,18 @@ __global__ void __launch_bounds__(128) combine_kernel(CombineArgs a) {
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long)gridDim.x * blockDim.x) {
     const long t = i / chunks;
     const int c = (int)(i - t * chunks);
-    uint4 v[kMaxSlots];
-    int r[kMaxSlots];
+    uint4 v[MS];
+    int r[MS];
 #pragma unroll
-    for (int j = 0; j < kMaxSlots; ++j) {
+    for (int j = 0; j < MS; ++j) {
       r[j] = j < a.Kp ? __ldg(a.pos + t * a.Kp + j) : -1;
-      v[j] = r[j] >= 0 ? __ldg(reinterpret_cast<const uint4*>(a.z + (size_t)r[j] * a.H) + c) : make_uint4(0, 0, 0, 0);
+      v[j] = r[j] >= 0 ? ld_stream(reinterpret_cast<const uint4*>(a.z + (size_t)r[j] * a.H) + c) : make_uint4(0, 0, 0, 0);
     }
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kMaxSlots; ++j) {
+    for (int j = 0; j < MS; ++j) {
       if (r[j] < 0) continue;
       const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
@@ -561,9 +572,11 @@ extern "C" int mm_launch_combine(const mm::CombineArgs* a, void* stream, bool pd
   if (a->T <= 0) return 0;
   const long threads = (long)a->T * (a->H / 8);
   long blocks = (threads + 127) / 128;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  return (int)mm::launch_kernel(mm::combine_kernel, dim3((unsigned)blocks), dim3(128), 0, (cudaStream_t)stream, pdl,
-                                *a);
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  return (int)(a->Kp <= 8 ? mm::launch_kernel(mm::combine_kernel<8>, dim3((unsigned)blocks), dim3(128), 0,
+                                              (cudaStream_t)stream, pdl, *a)
+                          : mm::launch_kernel(mm::combine_kernel<mm::kMaxSlots>, dim3((unsigned)blocks), dim3(128), 0,
+                                              (cudaStream_t)stream, pdl, *a));
 }
 
 extern "C" int mm_launch_div_check(unsigned long long pairs, unsigned long long seed, unsigned long long* counts,
