@@ -97,8 +97,9 @@ class DeviceRun:
     def status(self, stream=None) -> int:
         return self.moe.status(stream)
 
-    def intermediates(self, T: int):
-        """Host copies of the routing tables and the pool-order intermediates."""
+    def intermediates(self, T: int, pool: bool = False):
+        """Host copies of the routing tables and the pool-order intermediates
+        (with pool=True also the gathered token rows and scale rows)."""
         import torch
         v = self.moe.views(T)
         w = self.w
@@ -122,4 +123,6 @@ class DeviceRun:
             l2a=grab(v.l2a, n * w.I, np.uint8).reshape(n, w.I), l2a_sf=grab(v.l2a_sf, n * (w.I // 32), np.uint8).reshape(n, w.I // 32),
             z=grab(v.z, n * w.H, np.uint16).reshape(n, w.H),
             status=int(grab(v.status, 1, np.uint32)[0]),
+            **(dict(pool_x=grab(v.pool_x, n * w.H, np.uint8).reshape(n, w.H),
+                    pool_sf=grab(v.pool_sf, n * (w.H // 32), np.uint8).reshape(n, w.H // 32)) if pool else {}),
         )

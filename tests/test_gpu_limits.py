@@ -1,7 +1,8 @@
 """Limits of the supported shapes and reuse under CUDA-graph replay: the most
-experts and slots the handle accepts, the routing boundary between the
-one-CTA and the multi-CTA routing kernels, the largest hidden and
-intermediate sizes, and a forward captured into a CUDA graph and replayed."""
+experts and slots the handle accepts, the gather's chunk-width boundary, the
+routing boundary between the one-CTA and the multi-CTA routing kernels, the
+largest hidden and intermediate sizes, and a forward captured into a CUDA
+graph and replayed."""
 import numpy as np
 import pytest
 
@@ -37,6 +38,23 @@ def test_most_experts_and_slots(orc):
     assert inter["status"] == 0
     assert np.array_equal(inter["counts"], ref["counts"]) and np.array_equal(inter["offsets"], ref["offsets"])
     G.assert_out_close(out, ref["out"])
+
+
+@pytest.mark.parametrize("T,S", [(511, 0), (512, 0), (512, 1), (37, 1)])
+def test_gather_pool_rows_bit_exact(T, S):
+    """The gather copies each routed slot's token row and scale row into its
+    expert-sorted pool row byte for byte, on both sides of the switch between
+    1 KB and 4 KB chunks per warp (512 tokens), with rows of 7168 bytes (several
+    chunks per row) and with a shared expert (nine slots per token)."""
+    w = Workload(f"gather_{T}_{S}", T=T, H=7168, I=128, E=16, k=8, S=S, seed=404)
+    h = workloads.host_inputs(w)
+    run = G.DeviceRun(w, inputs=h)
+    run.run()
+    inter = run.intermediates(w.T, pool=True)
+    assert inter["status"] == 0
+    tok = inter["perm"] // w.Kp
+    assert np.array_equal(inter["pool_x"], np.asarray(h["x"]).reshape(w.T, w.H)[tok])
+    assert np.array_equal(inter["pool_sf"], np.asarray(h["x_sf"]).reshape(w.T, w.H // 32)[tok])
 
 
 @pytest.mark.parametrize("T", [2048, 2049])

@@ -47,6 +47,9 @@ SMALL_CASES = {
     "f128_mid": Workload("f128_mid", T=64, H=768, I=384, E=4, k=2, S=1, clamp=3.0, seed=121, w_fmt=2),
     "f128_ragged": Workload("f128_ragged", T=37, H=384, I=384, E=5, k=3, S=1, seed=122, w_fmt=2),
     "f128_multi": Workload("f128_multi", T=300, H=512, I=256, E=2, k=2, seed=123, w_fmt=2),
+    # 33 K blocks in L1 (past the 32 weight-block scales one load of the
+    # promotion covers, and not a multiple of its four-block scale ring)
+    "f128_kb33": Workload("f128_kb33", T=40, H=4224, I=256, E=3, k=2, seed=128, w_fmt=2),
     # Zipf-skewed load with a shared expert: experts above and below 112 rows
     # (both classes of the per-expert tile widths)
     "dual_mix": Workload("dual_mix", T=256, H=512, I=256, E=16, k=4, S=1, zipf=1.2, seed=124),
@@ -185,7 +188,8 @@ def test_parity_with_the_other_tile_width(name, tiles, orc):
         G.assert_out_close(out, ref["out"])
 
 
-@pytest.mark.parametrize("name", ["wide_shared", "prefill_t256", "fp8w_wide", "fp8w_small", "f128_mid", "f128_multi"])
+@pytest.mark.parametrize("name", ["wide_shared", "prefill_t256", "fp8w_wide", "fp8w_small", "f128_mid", "f128_multi",
+                                  "f128_kb33"])
 def test_tile_widths_agree_bit_for_bit(name):
     """Every token-tile width runs each output element's K loop in the same
     order: the outputs and intermediates of the four widths are identical
