@@ -226,6 +226,35 @@ MM_API mm_status_t mm_token_tile_width(mm_handle_t h, int T, int* width);
 #define MM_WEIGHTS_FP8_F128 2
 MM_API mm_status_t mm_set_weight_format(mm_handle_t h, int format);
 
+/* Weight-scale transform ("MegaMoE research report" sec. 6.4, the SM100
+ * kernel's transform_weights_for_mega_moe, which transposes the UE8M0 scale
+ * factors for the tensor core's scale copy ahead of time; "MEGAMOE_SM90_DESIGN"
+ * sec. 15.2 Weight SF Layout, SM100: UE8M0, 4 x 32 transposed, per 32 along
+ * K). The transformed copy holds, for every 128-row block of a weight tensor
+ * and every 128-long K step, the 512 bytes that the grouped GEMM copies into
+ * TMEM for that block and step: byte 16 * l + 4 * i + b is the scale byte b
+ * (32-element block b of the step) of row 32 * i + l of the block. Each such
+ * piece then arrives in shared memory as one 512-byte bulk copy instead of
+ * 128 strided 16-byte rows.
+ *   mm_transformed_scale_bytes(h, &bytes): device bytes of the copy for both
+ *     weight scale tensors ([E+S][2I][H/32] + [E+S][H][I/32] bytes, the same as
+ *     the two inputs).
+ *   mm_transform_weight_scales(h, w1_sf, w2_sf, dst, dst_bytes, stream): writes
+ *     the copy of w1_sf and w2_sf (device, read only) into dst (device, caller
+ *     owned, at least mm_transformed_scale_bytes, 16-byte aligned) on stream,
+ *     and registers it on the handle: a later mm_run (on a stream ordered
+ *     after this one) whose w1_sf and w2_sf arguments are these two pointers
+ *     reads the copy instead; a run with other scale pointers reads its
+ *     arguments. Rewrite the copy (call again) whenever the scales' contents
+ *     change; dst = NULL unregisters. The transform is weight preparation, not
+ *     part of a forward. UE8M0 formats only (MXFP4, MXFP8), H and I multiples of
+ *     512 (else MM_ERR_UNSUPPORTED); runs on CTA pairs read the arguments.
+ *     Errors: MM_ERR_INVALID_ARG for a null handle, null scale pointers, an
+ *     unaligned dst or dst_bytes too small; MM_ERR_CUDA if the launch fails. */
+MM_API mm_status_t mm_transformed_scale_bytes(mm_handle_t h, size_t* bytes);
+MM_API mm_status_t mm_transform_weight_scales(mm_handle_t h, const void* w1_sf, const void* w2_sf, void* dst,
+                                              size_t dst_bytes, mm_stream_t stream);
+
 /* Expert-parallel-ready routing outputs ("MegaMoE research report" sec. 4.1,
  * the dispatch warps' expert counts and source metadata; "MEGAMOE_SM90_DESIGN"
  * sec. 16.1, the cumulative_local_expert_recv_stats argument, and sec. 21

@@ -27,7 +27,8 @@ EXPORTS = ["mm_status_string", "mm_create", "mm_set_options", "mm_set_schedule",
            "mm_token_tile_width",
            "mm_set_weight_format",
            "mm_set_ep_ranks",
-           "mm_set_expert_stats", "mm_workspace_bytes", "mm_run",
+           "mm_set_expert_stats", "mm_transformed_scale_bytes", "mm_transform_weight_scales", "mm_workspace_bytes",
+           "mm_run",
            "mm_get_status", "mm_launches_per_run", "mm_debug_views", "mm_debug_timeout_probe", "mm_debug_div_check",
            "mm_profile_enable",
            "mm_profile_last", "mm_profile_name", "mm_run_noalloc", "mm_destroy"]
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
         L.mm_profile_name.argtypes = [p, i32]
         L.mm_profile_name.restype = ctypes.c_char_p
         L.mm_run_noalloc.argtypes = [p, i32] + [p] * 9 + [p]
+        L.mm_transformed_scale_bytes.argtypes = [p, ctypes.POINTER(ctypes.c_size_t)]
+        L.mm_transform_weight_scales.argtypes = [p, p, p, p, ctypes.c_size_t, p]
         L.mm_destroy.argtypes = [p]
         L.mm_destroy.restype = None
         for n in EXPORTS:
@@ -154,6 +157,19 @@ def mm_set_ep_ranks(h: int, num_ranks: int) -> None:
 def mm_set_expert_stats(h: int, cumulative_counts_ptr) -> None:
     """Device pointer to E + S int32 counters (or None to disable)."""
     _check(lib().mm_set_expert_stats(h, cumulative_counts_ptr or None), "mm_set_expert_stats")
+
+
+def mm_transformed_scale_bytes(h: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().mm_transformed_scale_bytes(h, ctypes.byref(n)), "mm_transformed_scale_bytes")
+    return n.value
+
+
+def mm_transform_weight_scales(h: int, w1_sf: int, w2_sf: int, dst: int, dst_bytes: int, stream: int) -> None:
+    """Writes the transformed copy of both weight scale tensors into dst and
+    registers it for runs with these w1_sf / w2_sf pointers (dst = 0 unregisters)."""
+    _check(lib().mm_transform_weight_scales(h, w1_sf or None, w2_sf or None, dst or None, dst_bytes, stream or None),
+           "mm_transform_weight_scales")
 
 
 def mm_workspace_bytes(h: int, T: int) -> int:
@@ -259,6 +275,16 @@ class MegaMoE:
 
     def launches(self, T: int) -> int:
         return mm_launches_per_run(self.h, T)
+
+    def transform_weight_scales(self, w1_sf, w2_sf, stream=None):
+        """Weight preparation: the tcgen05 scale layout of both weight scale
+        tensors in a device buffer this object keeps; later runs with these
+        two tensors read it. Call again after the scales change."""
+        import torch
+        n = mm_transformed_scale_bytes(self.h)
+        self.tsf = torch.empty(n, dtype=torch.uint8, device=w1_sf.device)
+        s = (stream or torch.cuda.current_stream(w1_sf.device)).cuda_stream
+        mm_transform_weight_scales(self.h, w1_sf.data_ptr(), w2_sf.data_ptr(), self.tsf.data_ptr(), n, s)
 
     def run(self, x_fp8, x_sf, topk_idx, topk_w, w1, w1_sf, w2, w2_sf, out=None, stream=None):
         """Enqueue one forward on `stream` (default: torch's current stream)."""

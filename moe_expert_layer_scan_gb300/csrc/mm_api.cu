@@ -46,6 +46,11 @@ struct mm_handle {
   const void* w1sfh_key;
   CUtensorMap tm_w1h;
   CUtensorMap tm_w1sfh;
+  // transformed weight scales (mm_transform_weight_scales): the caller's copy
+  // and the two scale tensors it was made from (null: none registered)
+  const void* tsf_w1;
+  const void* tsf_w2;
+  uint8_t* tsf_dst;
   // GEMM schedule: MM_SCHEDULE_AUTO / _SPLIT / _FUSED
   int schedule;
   // expert-parallel-ready routing: destination ranks and the caller's
@@ -218,6 +223,8 @@ mm_status_t mm_create(mm_handle_t* out, int E, int H, int I, int topk, int num_s
   }
   h->w1_key = h->w2_key = h->w1sf_key = h->w2sf_key = nullptr;
   h->w1h_key = h->w1sfh_key = nullptr;
+  h->tsf_w1 = h->tsf_w2 = nullptr;
+  h->tsf_dst = nullptr;
   h->schedule = MM_SCHEDULE_AUTO;
   h->ep_ranks = 1;
   h->expert_stats = nullptr;
@@ -265,6 +272,39 @@ mm_status_t mm_set_weight_format(mm_handle_t h, int format) {
     return MM_ERR_INVALID_ARG;
   if (format != h->w_fmt) h->w1_key = h->w2_key = h->w1h_key = nullptr;  // cached weight maps describe the old layout
   h->w_fmt = format;
+  return MM_OK;
+}
+
+mm_status_t mm_transformed_scale_bytes(mm_handle_t h, size_t* bytes) {
+  if (!h || !bytes) return MM_ERR_INVALID_ARG;
+  const size_t ep = (size_t)(h->E + h->S);
+  *bytes = ep * 2 * h->I * (h->H / 32) + ep * h->H * (h->I / 32);
+  return MM_OK;
+}
+
+mm_status_t mm_transform_weight_scales(mm_handle_t h, const void* w1_sf, const void* w2_sf, void* dst,
+                                       size_t dst_bytes, mm_stream_t stream) {
+  if (!h) return MM_ERR_INVALID_ARG;
+  if (!dst) {
+    h->tsf_w1 = h->tsf_w2 = nullptr;
+    h->tsf_dst = nullptr;
+    return MM_OK;
+  }
+  size_t need = 0;
+  mm_transformed_scale_bytes(h, &need);
+  if (!w1_sf || !w2_sf || !aligned(dst, 16) || dst_bytes < need) return MM_ERR_INVALID_ARG;
+  if (h->w_fmt == MM_WEIGHTS_FP8_F128 || h->H % 512 || h->I % 512 || !aligned(w1_sf, 16) || !aligned(w2_sf, 16))
+    return MM_ERR_UNSUPPORTED;
+  if (cudaSetDevice(h->device) != cudaSuccess) return MM_ERR_CUDA;
+  const long ep = h->E + h->S;
+  uint8_t* d1 = static_cast<uint8_t*>(dst);
+  uint8_t* d2 = d1 + (size_t)ep * 2 * h->I * (h->H / 32);
+  if (mm_launch_transform_sf(static_cast<const uint8_t*>(w1_sf), d1, ep * 2 * h->I / 128, h->H, stream) != 0 ||
+      mm_launch_transform_sf(static_cast<const uint8_t*>(w2_sf), d2, ep * h->H / 128, h->I, stream) != 0)
+    return MM_ERR_CUDA;
+  h->tsf_w1 = w1_sf;
+  h->tsf_w2 = w2_sf;
+  h->tsf_dst = d1;
   return MM_OK;
 }
 
@@ -474,6 +514,10 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
   g1.act_sf_vec = (h->H / 32) % 16 == 0;
   g1.w_fp8 = fp4 ? 0 : 1;
   g1.sf_tma = sf_tma ? 1 : 0;
+  // the registered transformed weight scales, when this call's scale tensors
+  // are the ones they were made from
+  const bool tsf = sf_tma && h->tsf_dst && h->tsf_w1 == w1_sf && h->tsf_w2 == w2_sf;
+  g1.w_sf_t = tsf ? h->tsf_dst : nullptr;
   g1.ready = reinterpret_cast<int32_t*>(base + L.ready);
   g1.ready_target = f1 * mm_gemm_epilogue_warps(variant);
   g1.tile_ctr = ra.sched + 0;
@@ -481,6 +525,7 @@ mm_status_t mm_run(mm_handle_t h, int T, const void* x_fp8, const void* x_sf, co
 
   GemmArgs g2 = g1;
   g2.w_sf = static_cast<const uint8_t*>(w2_sf);
+  g2.w_sf_t = tsf ? h->tsf_dst + (size_t)Ep * 2 * h->I * (h->H / 32) : nullptr;
   g2.act_sf = base + L.l2a_sf;
   g2.tile_start = ra.tiles_l2;
   g2.row_w = nullptr;

@@ -554,6 +554,39 @@ extern "C" int mm_launch_route(const mm::RouteArgs* a, void* stream) {
   return (int)e;
 }
 
+namespace mm {
+// Weight-scale transform (the SM100 weight transform's scale transpose): one
+// warp per (128-row block, K step of 128); lane l gathers the step's four
+// scale bytes of rows l, l + 32, l + 64 and l + 96 of the block and stores
+// them as its 16 bytes of the block's 512-byte piece (the layout the grouped
+// GEMM's scale warp would otherwise build in shared memory).
+__global__ void __launch_bounds__(256) transform_sf_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                                           long blocks, int K) {
+  const int lane = threadIdx.x & 31;
+  const long gw = ((long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long nw = ((long)gridDim.x * blockDim.x) >> 5;
+  const int steps = K / 128, ld = K / 32;
+  for (long p = gw; p < blocks * steps; p += nw) {
+    const long b = p / steps;
+    const int ks = (int)(p - b * steps);
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = __ldg(reinterpret_cast<const uint32_t*>(src + (b * 128 + 32 * i + lane) * ld + 4 * ks));
+    *reinterpret_cast<uint4*>(dst + p * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+}  // namespace mm
+
+extern "C" int mm_launch_transform_sf(const uint8_t* src, uint8_t* dst, long blocks, int K, void* stream) {
+  const long warps = blocks * (K / 128);
+  if (warps <= 0) return 0;
+  long grid = (warps + 7) / 8;
+  if (grid > 152 * 16) grid = 152 * 16;
+  return (int)mm::launch_kernel(mm::transform_sf_kernel, dim3((unsigned)grid), dim3(256), 0, (cudaStream_t)stream,
+                                false, src, dst, blocks, K);
+}
+
 extern "C" int mm_launch_gather(const mm::GatherArgs* a, void* stream) {
   if (a->T <= 0) return 0;
   // 4 KB chunks per warp from kGatherRowsMin tokens up, else 1 KB chunks

@@ -185,6 +185,7 @@ struct GemmCfg {
 // from the L1 or L2 argument block (each a constant-bank read).
 struct Phase {
   const uint8_t* w_sf;
+  const uint8_t* w_sf_t;  // transformed weight scales (512 bytes per 128-row block and K step), or null
   const uint8_t* act_sf;
   int K, rows_w, second, w_sf_vec, act_sf_vec;
   bool l1;
@@ -193,6 +194,7 @@ __device__ __forceinline__ Phase phase_of(bool l1, const GemmArgs& g1, const Gem
   Phase p;
   p.l1 = l1;
   p.w_sf = l1 ? g1.w_sf : g2.w_sf;
+  p.w_sf_t = l1 ? g1.w_sf_t : g2.w_sf_t;
   p.act_sf = l1 ? g1.act_sf : g2.act_sf;
   p.K = l1 ? g1.K : g2.K;
   p.rows_w = l1 ? g1.rows_w : g2.rows_w;
@@ -377,12 +379,14 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
   // the stage's TMEM slot (the weight blocks' and the token tile's, the latter
   // shared by both MMA streams) and commits the copies to sfready[s]; the MMA
   // threads then issue only MMAs. The slot is free once empty[s] completed.
-  auto copy_scales = [&](int s, uint32_t amask, const uint8_t* sF) {
+  // (the weight blocks' 512-byte pieces at wsrc + u * wstride: the stage's
+  // scale slot, or a raw group holding transformed weight scales)
+  auto copy_scales = [&](int s, uint32_t amask, const uint8_t* sF, const uint8_t* wsrc, int wstride) {
     tc_fence_after();
     const uint32_t slot = tmem + (uint32_t)(C::SF_BASE + s * C::SF_STAGE_COLS);
 #pragma unroll
     for (int u = 0; u < C::NA; ++u)
-      if ((amask >> u) & 1u) tc_cp_32x128b_warpx4(slot + 4u * u, sdesc_sf_32x16(smem_u32(sF + 512 * u)));
+      if ((amask >> u) & 1u) tc_cp_32x128b_warpx4(slot + 4u * u, sdesc_sf_32x16(smem_u32(wsrc + wstride * u)));
 #pragma unroll
     for (int gq = 0; gq < C::SFB_ROWS / 128; ++gq)
       tc_cp_32x128b_warpx4(slot + 4u * C::NA + 4u * gq, sdesc_sf_32x16(smem_u32(sF + C::NA * 512 + gq * 512)));
@@ -484,8 +488,14 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
             mbar_arrive_expect_tx(&rfull[gslot], nact * C::RAW_ROWS_BYTES + C::RAW_B_BYTES);
 #pragma unroll
             for (int u = 0; u < C::NA; ++u)
-              if ((amask >> u) & 1u)
-                tma_load_2d(raw + u * C::RAW_ROWS_BYTES, twsf, &rfull[gslot], kb * 4, block_wrow(g, t, u, C::NA));
+              if ((amask >> u) & 1u) {
+                if (g.w_sf_t)  // transformed: the group's four 512-byte pieces are contiguous
+                  bulk_load(raw + u * C::RAW_ROWS_BYTES,
+                            g.w_sf_t + ((size_t)(block_wrow(g, t, u, C::NA) / 128) * kblocks + kb) * 512,
+                            (uint32_t)C::RAW_ROWS_BYTES, &rfull[gslot]);
+                else
+                  tma_load_2d(raw + u * C::RAW_ROWS_BYTES, twsf, &rfull[gslot], kb * 4, block_wrow(g, t, u, C::NA));
+              }
             tma_load_2d(raw + C::NA * C::RAW_ROWS_BYTES, tasf, &rfull[gslot], kb * 4, t.row0);
           }
           ++gi;
@@ -557,6 +567,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
       const uint32_t amask = block_mask(g, t);
       const int nb = (t.nrows + 31) / 32;
       const int kblocks = g.K / C::BK;
+      const bool tw = g.w_sf_t != nullptr;  // weight scales arrive already laid out (read in place by the copies)
       for (int kg = 0; kg < kblocks && ok; kg += 4, ++gi) {
         const int gslot = (int)(gi % C::RAW_G);
         const uint32_t gph = (gi / C::RAW_G) & 1u;
@@ -567,7 +578,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
         for (int op = 0; op < C::NA; ++op)
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            wa[op][i] = ((amask >> op) & 1u)
+            wa[op][i] = ((amask >> op) & 1u) && !tw
                             ? *reinterpret_cast<const uint4*>(raw + op * C::RAW_ROWS_BYTES + (32 * i + lane) * 16)
                             : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -576,26 +587,36 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
                       ? *reinterpret_cast<const uint4*>(raw + C::NA * C::RAW_ROWS_BYTES + (32 * j + lane) * 16)
                       : make_uint4(0u, 0u, 0u, 0u);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&rempty[gslot]);  // the raw slot may be refilled
+        // the raw slot may be refilled (transformed weight scales: once the
+        // group's copies, which read them in place, have completed)
+        if (lane == 0 && !tw) mbar_arrive(&rempty[gslot]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int s = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, g1.status, g1.timeout_ns, site0 + 5)) { ok = false; break; }
           uint8_t* sF = smem + C::SF_OFF + s * C::SF_STAGE_BYTES;
+          if (!tw) {
 #pragma unroll
-          for (int op = 0; op < C::NA; ++op)
-            st_shared_v4(sF + op * 512 + lane * 16, word(wa[op][0], c), word(wa[op][1], c), word(wa[op][2], c),
-                         word(wa[op][3], c));
+            for (int op = 0; op < C::NA; ++op)
+              st_shared_v4(sF + op * 512 + lane * 16, word(wa[op][0], c), word(wa[op][1], c), word(wa[op][2], c),
+                           word(wa[op][3], c));
+          }
 #pragma unroll
           for (int q = 0; q < NB / 4; ++q)
             st_shared_v4(sF + C::NA * 512 + q * 512 + lane * 16, word(wb[4 * q], c), word(wb[4 * q + 1], c),
                          word(wb[4 * q + 2], c), word(wb[4 * q + 3], c));
           fence_proxy_async_smem();  // generic-proxy writes, read next by tcgen05.cp
           __syncwarp();
-          if (lane == 0) copy_scales(s, amask, sF);
+          if (lane == 0) {
+            if (tw)
+              copy_scales(s, amask, sF, raw + c * 512, C::RAW_ROWS_BYTES);
+            else
+              copy_scales(s, amask, sF, sF, 512);
+          }
           ++it;
         }
+        if (lane == 0 && tw) tc_commit(&rempty[gslot]);  // after the group's copies complete
         if (ok && kg == 0) next = take_tile(tn, true);
       }
       if (!ok) break;
@@ -696,7 +717,7 @@ __global__ void __launch_bounds__(Warps<BN, NA>::THREADS, 1)
                        word(cb[4 * q + 2], c), word(cb[4 * q + 3], c));
         fence_proxy_async_smem();  // generic-proxy writes, read next by tcgen05.cp
         __syncwarp();
-        if (lane == 0) copy_scales(s, cur_mask, sF);
+        if (lane == 0) copy_scales(s, cur_mask, sF, sF, 512);
         ++it;
       }
       if (!ok || !has_next) break;

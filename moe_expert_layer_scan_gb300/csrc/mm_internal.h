@@ -176,6 +176,9 @@ struct GemmArgs {
   int tile_class;
   const int32_t* sched;  // the forward's scheduling words (kSched*)
   int sf_tma;  // scale rows are loaded by TMA (every K a multiple of 512, 16-byte aligned scale tensors)
+  // with sf_tma: the transformed weight scales (mm_transform_weight_scales),
+  // 512 bytes per 128-row block and K step in the tcgen05.cp layout, or null
+  const uint8_t* w_sf_t;
 };
 
 // Tensor maps of one GEMM launch (L1 and L2; a single-linear launch repeats its
@@ -206,6 +209,10 @@ extern "C" {
 int mm_launch_route(const mm::RouteArgs* a, void* stream);
 int mm_route_launches(int slots);  // kernels mm_launch_route enqueues for this many slots
 int mm_launch_gather(const mm::GatherArgs* a, void* stream);
+// Weight-scale transform: for `blocks` 128-row blocks of a UE8M0 scale tensor
+// with K/32 bytes per row, the 512-byte tcgen05.cp piece of every (block, K
+// step of 128) into dst, block-major.
+int mm_launch_transform_sf(const uint8_t* src, uint8_t* dst, long blocks, int K, void* stream);
 int mm_launch_combine(const mm::CombineArgs* a, void* stream, bool pdl);
 // variant: 0 = small tiles, 1 = large tiles, 2 = small tiles with six stages
 // (E + S <= kDeepMaxExperts), 3 = 224-token tiles, 4 = small tiles with four
