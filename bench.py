@@ -46,14 +46,14 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
 # capture, keyed by workload, valid only while the GEMM sources hash to `src`
 # (gemm_source_hash) and for the kernel named (fused "gemm" or "l1_gemm").
 NCU_TRAFFIC = {
-    # decode (fused GEMM): E=64 capture (42 experts touched, 992,482,048 bytes) scaled to the 61
+    # decode (fused GEMM): E=64 capture (42 experts touched, 988,569,856 bytes) scaled to the 61
     # experts one launch touches
-    "decode": {"src": "e36b1c898440f3f6", "kernel": "gemm", "bytes": 1441462022},
+    "decode": {"src": "e7f04684463aacd7", "kernel": "gemm", "bytes": 1435780029},
     # prefill (split schedule, per-expert widths: every expert above 112 rows, so both linears
     # run the 224-token tiles, one CTA per tile; the light-class launches are empty): T=2048/E=32
-    # capture of the four GEMM launches (16384 rows; L1 670,116,352 + L2 483,447,552 bytes) scaled
+    # capture of the four GEMM launches (16384 rows; L1 666,591,232 + L2 483,426,304 bytes) scaled
     # x8 to 131072 rows
-    "prefill": {"src": "e36b1c898440f3f6", "kernel": "gemms", "bytes": 9228511232},
+    "prefill": {"src": "e7f04684463aacd7", "kernel": "gemms", "bytes": 9200140288},
 }
 
 
