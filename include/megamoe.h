@@ -248,7 +248,9 @@ MM_API mm_status_t mm_set_weight_format(mm_handle_t h, int format);
  *     arguments. Rewrite the copy (call again) whenever the scales' contents
  *     change; dst = NULL unregisters. The transform is weight preparation, not
  *     part of a forward. UE8M0 formats only (MXFP4, MXFP8), H and I multiples of
- *     512 (else MM_ERR_UNSUPPORTED); runs on CTA pairs read the arguments.
+ *     512, both scale tensors 16-byte aligned (else MM_ERR_UNSUPPORTED); runs on
+ *     CTA pairs, and runs after a switch to MM_WEIGHTS_FP8_F128, read the
+ *     arguments.
  *     Errors: MM_ERR_INVALID_ARG for a null handle, null scale pointers, an
  *     unaligned dst or dst_bytes too small; MM_ERR_CUDA if the launch fails. */
 MM_API mm_status_t mm_transformed_scale_bytes(mm_handle_t h, size_t* bytes);
